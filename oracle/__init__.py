@@ -1,0 +1,188 @@
+"""fp64 CPU oracle for Gated MLA / Gated DSA attention (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The library's GPU path neither imports
+it nor shares code with it.
+
+The arithmetic lives in ``mla_oracle.c`` (plain C, fp64, OpenMP over
+independent rows); this module builds it with gcc, converts inputs to
+contiguous float64 arrays and calls it through ctypes. Each wrapper names the
+passage it follows in the C file's header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libmla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.POINTER(ctypes.c_int64)
+_I32 = ctypes.POINTER(ctypes.c_int32)
+
+
+def build(force: bool = False, extra_flags=(), out: str | None = None,
+          src: str | None = None) -> str:
+    """Compile the oracle with gcc (no -ffast-math, no FMA contraction)."""
+    out = out or _LIB
+    src = src or _SRC
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           *extra_flags, "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            # MLA_ORACLE_LIB lets the mutation test point the pins at a planted-bug build
+            _lib = _bind(ctypes.CDLL(os.environ.get("MLA_ORACLE_LIB") or build()))
+    return _lib
+
+
+def _bind(lib):
+    lib.orc_set_threads.argtypes = [ctypes.c_int]
+    lib.orc_set_threads.restype = ctypes.c_int
+    lib.orc_mla_prefill.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int] * 6 + [ctypes.c_double]
+    lib.orc_mla_decode.argtypes = [_D, _D, _D, _I64] + [ctypes.c_int] * 4 + [_D, _D, ctypes.c_double]
+    lib.orc_attention_probs.argtypes = [_D, _D, _D, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_double, _D, _D]
+    lib.orc_dsa_index_scores.argtypes = [_D, _D, _D, _I64, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, _D]
+    lib.orc_dsa_topk.argtypes = [_D, _I64, ctypes.c_int, ctypes.c_int, _I32]
+    lib.orc_dsa_sparse_decode.argtypes = [_D, _D, _D, _I64, _I32] + [ctypes.c_int] * 5 + \
+        [_D, _D, ctypes.c_double]
+    for f in ("orc_mla_prefill", "orc_mla_decode", "orc_attention_probs",
+              "orc_dsa_index_scores", "orc_dsa_topk", "orc_dsa_sparse_decode"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening of bf16/fp32 (torch or numpy) to a contiguous float64 array."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i64(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int64)
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _p(a, t=_D):
+    return None if a is None else a.ctypes.data_as(t)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (code {rc})")
+
+
+def set_threads(n: int = 0, lib=None) -> int:
+    """Set the OpenMP thread count (0 keeps the default); returns the count in use."""
+    return (lib or load()).orc_set_threads(int(n))
+
+
+def mla_prefill(q, k, v, gate, scale: float, lib=None) -> np.ndarray:
+    """Causal gated MLA prefill; returns out [B,Tq,H*Dv] in float64."""
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(gate)
+    B, H, Tq, Dqk = q.shape
+    Tk, Dv = k.shape[2], v.shape[3]
+    if k.shape != (B, H, Tk, Dqk) or v.shape != (B, H, Tk, Dv):
+        raise ValueError("prefill shape mismatch")
+    if g is not None and g.shape != (B, Tq, H * Dv):
+        raise ValueError("gate shape mismatch")
+    out = np.empty((B, Tq, H * Dv))
+    _check((lib or load()).orc_mla_prefill(_p(q), _p(k), _p(v), _p(g), _p(out), B, H, Tq, Tk,
+                                           Dqk, Dv, float(scale)), "prefill")
+    return out
+
+
+def mla_decode(q, k, v, cu_seqlens, gate, scale: float, lib=None) -> np.ndarray:
+    """Decode over the packed cache; returns out [B,H*Dv] in float64."""
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(gate)
+    cu = _i64(cu_seqlens)
+    B, H, Dqk = q.shape
+    Dv = v.size // (int(cu[-1]) * H)
+    if k.size != int(cu[-1]) * H * Dqk:
+        raise ValueError("decode cache size mismatch")
+    out = np.empty((B, H * Dv))
+    _check((lib or load()).orc_mla_decode(_p(q), _p(k), _p(v), _p(cu, _I64), B, H, Dqk, Dv,
+                                          _p(g), _p(out), float(scale)), "decode")
+    return out
+
+
+def attention_probs(q, k, v, scale: float, lib=None):
+    """One attention row over all n keys: returns (z [Dv], p [n])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n, Dqk = k.shape
+    Dv = v.shape[1]
+    z, p = np.empty(Dv), np.empty(n)
+    _check((lib or load()).orc_attention_probs(_p(q), _p(k), _p(v), n, Dqk, Dv, float(scale),
+                                               _p(z), _p(p)), "probs")
+    return z, p
+
+
+def dsa_index_scores(index_q, index_k, w, cu_seqlens, lib=None) -> np.ndarray:
+    """Packed index scores [cu[B]] in float64."""
+    iq, ik, ww = _f64(index_q), _f64(index_k), _f64(w)
+    cu = _i64(cu_seqlens)
+    B, NH, Di = iq.shape
+    out = np.empty(int(cu[-1]))
+    _check((lib or load()).orc_dsa_index_scores(_p(iq), _p(ik), _p(ww), _p(cu, _I64), B, NH, Di,
+                                                _p(out)), "index scores")
+    return out
+
+
+def dsa_topk(scores, cu_seqlens, topk: int, lib=None) -> np.ndarray:
+    """Top-k positions per sequence, ascending, -1 padded: int32 [B,topk]."""
+    s = _f64(scores)
+    cu = _i64(cu_seqlens)
+    B = cu.size - 1
+    idx = np.empty((B, topk), dtype=np.int32)
+    _check((lib or load()).orc_dsa_topk(_p(s), _p(cu, _I64), B, int(topk), _p(idx, _I32)), "topk")
+    return idx
+
+
+def dsa_sparse_decode(q, k, v, cu_seqlens, idx, gate, scale: float, lib=None) -> np.ndarray:
+    """Gated MLA over the selected positions only; returns out [B,H*Dv]."""
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(gate)
+    cu = _i64(cu_seqlens)
+    ix = _i32(idx)
+    B, H, Dqk = q.shape
+    topk = ix.shape[1]
+    Dv = v.size // (int(cu[-1]) * H)
+    out = np.empty((B, H * Dv))
+    _check((lib or load()).orc_dsa_sparse_decode(_p(q), _p(k), _p(v), _p(cu, _I64), _p(ix, _I32),
+                                                 topk, B, H, Dqk, Dv, _p(g), _p(out),
+                                                 float(scale)), "sparse decode")
+    return out
