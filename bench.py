@@ -1,0 +1,372 @@
+"""Benchmark of the Gated MLA decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one gated MLA decode call (scores, softmax, P.V, split-KV
+log-sum-exp merge and sigmoid gate) over the whole synthetic cache of the
+workload: B=32 sequences, 96 heads, 8192 cached positions each, bf16
+(16.1 GB of keys and values per step, far larger than the 129 MB L2, so no
+flush is needed between steps). The metric is KV-read GB/s: the algorithmic
+bytes of the cache (every head's full 192+128 features per position) per
+step divided by the device time per step.
+
+Under torchrun with N>1 each rank runs its own replica on its own GPU (the
+path shards by sequence with no exchange step); value = all ranks' bytes
+divided by the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload on this host's cores (the only reference implementation there is).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import mla_inputs as mi  # noqa: E402
+from mla_family_attention_gb300 import accounting as acc  # noqa: E402
+
+METRIC = "MLA decode KV-read GB/s (% HBM peak); prefill attn TFLOP/s (% bf16 peak)"
+DEFAULT_WORKLOAD = "decode_b32_h96_t8192"
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while the bench runs."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 10:
+                continue
+            r = [x.strip() for x in r]
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(r[2]), float(r[3]), r[4], r[5:]))
+            except ValueError:
+                continue
+        inside = [x for x in rows if self.t0 - 1 <= x[0] <= self.t1 + 1] or rows
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for x in inside for i in range(1, 5)
+                          if x[4][i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median([x[1] for x in inside]) if inside else None,
+                "sm_max_mhz": max([x[2] for x in inside]) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's source
+    has not changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha256_16"]:
+        return None
+    return d["dram_bytes_per_launch"]
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ------------------------------------------------------------------------------------------
+def oracle_inputs(dec, n_seq: int):
+    """fp64 copies of the first n_seq sequences (all heads): the oracle's inputs."""
+    H = dec.H
+    npos = sum(dec.lengths[:n_seq])
+    return dict(q=dec.q[:n_seq].to("cpu", torch.float64).numpy(),
+                k=dec.k[:npos * H * 192].to("cpu", torch.float64).numpy(),
+                v=dec.v[:npos * H * 128].to("cpu", torch.float64).numpy(),
+                cu_seqlens=dec.cu_seqlens[:n_seq + 1].to("cpu").numpy(),
+                gate=dec.gate[:n_seq].to("cpu", torch.float64).numpy(),
+                scale=dec.scale)
+
+
+def oracle_decode_sample(dec, n_seq: int, min_seconds: float):
+    """Time the fp64 oracle over the first n_seq sequences (all heads), repeated
+    until min_seconds of CPU work; returns (GB/s, seconds, threads, repeats, n_seq)."""
+    import oracle
+    threads = oracle.set_threads(len(os.sched_getaffinity(0)))
+    x = oracle_inputs(dec, n_seq)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.mla_decode(**x)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    nbytes = acc.decode_kv_bytes(dec.lengths[:n_seq], dec.H) * reps
+    return nbytes / el / 1e9, el, threads, reps, n_seq
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle on this host's cores, one sequence
+    (all heads) of the workload per step (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    name = args.workload
+    w = mi.WORKLOADS[name]
+    lengths = mi.workload_lengths(name)
+    n_seq = 1
+    dec = mi.make_decode(lengths[:n_seq], w["H"], True, device="cpu", config=w["config"])
+    threads = oracle.set_threads(len(os.sched_getaffinity(0)))
+    x = oracle_inputs(dec, n_seq)
+    for _ in range(args.warmup):
+        oracle.mla_decode(**x)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mla_decode(**x)
+    per_step = (time.perf_counter() - t0) / args.steps
+    nbytes = acc.decode_kv_bytes(lengths[:n_seq], w["H"])
+    value = nbytes / per_step / 1e9
+    sample = (f"{n_seq} of {len(lengths)} sequences x {w['H']} heads x {lengths[0]} positions "
+              "per step (fp64 inputs prepared once)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(name),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name):
+    w = mi.WORKLOADS[name]
+    cfg = {"workload": name, "B": w["B"], "H": w["H"], "head_dims": "qk 192 (128+64 shared), v 128",
+           "gate": bool(w.get("gated", True))}
+    if "T" in w:
+        cfg["T"] = w["T"]
+    if "lo" in w:
+        cfg["T_range"] = [w["lo"], w["hi"]]
+    cfg["l2"] = "inputs larger than L2 (no flush needed)"
+    return cfg
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import mla_family_attention_gb300 as mla
+    from mla_family_attention_gb300 import _lib
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload
+    w = mi.WORKLOADS[name]
+    if w["kind"] != "decode":
+        raise SystemExit(f"workload {name} is not a decode workload")
+    lengths = mi.workload_lengths(name)
+    max_len = max(lengths)
+    dec = mi.make_decode(lengths, w["H"], True, device=dev, config=w["config"])
+    H, B = w["H"], w["B"]
+    nbytes = acc.decode_kv_bytes(lengths, H)
+    out = torch.empty((B, H * 128), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mla.workspace_size(_lib.OP_DECODE, B, H, max_len, 0), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mla.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, max_len, gate=dec.gate, out=out,
+                       scale=dec.scale, ws=ws, stream=stream)
+
+    sampler = ClockSampler(local)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    mla.check_device_status(stream)
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region ----
+    mla.timing_enable(True)
+    mla.timing_read(_lib.OP_DECODE)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.mark_start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark_end()
+    barrier(world)
+    mla.timing_enable(False)
+    ms_total = ev0.elapsed_time(ev1)
+    k_ms, k_launches = mla.timing_read(_lib.OP_DECODE)
+    mla.check_device_status(stream)
+    clocks = sampler.finish()
+
+    ms_per_step = max_over_ranks(ms_total / args.steps, world)
+    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
+    k_avg_ms = max_over_ranks(k_ms / max(k_launches, 1), world)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(dec, lengths, max_len, dev, stream, world, args)
+
+    peak, peak_kind = peaks()
+    achieved = nbytes / (k_avg_ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(name),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": peak_kind,
+                         "frac_of_nominal_7900": round(achieved / 7900.0, 4),
+                         "kernel": "decode_partial_kernel",
+                         "traffic": traffic_for("decode_partial_kernel"),
+                         "algorithmic_bytes_per_launch": nbytes},
+            "e2e": e2e, "gpu_launches": 3 * args.steps * world, "clocks": clocks}
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, el, threads, reps, n_seq = oracle_decode_sample(dec, 1, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{n_seq} of {B} sequences x {H} heads x "
+                                          f"{lengths[0]} positions, {reps} repeats, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(dec, lengths, max_len, dev, stream, world, args):
+    """Same metric through the public API with pinned host buffers: every step
+    copies the inputs host->device, runs the call and reads the output back."""
+    import mla_family_attention_gb300 as mla
+    host = {n: getattr(dec, n).to("cpu").pin_memory() for n in ("q", "k", "v", "gate",
+                                                                 "cu_seqlens")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty((len(lengths), dec.H * 128), dtype=torch.bfloat16).pin_memory()
+    out_d = torch.empty_like(out_h, device=dev)
+    d2h = out_h.numel() * out_h.element_size()
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def step():
+        for n in host:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        mla.mla_decode(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["cu_seqlens"], max_len,
+                       gate=dev_in["gate"], out=out_d, scale=dec.scale, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    el = max_over_ranks((time.perf_counter() - t0) / steps, world)
+    barrier(world)
+    nbytes = acc.decode_kv_bytes(lengths, dec.H)
+    del dev_in, host
+    return {"value": round(nbytes * world / el / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[n for n, w in mi.WORKLOADS.items() if w["kind"] == "decode"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * mla.h - C ABI of the GB300 (sm_103a) Gated MLA / Gated DSA attention library.
+ *
+ * The library computes the attention core of Kimi K3's Gated MLA layer and of
+ * its K3.1 Gated DSA variant, below the modules the pages show:
+ *
+ *   - Kimi K3 modeling code, MLA forward: per-head queries and cached keys of
+ *     192 features (128 content + 64 shared key part, unrotated, identical for
+ *     every head), cached values of 128 features, scale 192^-1/2
+ *     ("self.scaling"), causal ("is_causal = True"), then the output reshaped
+ *     to [B,T,H*128] and multiplied by sigmoid of the gate logits before
+ *     o_proj.
+ *   - Kimi K2 "Latent attention > KV cache" page: the same layout with 64
+ *     heads, the last 64 key features a pre-rotated rotary key, no gate.
+ *   - K3.1 Gated DSA post, eqs. (5), (6), (9), (10): a 32-head ReLU-weighted
+ *     index score over the cached index keys, the top min(2048, t) positions,
+ *     and gated MLA over those positions only.
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are passed as raw 16-bit patterns (mla_bf16).
+ *   - Every pointer is DEVICE memory owned by the caller, contiguous, and
+ *     16-byte aligned; the library never allocates, frees or keeps a pointer
+ *     after the call returns.  Scratch memory is the caller's workspace
+ *     `ws` of at least mla_workspace_size(...) bytes, 256-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream): they validate arguments on the host, enqueue kernels
+ *     and return.  They never synchronise.  Calls that share a workspace must
+ *     be ordered (same stream or events); overlapping calls on one workspace
+ *     race.
+ *   - Errors: a non-MLA_OK status means nothing was enqueued (except
+ *     MLA_ERR_CUDA after a launch failure); mla_last_error() returns a
+ *     message for the calling thread.  Faults that only the GPU can see
+ *     (a cache length outside [1, max_seqlen], a selected index outside the
+ *     sequence, a pipeline wait that ran out) never trap: the kernel skips
+ *     the offending work, records a code in a device status word, and
+ *     mla_check_device_status() reports it.
+ *   - Positions are 0-based (the DSA post counts from 1).
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mla_bf16;   /* bfloat16 bit pattern */
+typedef void* mla_stream;    /* cudaStream_t */
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+    MLA_ERR_UNSUPPORTED = 2,  /* a shape the kernels do not implement */
+    MLA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    MLA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    MLA_ERR_TIMEOUT = 5,      /* a device-side pipeline wait ran out (device status) */
+    MLA_ERR_BAD_INDEX = 6     /* a selected position outside its sequence (device status) */
+} mla_status;
+
+/* Operation ids for mla_workspace_size. */
+enum { MLA_OP_PREFILL = 0, MLA_OP_DECODE = 1, MLA_OP_INDEX_TOPK = 2, MLA_OP_SPARSE_DECODE = 3 };
+
+/*
+ * Causal gated MLA prefill (Kimi K3 MLA forward; Kimi K2 score line
+ * attn_weights = matmul(q, k^T) * softmax_scale; DSA post eq. (9), (10)).
+ *
+ *   q    [B,H,Tq,192]  queries (128 content ++ 64 shared-key partner)
+ *   k    [B,H,Tk,192]  cached keys including the Tq new ones at the end
+ *   v    [B,H,Tk,128]  cached values
+ *   gate [B,Tq,H*128]  gate logits, or NULL for no gate (K2 shape)
+ *   out  [B,Tq,H*128]  out[b,i,h*128+d] = z[b,h,i,d] * sigmoid(gate[b,i,h*128+d])
+ *
+ * Query i is at absolute position Tk-Tq+i and sees keys j <= Tk-Tq+i
+ * (bottom-right aligned causal mask; Tq == Tk is an empty-cache prefill).
+ * Requires 1 <= Tq <= Tk, H >= 1, B >= 1.  Softmax and gate in fp32, one
+ * rounding to bf16 at the output.
+ */
+mla_status mla_prefill(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                       const mla_bf16* gate, mla_bf16* out, int B, int H, int Tq, int Tk,
+                       float scale, void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
+ * Split-KV gated MLA decode: one query per sequence over a packed cache
+ * (Kimi K3 MLA forward in decode mode; DSA post eq. (9), (10)).
+ *
+ *   q          [B,H,192]
+ *   k          packed: sequence b is [H, T_b, 192] starting at element cu[b]*H*192
+ *   v          packed: sequence b is [H, T_b, 128] starting at element cu[b]*H*128
+ *   cu_seqlens [B+1] int64 on the device, cu[0] = 0, T_b = cu[b+1]-cu[b]
+ *   gate       [B,H*128] logits or NULL
+ *   out        [B,H*128]
+ *
+ * Every cached position is visible (the current token is already in the
+ * cache).  Each sequence must have 1 <= T_b <= max_seqlen; a sequence that
+ * violates this is skipped (its output is left untouched) and the device
+ * status records MLA_ERR_INVALID_ARG.  A uniform cache [B,H,T,D] is the case
+ * cu[b] = b*T.  Partial results of position chunks are merged by
+ * log-sum-exp in a fixed order, so reruns are bitwise identical.
+ */
+mla_status mla_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                      const int64_t* cu_seqlens, int B, int H, int max_seqlen,
+                      const mla_bf16* gate, mla_bf16* out, float scale,
+                      void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
+ * DSA indexer score and top-k (DSA post eqs. (5) and (6)).
+ *
+ *   index_q     [B,NH,128]  index queries (NH must be 32)
+ *   index_k     packed [cu[B],128]: sequence b's keys are rows cu[b]..cu[b+1]-1
+ *   w           [B,NH] fp32 head weights, with the eq. (5) constant
+ *               1/(sqrt(32)*sqrt(128)) already folded in by the caller
+ *   topk_idx    [B,topk] int32 out: the min(topk, T_b) positions of largest
+ *               score_s = sum_h w_h * max(0, q_h . k_s), ranked by (score
+ *               descending, position ascending), written in ascending
+ *               position order and padded with -1.  When T_b <= topk every
+ *               position is returned.
+ *   topk_scores [B,topk] fp32 out (score of each returned position, -inf on
+ *               padding) or NULL
+ *
+ * Requires 1 <= topk <= 2048 and 1 <= T_b <= max_seqlen <= 2^24.
+ */
+mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,
+                          const int64_t* cu_seqlens, int B, int NH, int max_seqlen, int topk,
+                          int32_t* topk_idx, float* topk_scores,
+                          void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
+ * Gated MLA over the selected positions only (DSA post eqs. (9), (10)); all
+ * H heads of a sequence share its selection.
+ *
+ *   q, k, v, cu_seqlens, gate, out as in mla_decode
+ *   topk_idx [B,topk] int32 positions within each sequence; -1 entries are
+ *            skipped; an entry >= T_b or < -1 is skipped and recorded as
+ *            MLA_ERR_BAD_INDEX in the device status.  The order of the
+ *            entries does not matter.  A sequence with no valid entry gets a
+ *            zero output.
+ */
+mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                             const int64_t* cu_seqlens, const int32_t* topk_idx, int topk,
+                             int B, int H, const mla_bf16* gate, mla_bf16* out, float scale,
+                             void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
+ * Bytes of workspace an operation needs (a multiple of 256; 0 if none).
+ * `op` is one of MLA_OP_*; arguments an operation does not use are ignored
+ * (prefill: none needed; decode: B, H, max_seqlen; index_topk: B,
+ * max_seqlen; sparse_decode: B, H, topk).  Returns 0 for invalid arguments.
+ */
+size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: MLA_OK, or the first MLA_ERR_TIMEOUT /
+ * MLA_ERR_BAD_INDEX / MLA_ERR_INVALID_ARG a kernel recorded since the last
+ * check.  MLA_ERR_CUDA if the synchronisation itself failed.
+ */
+mla_status mla_check_device_status(mla_stream stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* mla_last_error(void);
+
+/*
+ * Test hooks for the device-side failure paths (never needed in normal use).
+ *   MLA_DEBUG_WAIT_LIMIT_NS: limit of every pipeline wait in ns (default 2e9;
+ *                            value <= 0 restores the default).
+ *   MLA_DEBUG_STALL_STAGE:   when >= 0, the decode producer withholds the copy
+ *                            of that pipeline stage of each CTA, so the wait
+ *                            for it runs out and the kernel returns
+ *                            MLA_ERR_TIMEOUT through the device status
+ *                            (default -1 = off).
+ * Returns MLA_OK or MLA_ERR_INVALID_ARG for an unknown knob.
+ */
+enum { MLA_DEBUG_WAIT_LIMIT_NS = 1, MLA_DEBUG_STALL_STAGE = 2 };
+mla_status mla_debug_set(int knob, long long value);
+
+/*
+ * Kernel timing (instrumentation for roofline figures).  While enabled, every
+ * call records a CUDA event pair on its stream around its dominant kernel
+ * (decode: the split-KV partial kernel; sparse decode: the same kernel in
+ * gather mode; index_topk: the scoring kernel; prefill: the attention
+ * kernel).  mla_timing_read synchronises those events, returns the summed
+ * kernel time in milliseconds and the number of launches of operation `op`
+ * (MLA_OP_*) since the last read, and resets the count.  Events are created
+ * on first use and reused; no device memory is allocated.
+ */
+mla_status mla_timing_enable(int on);
+mla_status mla_timing_read(int op, double* total_ms, long long* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -1,0 +1,219 @@
+"""GB300 (sm_103a) Gated MLA / Gated DSA attention.
+
+Thin PyTorch-facing binding of the C ABI in ``include/mla.h``: the functions
+below check shapes, dtypes, devices and contiguity (raising ``ValueError``
+on a mismatch, as the Kimi K2 modeling code does for a wrong attention-weight
+shape), allocate outputs and workspace with torch when the caller does not
+pass them, and call the library on the current CUDA stream. Every step of the
+computation runs in the library's CUDA kernels; nothing here computes.
+
+Entry points (names as in the C ABI):
+
+* ``mla_prefill(q, k, v, gate)``            causal gated MLA prefill
+* ``mla_decode(q, k, v, cu_seqlens, ...)``  split-KV gated MLA decode
+* ``dsa_index_topk(index_q, index_k, w, cu_seqlens, ...)``  DSA indexer + top-k
+* ``dsa_sparse_decode(q, k, v, cu_seqlens, topk_idx, ...)`` gated MLA over a selection
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import MlaError  # noqa: F401
+
+DQK, DV, INDEX_HEADS, INDEX_DIM, MAX_TOPK = 192, 128, 32, 128, 2048
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _need(t, name, dtype, shape=None, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} should be of size {tuple(shape)}, but is {tuple(t.shape)}")
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes_ptr(s.cuda_stream)
+
+
+def ctypes_ptr(x):
+    import ctypes
+    return ctypes.c_void_p(int(x))
+
+
+def _ptr(t):
+    return None if t is None else ctypes_ptr(t.data_ptr())
+
+
+def workspace_size(op: int, B: int = 1, H: int = 1, max_seqlen: int = 1, topk: int = 1) -> int:
+    return int(_lib.load().mla_workspace_size(op, B, H, max_seqlen, topk))
+
+
+def _workspace(ws, nbytes, device):
+    torch = _torch()
+    if nbytes == 0:
+        return None, 0
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if ws.numel() * ws.element_size() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    return ws, ws.numel() * ws.element_size()
+
+
+def default_scale() -> float:
+    return DQK ** -0.5
+
+
+def mla_prefill(q, k, v, gate=None, out=None, scale=None, ws=None, stream=None):
+    """Causal gated MLA prefill.  q [B,H,Tq,192], k [B,H,Tk,192], v [B,H,Tk,128],
+    gate [B,Tq,H*128] or None -> out [B,Tq,H*128] (bf16)."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4 or q.shape[3] != DQK:
+        raise ValueError("q must be [B,H,Tq,192]")
+    B, H, Tq, _ = q.shape
+    Tk = k.shape[2] if k.dim() == 4 else -1
+    _need(k, "k", torch.bfloat16, (B, H, Tk, DQK), q.device)
+    _need(v, "v", torch.bfloat16, (B, H, Tk, DV), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, Tq, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, Tq, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, Tq, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_PREFILL, B, H, Tk, 0)
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), B, H, Tq, Tk,
+                               float(default_scale() if scale is None else scale), _ptr(ws), wsb,
+                               _stream(stream)), lib)
+    return out
+
+
+def _check_cache(q, k, v, cu_seqlens, H, total):
+    torch = _torch()
+    _need(k, "k", torch.bfloat16, None, q.device)
+    _need(v, "v", torch.bfloat16, None, q.device)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, (q.shape[0] + 1,), q.device)
+    if total is not None:
+        if k.numel() != total * H * DQK or v.numel() != total * H * DV:
+            raise ValueError("packed cache size does not match cu_seqlens[-1]")
+
+
+def mla_decode(q, k, v, cu_seqlens, max_seqlen: int, gate=None, out=None, scale=None,
+               ws=None, stream=None, total_positions: int | None = None):
+    """Split-KV gated MLA decode over a packed cache.  q [B,H,192]; k/v packed with
+    sequence b = [H,T_b,D] from element cu[b]*H*D; gate [B,H*128] or None."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [B,H,192]")
+    B, H, _ = q.shape
+    _check_cache(q, k, v, cu_seqlens, H, total_positions)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_DECODE, B, H, int(max_seqlen), 0)
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, H, int(max_seqlen),
+                              _ptr(gate), _ptr(out),
+                              float(default_scale() if scale is None else scale), _ptr(ws), wsb,
+                              _stream(stream)), lib)
+    return out
+
+
+def dsa_index_topk(index_q, index_k, w, cu_seqlens, max_seqlen: int, topk: int = MAX_TOPK,
+                   topk_idx=None, topk_scores=None, ws=None, stream=None):
+    """DSA indexer score + top-k.  index_q [B,32,128] bf16, index_k [cu[B],128] bf16,
+    w [B,32] fp32 -> topk_idx [B,topk] int32 (ascending, -1 padded)."""
+    torch = _torch()
+    _need(index_q, "index_q", torch.bfloat16)
+    if index_q.dim() != 3 or index_q.shape[2] != INDEX_DIM:
+        raise ValueError("index_q must be [B,NH,128]")
+    B, NH, _ = index_q.shape
+    _need(index_k, "index_k", torch.bfloat16, None, index_q.device)
+    if index_k.dim() != 2 or index_k.shape[1] != INDEX_DIM:
+        raise ValueError("index_k must be [total,128]")
+    _need(w, "w", torch.float32, (B, NH), index_q.device)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,), index_q.device)
+    if topk_idx is None:
+        topk_idx = torch.empty((B, topk), dtype=torch.int32, device=index_q.device)
+    _need(topk_idx, "topk_idx", torch.int32, (B, topk), index_q.device)
+    if topk_scores is not None:
+        _need(topk_scores, "topk_scores", torch.float32, (B, topk), index_q.device)
+    nbytes = workspace_size(_lib.OP_INDEX_TOPK, B, NH, int(max_seqlen), topk)
+    ws, wsb = _workspace(ws, nbytes, index_q.device)
+    lib = _lib.load()
+    _lib.check(lib.dsa_index_topk(_ptr(index_q), _ptr(index_k), _ptr(w), _ptr(cu_seqlens), B, NH,
+                                  int(max_seqlen), int(topk), _ptr(topk_idx), _ptr(topk_scores),
+                                  _ptr(ws), wsb, _stream(stream)), lib)
+    return topk_idx
+
+
+def dsa_sparse_decode(q, k, v, cu_seqlens, topk_idx, gate=None, out=None, scale=None,
+                      ws=None, stream=None):
+    """Gated MLA over the selected positions only (all heads share a selection)."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [B,H,192]")
+    B, H, _ = q.shape
+    _check_cache(q, k, v, cu_seqlens, H, None)
+    _need(topk_idx, "topk_idx", torch.int32, None, q.device)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != B:
+        raise ValueError("topk_idx must be [B,topk]")
+    topk = topk_idx.shape[1]
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_SPARSE_DECODE, B, H, 0, topk)
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.dsa_sparse_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(topk_idx),
+                                     topk, B, H, _ptr(gate), _ptr(out),
+                                     float(default_scale() if scale is None else scale),
+                                     _ptr(ws), wsb, _stream(stream)), lib)
+    return out
+
+
+def check_device_status(stream=None) -> None:
+    """Synchronise and raise MlaError if a kernel recorded a device-side fault."""
+    lib = _lib.load()
+    _lib.check(lib.mla_check_device_status(_stream(stream)), lib)
+
+
+def debug_set(knob: int, value: int) -> None:
+    lib = _lib.load()
+    _lib.check(lib.mla_debug_set(int(knob), int(value)), lib)
+
+
+def timing_enable(on: bool = True) -> None:
+    """Record CUDA events around each call's dominant kernel (instrumentation)."""
+    lib = _lib.load()
+    _lib.check(lib.mla_timing_enable(1 if on else 0), lib)
+
+
+def timing_read(op: int):
+    """(total kernel ms, launches) of operation `op` since the last read."""
+    import ctypes
+    lib = _lib.load()
+    ms, n = ctypes.c_double(0), ctypes.c_longlong(0)
+    _lib.check(lib.mla_timing_read(int(op), ctypes.byref(ms), ctypes.byref(n)), lib)
+    return ms.value, n.value

@@ -1,0 +1,268 @@
+// C ABI of the library (declared in include/mla.h): host-side argument
+// validation, workspace sizing, the per-device status word, and dispatch to
+// the kernel launchers.  Nothing here allocates device memory.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/mla.h"
+#include "kernels.h"
+
+namespace {
+
+__device__ int g_status;   // device status word (one per device context)
+
+thread_local std::string t_err;
+std::atomic<long long> g_wait_limit_ns{2000000000LL};
+std::atomic<int> g_stall_stage{-1};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+mla::DeviceInfo g_dev[kMaxDevices];
+
+mla_status fail(mla_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+mla_status fail(mla_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return s;
+}
+
+mla_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device facts and the status word address for the current device; set up
+// once per device on first use.
+mla_status device_info(mla::DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device %d", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    mla::DeviceInfo& d = g_dev[dev];
+    if (d.status == nullptr) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(MLA_ERR_UNSUPPORTED,
+                        "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                        major, minor);
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        d.status = static_cast<int*>(p);
+    }
+    *out = d;
+    return MLA_OK;
+}
+
+mla::Knobs knobs() { return mla::Knobs{g_wait_limit_ns.load(), g_stall_stage.load()}; }
+
+// ----- kernel timing (instrumentation) -----
+std::atomic<bool> g_timing{false};
+std::mutex g_tm_mu;
+struct TimerPool {
+    std::vector<mla::KernelTimer> ev;
+    size_t used = 0;
+};
+TimerPool g_pool[4];
+
+// Next event pair for `op` when timing is on, else an empty timer.
+mla::KernelTimer take_timer(int op) {
+    mla::KernelTimer t;
+    if (!g_timing.load() || op < 0 || op > 3) return t;
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    TimerPool& p = g_pool[op];
+    if (p.used == p.ev.size()) {
+        mla::KernelTimer n;
+        if (cudaEventCreate(&n.begin) != cudaSuccess) return t;
+        if (cudaEventCreate(&n.end) != cudaSuccess) {
+            cudaEventDestroy(n.begin);
+            return t;
+        }
+        p.ev.push_back(n);
+    }
+    return p.ev[p.used++];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, code, ...) \
+    do {                         \
+        if (!(cond)) return fail(code, __VA_ARGS__); \
+    } while (0)
+
+mla_status check_ws(void* ws, size_t have, size_t need) {
+    if (need == 0) return MLA_OK;
+    REQUIRE(ws != nullptr, MLA_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL", need);
+    REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, MLA_ERR_WORKSPACE,
+            "workspace must be 256-byte aligned");
+    REQUIRE(have >= need, MLA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", have, need);
+    return MLA_OK;
+}
+
+mla_status check_decode_common(const void* q, const void* k, const void* v, const void* cu,
+                               const void* gate, const void* out, int B, int H, int max_len) {
+    REQUIRE(q && k && v && cu && out, MLA_ERR_INVALID_ARG, "null tensor pointer");
+    REQUIRE(B >= 1 && H >= 1 && max_len >= 1, MLA_ERR_INVALID_ARG,
+            "need B >= 1, H >= 1, max length >= 1 (got %d, %d, %d)", B, H, max_len);
+    REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) &&
+                (gate == nullptr || aligned16(gate)) && (reinterpret_cast<uintptr_t>(cu) & 7u) == 0,
+            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    REQUIRE(int64_t(B) * H * ((int64_t(max_len) + 63) / 64) < (int64_t(1) << 31),
+            MLA_ERR_UNSUPPORTED, "B*H*max_len too large for one call");
+    return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_last_error(void) { return t_err.c_str(); }
+
+mla_status mla_debug_set(int knob, long long value) {
+    switch (knob) {
+        case MLA_DEBUG_WAIT_LIMIT_NS:
+            g_wait_limit_ns.store(value > 0 ? value : 2000000000LL);
+            return MLA_OK;
+        case MLA_DEBUG_STALL_STAGE:
+            g_stall_stage.store(value >= 0 && value < (1LL << 30) ? int(value) : -1);
+            return MLA_OK;
+        default:
+            return fail(MLA_ERR_INVALID_ARG, "unknown debug knob %d", knob);
+    }
+}
+
+size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
+    switch (op) {
+        case MLA_OP_PREFILL:
+            return 0;
+        case MLA_OP_DECODE:
+            if (B < 1 || H < 1 || max_seqlen < 1) return 0;
+            return mla::plan_decode(B, H, max_seqlen, false).total;
+        case MLA_OP_SPARSE_DECODE:
+            if (B < 1 || H < 1 || topk < 1 || topk > mla::kMaxTopk) return 0;
+            return mla::plan_decode(B, H, topk, true).total;
+        default:
+            return 0;
+    }
+}
+
+mla_status mla_timing_enable(int on) {
+    g_timing.store(on != 0);
+    return MLA_OK;
+}
+
+mla_status mla_timing_read(int op, double* total_ms, long long* launches) {
+    REQUIRE(op >= 0 && op <= 3 && total_ms && launches, MLA_ERR_INVALID_ARG,
+            "mla_timing_read: bad op or null output");
+    std::lock_guard<std::mutex> lk(g_tm_mu);
+    TimerPool& p = g_pool[op];
+    double sum = 0.0;
+    for (size_t i = 0; i < p.used; ++i) {
+        cudaError_t e = cudaEventSynchronize(p.ev[i].end);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, p.ev[i].begin, p.ev[i].end);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        sum += ms;
+    }
+    *total_ms = sum;
+    *launches = static_cast<long long>(p.used);
+    p.used = 0;
+    return MLA_OK;
+}
+
+mla_status mla_check_device_status(mla_stream stream) {
+    mla::DeviceInfo d;
+    mla_status s = device_info(&d);
+    if (s != MLA_OK) return s;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "read status");
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    switch (v) {
+        case 0: return MLA_OK;
+        case MLA_ERR_TIMEOUT: return fail(MLA_ERR_TIMEOUT, "a device pipeline wait ran out");
+        case MLA_ERR_BAD_INDEX:
+            return fail(MLA_ERR_BAD_INDEX, "a selected position lies outside its sequence");
+        case MLA_ERR_INVALID_ARG:
+            return fail(MLA_ERR_INVALID_ARG, "a sequence length is outside [1, max_seqlen]");
+        default: return fail(static_cast<mla_status>(v), "device status %d", v);
+    }
+}
+
+mla_status mla_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                      const int64_t* cu_seqlens, int B, int H, int max_seqlen,
+                      const mla_bf16* gate, mla_bf16* out, float scale, void* ws,
+                      size_t ws_bytes, mla_stream stream) {
+    mla_status s = check_decode_common(q, k, v, cu_seqlens, gate, out, B, H, max_seqlen);
+    if (s != MLA_OK) return s;
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    const mla::DecodePlan pl = mla::plan_decode(B, H, max_seqlen, false);
+    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    mla::DecodeArgs a{q, k, v, cu_seqlens, nullptr, gate, out, B, H, max_seqlen, 0, scale,
+                      ws, ws_bytes};
+    cudaError_t e = mla::launch_decode(a, pl, false, d, knobs(), take_timer(MLA_OP_DECODE),
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode launch");
+}
+
+mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                             const int64_t* cu_seqlens, const int32_t* topk_idx, int topk,
+                             int B, int H, const mla_bf16* gate, mla_bf16* out, float scale,
+                             void* ws, size_t ws_bytes, mla_stream stream) {
+    mla_status s = check_decode_common(q, k, v, cu_seqlens, gate, out, B, H, topk > 0 ? topk : 1);
+    if (s != MLA_OK) return s;
+    REQUIRE(topk_idx != nullptr && (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0,
+            MLA_ERR_INVALID_ARG, "topk_idx must be a 4-byte aligned device pointer");
+    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
+            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    const mla::DecodePlan pl = mla::plan_decode(B, H, topk, true);
+    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    mla::DecodeArgs a{q, k, v, cu_seqlens, topk_idx, gate, out, B, H, 1 << 30, topk, scale,
+                      ws, ws_bytes};
+    cudaError_t e = mla::launch_decode(a, pl, true, d, knobs(), take_timer(MLA_OP_SPARSE_DECODE),
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_sparse_decode launch");
+}
+
+mla_status mla_prefill(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                       const mla_bf16* gate, mla_bf16* out, int B, int H, int Tq, int Tk,
+                       float scale, void* ws, size_t ws_bytes, mla_stream stream) {
+    (void)q; (void)k; (void)v; (void)gate; (void)out; (void)B; (void)H; (void)Tq; (void)Tk;
+    (void)scale; (void)ws; (void)ws_bytes; (void)stream;
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill is not built yet");
+}
+
+mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,
+                          const int64_t* cu_seqlens, int B, int NH, int max_seqlen, int topk,
+                          int32_t* topk_idx, float* topk_scores, void* ws, size_t ws_bytes,
+                          mla_stream stream) {
+    (void)index_q; (void)index_k; (void)w; (void)cu_seqlens; (void)B; (void)NH;
+    (void)max_seqlen; (void)topk; (void)topk_idx; (void)topk_scores; (void)ws; (void)ws_bytes;
+    (void)stream;
+    return fail(MLA_ERR_UNSUPPORTED, "dsa_index_topk is not built yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,538 @@
+// Split-KV gated MLA decode and DSA sparse decode for sm_103a.
+//
+// What it computes (Kimi K3 MLA forward in decode mode; K3.1 Gated DSA post,
+// eqs. (9) and (10)): for every sequence b and head h,
+//   z = sum_s softmax_s(scale * q.k_s) v_s over the visible positions s
+//   out[b, h*128+d] = z_d * sigmoid(gate[b, h*128+d])
+// where the visible positions are all T_b cached positions (decode) or the
+// selected ones (sparse decode).
+//
+// Design.  Decode reads 640 bytes (a 384-byte key row and a 256-byte value
+// row) per position and head and does 320 multiply-adds on them: about one
+// flop per byte, so the kernel is bound by HBM bandwidth and the work is done
+// on the CUDA cores.  A persistent grid of one CTA per SM walks a list of work
+// items, each a chunk of up to `chunk` positions of one (sequence, head):
+//   - warp 0 is the producer: one elected lane issues bulk (TMA) copies of
+//     64 contiguous key rows and value rows per pipeline stage into shared
+//     memory (four stages), completing on an mbarrier; for sparse decode all
+//     32 lanes issue one row copy each per selected position;
+//   - eight consumer warps split each stage into 8-lane groups, one position
+//     per group at a time: every lane dots 24 query features with its three
+//     16-byte slices of the key row, three xor-shuffles finish the score,
+//     and an online softmax (running max and sum in the log2 domain) folds
+//     the position's value slice into 16 accumulators per lane;
+//   - at the end of an item the 32 group states are merged (shuffles, then
+//     shared memory) into one unnormalised partial (acc[128], max, sum)
+//     written to the workspace.
+// A second kernel merges the partials of each (b,h) by log-sum-exp in a fixed
+// order and applies the sigmoid gate, so results do not depend on timing.
+//
+// Every wait on an mbarrier is bounded; when one runs out the kernel records
+// MLA_ERR_TIMEOUT in the status word, skips the rest of its work, waits (again
+// bounded) for the copies it has in flight and returns.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mla {
+namespace {
+
+constexpr int kKRow = kDqk * 2;                 // 384 bytes
+constexpr int kVRow = kDv * 2;                  // 256 bytes
+constexpr int kSP = 64;                         // positions per pipeline stage
+constexpr int kStages = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kGroups = kConsumerWarps * 4;     // 8-lane groups
+constexpr int kPPG = kSP / kGroups;             // positions per group per stage
+constexpr int kKStage = kSP * kKRow;            // 24 KB
+constexpr int kVStage = kSP * kVRow;            // 16 KB
+constexpr int kMergeFloats = kConsumerWarps * (kDv + 2);
+constexpr size_t kSmemBytes =
+    size_t(kStages) * (kKStage + kVStage) + kMergeFloats * 4 + 2 * kStages * 8 + 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+static_assert(kPPG * kGroups == kSP, "stage must split evenly over groups");
+
+struct Params {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    const int64_t* cu;
+    const int32_t* idx;      // sparse: [B,topk]
+    int B, H, chunk, max_chunks, topk, max_seqlen;
+    const int* item_start;   // dense: [B+1]
+    float* part_acc;         // [slots][128]
+    float* part_ml;          // [slots][2]
+    float scale_log2;
+    long long wait_ns;
+    int stall_stage;
+    int* status;
+};
+
+struct Item {
+    int b, h, c;
+    int64_t base;   // first cached position of sequence b (cu[b])
+    int T;          // T_b
+    int e0, e1;     // range of positions (dense) or index entries (sparse)
+};
+
+// Work item `it` -> (b, h, chunk).  Dense items come from the prefix table
+// item_start; sparse items are a plain (b, chunk, h) grid.
+template <bool kSparse>
+__device__ __forceinline__ Item item_of(const Params& p, int it) {
+    Item r;
+    if (kSparse) {
+        const int nch = (p.topk + p.chunk - 1) / p.chunk;
+        r.b = it / (p.H * nch);
+        const int rem = it - r.b * p.H * nch;
+        r.c = rem / p.H;
+        r.h = rem - r.c * p.H;
+        r.base = p.cu[r.b];
+        r.T = static_cast<int>(p.cu[r.b + 1] - r.base);
+        r.e0 = r.c * p.chunk;
+        r.e1 = min(p.topk, r.e0 + p.chunk);
+    } else {
+        int lo = 0, hi = p.B;   // largest b with item_start[b] <= it
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.item_start[mid] <= it) lo = mid; else hi = mid;
+        }
+        r.b = lo;
+        r.base = p.cu[r.b];
+        r.T = static_cast<int>(p.cu[r.b + 1] - r.base);
+        const int rem = it - p.item_start[r.b];
+        r.c = rem / p.H;
+        r.h = rem - r.c * p.H;
+        r.e0 = r.c * p.chunk;
+        r.e1 = min(r.T, r.e0 + p.chunk);
+    }
+    return r;
+}
+
+template <bool kSparse>
+__device__ __forceinline__ int total_items(const Params& p) {
+    if (kSparse) return p.B * p.H * ((p.topk + p.chunk - 1) / p.chunk);
+    return p.item_start[p.B];
+}
+
+__device__ __forceinline__ bool valid_pos(int s, int T) { return s >= 0 && s < T; }
+
+template <bool kSparse>
+__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* ks = smem;                                        // [stages][64][384]
+    uint8_t* vs = smem + kStages * kKStage;                    // [stages][64][256]
+    float* red = reinterpret_cast<float*>(vs + kStages * kVStage);   // [8][130]
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + kMergeFloats);
+    uint64_t* empty = full + kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int n_items = total_items<kSparse>(p);
+
+    if (warp == 0) {
+        // ---------------------------- producer ----------------------------
+        const uint64_t policy = l2_evict_first_policy();
+        int it = 0;                    // pipeline stages issued (or skipped) so far
+        int filled[kStages];           // stage count of the last real fill per slot (+1)
+        for (int s = 0; s < kStages; ++s) filled[s] = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item w = item_of<kSparse>(p, item);
+            for (int e = w.e0; e < w.e1; e += kSP, ++it) {
+                const int slot = it % kStages;
+                const int round = it / kStages;
+                if (*abort_flag) { ok = false; break; }
+                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                    if (lane == 0) report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                if (it == p.stall_stage) continue;   // test hook: withhold this stage
+                const int n = min(kSP, w.e1 - e);
+                if (!kSparse) {
+                    if (lane == 0) {
+                        const int64_t row = w.base * p.H + int64_t(w.h) * w.T + e;
+                        mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow));
+                        bulk_load(ks + slot * kKStage, p.k + row * kDqk, n * kKRow, &full[slot],
+                                  policy);
+                        bulk_load(vs + slot * kVStage, p.v + row * kDv, n * kVRow, &full[slot],
+                                  policy);
+                    }
+                } else {
+                    int sel[kSP / 32];
+                    unsigned cnt = 0;
+#pragma unroll
+                    for (int r = 0; r < kSP / 32; ++r) {
+                        const int j = r * 32 + lane;
+                        sel[r] = j < n ? p.idx[int64_t(w.b) * p.topk + e + j] : -1;
+                        if (sel[r] < -1 || sel[r] >= w.T) {
+                            report(p.status, kStBadIndex);
+                            sel[r] = -1;
+                        }
+                        cnt += __popc(__ballot_sync(0xffffffffu, valid_pos(sel[r], w.T)));
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&full[slot], cnt * (kKRow + kVRow));
+                    __syncwarp();
+#pragma unroll
+                    for (int r = 0; r < kSP / 32; ++r) {
+                        if (valid_pos(sel[r], w.T)) {
+                            const int j = r * 32 + lane;
+                            const int64_t row = w.base * p.H + int64_t(w.h) * w.T + sel[r];
+                            bulk_load(ks + slot * kKStage + j * kKRow, p.k + row * kDqk, kKRow,
+                                      &full[slot], policy);
+                            bulk_load(vs + slot * kVStage + j * kVRow, p.v + row * kDv, kVRow,
+                                      &full[slot], policy);
+                        }
+                    }
+                }
+                filled[slot] = round + 1;
+            }
+        }
+        // Drain: every copy this CTA issued lands before the CTA may exit.
+        for (int s = 0; s < kStages; ++s) {
+            if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns)) {
+                if (lane == 0) report(p.status, kStTimeout);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    const int cw = warp - 1;                 // consumer warp 0..7
+    const int g = cw * 4 + (lane >> 3);      // group 0..31
+    const int j = lane & 7;                  // lane within the group
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const Item w = item_of<kSparse>(p, item);
+        // query slices of this lane: features 8j.., 64+8j.., 128+8j..
+        float qf[24];
+        {
+            const uint4* qp =
+                reinterpret_cast<const uint4*>(p.q + (int64_t(w.b) * p.H + w.h) * kDqk);
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+                const uint4 u = __ldg(qp + c * 8 + j);
+                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    qf[c * 8 + 2 * t] = bf_lo(wd[t]) * p.scale_log2;
+                    qf[c * 8 + 2 * t + 1] = bf_hi(wd[t]) * p.scale_log2;
+                }
+            }
+        }
+        float m = -INFINITY, l = 0.f, acc[16];
+#pragma unroll
+        for (int d = 0; d < 16; ++d) acc[d] = 0.f;
+
+        for (int e = w.e0; e < w.e1; e += kSP, ++it) {
+            const int slot = it % kStages;
+            const int round = it / kStages;
+            bool have = !*abort_flag;
+            if (have && !mbar_wait(&full[slot], round & 1, p.wait_ns)) {
+                if (lane == 0) report(p.status, kStTimeout);
+                *abort_flag = 1;
+                have = false;
+            }
+            have = __all_sync(0xffffffffu, have);
+            if (have) {
+                const int n = min(kSP, w.e1 - e);
+                const uint8_t* kst = ks + slot * kKStage;
+                const uint8_t* vst = vs + slot * kVStage;
+                float s[kPPG];
+                bool ok[kPPG];
+#pragma unroll
+                for (int r = 0; r < kPPG; ++r) {
+                    const int pos = g + kGroups * r;
+                    ok[r] = pos < n;
+                    if (kSparse && ok[r]) ok[r] = valid_pos(p.idx[int64_t(w.b) * p.topk + e + pos], w.T);
+                    float dot = 0.f;
+                    if (ok[r]) {
+                        const uint8_t* kr = kst + pos * kKRow;
+#pragma unroll
+                        for (int c = 0; c < 3; ++c) {
+                            const uint4 u =
+                                *reinterpret_cast<const uint4*>(kr + (c * 8 + j) * 16);
+                            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                dot = fmaf(qf[c * 8 + 2 * t], bf_lo(wd[t]), dot);
+                                dot = fmaf(qf[c * 8 + 2 * t + 1], bf_hi(wd[t]), dot);
+                            }
+                        }
+                    }
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                    s[r] = ok[r] ? dot : -INFINITY;
+                }
+                float mn = m;
+#pragma unroll
+                for (int r = 0; r < kPPG; ++r) mn = fmaxf(mn, s[r]);
+                if (mn != -INFINITY) {
+                    const float alpha = ex2(m - mn);    // m = -inf -> 0
+                    l *= alpha;
+#pragma unroll
+                    for (int d = 0; d < 16; ++d) acc[d] *= alpha;
+#pragma unroll
+                    for (int r = 0; r < kPPG; ++r) {
+                        if (ok[r]) {
+                            const float pr = ex2(s[r] - mn);
+                            l += pr;
+                            const uint8_t* vr = vst + (g + kGroups * r) * kVRow;
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                const uint4 u =
+                                    *reinterpret_cast<const uint4*>(vr + (c * 8 + j) * 16);
+                                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    acc[c * 8 + 2 * t] = fmaf(pr, bf_lo(wd[t]), acc[c * 8 + 2 * t]);
+                                    acc[c * 8 + 2 * t + 1] =
+                                        fmaf(pr, bf_hi(wd[t]), acc[c * 8 + 2 * t + 1]);
+                                }
+                            }
+                        }
+                    }
+                    m = mn;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        // ---- merge the 4 groups of this warp (butterfly over lanes 8, 16) ----
+#pragma unroll
+        for (int off = 8; off <= 16; off <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+            const float mn = fmaxf(m, m2);
+            const float a1 = mn == -INFINITY ? 0.f : ex2(m - mn);
+            const float a2 = mn == -INFINITY ? 0.f : ex2(m2 - mn);
+            l = l * a1 + l2 * a2;
+#pragma unroll
+            for (int d = 0; d < 16; ++d) {
+                const float o = __shfl_xor_sync(0xffffffffu, acc[d], off);
+                acc[d] = acc[d] * a1 + o * a2;
+            }
+            m = mn;
+        }
+        // lanes 0..7 hold the warp's state: features 8j..8j+7 and 64+8j..64+8j+7
+        float* rw = red + cw * (kDv + 2);
+        if (lane < 8) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                rw[8 * j + t] = acc[t];
+                rw[64 + 8 * j + t] = acc[8 + t];
+            }
+        }
+        if (lane == 0) {
+            rw[kDv] = m;
+            rw[kDv + 1] = l;
+        }
+        named_bar_sync(1, 32 * kConsumerWarps);
+        const bool aborted = *abort_flag != 0;
+        if (cw < 4 && !aborted) {
+            const int d = cw * 32 + lane;     // one feature per thread
+            float mx = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kConsumerWarps; ++u) mx = fmaxf(mx, red[u * (kDv + 2) + kDv]);
+            float a = 0.f, ls = 0.f;
+            if (mx != -INFINITY) {
+#pragma unroll
+                for (int u = 0; u < kConsumerWarps; ++u) {
+                    const float wgt = ex2(red[u * (kDv + 2) + kDv] - mx);
+                    a += wgt * red[u * (kDv + 2) + d];
+                    ls += wgt * red[u * (kDv + 2) + kDv + 1];
+                }
+            }
+            const int64_t slotid = (int64_t(w.b) * p.H + w.h) * p.max_chunks + w.c;
+            p.part_acc[slotid * kDv + d] = a;
+            if (d == 0) {
+                p.part_ml[slotid * 2] = mx;
+                p.part_ml[slotid * 2 + 1] = ls;
+            }
+        }
+        named_bar_sync(1, 32 * kConsumerWarps);
+    }
+}
+
+// Per-sequence work-item prefix: item_start[b] = sum_{b'<b} H*ceil(T_b'/chunk).
+// A sequence with T_b outside [1, max_seqlen] gets no items and is reported.
+__global__ void __launch_bounds__(1024) decode_items_kernel(const int64_t* cu, int B, int H,
+                                                            int chunk, int max_seqlen,
+                                                            int* item_start, int* status) {
+    __shared__ int warp_sums[32];
+    const int per = (B + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(B, int(threadIdx.x) * per), b1 = min(B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int64_t T = cu[b + 1] - cu[b];
+        if (T < 1 || T > max_seqlen) { report(status, kStInvalid); continue; }
+        local += H * int((T + chunk - 1) / chunk);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < int(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        warp_sums[lane] = v;   // inclusive over warps
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        item_start[b] = run;
+        const int64_t T = cu[b + 1] - cu[b];
+        if (T >= 1 && T <= max_seqlen) run += H * int((T + chunk - 1) / chunk);
+    }
+    if (threadIdx.x == blockDim.x - 1) item_start[B] = run;
+}
+
+// One warp per (b,h): log-sum-exp merge of the chunk partials, then the gate.
+__global__ void __launch_bounds__(256) decode_merge_kernel(
+    const float* part_acc, const float* part_ml, const int64_t* cu, const uint16_t* gate,
+    uint16_t* out, int B, int H, int chunk, int max_chunks, int max_seqlen, int sparse_topk) {
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= B * H) return;
+    const int b = gw / H;
+    const int64_t T = cu[b + 1] - cu[b];
+    if (T < 1 || T > max_seqlen) return;        // reported by the item pass
+    const int span = sparse_topk > 0 ? sparse_topk : int(T);
+    const int nch = (span + chunk - 1) / chunk;
+    const int64_t s0 = int64_t(gw) * max_chunks;
+    float mx = -INFINITY;
+    for (int c = lane; c < nch; c += 32) mx = fmaxf(mx, part_ml[(s0 + c) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
+    if (mx != -INFINITY) {
+        for (int c = 0; c < nch; ++c) {
+            const float wgt = ex2(part_ml[(s0 + c) * 2] - mx);
+            L += wgt * part_ml[(s0 + c) * 2 + 1];
+            const float4 pa = *reinterpret_cast<const float4*>(part_acc + (s0 + c) * kDv + lane * 4);
+            a[0] += wgt * pa.x;
+            a[1] += wgt * pa.y;
+            a[2] += wgt * pa.z;
+            a[3] += wgt * pa.w;
+        }
+    }
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    const int64_t o = int64_t(gw) * kDv + lane * 4;
+    uint32_t packed[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        float z0 = a[2 * t] * inv, z1 = a[2 * t + 1] * inv;
+        if (gate) {
+            const uint32_t gw2 = *reinterpret_cast<const uint32_t*>(gate + o + 2 * t);
+            z0 *= sigmoidf_fast(bf_lo(gw2));
+            z1 *= sigmoidf_fast(bf_hi(gw2));
+        }
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(z0, z1);
+        packed[t] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint2*>(out + o) = make_uint2(packed[0], packed[1]);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+DecodePlan plan_decode(int B, int H, int max_len, bool sparse) {
+    // Largest chunk (<= 1024, >= one stage) that still gives >= 2432 work
+    // items (16 per SM on a 152-SM part) when every sequence is max_len long.
+    DecodePlan pl{};
+    int chunk = 1024;
+    auto items = [&](int c) { return int64_t(B) * H * ((int64_t(max_len) + c - 1) / c); };
+    while (chunk > kSP && items(chunk) < 2432) chunk >>= 1;
+    pl.chunk = chunk;
+    pl.max_chunks = int((int64_t(max_len) + chunk - 1) / chunk);
+    const size_t slots = size_t(B) * H * pl.max_chunks;
+    pl.acc_off = 0;
+    pl.ml_off = align256(slots * kDv * 4);
+    pl.items_off = pl.ml_off + align256(slots * 2 * 4);
+    pl.total = pl.items_off + (sparse ? 0 : align256(size_t(B + 1) * 4));
+    return pl;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse,
+                          const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
+                          cudaStream_t st) {
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    Params p{};
+    p.q = a.q;
+    p.k = a.k;
+    p.v = a.v;
+    p.cu = a.cu;
+    p.idx = a.idx;
+    p.B = a.B;
+    p.H = a.H;
+    p.chunk = pl.chunk;
+    p.max_chunks = pl.max_chunks;
+    p.topk = a.topk;
+    p.max_seqlen = a.max_seqlen;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    p.part_acc = reinterpret_cast<float*>(ws + pl.acc_off);
+    p.part_ml = reinterpret_cast<float*>(ws + pl.ml_off);
+    p.item_start = sparse ? nullptr : reinterpret_cast<int*>(ws + pl.items_off);
+    p.scale_log2 = a.scale * kLog2e;
+    p.wait_ns = kn.wait_limit_ns;
+    p.stall_stage = kn.stall_stage;
+    p.status = dev.status;
+
+    cudaError_t e;
+    int grid = dev.sms;
+    if (sparse) {
+        const int items = a.B * a.H * ((a.topk + pl.chunk - 1) / pl.chunk);
+        grid = items < grid ? items : grid;
+        e = cudaFuncSetAttribute(decode_partial_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        if (tm.begin) cudaEventRecord(tm.begin, st);
+        decode_partial_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+        if (tm.end) cudaEventRecord(tm.end, st);
+    } else {
+        decode_items_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.H, pl.chunk, a.max_seqlen,
+                                               const_cast<int*>(p.item_start), dev.status);
+        e = cudaFuncSetAttribute(decode_partial_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        if (tm.begin) cudaEventRecord(tm.begin, st);
+        decode_partial_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+        if (tm.end) cudaEventRecord(tm.end, st);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int warps = a.B * a.H;
+    decode_merge_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
+        p.part_acc, p.part_ml, a.cu, a.gate, a.out, a.B, a.H, pl.chunk, pl.max_chunks,
+        sparse ? (1 << 30) : a.max_seqlen, sparse ? a.topk : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

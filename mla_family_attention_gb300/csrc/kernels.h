@@ -1,0 +1,60 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host-side validation happens in api.cu; these launchers
+// only enqueue work and return the CUDA launch error.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kDqk = 192;   // 128 content + 64 shared key features
+constexpr int kDv = 128;    // value features
+constexpr int kIndexHeads = 32;
+constexpr int kIndexDim = 128;
+constexpr int kMaxTopk = 2048;
+
+struct DeviceInfo {
+    int sms = 0;
+    int* status = nullptr;  // device status word
+};
+
+struct Knobs {
+    long long wait_limit_ns;
+    int stall_stage;
+};
+
+// Optional event pair recorded around an operation's dominant kernel.
+struct KernelTimer {
+    cudaEvent_t begin = nullptr, end = nullptr;
+};
+
+// ------------------------------ decode ------------------------------------
+struct DecodeArgs {
+    const uint16_t* q;       // [B,H,192]
+    const uint16_t* k;       // packed [H,T_b,192] per sequence
+    const uint16_t* v;       // packed [H,T_b,128] per sequence
+    const int64_t* cu;       // [B+1]
+    const int32_t* idx;      // sparse only: [B,topk]
+    const uint16_t* gate;    // [B,H*128] or null
+    uint16_t* out;           // [B,H*128]
+    int B, H, max_seqlen, topk;
+    float scale;
+    void* ws;
+    size_t ws_bytes;
+};
+
+// Work decomposition shared by workspace sizing and launch.
+struct DecodePlan {
+    int chunk;           // positions (dense) or index entries (sparse) per work item
+    int max_chunks;      // work items per (b,h) at most
+    size_t acc_off, ml_off, items_off, total;  // workspace layout in bytes
+};
+
+DecodePlan plan_decode(int B, int H, int max_len, bool sparse);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, bool sparse,
+                          const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
+                          cudaStream_t st);
+
+}  // namespace mla
