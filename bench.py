@@ -213,9 +213,10 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(name):
+def workload_config(name, B=None):
     w = mi.WORKLOADS[name]
-    cfg = {"workload": name, "B": w["B"], "H": w["H"], "head_dims": "qk 192 (128+64 shared), v 128",
+    cfg = {"workload": name if B in (None, w["B"]) else f"{name} (first {B} sequences)",
+           "B": B or w["B"], "H": w["H"], "head_dims": "qk 192 (128+64 shared), v 128",
            "gate": bool(w.get("gated", True))}
     if "T" in w:
         cfg["T"] = w["T"]
@@ -239,9 +240,11 @@ def run_ours(args, world, rank, local):
     if w["kind"] != "decode":
         raise SystemExit(f"workload {name} is not a decode workload")
     lengths = mi.workload_lengths(name)
+    if args.batch:
+        lengths = lengths[:args.batch]        # smaller case of the same kernel (profiling)
     max_len = max(lengths)
     dec = mi.make_decode(lengths, w["H"], True, device=dev, config=w["config"])
-    H, B = w["H"], w["B"]
+    H, B = w["H"], len(lengths)
     nbytes = acc.decode_kv_bytes(lengths, H)
     out = torch.empty((B, H * 128), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(mla.workspace_size(_lib.OP_DECODE, B, H, max_len, 0), dtype=torch.uint8,
@@ -290,7 +293,7 @@ def run_ours(args, world, rank, local):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(name),
+            "data": "synthetic", "config": workload_config(name, B),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_kind,
@@ -355,6 +358,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first N sequences (small profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
