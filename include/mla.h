@@ -105,6 +105,33 @@ mla_status mla_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
                       void* ws, size_t ws_bytes, mla_stream stream);
 
 /*
+ * mla_decode for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point: it exists for callers with no device
+ * allocator of their own, such as a plugin inside a host runtime that owns
+ * every device allocation, or a latency-critical loop that must not call
+ * cudaMalloc (which synchronises the device).
+ *
+ * Same arguments, layouts and results as mla_decode, without ws/ws_bytes:
+ * the scratch comes from one fixed array of MLA_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits.  The call allocates and frees nothing.
+ *   - Rejects, with MLA_ERR_WORKSPACE and a message, any (B, H, max_seqlen)
+ *     whose scratch need, mla_workspace_size(MLA_OP_DECODE, ...), exceeds
+ *     the array (B=32, H=96, max_seqlen=8192 needs about 12.8 MB and fits).
+ *   - The first call on each device, with that device current, looks up the
+ *     array's device address; make that first call before any stream
+ *     capture.
+ *   - Every call shares the array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *     the GPU race on the array: order them (one stream, or events).
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (16u << 20)
+mla_status mla_decode_noalloc(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
+                              const int64_t* cu_seqlens, int B, int H, int max_seqlen,
+                              const mla_bf16* gate, mla_bf16* out, float scale,
+                              mla_stream stream);
+
+/*
  * DSA indexer score and top-k (DSA post eqs. (5) and (6)).
  *
  *   index_q     [B,NH,128]  index queries (NH must be 32)

@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 6: "MLA_ERR_BAD_INDEX"}
 OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE = range(4)
 DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE = 1, 2
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every symbol include/mla.h declares, with (restype, argtypes).
 _P = ctypes.c_void_p
@@ -28,6 +29,7 @@ _Z = ctypes.c_size_t
 SIGNATURES = {
     "mla_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "mla_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _F, _P, _Z, _P]),
+    "mla_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _F, _P]),
     "dsa_index_topk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "dsa_sparse_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _F, _P, _Z, _P]),
     "mla_workspace_size": (_Z, [_I, _I, _I, _I, _I]),

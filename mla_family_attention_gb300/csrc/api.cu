@@ -266,3 +266,25 @@ mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, cons
 }
 
 }  // extern "C"
+
+// ---- helpers shared with other entry-point files (see abi_util.h) ----
+#include "abi_util.h"
+
+namespace mla {
+
+mla_status set_error(mla_status s, const char* msg) { return fail(s, "%s", msg); }
+
+mla_status current_device(DeviceInfo* out) { return device_info(out); }
+
+Knobs current_knobs() { return knobs(); }
+
+mla_status check_decode_args(const void* q, const void* k, const void* v, const void* cu,
+                             const void* gate, const void* out, int B, int H, int max_len,
+                             float scale) {
+    mla_status s = check_decode_common(q, k, v, cu, gate, out, B, H, max_len);
+    if (s != MLA_OK) return s;
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    return MLA_OK;
+}
+
+}  // namespace mla
