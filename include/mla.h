@@ -135,22 +135,28 @@ mla_status mla_decode_noalloc(const mla_bf16* q, const mla_bf16* k, const mla_bf
  * DSA indexer score and top-k (DSA post eqs. (5) and (6)).
  *
  *   index_q     [B,NH,128]  index queries (NH must be 32)
- *   index_k     packed [cu[B],128]: sequence b's keys are rows cu[b]..cu[b+1]-1
+ *   index_k     [total_keys,128] packed index keys: sequence b's keys are rows
+ *               cu[b]..cu[b+1]-1; total_keys is the number of rows the
+ *               allocation holds (the kernels never read past it)
  *   w           [B,NH] fp32 head weights, with the eq. (5) constant
  *               1/(sqrt(32)*sqrt(128)) already folded in by the caller
  *   topk_idx    [B,topk] int32 out: the min(topk, T_b) positions of largest
  *               score_s = sum_h w_h * max(0, q_h . k_s), ranked by (score
  *               descending, position ascending), written in ascending
  *               position order and padded with -1.  When T_b <= topk every
- *               position is returned.
- *   topk_scores [B,topk] fp32 out (score of each returned position, -inf on
- *               padding) or NULL
+ *               position is returned and no score is computed.
+ *   topk_scores [B,topk] fp32 out (score of each returned position; -inf on
+ *               padding and when T_b <= topk) or NULL
  *
- * Requires 1 <= topk <= 2048 and 1 <= T_b <= max_seqlen <= 2^24.
+ * Requires 1 <= topk <= 2048, NH == 32, 1 <= max_seqlen <= 2^24 and
+ * total_keys < 2^31.  A sequence with T_b outside [0, max_seqlen] or rows
+ * past total_keys gets an all -1 output and MLA_ERR_INVALID_ARG in the
+ * device status.  Workspace: mla_workspace_size(MLA_OP_INDEX_TOPK, B, 0,
+ * max_seqlen, topk) bytes (fp32 scores, histograms, tile table).
  */
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,
-                          const int64_t* cu_seqlens, int B, int NH, int max_seqlen, int topk,
-                          int32_t* topk_idx, float* topk_scores,
+                          const int64_t* cu_seqlens, int B, int NH, int64_t total_keys,
+                          int max_seqlen, int topk, int32_t* topk_idx, float* topk_scores,
                           void* ws, size_t ws_bytes, mla_stream stream);
 
 /*

@@ -160,8 +160,9 @@ def dsa_index_topk(index_q, index_k, w, cu_seqlens, max_seqlen: int, topk: int =
     ws, wsb = _workspace(ws, nbytes, index_q.device)
     lib = _lib.load()
     _lib.check(lib.dsa_index_topk(_ptr(index_q), _ptr(index_k), _ptr(w), _ptr(cu_seqlens), B, NH,
-                                  int(max_seqlen), int(topk), _ptr(topk_idx), _ptr(topk_scores),
-                                  _ptr(ws), wsb, _stream(stream)), lib)
+                                  int(index_k.shape[0]), int(max_seqlen), int(topk),
+                                  _ptr(topk_idx), _ptr(topk_scores), _ptr(ws), wsb,
+                                  _stream(stream)), lib)
     return topk_idx
 
 

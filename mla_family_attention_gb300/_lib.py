@@ -30,7 +30,8 @@ SIGNATURES = {
     "mla_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "mla_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _F, _P, _Z, _P]),
     "mla_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _F, _P]),
-    "dsa_index_topk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    "dsa_index_topk": (_I, [_P, _P, _P, _P, _I, _I, ctypes.c_int64, _I, _I, _P, _P, _P, _Z,
+                            _P]),
     "dsa_sparse_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _F, _P, _Z, _P]),
     "mla_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "mla_check_device_status": (_I, [_P]),

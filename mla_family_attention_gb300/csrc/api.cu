@@ -154,6 +154,9 @@ size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
         case MLA_OP_SPARSE_DECODE:
             if (B < 1 || H < 1 || topk < 1 || topk > mla::kMaxTopk) return 0;
             return mla::plan_decode(B, H, topk, true).total;
+        case MLA_OP_INDEX_TOPK:
+            if (B < 1 || max_seqlen < 1 || max_seqlen > (1 << 24)) return 0;
+            return mla::plan_index(B, max_seqlen).total;
         default:
             return 0;
     }
@@ -256,13 +259,36 @@ mla_status mla_prefill(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,
-                          const int64_t* cu_seqlens, int B, int NH, int max_seqlen, int topk,
-                          int32_t* topk_idx, float* topk_scores, void* ws, size_t ws_bytes,
-                          mla_stream stream) {
-    (void)index_q; (void)index_k; (void)w; (void)cu_seqlens; (void)B; (void)NH;
-    (void)max_seqlen; (void)topk; (void)topk_idx; (void)topk_scores; (void)ws; (void)ws_bytes;
-    (void)stream;
-    return fail(MLA_ERR_UNSUPPORTED, "dsa_index_topk is not built yet");
+                          const int64_t* cu_seqlens, int B, int NH, int64_t total_keys,
+                          int max_seqlen, int topk, int32_t* topk_idx, float* topk_scores,
+                          void* ws, size_t ws_bytes, mla_stream stream) {
+    REQUIRE(index_q && index_k && w && cu_seqlens && topk_idx, MLA_ERR_INVALID_ARG,
+            "null pointer");
+    REQUIRE(aligned16(index_q) && aligned16(index_k), MLA_ERR_INVALID_ARG,
+            "index_q and index_k must be 16-byte aligned");
+    REQUIRE((reinterpret_cast<uintptr_t>(w) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(topk_scores) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u) == 0,
+            MLA_ERR_INVALID_ARG, "misaligned w, cu_seqlens or outputs");
+    REQUIRE(NH == mla::kIndexHeads, MLA_ERR_UNSUPPORTED, "NH must be 32 (got %d)", NH);
+    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
+            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
+    REQUIRE(B >= 1 && B <= 65535, MLA_ERR_INVALID_ARG, "B must be in [1, 65535]");
+    REQUIRE(max_seqlen >= 1 && max_seqlen <= (1 << 24), MLA_ERR_UNSUPPORTED,
+            "max_seqlen must be in [1, 2^24]");
+    REQUIRE(total_keys >= 0 && total_keys < (int64_t(1) << 31), MLA_ERR_UNSUPPORTED,
+            "total_keys must be in [0, 2^31)");
+    const mla::IndexPlan pl = mla::plan_index(B, max_seqlen);
+    mla_status s = check_ws(ws, ws_bytes, pl.total);
+    if (s != MLA_OK) return s;
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    mla::IndexArgs a{index_q, index_k, w, cu_seqlens, B, max_seqlen, topk, total_keys,
+                     topk_idx, topk_scores, ws};
+    cudaError_t e = mla::launch_index_topk(a, pl, d, knobs(), take_timer(MLA_OP_INDEX_TOPK),
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_index_topk launch");
 }
 
 }  // extern "C"

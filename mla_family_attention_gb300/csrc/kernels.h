@@ -3,6 +3,7 @@
 // only enqueue work and return the CUDA launch error.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -56,5 +57,31 @@ DecodePlan plan_decode(int B, int H, int max_len, bool sparse);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, bool sparse,
                           const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
                           cudaStream_t st);
+
+// --------------------------- TMA tensor maps ------------------------------
+// 2-D bf16 map over a row-major [outer][inner] array with 128-byte swizzle.
+cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---------------------------- DSA indexer --------------------------------
+struct IndexArgs {
+    const uint16_t* index_q;   // [B,32,128]
+    const uint16_t* index_k;   // packed [total_keys,128]
+    const float* w;            // [B,32]
+    const int64_t* cu;         // [B+1]
+    int B, max_seqlen, topk;
+    int64_t total_keys;
+    int32_t* topk_idx;         // [B,topk]
+    float* topk_scores;        // [B,topk] or null
+    void* ws;
+};
+
+struct IndexPlan {
+    size_t scores_off, hist_off, tiles_off, total;
+};
+
+IndexPlan plan_index(int B, int max_seqlen);
+cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& p, const DeviceInfo& dev,
+                              const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 
 }  // namespace mla

@@ -1,0 +1,184 @@
+"""GPU parity of dsa_index_topk (indexer score + top-k) and of the whole DSA
+decode path against the fp64 oracle, through the C ABI.
+
+Top-k sets are compared the way the scores allow: every position whose
+oracle score is outside the band of 1e-5 (relative) around the oracle's k-th
+score must be classified identically; inside the band the GPU may pick any
+positions, as long as it picks the right number of them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+import oracle
+import mla_family_attention_gb300 as mla
+from mla_family_attention_gb300 import _lib
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BAND = 1e-5
+
+
+def check_selection(got_idx, got_scores, scores64, lengths, topk):
+    """got_idx [B,topk] from the GPU; scores64 packed oracle scores."""
+    got_idx = got_idx.cpu().numpy()
+    off = 0
+    for b, T in enumerate(lengths):
+        row = got_idx[b]
+        K = min(T, topk)
+        sel = row[:K]
+        assert np.all(row[K:] == -1), f"b{b}: padding"
+        assert np.all(np.diff(sel) > 0), f"b{b}: not strictly ascending"
+        assert sel.min() >= 0 and sel.max() < T
+        if T <= topk:
+            assert np.array_equal(sel, np.arange(T))
+            off += T
+            continue
+        s = scores64[off:off + T]
+        order = np.lexsort((np.arange(T), -s))
+        kth = s[order[K - 1]]
+        tol = BAND * abs(kth)
+        must = set(np.nonzero(s > kth + tol)[0].tolist())
+        band = set(np.nonzero(np.abs(s - kth) <= tol)[0].tolist())
+        chosen = set(sel.tolist())
+        assert must <= chosen, f"b{b}: {len(must - chosen)} clear winners missing"
+        assert chosen <= must | band, f"b{b}: {len(chosen - must - band)} clear losers chosen"
+        if got_scores is not None:
+            gs = got_scores[b, :K].cpu().double().numpy()
+            np.testing.assert_allclose(gs, s[sel], rtol=0, atol=1e-5 * np.abs(s).max() + 1e-6)
+        off += T
+
+
+def run_index(d, lengths, topk, max_seqlen=None):
+    B = len(lengths)
+    idx = torch.empty((B, topk), dtype=torch.int32, device=DEV)
+    sc = torch.empty((B, topk), dtype=torch.float32, device=DEV)
+    mla.dsa_index_topk(d.index_q, d.index_k, d.w, mi.cu_from_lengths(lengths).to(DEV),
+                       max_seqlen or max(lengths), topk, topk_idx=idx, topk_scores=sc)
+    mla.check_device_status()
+    return idx, sc
+
+
+@pytest.mark.parametrize("lengths,topk", [
+    ([1, 100, 2048, 2049, 5000, 20000], 2048),   # short contexts, one-past, ragged tails
+    ([3000, 129, 777], 64),
+    ([400], 1),
+    ([131072], 2048),
+])
+def test_index_topk_matches_oracle(lengths, topk):
+    d = mi.make_dsa(lengths, device=DEV, config=51, with_main=False)
+    idx, sc = run_index(d, lengths, topk)
+    cu = mi.cu_from_lengths(lengths)
+    s64 = oracle.dsa_index_scores(d.index_q, d.index_k, d.w, cu)
+    check_selection(idx, sc, s64, lengths, topk)
+
+
+def test_index_topk_exact_ties_prefer_lower_positions():
+    """Keys drawn from 40 distinct rows: scores tie exactly in fp32 and fp64,
+    so the selection must equal the oracle's bit for bit."""
+    g = torch.Generator(device="cpu").manual_seed(9)
+    T, topk = 6000, 2048
+    base = torch.randn((40, 128), generator=g).to(torch.bfloat16)
+    pick = torch.randint(0, 40, (T,), generator=g)
+    ik = base[pick].contiguous()
+    iq = torch.randn((1, 32, 128), generator=g).to(torch.bfloat16)
+    w = torch.randn((1, 32), generator=g)
+    cu = torch.tensor([0, T])
+    idx = mla.dsa_index_topk(iq.to(DEV), ik.to(DEV), w.to(DEV), cu.to(DEV), T, topk)
+    mla.check_device_status()
+    ref = oracle.dsa_topk(oracle.dsa_index_scores(iq, ik, w, cu), cu, topk)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+
+
+def test_index_topk_all_equal_scores():
+    T, topk = 5000, 2048
+    ik = torch.ones((T, 128), dtype=torch.bfloat16)
+    iq = torch.ones((1, 32, 128), dtype=torch.bfloat16)
+    w = torch.ones((1, 32))
+    cu = torch.tensor([0, T])
+    idx = mla.dsa_index_topk(iq.to(DEV), ik.to(DEV), w.to(DEV), cu.to(DEV), T, topk)
+    mla.check_device_status()
+    np.testing.assert_array_equal(idx.cpu().numpy()[0], np.arange(topk))
+
+
+def test_index_topk_negative_weights_and_zero_scores():
+    """Negative head weights make scores negative; all-negative dots give 0."""
+    g = torch.Generator(device="cpu").manual_seed(10)
+    T, topk = 3000, 512
+    ik = torch.randn((T, 128), generator=g).to(torch.bfloat16)
+    iq = torch.randn((1, 32, 128), generator=g).to(torch.bfloat16)
+    w = -torch.rand((1, 32), generator=g)
+    cu = torch.tensor([0, T])
+    idx = mla.dsa_index_topk(iq.to(DEV), ik.to(DEV), w.to(DEV), cu.to(DEV), T, topk)
+    mla.check_device_status()
+    s64 = oracle.dsa_index_scores(iq, ik, w, cu)
+    check_selection(idx, None, s64, [T], topk)
+
+
+def test_index_topk_is_deterministic():
+    lengths = [70000, 9000]
+    d = mi.make_dsa(lengths, device=DEV, config=52, with_main=False)
+    a, _ = run_index(d, lengths, 2048)
+    b, _ = run_index(d, lengths, 2048)
+    assert torch.equal(a, b)
+
+
+def test_index_topk_length_outside_bound_is_reported():
+    lengths = [3000, 5000]
+    d = mi.make_dsa(lengths, device=DEV, config=53, with_main=False)
+    idx = torch.zeros((2, 256), dtype=torch.int32, device=DEV)
+    mla.dsa_index_topk(d.index_q, d.index_k, d.w, mi.cu_from_lengths(lengths).to(DEV), 4000, 256,
+                       topk_idx=idx)
+    with pytest.raises(mla.MlaError) as ei:
+        mla.check_device_status()
+    assert ei.value.status == _lib.MLA_ERR_INVALID_ARG
+    assert torch.all(idx[1] == -1)
+    s64 = oracle.dsa_index_scores(d.index_q[:1], d.index_k[:3000], d.w[:1], torch.tensor([0, 3000]))
+    check_selection(idx[:1], None, s64, [3000], 256)
+
+
+def test_dsa_decode_path_small():
+    """Indexer -> top-k -> sparse gated decode against the oracle's own selection."""
+    lengths = [9000, 2500, 700]
+    topk = 1024
+    d = mi.make_dsa(lengths, H=8, device=DEV, config=54)
+    m = d.main
+    idx, _ = run_index(d, lengths, topk)
+    out = mla.dsa_sparse_decode(m.q, m.k, m.v, m.cu_seqlens, idx, gate=m.gate, scale=m.scale)
+    mla.check_device_status()
+    cu = mi.cu_from_lengths(lengths)
+    sel = oracle.dsa_topk(oracle.dsa_index_scores(d.index_q, d.index_k, d.w, cu), cu, topk)
+    ref = oracle.dsa_sparse_decode(m.q, m.k, m.v, m.cu_seqlens, sel, m.gate, m.scale)
+    assert_close(out, ref)
+
+
+def test_dsa_decode_full_size_sampled():
+    """B=8, T=131072, 32 index heads, top-2048, 96-head gated MLA (64 GB cache),
+    in the launch configuration the benchmark times."""
+    name = "dsa_decode_b8_t131072"
+    w = mi.WORKLOADS[name]
+    lengths = mi.workload_lengths(name)
+    d = mi.make_dsa(lengths, H=w["H"], device=DEV, config=w["config"])
+    m = d.main
+    idx, sc = run_index(d, lengths, w["topk"])
+    out = mla.dsa_sparse_decode(m.q, m.k, m.v, m.cu_seqlens, idx, gate=m.gate, scale=m.scale)
+    mla.check_device_status()
+    cu = mi.cu_from_lengths(lengths)
+    s64 = oracle.dsa_index_scores(d.index_q, d.index_k, d.w, cu)
+    check_selection(idx, sc, s64, lengths, w["topk"])
+    sel = oracle.dsa_topk(s64, cu, w["topk"])
+    for b in (0, 5):
+        T = lengths[b]
+        H = w["H"]
+        for h in (0, 77):
+            o = int(cu[b]) * H + h * T
+            kb = m.k[o * 192:(o + T) * 192].view(T, 192)
+            vb = m.v[o * 128:(o + T) * 128].view(T, 128)
+            ref = oracle.dsa_sparse_decode(m.q[b:b + 1, h:h + 1], kb, vb, torch.tensor([0, T]),
+                                           sel[b:b + 1], m.gate[b:b + 1, h * 128:(h + 1) * 128],
+                                           m.scale)
+            assert_close(out[b:b + 1, h * 128:(h + 1) * 128], ref, what=f"b{b} h{h}")
+    del d, m
+    torch.cuda.empty_cache()
