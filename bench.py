@@ -229,122 +229,255 @@ def workload_config(name, B=None):
 # ------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------
-def run_ours(args, world, rank, local):
-    import mla_family_attention_gb300 as mla
-    from mla_family_attention_gb300 import _lib
+class DecodeWork:
+    """Gated MLA decode over a packed cache (rows a1-a6)."""
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    name = args.workload
-    w = mi.WORKLOADS[name]
-    if w["kind"] != "decode":
-        raise SystemExit(f"workload {name} is not a decode workload")
-    lengths = mi.workload_lengths(name)
-    if args.batch:
-        lengths = lengths[:args.batch]        # smaller case of the same kernel (profiling)
-    max_len = max(lengths)
-    dec = mi.make_decode(lengths, w["H"], True, device=dev, config=w["config"])
-    H, B = w["H"], len(lengths)
-    nbytes = acc.decode_kv_bytes(lengths, H)
-    out = torch.empty((B, H * 128), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(mla.workspace_size(_lib.OP_DECODE, B, H, max_len, 0), dtype=torch.uint8,
-                     device=dev)
-    stream = torch.cuda.current_stream(dev)
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        lengths = mi.workload_lengths(name)
+        if batch:
+            lengths = lengths[:batch]          # smaller case of the same kernel (profiling)
+        self.name, self.lengths, self.H, self.B = name, lengths, w["H"], len(lengths)
+        self.max_len = max(lengths)
+        self.dec = mi.make_decode(lengths, self.H, True, device=dev, config=w["config"])
+        self.out = torch.empty((self.B, self.H * 128), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(mla.workspace_size(_lib.OP_DECODE, self.B, self.H, self.max_len, 0),
+                              dtype=torch.uint8, device=dev)
+        self.work = acc.decode_kv_bytes(lengths, self.H)
+        self.unit, self.bound = "GB/s", "hbm"
+        self.launches_per_step = 3
+        # (timer op, kernel name, algorithmic bytes per launch)
+        self.kernels = [(_lib.OP_DECODE, "decode_partial_kernel", self.work)]
 
-    def step():
-        mla.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, max_len, gate=dec.gate, out=out,
-                       scale=dec.scale, ws=ws, stream=stream)
+    def step(self, stream):
+        d = self.dec
+        self.mla.mla_decode(d.q, d.k, d.v, d.cu_seqlens, self.max_len, gate=d.gate, out=self.out,
+                            scale=d.scale, ws=self.ws, stream=stream)
 
-    sampler = ClockSampler(local)
-    for _ in range(max(args.warmup, 0)):
-        step()
-    mla.check_device_status(stream)
-    torch.cuda.synchronize(dev)
+    def cpu_sample(self, seconds):
+        gbs, el, threads, reps, n_seq = oracle_decode_sample(self.dec, 1, seconds)
+        return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                "sample": f"{n_seq} of {self.B} sequences x {self.H} heads x "
+                          f"{self.lengths[0]} positions, {reps} repeats, {el:.1f} s"}
 
-    # ---- timed region ----
-    mla.timing_enable(True)
-    mla.timing_read(_lib.OP_DECODE)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    sampler.mark_start()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    sampler.mark_end()
-    barrier(world)
-    mla.timing_enable(False)
-    ms_total = ev0.elapsed_time(ev1)
-    k_ms, k_launches = mla.timing_read(_lib.OP_DECODE)
-    mla.check_device_status(stream)
-    clocks = sampler.finish()
+    def e2e(self, dev, stream, world, steps):
+        """Same metric through the public API with pinned host buffers: every step
+        copies the inputs host->device, runs the call and reads the output back."""
+        d = self.dec
+        host = {n: getattr(d, n).to("cpu").pin_memory()
+                for n in ("q", "k", "v", "gate", "cu_seqlens")}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        out_h = torch.empty((self.B, self.H * 128), dtype=torch.bfloat16).pin_memory()
+        out_d = torch.empty_like(out_h, device=dev)
+        d2h = out_h.numel() * out_h.element_size()
 
-    ms_per_step = max_over_ranks(ms_total / args.steps, world)
-    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
-    k_avg_ms = max_over_ranks(k_ms / max(k_launches, 1), world)
+        def one():
+            for n in host:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            self.mla.mla_decode(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["cu_seqlens"],
+                                self.max_len, gate=dev_in["gate"], out=out_d, scale=d.scale,
+                                stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
 
-    # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(dec, lengths, max_len, dev, stream, world, args)
+        return _time_e2e(one, self.work, dev, world, steps, h2d, d2h)
 
-    peak, peak_kind = peaks()
-    achieved = nbytes / (k_avg_ms * 1e-3) / 1e9
-    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(name, B),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": peak_kind,
-                         "frac_of_nominal_7900": round(achieved / 7900.0, 4),
-                         "kernel": "decode_partial_kernel",
-                         "traffic": traffic_for("decode_partial_kernel"),
-                         "algorithmic_bytes_per_launch": nbytes},
-            "e2e": e2e, "gpu_launches": 3 * args.steps * world, "clocks": clocks}
-    if rank == 0 and not args.no_cpu_baseline:
-        gbs, el, threads, reps, n_seq = oracle_decode_sample(dec, 1, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"{n_seq} of {B} sequences x {H} heads x "
-                                          f"{lengths[0]} positions, {reps} repeats, {el:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    def free(self):
+        del self.dec, self.out, self.ws
 
 
-def run_e2e(dec, lengths, max_len, dev, stream, world, args):
-    """Same metric through the public API with pinned host buffers: every step
-    copies the inputs host->device, runs the call and reads the output back."""
-    import mla_family_attention_gb300 as mla
-    host = {n: getattr(dec, n).to("cpu").pin_memory() for n in ("q", "k", "v", "gate",
-                                                                 "cu_seqlens")}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    out_h = torch.empty((len(lengths), dec.H * 128), dtype=torch.bfloat16).pin_memory()
-    out_d = torch.empty_like(out_h, device=dev)
-    d2h = out_h.numel() * out_h.element_size()
-    steps = max(3, min(args.steps, args.e2e_steps))
+class DsaWork:
+    """K3.1 Gated DSA decode: indexer score + top-k, then sparse gated MLA (rows a7-a9)."""
 
-    def step():
-        for n in host:
-            dev_in[n].copy_(host[n], non_blocking=True)
-        mla.mla_decode(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["cu_seqlens"], max_len,
-                       gate=dev_in["gate"], out=out_d, scale=dec.scale, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        lengths = mi.workload_lengths(name)
+        if batch:
+            lengths = lengths[:batch]
+        self.name, self.lengths, self.H, self.B = name, lengths, w["H"], len(lengths)
+        self.topk = w["topk"]
+        self.max_len = max(lengths)
+        self.d = mi.make_dsa(lengths, H=self.H, device=dev, config=w["config"])
+        self.cu = mi.cu_from_lengths(lengths).to(dev)
+        self.idx = torch.empty((self.B, self.topk), dtype=torch.int32, device=dev)
+        self.out = torch.empty((self.B, self.H * 128), dtype=torch.bfloat16, device=dev)
+        self.ws_i = torch.empty(mla.workspace_size(_lib.OP_INDEX_TOPK, self.B, 0, self.max_len,
+                                                   self.topk), dtype=torch.uint8, device=dev)
+        self.ws_s = torch.empty(mla.workspace_size(_lib.OP_SPARSE_DECODE, self.B, self.H, 0,
+                                                   self.topk), dtype=torch.uint8, device=dev)
+        ib = acc.index_key_bytes(lengths)
+        sb = acc.sparse_kv_bytes(lengths, self.H, self.topk)
+        self.work = ib + sb
+        self.unit, self.bound = "GB/s", "hbm"
+        self.launches_per_step = 5      # tiles, score, top-k, sparse partial, merge
+        self.kernels = [(_lib.OP_INDEX_TOPK, "dsa_score_kernel", ib),
+                        (_lib.OP_SPARSE_DECODE, "decode_partial_kernel<sparse>", sb)]
 
-    step()
+    def step(self, stream):
+        d, m = self.d, self.d.main
+        self.mla.dsa_index_topk(d.index_q, d.index_k, d.w, self.cu, self.max_len, self.topk,
+                                topk_idx=self.idx, ws=self.ws_i, stream=stream)
+        self.mla.dsa_sparse_decode(m.q, m.k, m.v, m.cu_seqlens, self.idx, gate=m.gate,
+                                   out=self.out, scale=m.scale, ws=self.ws_s, stream=stream)
+
+    def free(self):
+        del self.d, self.idx, self.out, self.ws_i, self.ws_s
+
+
+class IndexWork:
+    """The DSA indexer alone: scores and top-k (rows a7-a8)."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        lengths = mi.workload_lengths(name)
+        if batch:
+            lengths = lengths[:batch]
+        self.name, self.lengths, self.H, self.B = name, lengths, w["H"], len(lengths)
+        self.topk = w["topk"]
+        self.max_len = max(lengths)
+        self.d = mi.make_dsa(lengths, H=self.H, device=dev, config=w["config"], with_main=False)
+        self.cu = mi.cu_from_lengths(lengths).to(dev)
+        self.idx = torch.empty((self.B, self.topk), dtype=torch.int32, device=dev)
+        self.ws_i = torch.empty(mla.workspace_size(_lib.OP_INDEX_TOPK, self.B, 0, self.max_len,
+                                                   self.topk), dtype=torch.uint8, device=dev)
+        self.work = acc.index_key_bytes(lengths)
+        self.unit, self.bound = "GB/s", "hbm"
+        self.launches_per_step = 3      # tiles, score, top-k
+        self.kernels = [(_lib.OP_INDEX_TOPK, "dsa_score_kernel", self.work)]
+
+    def step(self, stream):
+        d = self.d
+        self.mla.dsa_index_topk(d.index_q, d.index_k, d.w, self.cu, self.max_len, self.topk,
+                                topk_idx=self.idx, ws=self.ws_i, stream=stream)
+
+    def free(self):
+        del self.d, self.idx, self.ws_i
+
+
+WORK_KINDS = {"decode": DecodeWork, "dsa": DsaWork, "index": IndexWork}
+
+
+def _time_e2e(one, work, dev, world, steps, h2d, d2h):
+    one()
     torch.cuda.synchronize(dev)
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        one()
     torch.cuda.synchronize(dev)
     el = max_over_ranks((time.perf_counter() - t0) / steps, world)
     barrier(world)
-    nbytes = acc.decode_kv_bytes(lengths, dec.H)
-    del dev_in, host
-    return {"value": round(nbytes * world / el / 1e9, 2), "unit": "GB/s",
+    return {"value": round(work * world / el / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def time_work(work, steps, warmup, dev, stream, world, sampler=None):
+    """CUDA-event time of `steps` steps (after `warmup`), and each dominant
+    kernel's own event time over the same region."""
+    mla = work.mla
+    for _ in range(warmup):
+        work.step(stream)
+    mla.check_device_status(stream)
+    torch.cuda.synchronize(dev)
+    mla.timing_enable(True)
+    for op, _, _ in work.kernels:
+        mla.timing_read(op)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    ev0.record(stream)
+    for _ in range(steps):
+        work.step(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_end()
+    barrier(world)
+    mla.timing_enable(False)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
+    kern = []
+    for op, kname, units in work.kernels:
+        k_ms, n = mla.timing_read(op)
+        kern.append((kname, max_over_ranks(k_ms / max(n, 1), world), units))
+    mla.check_device_status(stream)
+    return ms, kern
+
+
+def roofline(work, kern):
+    """Roofline object for the dominant (longest) kernel of a step."""
+    peak, peak_kind = peaks()
+    kname, k_ms, units = max(kern, key=lambda x: x[1])
+    achieved = units / (k_ms * 1e-3) / 1e9
+    r = {"bound": work.bound, "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+         "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+         "frac_of_nominal_7900": round(achieved / 7900.0, 4), "kernel": kname,
+         "kernel_ms": round(k_ms, 4), "traffic": traffic_for(kname),
+         "algorithmic_bytes_per_launch": units}
+    others = {}
+    for kn, km, ku in kern:
+        if kn != kname:
+            a = ku / (km * 1e-3) / 1e9
+            others[kn] = {"achieved": round(a, 2), "frac": round(a / peak, 4),
+                          "kernel_ms": round(km, 4), "algorithmic_bytes_per_launch": ku}
+    if others:
+        r["other_kernels"] = others
+    return r
+
+
+def run_ours(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    name = args.workload
+    kind = mi.WORKLOADS[name]["kind"]
+    work = WORK_KINDS[kind](name, dev, args.batch)
+    sampler = ClockSampler(local)
+    ms, kern = time_work(work, args.steps, args.warmup, dev, stream, world, sampler)
+    clocks = sampler.finish()
+    value = work.work * world / (ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": round(value, 2), "unit": work.unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(name, work.B),
+            "roofline": roofline(work, kern),
+            "gpu_launches": work.launches_per_step * args.steps * world, "clocks": clocks}
+    if hasattr(work, "e2e"):
+        line["e2e"] = work.e2e(dev, stream, world, max(3, min(args.steps, args.e2e_steps)))
+    if rank == 0 and not args.no_cpu_baseline and hasattr(work, "cpu_sample"):
+        line["cpu_baseline"] = work.cpu_sample(args.cpu_seconds)
+    work.free()
+    del work
+    torch.cuda.empty_cache()
+    # the other workloads of the hot path, timed the same way (shorter)
+    if not args.only and not args.batch:
+        also = {}
+        for other, w in mi.WORKLOADS.items():
+            if other == name or w["kind"] not in WORK_KINDS:
+                continue
+            wk = WORK_KINDS[w["kind"]](other, dev)
+            k_steps = max(3, min(args.steps, 20))
+            ms_o, kern_o = time_work(wk, k_steps, 3, dev, stream, world)
+            also[other] = {"value": round(wk.work * world / (ms_o * 1e-3) / 1e9, 2),
+                           "unit": wk.unit, "ms_per_step": round(ms_o, 4), "steps": k_steps,
+                           "roofline": roofline(wk, kern_o)}
+            line["gpu_launches"] += wk.launches_per_step * (k_steps + 3) * world
+            wk.free()
+            del wk
+            torch.cuda.empty_cache()
+        line["also"] = also
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -354,7 +487,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[n for n, w in mi.WORKLOADS.items() if w["kind"] == "decode"])
+                    choices=[n for n, w in mi.WORKLOADS.items()
+                             if w["kind"] in ("decode", "dsa", "index")])
+    ap.add_argument("--only", action="store_true",
+                    help="time only --workload (skip the other workloads' short runs)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -166,6 +166,8 @@ WORKLOADS = {
     "prefill_b1_h64_t16384_nogate": dict(kind="prefill", config=3, B=1, H=64, T=16384,
                                          gated=False),
     "dsa_decode_b8_t131072": dict(kind="dsa", config=4, B=8, H=96, T=131072, topk=2048),
+    # the indexer part of the DSA workload alone (same index keys, queries, weights)
+    "dsa_index_b8_t131072": dict(kind="index", config=4, B=8, H=96, T=131072, topk=2048),
 }
 
 
