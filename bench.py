@@ -315,7 +315,7 @@ class DsaWork:
         sb = acc.sparse_kv_bytes(lengths, self.H, self.topk)
         self.work = ib + sb
         self.unit, self.bound = "GB/s", "hbm"
-        self.launches_per_step = 5      # tiles, score, top-k, sparse partial, merge
+        self.launches_per_step = 8      # tiles, score, 4 top-k passes, sparse partial, merge
         self.kernels = [(_lib.OP_INDEX_TOPK, "dsa_score_kernel", ib),
                         (_lib.OP_SPARSE_DECODE, "decode_partial_kernel<sparse>", sb)]
 
@@ -351,7 +351,7 @@ class IndexWork:
                                                    self.topk), dtype=torch.uint8, device=dev)
         self.work = acc.index_key_bytes(lengths)
         self.unit, self.bound = "GB/s", "hbm"
-        self.launches_per_step = 3      # tiles, score, top-k
+        self.launches_per_step = 6      # tiles, score, 4 top-k passes
         self.kernels = [(_lib.OP_INDEX_TOPK, "dsa_score_kernel", self.work)]
 
     def step(self, stream):

@@ -203,9 +203,13 @@ const char* mla_last_error(void);
  *                            for it runs out and the kernel returns
  *                            MLA_ERR_TIMEOUT through the device status
  *                            (default -1 = off).
- * Returns MLA_OK or MLA_ERR_INVALID_ARG for an unknown knob.
+ *   MLA_DEBUG_SPARSE_CHUNK:  index entries per sparse-decode work item (a
+ *                            power of two in [64, 2048]; 0 = default 256).
+ *                            Changes the sparse-decode workspace size, so
+ *                            query mla_workspace_size after setting it.
+ * Returns MLA_OK or MLA_ERR_INVALID_ARG for an unknown knob or bad value.
  */
-enum { MLA_DEBUG_WAIT_LIMIT_NS = 1, MLA_DEBUG_STALL_STAGE = 2 };
+enum { MLA_DEBUG_WAIT_LIMIT_NS = 1, MLA_DEBUG_STALL_STAGE = 2, MLA_DEBUG_SPARSE_CHUNK = 3 };
 mla_status mla_debug_set(int knob, long long value);
 
 /*

@@ -18,7 +18,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT",
                 6: "MLA_ERR_BAD_INDEX"}
 OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE = range(4)
-DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE = 1, 2
+DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE, DEBUG_SPARSE_CHUNK = 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every symbol include/mla.h declares, with (restype, argtypes).

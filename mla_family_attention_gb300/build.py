@@ -45,6 +45,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose else []
+    # extra nvcc flags (e.g. -D overrides of tile or stage counts for a sweep)
+    extra += os.environ.get("MLA_NVCC_FLAGS", "").split()
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")

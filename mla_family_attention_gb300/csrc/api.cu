@@ -19,6 +19,7 @@ __device__ int g_status;   // device status word (one per device context)
 thread_local std::string t_err;
 std::atomic<long long> g_wait_limit_ns{2000000000LL};
 std::atomic<int> g_stall_stage{-1};
+std::atomic<int> g_sparse_chunk{0};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -67,7 +68,9 @@ mla_status device_info(mla::DeviceInfo* out) {
     return MLA_OK;
 }
 
-mla::Knobs knobs() { return mla::Knobs{g_wait_limit_ns.load(), g_stall_stage.load()}; }
+mla::Knobs knobs() {
+    return mla::Knobs{g_wait_limit_ns.load(), g_stall_stage.load(), g_sparse_chunk.load()};
+}
 
 // ----- kernel timing (instrumentation) -----
 std::atomic<bool> g_timing{false};
@@ -139,6 +142,11 @@ mla_status mla_debug_set(int knob, long long value) {
         case MLA_DEBUG_STALL_STAGE:
             g_stall_stage.store(value >= 0 && value < (1LL << 30) ? int(value) : -1);
             return MLA_OK;
+        case MLA_DEBUG_SPARSE_CHUNK:
+            if (value != 0 && (value < 64 || value > 2048 || (value & (value - 1))))
+                return fail(MLA_ERR_INVALID_ARG, "sparse chunk must be 0 or a power of two in [64, 2048]");
+            g_sparse_chunk.store(int(value));
+            return MLA_OK;
         default:
             return fail(MLA_ERR_INVALID_ARG, "unknown debug knob %d", knob);
     }
@@ -153,7 +161,7 @@ size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
             return mla::plan_decode(B, H, max_seqlen, false).total;
         case MLA_OP_SPARSE_DECODE:
             if (B < 1 || H < 1 || topk < 1 || topk > mla::kMaxTopk) return 0;
-            return mla::plan_decode(B, H, topk, true).total;
+            return mla::plan_decode(B, H, topk, true, g_sparse_chunk.load()).total;
         case MLA_OP_INDEX_TOPK:
             if (B < 1 || max_seqlen < 1 || max_seqlen > (1 << 24)) return 0;
             return mla::plan_index(B, max_seqlen).total;
@@ -239,7 +247,7 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
     REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
             "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
     REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
-    const mla::DecodePlan pl = mla::plan_decode(B, H, topk, true);
+    const mla::DecodePlan pl = mla::plan_decode(B, H, topk, true, g_sparse_chunk.load());
     if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
     mla::DeviceInfo d;
     if ((s = device_info(&d)) != MLA_OK) return s;

@@ -14,8 +14,10 @@
 // items, each a chunk of up to `chunk` positions of one (sequence, head):
 //   - warp 0 is the producer: one elected lane issues bulk (TMA) copies of
 //     64 contiguous key rows and value rows per pipeline stage into shared
-//     memory (four stages), completing on an mbarrier; for sparse decode all
-//     32 lanes issue one row copy each per selected position;
+//     memory (four stages), completing on an mbarrier; for sparse decode four
+//     producer warps gather the selected rows with 16-byte cp.async copies
+//     (a bulk copy per 384- or 256-byte row is too small to keep HBM busy),
+//     each thread arriving on the stage's mbarrier when its copies land;
 //   - eight consumer warps split each stage into 8-lane groups, one position
 //     per group at a time: every lane dots 24 query features with its three
 //     16-byte slices of the key row, three xor-shuffles finish the score,
@@ -41,17 +43,30 @@ namespace {
 constexpr int kKRow = kDqk * 2;                 // 384 bytes
 constexpr int kVRow = kDv * 2;                  // 256 bytes
 constexpr int kSP = 64;                         // positions per pipeline stage
-constexpr int kStages = 4;
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// Dense decode: one producer warp (bulk copies).  Sparse decode: four
+// producer warps (16-byte cp.async gathers), completing on the same barrier.
+// Sparse decode keeps five stages in flight (gathered rows take longer to
+// arrive than streamed ones); dense decode four.
+template <bool kSparse>
+struct Roles {
+    static constexpr int kProducerWarps = kSparse ? 4 : 1;
+    static constexpr int kThreads = 32 * (kProducerWarps + kConsumerWarps);
+    static constexpr int kFullArrivals = kSparse ? 32 * kProducerWarps : 1;
+    static constexpr int kStages = kSparse ? 5 : 4;
+};
 constexpr int kGroups = kConsumerWarps * 4;     // 8-lane groups
 constexpr int kPPG = kSP / kGroups;             // positions per group per stage
 constexpr int kKStage = kSP * kKRow;            // 24 KB
 constexpr int kVStage = kSP * kVRow;            // 16 KB
 constexpr int kMergeFloats = kConsumerWarps * (kDv + 2);
-constexpr size_t kSmemBytes =
-    size_t(kStages) * (kKStage + kVStage) + kMergeFloats * 4 + 2 * kStages * 8 + 16;
 constexpr float kLog2e = 1.4426950408889634f;
+
+template <bool kSparse>
+constexpr size_t smem_bytes() {
+    return size_t(Roles<kSparse>::kStages) * (kKStage + kVStage) + kMergeFloats * 4 +
+           2 * Roles<kSparse>::kStages * 8 + 16;
+}
 
 static_assert(kPPG * kGroups == kSP, "stage must split evenly over groups");
 
@@ -76,10 +91,17 @@ struct Item {
     int64_t base;   // first cached position of sequence b (cu[b])
     int T;          // T_b
     int e0, e1;     // range of positions (dense) or index entries (sparse)
+    int nst;        // pipeline stages in the item
 };
 
+__device__ __forceinline__ int stage_entry(const Item& w, int k) { return w.e0 + k * kSP; }
+
 // Work item `it` -> (b, h, chunk).  Dense items come from the prefix table
-// item_start; sparse items are a plain (b, chunk, h) grid.
+// item_start, heads fastest: concurrent CTAs stream different heads'
+// contiguous chunks.  Sparse items are a (b, h, chunk) grid, chunk fastest:
+// the selected rows of one head are scattered over its whole cache region
+// (dozens of 2 MB pages), so concurrent CTAs share a few heads' pages
+// instead of each walking its own head's pages (translation-cache reach).
 template <bool kSparse>
 __device__ __forceinline__ Item item_of(const Params& p, int it) {
     Item r;
@@ -87,12 +109,13 @@ __device__ __forceinline__ Item item_of(const Params& p, int it) {
         const int nch = (p.topk + p.chunk - 1) / p.chunk;
         r.b = it / (p.H * nch);
         const int rem = it - r.b * p.H * nch;
-        r.c = rem / p.H;
-        r.h = rem - r.c * p.H;
+        r.h = rem / nch;
+        r.c = rem - r.h * nch;
         r.base = p.cu[r.b];
         r.T = static_cast<int>(p.cu[r.b + 1] - r.base);
         r.e0 = r.c * p.chunk;
         r.e1 = min(p.topk, r.e0 + p.chunk);
+        r.nst = (r.e1 - r.e0 + kSP - 1) / kSP;
     } else {
         int lo = 0, hi = p.B;   // largest b with item_start[b] <= it
         while (hi - lo > 1) {
@@ -107,6 +130,7 @@ __device__ __forceinline__ Item item_of(const Params& p, int it) {
         r.h = rem - r.c * p.H;
         r.e0 = r.c * p.chunk;
         r.e1 = min(r.T, r.e0 + p.chunk);
+        r.nst = (r.e1 - r.e0 + kSP - 1) / kSP;
     }
     return r;
 }
@@ -119,21 +143,38 @@ __device__ __forceinline__ int total_items(const Params& p) {
 
 __device__ __forceinline__ bool valid_pos(int s, int T) { return s >= 0 && s < T; }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 template <bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
+__global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
+    decode_partial_kernel(const Params p) {
+    using R = Roles<kSparse>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* ks = smem;                                        // [stages][64][384]
-    uint8_t* vs = smem + kStages * kKStage;                    // [stages][64][256]
-    float* red = reinterpret_cast<float*>(vs + kStages * kVStage);   // [8][130]
+    uint8_t* vs = smem + R::kStages * kKStage;                    // [stages][64][256]
+    float* red = reinterpret_cast<float*>(vs + R::kStages * kVStage);   // [8][130]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + kMergeFloats);
-    uint64_t* empty = full + kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    uint64_t* empty = full + R::kStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + R::kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+        for (int s = 0; s < R::kStages; ++s) {
+            mbar_init(&full[s], R::kFullArrivals);
             mbar_init(&empty[s], kConsumerWarps);
         }
         *abort_flag = 0;
@@ -143,18 +184,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
 
     const int n_items = total_items<kSparse>(p);
 
-    if (warp == 0) {
-        // ---------------------------- producer ----------------------------
+    if (!kSparse && warp == 0) {
+        // ------------------------- producer (dense) -------------------------
         const uint64_t policy = l2_evict_first_policy();
         int it = 0;                    // pipeline stages issued (or skipped) so far
-        int filled[kStages];           // stage count of the last real fill per slot (+1)
-        for (int s = 0; s < kStages; ++s) filled[s] = 0;
+        int filled[R::kStages];           // stage count of the last real fill per slot (+1)
+        for (int s = 0; s < R::kStages; ++s) filled[s] = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item w = item_of<kSparse>(p, item);
-            for (int e = w.e0; e < w.e1; e += kSP, ++it) {
-                const int slot = it % kStages;
-                const int round = it / kStages;
+            for (int st = 0; st < w.nst; ++st, ++it) {
+                const int e = stage_entry(w, st);
+                const int slot = it % R::kStages;
+                const int round = it / R::kStages;
                 if (*abort_flag) { ok = false; break; }
                 if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
                     if (lane == 0) report(p.status, kStTimeout);
@@ -164,56 +206,91 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
                 }
                 if (it == p.stall_stage) continue;   // test hook: withhold this stage
                 const int n = min(kSP, w.e1 - e);
-                if (!kSparse) {
-                    if (lane == 0) {
-                        const int64_t row = w.base * p.H + int64_t(w.h) * w.T + e;
-                        mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow));
-                        bulk_load(ks + slot * kKStage, p.k + row * kDqk, n * kKRow, &full[slot],
-                                  policy);
-                        bulk_load(vs + slot * kVStage, p.v + row * kDv, n * kVRow, &full[slot],
-                                  policy);
-                    }
-                } else {
-                    int sel[kSP / 32];
-                    unsigned cnt = 0;
-#pragma unroll
-                    for (int r = 0; r < kSP / 32; ++r) {
-                        const int j = r * 32 + lane;
-                        sel[r] = j < n ? p.idx[int64_t(w.b) * p.topk + e + j] : -1;
-                        if (sel[r] < -1 || sel[r] >= w.T) {
-                            report(p.status, kStBadIndex);
-                            sel[r] = -1;
-                        }
-                        cnt += __popc(__ballot_sync(0xffffffffu, valid_pos(sel[r], w.T)));
-                    }
-                    if (lane == 0) mbar_arrive_expect_tx(&full[slot], cnt * (kKRow + kVRow));
-                    __syncwarp();
-#pragma unroll
-                    for (int r = 0; r < kSP / 32; ++r) {
-                        if (valid_pos(sel[r], w.T)) {
-                            const int j = r * 32 + lane;
-                            const int64_t row = w.base * p.H + int64_t(w.h) * w.T + sel[r];
-                            bulk_load(ks + slot * kKStage + j * kKRow, p.k + row * kDqk, kKRow,
-                                      &full[slot], policy);
-                            bulk_load(vs + slot * kVStage + j * kVRow, p.v + row * kDv, kVRow,
-                                      &full[slot], policy);
-                        }
-                    }
+                if (lane == 0) {
+                    const int64_t row = w.base * p.H + int64_t(w.h) * w.T + e;
+                    mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow));
+                    bulk_load(ks + slot * kKStage, p.k + row * kDqk, n * kKRow, &full[slot],
+                              policy);
+                    bulk_load(vs + slot * kVStage, p.v + row * kDv, n * kVRow, &full[slot],
+                              policy);
                 }
                 filled[slot] = round + 1;
             }
         }
         // Drain: every copy this CTA issued lands before the CTA may exit.
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < R::kStages; ++s) {
             if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns)) {
                 if (lane == 0) report(p.status, kStTimeout);
             }
         }
         return;
     }
+    if (kSparse && warp < R::kProducerWarps) {
+        // ------------------------ producers (sparse) ------------------------
+        // 128 threads gather the selected rows in 16-byte pieces: a stage holds
+        // 64 x 24 key pieces and 64 x 16 value pieces; consecutive threads take
+        // consecutive pieces of a row.  Each thread's copies complete with one
+        // arrival on the stage's barrier (expected count 128).
+        const int pt = threadIdx.x;
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k);
+        const uint8_t* vb = reinterpret_cast<const uint8_t*>(p.v);
+        int it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Item w = item_of<kSparse>(p, item);
+            const int64_t rbase = w.base * p.H + int64_t(w.h) * w.T;
+            for (int st = 0; st < w.nst; ++st, ++it) {
+                const int e = stage_entry(w, st);
+                const int slot = it % R::kStages;
+                const int round = it / R::kStages;
+                if (*abort_flag) { ok = false; break; }
+                // Selections of this stage are loaded before waiting for the
+                // slot, so their latency hides behind the wait.
+                const int n = min(kSP, w.e1 - e);
+                const int32_t* ix = p.idx + int64_t(w.b) * p.topk + e;
+                int selk[kSP * 24 / 128], selv[kSP * 16 / 128];
+#pragma unroll
+                for (int i = 0; i < kSP * 24 / 128; ++i) {
+                    const int j = (pt + 128 * i) / 24;
+                    selk[i] = j < n ? ix[j] : -1;
+                }
+#pragma unroll
+                for (int i = 0; i < kSP * 16 / 128; ++i) {
+                    const int j = (pt + 128 * i) >> 4;
+                    selv[i] = j < n ? ix[j] : -1;
+                }
+                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                if (it == p.stall_stage) continue;   // test hook: withhold this stage
+#pragma unroll
+                for (int i = 0; i < kSP * 24 / 128; ++i) {
+                    const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
+                    if (valid_pos(selk[i], w.T))
+                        cp_async16(ks + slot * kKStage + j * kKRow + off,
+                                   kb + (rbase + selk[i]) * kKRow + off);
+                    else if (selk[i] < -1 || selk[i] >= w.T)
+                        report(p.status, kStBadIndex);
+                }
+#pragma unroll
+                for (int i = 0; i < kSP * 16 / 128; ++i) {
+                    const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
+                    if (valid_pos(selv[i], w.T))
+                        cp_async16(vs + slot * kVStage + j * kVRow + off,
+                                   vb + (rbase + selv[i]) * kVRow + off);
+                }
+                cp_async_arrive_noinc(&full[slot]);
+            }
+        }
+        cp_async_wait_all();   // nothing this thread started is still in flight at exit
+        return;
+    }
 
     // ------------------------------ consumers ------------------------------
-    const int cw = warp - 1;                 // consumer warp 0..7
+    const int cw = warp - R::kProducerWarps;   // consumer warp 0..7
     const int g = cw * 4 + (lane >> 3);      // group 0..31
     const int j = lane & 7;                  // lane within the group
     int it = 0;
@@ -239,9 +316,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
 #pragma unroll
         for (int d = 0; d < 16; ++d) acc[d] = 0.f;
 
-        for (int e = w.e0; e < w.e1; e += kSP, ++it) {
-            const int slot = it % kStages;
-            const int round = it / kStages;
+        for (int st = 0; st < w.nst; ++st, ++it) {
+            const int e = stage_entry(w, st);
+            const int slot = it % R::kStages;
+            const int round = it / R::kStages;
+            // Which of this group's positions hold data: known before the
+            // wait (sparse: the selection is read while the copies land).
+            const int n = min(kSP, w.e1 - e);
+            bool ok[kPPG];
+#pragma unroll
+            for (int r = 0; r < kPPG; ++r) {
+                const int pos = g + kGroups * r;
+                ok[r] = pos < n;
+                if (kSparse && ok[r])
+                    ok[r] = valid_pos(p.idx[int64_t(w.b) * p.topk + e + pos], w.T);
+            }
             bool have = !*abort_flag;
             if (have && !mbar_wait(&full[slot], round & 1, p.wait_ns)) {
                 if (lane == 0) report(p.status, kStTimeout);
@@ -250,16 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
             }
             have = __all_sync(0xffffffffu, have);
             if (have) {
-                const int n = min(kSP, w.e1 - e);
                 const uint8_t* kst = ks + slot * kKStage;
                 const uint8_t* vst = vs + slot * kVStage;
                 float s[kPPG];
-                bool ok[kPPG];
 #pragma unroll
                 for (int r = 0; r < kPPG; ++r) {
                     const int pos = g + kGroups * r;
-                    ok[r] = pos < n;
-                    if (kSparse && ok[r]) ok[r] = valid_pos(p.idx[int64_t(w.b) * p.topk + e + pos], w.T);
                     float dot = 0.f;
                     if (ok[r]) {
                         const uint8_t* kr = kst + pos * kKRow;
@@ -463,13 +548,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
-DecodePlan plan_decode(int B, int H, int max_len, bool sparse) {
-    // Largest chunk (<= 1024, >= one stage) that still gives >= 2432 work
-    // items (16 per SM on a 152-SM part) when every sequence is max_len long.
+DecodePlan plan_decode(int B, int H, int max_len, bool sparse, int sparse_chunk) {
+    // Dense: largest chunk (<= 1024, >= one stage) that still gives >= 2432
+    // work items (16 per SM on a 152-SM part) when every sequence is max_len
+    // long.  Sparse: `sparse_chunk` entries (a power of two, one stage at
+    // least), 256 unless the test knob sets it (a sweep over 64..2048 on the
+    // B=8, T=131072 workload peaked at 256).
     DecodePlan pl{};
     int chunk = 1024;
     auto items = [&](int c) { return int64_t(B) * H * ((int64_t(max_len) + c - 1) / c); };
     while (chunk > kSP && items(chunk) < 2432) chunk >>= 1;
+    if (sparse) chunk = sparse_chunk > 0 ? sparse_chunk : 256;
     pl.chunk = chunk;
     pl.max_chunks = int((int64_t(max_len) + chunk - 1) / chunk);
     const size_t slots = size_t(B) * H * pl.max_chunks;
@@ -483,7 +572,8 @@ DecodePlan plan_decode(int B, int H, int max_len, bool sparse) {
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse,
                           const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
                           cudaStream_t st) {
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(smem_bytes<true>() <= 227 * 1024 && smem_bytes<false>() <= 227 * 1024,
+                  "shared memory budget");
     Params p{};
     p.q = a.q;
     p.k = a.k;
@@ -511,19 +601,21 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse
         const int items = a.B * a.H * ((a.topk + pl.chunk - 1) / pl.chunk);
         grid = items < grid ? items : grid;
         e = cudaFuncSetAttribute(decode_partial_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_bytes<true>()));
         if (e != cudaSuccess) return e;
         if (tm.begin) cudaEventRecord(tm.begin, st);
-        decode_partial_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+        decode_partial_kernel<true><<<grid, Roles<true>::kThreads, smem_bytes<true>(), st>>>(p);
         if (tm.end) cudaEventRecord(tm.end, st);
     } else {
         decode_items_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.H, pl.chunk, a.max_seqlen,
                                                const_cast<int*>(p.item_start), dev.status);
         e = cudaFuncSetAttribute(decode_partial_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_bytes<false>()));
         if (e != cudaSuccess) return e;
         if (tm.begin) cudaEventRecord(tm.begin, st);
-        decode_partial_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+        decode_partial_kernel<false><<<grid, Roles<false>::kThreads, smem_bytes<false>(), st>>>(p);
         if (tm.end) cudaEventRecord(tm.end, st);
     }
     e = cudaGetLastError();

@@ -40,23 +40,29 @@ namespace mla {
 namespace {
 
 constexpr int kTile = 128;                                   // positions per MMA tile
-constexpr int kIStages = 4;
+#ifndef MLA_INDEX_STAGES
+#define MLA_INDEX_STAGES 6
+#endif
+constexpr int kIStages = MLA_INDEX_STAGES;
 constexpr int kAHalf = kTile * 64 * 2;                       // 16 KB: 128 rows x 128 B
 constexpr int kBHalf = kIndexHeads * 64 * 2;                 // 4 KB: 32 rows x 128 B
-constexpr int kStageBytes = 2 * kAHalf + 2 * kBHalf;         // 40 KB
+constexpr int kStageBytes = 2 * kAHalf;                      // 32 KB of index keys
+constexpr int kQBytes = 2 * kBHalf;                          // 8 KB: one sequence's queries
 constexpr int kBins = 2048;
 constexpr int kScoreThreads = 6 * 32;
-constexpr uint32_t kTmemCols = 64;
-constexpr size_t kScoreSmem = 1024 + size_t(kIStages) * kStageBytes + kBins * 4 + 256;
+constexpr int kAcc = 4;                                      // TMEM accumulators (32 columns each)
+constexpr uint32_t kTmemCols = 32 * kAcc;
+constexpr size_t kScoreSmem =
+    1024 + size_t(kIStages) * kStageBytes + 2 * kQBytes + kBins * 4 + 256;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kIndexHeads, false, false);
 
 struct ScoreParams {
     const float* w;
     const int64_t* cu;
     const int* tile_start;   // [B+1]
-    float* scores;           // [B][max_seqlen]
+    float* scores;           // [B][stride]
     unsigned* hist;          // [B][2048]
-    int B, max_seqlen;
+    int B, stride;
     long long wait_ns;
     int* status;
 };
@@ -75,18 +81,36 @@ __device__ __forceinline__ int tile_owner(const int* tile_start, int B, int t) {
     return lo;
 }
 
+// Sequence of consecutive tiles t, t+1, ...: found once by binary search,
+// then advanced without searching.
+struct SeqCursor {
+    int b, next;   // sequence of the current tile; first tile of sequence b+1
+    __device__ __forceinline__ void init(const int* tile_start, int B, int t) {
+        b = tile_owner(tile_start, B, t);
+        next = tile_start[b + 1];
+    }
+    __device__ __forceinline__ void advance(const int* tile_start, int t) {
+        while (t >= next) {
+            ++b;
+            next = tile_start[b + 1];
+        }
+    }
+};
+
 __global__ void __launch_bounds__(kScoreThreads, 1)
     dsa_score_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap qmap, const ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned* hist = reinterpret_cast<unsigned*>(smem + kIStages * kStageBytes);
+    uint8_t* qbuf = smem + kIStages * kStageBytes;            // [2][8 KB] query tiles
+    unsigned* hist = reinterpret_cast<unsigned*>(qbuf + 2 * kQBytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(hist + kBins);
     uint64_t* empty = full + kIStages;
     uint64_t* tfull = empty + kIStages;
-    uint64_t* tempty = tfull + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* tempty = tfull + kAcc;
+    uint64_t* qfull = tempty + kAcc;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qfull + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,10 +123,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 4);
         }
+        mbar_init(&qfull[0], 1);
+        mbar_init(&qfull[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -119,7 +145,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&qmap);
             const uint64_t stream_policy = l2_evict_first_policy();
-            int filled[kIStages] = {0, 0, 0, 0};
+            // Queries are loaded once per sequence into one of two buffers; a
+            // buffer is refilled only after the MMAs of the last tile that read
+            // it have completed (the commit of that tile's stage).
+            int filled[kIStages];
+            for (int i = 0; i < kIStages; ++i) filled[i] = 0;
+            int qfilled[2] = {0, 0}, last_use[2] = {-1, -1};
+            int cur_b = -1, seg = 0;
+            SeqCursor cs;
+            if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
             for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
                 const int slot = j % kIStages, round = j / kIStages;
                 if (*abort_flag) break;
@@ -128,36 +162,67 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                const int b = tile_owner(p.tile_start, p.B, t);
+                cs.advance(p.tile_start, t);
+                const int b = cs.b;
+                if (b != cur_b) {
+                    const int qb = seg & 1;
+                    const int lu = last_use[qb];
+                    if (lu >= 0 && j - lu < kIStages &&
+                        !mbar_wait(&empty[lu % kIStages], (lu / kIStages) & 1, p.wait_ns)) {
+                        report(p.status, kStTimeout);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&qfull[qb], kQBytes);
+                    tma_load_2d(qbuf + qb * kQBytes, &qmap, 0, b * kIndexHeads, &qfull[qb]);
+                    tma_load_2d(qbuf + qb * kQBytes + kBHalf, &qmap, 64, b * kIndexHeads,
+                                &qfull[qb]);
+                    qfilled[qb] = (seg >> 1) + 1;
+                    cur_b = b;
+                    ++seg;
+                }
+                last_use[(seg - 1) & 1] = j;
                 const int row = int(p.cu[b]) + (t - p.tile_start[b]) * kTile;
                 uint8_t* st = smem + slot * kStageBytes;
                 mbar_arrive_expect_tx(&full[slot], kStageBytes);
                 tma_load_2d_hint(st, &kmap, 0, row, &full[slot], stream_policy);
                 tma_load_2d_hint(st + kAHalf, &kmap, 64, row, &full[slot], stream_policy);
-                tma_load_2d(st + 2 * kAHalf, &qmap, 0, b * kIndexHeads, &full[slot]);
-                tma_load_2d(st + 2 * kAHalf + kBHalf, &qmap, 64, b * kIndexHeads, &full[slot]);
                 filled[slot] = round + 1;
             }
-            for (int s = 0; s < kIStages; ++s)
-                if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
+            for (int i = 0; i < kIStages; ++i)
+                if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, p.wait_ns))
+                    report(p.status, kStTimeout);
+            for (int i = 0; i < 2; ++i)
+                if (qfilled[i] > 0 && !mbar_wait(&qfull[i], (qfilled[i] - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer -------------------------------
         if (lane == 0) {
             int last_acc = -1, last_phase = 0;
+            int cur_b = -1, seg = 0;
+            SeqCursor cs;
+            if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
             for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
-                const int slot = j % kIStages, acc = j & 1;
+                const int slot = j % kIStages, acc = j % kAcc;
                 if (*abort_flag) break;
-                if (!mbar_wait(&full[slot], (j / kIStages) & 1, p.wait_ns) ||
-                    (j >= 2 && !mbar_wait(&tempty[acc], ((j >> 1) - 1) & 1, p.wait_ns))) {
+                cs.advance(p.tile_start, t);
+                const int b = cs.b;
+                bool ok = true;
+                if (b != cur_b) {                     // this sequence's queries
+                    ok = mbar_wait(&qfull[seg & 1], (seg >> 1) & 1, p.wait_ns);
+                    cur_b = b;
+                    ++seg;
+                }
+                if (!ok || !mbar_wait(&full[slot], (j / kIStages) & 1, p.wait_ns) ||
+                    (j >= kAcc && !mbar_wait(&tempty[acc], ((j / kAcc) - 1) & 1, p.wait_ns))) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(smem + slot * kStageBytes);
-                const uint32_t b0 = a0 + 2 * kAHalf;
+                const uint32_t b0 = smem_u32(qbuf + ((seg - 1) & 1) * kQBytes);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * kAHalf + (kk & 3) * 32, 16, 1024);
@@ -167,7 +232,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 mma_commit(&empty[slot]);
                 mma_commit(&tfull[acc]);
                 last_acc = acc;
-                last_phase = (j >> 1) & 1;
+                last_phase = (j / kAcc) & 1;
             }
             // the accumulator must not be released while an MMA still writes it
             if (last_acc >= 0 && !mbar_wait(&tfull[last_acc], last_phase, p.wait_ns))
@@ -177,10 +242,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // ------------------------------- epilogue --------------------------------
         const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
         const int r = quad * 32 + lane;            // position within the tile
-        int cur_b = -1;
+        int cur_b = -1, T = 0, tstart = 0;
+        float wr[kIndexHeads];                     // head weights of the current sequence
+        SeqCursor cs;
+        if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
         for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
-            const int acc = j & 1;
-            const int b = tile_owner(p.tile_start, p.B, t);
+            const int acc = j % kAcc;
+            cs.advance(p.tile_start, t);
+            const int b = cs.b;
             if (b != cur_b) {
                 if (cur_b >= 0) {                  // flush the previous sequence's bins
                     named_bar_sync(1, 128);
@@ -194,11 +263,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     named_bar_sync(1, 128);
                 }
                 cur_b = b;
+                T = int(p.cu[b + 1] - p.cu[b]);
+                tstart = p.tile_start[b];
+#pragma unroll
+                for (int h = 0; h < kIndexHeads; ++h) wr[h] = __ldg(p.w + size_t(b) * kIndexHeads + h);
             }
             // After a timeout every warp keeps walking the tile list without
             // touching TMEM, so all four warps meet the same named barriers.
             bool ok = !*abort_flag;
-            if (ok && !mbar_wait(&tfull[acc], (j >> 1) & 1, p.wait_ns)) {
+            if (ok && !mbar_wait(&tfull[acc], (j / kAcc) & 1, p.wait_ns)) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
                 ok = false;
@@ -213,16 +286,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
 
-            const float* wb = p.w + size_t(b) * kIndexHeads;
             float s = 0.f;
 #pragma unroll
-            for (int h = 0; h < kIndexHeads; ++h) s = fmaf(__ldg(wb + h), fmaxf(d[h], 0.f), s);
+            for (int h = 0; h < kIndexHeads; ++h) s = fmaf(wr[h], fmaxf(d[h], 0.f), s);
             s += 0.0f;                             // -0 -> +0: equal scores compare equal
-            const int64_t T = p.cu[b + 1] - p.cu[b];
-            const int pos = (t - p.tile_start[b]) * kTile + r;
-            if (pos < T) {
-                p.scores[size_t(b) * p.max_seqlen + pos] = s;
-                atomicAdd(&hist[okey(s) >> 21], 1u);
+            const int pos = (t - tstart) * kTile + r;
+            const bool in = pos < T;
+            if (in) p.scores[size_t(b) * p.stride + pos] = s;
+            // histogram of the top 11 key bits, one atomic per distinct bin per warp
+            const unsigned mask = __ballot_sync(0xffffffffu, in);
+            if (in) {
+                const unsigned bin = okey(s) >> 21;
+                const unsigned peers = __match_any_sync(mask, bin);
+                if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], unsigned(__popc(peers)));
             }
         }
         named_bar_sync(1, 128);
@@ -342,106 +418,259 @@ __device__ __forceinline__ void find_bin(const unsigned* hist, int nbins, int K,
     __syncthreads();
 }
 
-constexpr int kSelPer = 16;                        // positions per thread per collect tile
+constexpr int kSelPer = 16;                        // positions per thread per pass step
+constexpr int kStep = 1024 * kSelPer;              // positions per CTA per pass step
+constexpr int kCluster = 8;                        // CTAs cooperating on one sequence
 
-__global__ void __launch_bounds__(1024) dsa_topk_kernel(const float* scores, const unsigned* ghist,
-                                                        const int64_t* cu, int max_seqlen,
-                                                        int64_t total_keys, int topk,
-                                                        int32_t* out_idx, float* out_scores,
-                                                        int* status) {
-    __shared__ unsigned hist[kBins];
+// Load this thread's 16 consecutive scores (positions i0..i0+15, rows padded
+// to 16 bytes so the float4 reads stay inside the row).
+__device__ __forceinline__ void load16(const float* s, int i0, int T, float (&v)[kSelPer]) {
+    const float4* s4 = reinterpret_cast<const float4*>(s);
+#pragma unroll
+    for (int u = 0; u < kSelPer / 4; ++u) {
+        const float4 x = (i0 + 4 * u) < T ? s4[(i0 >> 2) + u] : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * u] = x.x;
+        v[4 * u + 1] = x.y;
+        v[4 * u + 2] = x.z;
+        v[4 * u + 3] = x.w;
+    }
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory writes before
+// the barrier with reads (local or remote) after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+struct TopkParams {
+    const float* scores;     // [B][stride]
+    const unsigned* hist1;   // [B][2048]  top 11 key bits (built by the scoring pass)
+    const int64_t* cu;
+    int max_seqlen, stride, topk;
+    int64_t total_keys;
+    int32_t* out_idx;
+    float* out_scores;
+    int* status;
+};
+
+__device__ __forceinline__ int seq_len(const TopkParams& p, int b) {
+    const int64_t T = p.cu[b + 1] - p.cu[b];
+    const bool ok = !(T < 0 || T > p.max_seqlen || p.cu[b] < 0 || p.cu[b + 1] > p.total_keys);
+    return ok ? int(T) : 0;
+}
+
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ void dsmem_add(uint32_t addr, unsigned v) {
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+constexpr size_t kTopkSmem = size_t(kStep) * 4 + (kBins + 1024 + kBins + kBins) * 4 +
+                             2 * kCluster * 4;
+
+// Top-k of one sequence per cluster of eight CTAs; CTA r owns positions
+// [r*span, (r+1)*span) and keeps them in shared memory when they fit (one
+// 16,384-position step; otherwise every pass re-reads its steps from L2).
+// Levels 2 and 3 of the radix select histogram the keys that share the prefix
+// found so far; each CTA pushes its partial bins into every CTA's total with
+// remote (distributed shared memory) atomics, so after a cluster barrier all
+// CTAs hold the same totals and find the same bin.  Then each CTA writes its
+// counts of keys above and equal to the k-th key into every CTA, and after a
+// last barrier writes its kept positions at their place in the ascending
+// output.  Four cluster barriers in all.
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
+    dsa_topk_cluster_kernel(const TopkParams p) {
+    extern __shared__ float4 topk_dyn[];
+    // scores of one step: element u of thread t (position t0 + 16t + u) at
+    // vals[u*1024 + t], so a warp's accesses hit 32 different banks
+    float* vals = reinterpret_cast<float*>(topk_dyn);
+    unsigned* sum2 = reinterpret_cast<unsigned*>(vals + kStep);   // [2048] cluster totals
+    unsigned* sum3 = sum2 + kBins;                                // [1024] cluster totals
+    unsigned* hist1 = sum3 + 1024;                                // [2048] level 1
+    unsigned* part = hist1 + kBins;                               // [2048] this CTA's bins
+    int* cnts = reinterpret_cast<int*>(part + kBins);             // [kCluster][2]
     __shared__ int sh[40];
-    const int b = blockIdx.x;
+    const int b = blockIdx.y;
+    const uint32_t rank = cluster_rank();
     const int tid = threadIdx.x;
-    int32_t* oi = out_idx + size_t(b) * topk;
-    float* os = out_scores ? out_scores + size_t(b) * topk : nullptr;
-    const int64_t T64 = cu[b + 1] - cu[b];
-    const bool valid = !(T64 < 0 || T64 > max_seqlen || cu[b] < 0 || cu[b + 1] > total_keys);
-    const int T = valid ? int(T64) : 0;
-    const float* s = scores + size_t(b) * max_seqlen;
-    if (T <= topk) {                               // every position is kept
-        for (int i = tid; i < topk; i += blockDim.x) {
-            oi[i] = i < T ? i : -1;
-            if (os) os[i] = -INFINITY;
-        }
+    int32_t* oi = p.out_idx + size_t(b) * p.topk;
+    float* os = p.out_scores ? p.out_scores + size_t(b) * p.topk : nullptr;
+    const int T = seq_len(p, b);                    // the same for the whole cluster
+    if (T <= p.topk) {                              // every position is kept
+        if (rank == 0)
+            for (int i = tid; i < p.topk; i += blockDim.x) {
+                oi[i] = i < T ? i : -1;
+                if (os) os[i] = -INFINITY;
+            }
         return;
     }
-    const int K = topk;
-    // ---- level 1: top 11 key bits, histogram built by the scoring pass ----
-    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = ghist[size_t(b) * kBins + i];
+    const int K = p.topk;
+    const int span = ((T + kCluster - 1) / kCluster + kSelPer - 1) / kSelPer * kSelPer;
+    const int lo = int(rank) * span, hi = min(T, lo + span);
+    const bool resident = hi - lo <= kStep;
+    const float* s = p.scores + size_t(b) * p.stride;
+
+    // Load step [t0, t0+kStep) of this CTA's range into shared memory.
+    auto stage = [&](int t0) {
+        float v[kSelPer];
+        const int i0 = t0 + tid * kSelPer;
+        load16(s, i0, hi, v);
+#pragma unroll
+        for (int u = 0; u < kSelPer; ++u) vals[u * 1024 + tid] = v[u];
+    };
+    for (int i = tid; i < kBins; i += blockDim.x) {
+        sum2[i] = 0;
+        hist1[i] = p.hist1[size_t(b) * kBins + i];
+    }
+    for (int i = tid; i < 1024; i += blockDim.x) sum3[i] = 0;
+    if (resident) stage(lo);
     __syncthreads();
     int bin1, above1;
-    find_bin(hist, kBins, K, sh, &bin1, &above1);
-    // ---- level 2: next 11 bits among keys in bin1 ----
-    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < T; i += blockDim.x) {
-        const uint32_t k = okey(s[i]);
-        if ((k >> 21) == uint32_t(bin1)) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
-    }
-    __syncthreads();
-    int bin2, above2;
-    find_bin(hist, kBins, K - above1, sh, &bin2, &above2);
-    // ---- level 3: last 10 bits ----
-    const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
-    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < T; i += blockDim.x) {
-        const uint32_t k = okey(s[i]);
-        if ((k >> 10) == pre) atomicAdd(&hist[k & 1023u], 1u);
-    }
-    __syncthreads();
-    int bin3, above3;
-    find_bin(hist, 1024, K - above1 - above2, sh, &bin3, &above3);
-    const uint32_t kth = (pre << 10) | uint32_t(bin3);
-    const int need_eq = K - above1 - above2 - above3;          // >= 1
-    const bool all_eq = int(hist[bin3]) == need_eq;            // no tie to break
-    __syncthreads();
-    // ---- collect in position order ----
-    int out_base = 0, eq_base = 0;
-    for (int t0 = 0; t0 < T; t0 += 1024 * kSelPer) {
-        const int i0 = t0 + tid * kSelPer;
-        uint32_t gt = 0, eq = 0;
+    find_bin(hist1, kBins, K, sh, &bin1, &above1);
+    cluster_sync();                                 // (1) every CTA's totals are zero
+
+    // One refinement level: partial bins of the keys with top bits == pre.
+    auto level = [&](int shift, int nb, uint32_t pre, unsigned* total) {
+        for (int i = tid; i < nb; i += blockDim.x) part[i] = 0;
+        __syncthreads();
+        for (int t0 = lo; t0 < hi; t0 += kStep) {
+            if (!resident) {
+                stage(t0);
+                __syncthreads();
+            }
+            const int i0 = t0 + tid * kSelPer;
 #pragma unroll
-        for (int u = 0; u < kSelPer; ++u) {
-            if (i0 + u < T) {
-                const uint32_t k = okey(s[i0 + u]);
-                gt |= uint32_t(k > kth) << u;
-                eq |= uint32_t(k == kth) << u;
+            for (int u = 0; u < kSelPer; ++u) {
+                if (i0 + u < hi) {
+                    const uint32_t k = okey(vals[u * 1024 + tid]);
+                    if ((k >> (shift + (nb == 1024 ? 10 : 11))) == pre)
+                        atomicAdd(&part[(k >> shift) & uint32_t(nb - 1)], 1u);
+                }
+            }
+            if (!resident) __syncthreads();
+        }
+        __syncthreads();
+        for (int i = tid; i < nb; i += blockDim.x) {
+            const unsigned c = part[i];
+            if (c)
+                for (uint32_t r = 0; r < kCluster; ++r) dsmem_add(dsmem_addr(&total[i], r), c);
+        }
+    };
+    level(10, kBins, uint32_t(bin1), sum2);
+    cluster_sync();                                 // (2) level-2 totals everywhere
+    int bin2, above2;
+    find_bin(sum2, kBins, K - above1, sh, &bin2, &above2);
+    const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
+    level(0, 1024, pre, sum3);
+    cluster_sync();                                 // (3) level-3 totals everywhere
+    int bin3, above3;
+    find_bin(sum3, 1024, K - above1 - above2, sh, &bin3, &above3);
+    const uint32_t kth = (pre << 10) | uint32_t(bin3);
+    const int need_eq = K - above1 - above2 - above3;
+    const bool all_eq = int(sum3[bin3]) == need_eq;
+
+    // counts of this CTA's range, written into every CTA
+    int gt = 0, eq = 0;
+    for (int t0 = lo; t0 < hi; t0 += kStep) {
+        if (!resident) {
+            __syncthreads();
+            stage(t0);
+            __syncthreads();
+        }
+        const int i0 = t0 + tid * kSelPer;
+#pragma unroll
+        for (int u = 0; u < kSelPer; ++u)
+            if (i0 + u < hi) {
+                const uint32_t k = okey(vals[u * 1024 + tid]);
+                gt += k > kth;
+                eq += k == kth;
+            }
+    }
+    int tg, te;
+    block_excl_scan(gt, sh, &tg);
+    block_excl_scan(eq, sh, &te);
+    if (tid < kCluster) {
+        dsmem_st(dsmem_addr(&cnts[2 * rank], uint32_t(tid)), tg);
+        dsmem_st(dsmem_addr(&cnts[2 * rank + 1], uint32_t(tid)), te);
+    }
+    cluster_sync();                                 // (4) all counts everywhere; last remote access
+    int gt_before = 0, eq_before = 0;
+    for (uint32_t r = 0; r < rank; ++r) {
+        gt_before += cnts[2 * r];
+        eq_before += cnts[2 * r + 1];
+    }
+
+    // emit in position order
+    int out = gt_before + min(eq_before, need_eq), eq_seen = eq_before;
+    for (int t0 = lo; t0 < hi; t0 += kStep) {
+        if (!resident) {
+            __syncthreads();
+            stage(t0);
+            __syncthreads();
+        }
+        const int i0 = t0 + tid * kSelPer;
+        uint32_t g = 0, e = 0;
+#pragma unroll
+        for (int u = 0; u < kSelPer; ++u)
+            if (i0 + u < hi) {
+                const uint32_t k = okey(vals[u * 1024 + tid]);
+                g |= uint32_t(k > kth) << u;
+                e |= uint32_t(k == kth) << u;
+            }
+        uint32_t keep = e;
+        if (!all_eq) {                              // lowest positions among equal keys
+            int e_total;
+            int r = eq_seen + block_excl_scan(__popc(e), sh, &e_total);
+            keep = 0;
+            for (uint32_t m = e; m; m &= m - 1, ++r)
+                if (r < need_eq) keep |= m & (~m + 1);
+            eq_seen += e_total;
+        }
+        const uint32_t take = g | keep;
+        int total;
+        int o = out + block_excl_scan(__popc(take), sh, &total);
+        for (uint32_t m = take; m; m &= m - 1, ++o) {
+            const int u = __ffs(m) - 1;
+            if (o < K) {
+                oi[o] = i0 + u;
+                if (os) os[o] = vals[u * 1024 + tid];
+            } else {
+                report(p.status, kStInvalid);       // cannot happen for consistent counts
             }
         }
-        uint32_t sel = gt | eq;
-        if (!all_eq) {
-            int eq_total;
-            const int eq_before = eq_base + block_excl_scan(__popc(eq), sh, &eq_total);
-            uint32_t keep = 0;
-            int r = eq_before;
-            for (uint32_t m = eq; m; m &= m - 1, ++r)
-                if (r < need_eq) keep |= m & (~m + 1);
-            sel = gt | keep;
-            eq_base += eq_total;
-        }
-        int sel_total;
-        int o = out_base + block_excl_scan(__popc(sel), sh, &sel_total);
-        for (uint32_t m = sel; m; m &= m - 1, ++o) {
-            const int pos = i0 + (__ffs(m) - 1);
-            oi[o] = pos;
-            if (os) os[o] = s[pos];
-        }
-        out_base += sel_total;
+        out += total;
     }
-    if (out_base != K) report(status, kStInvalid);   // cannot happen for finite scores
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Score rows start on 16-byte boundaries so the top-k passes can load float4.
+int score_stride(int max_seqlen) { return (max_seqlen + 3) & ~3; }
+
 }  // namespace
 
 IndexPlan plan_index(int B, int max_seqlen) {
+    // scores | level-1 histograms | tile table
     IndexPlan p{};
     p.scores_off = 0;
-    p.hist_off = align256(size_t(B) * max_seqlen * 4);
-    p.tiles_off = p.hist_off + align256(size_t(B) * kBins * 4);
+    p.hist_off = align256(size_t(B) * score_stride(max_seqlen) * 4);
+    p.counts_off = p.hist_off + align256(size_t(B) * kBins * 4);
+    p.tiles_off = p.counts_off;
     p.total = p.tiles_off + align256(size_t(B + 1) * 4);
     return p;
 }
@@ -469,14 +698,19 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
     e = cudaFuncSetAttribute(dsa_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kScoreSmem));
     if (e != cudaSuccess) return e;
-    ScoreParams p{a.w, a.cu, tiles, scores, hist, a.B, a.max_seqlen, kn.wait_limit_ns, dev.status};
+    ScoreParams p{a.w, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
+                  kn.wait_limit_ns, dev.status};
     if (tm.begin) cudaEventRecord(tm.begin, st);
     dsa_score_kernel<<<dev.sms, kScoreThreads, kScoreSmem, st>>>(kmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dsa_topk_kernel<<<a.B, 1024, 0, st>>>(scores, hist, a.cu, a.max_seqlen, a.total_keys, a.topk,
-                                          a.topk_idx, a.topk_scores, dev.status);
+    TopkParams tp{scores, hist, a.cu, a.max_seqlen, score_stride(a.max_seqlen), a.topk,
+                  a.total_keys, a.topk_idx, a.topk_scores, dev.status};
+    e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTopkSmem));
+    if (e != cudaSuccess) return e;
+    dsa_topk_cluster_kernel<<<dim3(kCluster, a.B), 1024, kTopkSmem, st>>>(tp);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@ struct DeviceInfo {
 struct Knobs {
     long long wait_limit_ns;
     int stall_stage;
+    int sparse_chunk;   // 0 = default
 };
 
 // Optional event pair recorded around an operation's dominant kernel.
@@ -53,7 +54,7 @@ struct DecodePlan {
     size_t acc_off, ml_off, items_off, total;  // workspace layout in bytes
 };
 
-DecodePlan plan_decode(int B, int H, int max_len, bool sparse);
+DecodePlan plan_decode(int B, int H, int max_len, bool sparse, int sparse_chunk = 0);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, bool sparse,
                           const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
                           cudaStream_t st);
@@ -77,7 +78,7 @@ struct IndexArgs {
 };
 
 struct IndexPlan {
-    size_t scores_off, hist_off, tiles_off, total;
+    size_t scores_off, hist_off, counts_off, tiles_off, total;
 };
 
 IndexPlan plan_index(int B, int max_seqlen);
