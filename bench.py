@@ -47,12 +47,21 @@ CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
-def peaks():
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks(bound="hbm"):
+    """(peak, unit, source): HBM copy GB/s, or the dense bf16 TFLOP/s of a
+    kernel timed alone (burst), from the measured file if present."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        if bound == "tensor":
+            return float(d["bf16_tflops"]), "TFLOP/s", "measured (burst)"
+        return float(d["hbm_gbs"]), "GB/s", "measured"
+    if bound == "tensor":
+        return FALLBACK_BF16_TFLOPS, "TFLOP/s", "fallback"
+    return FALLBACK_HBM_GBS, "GB/s", "fallback"
 
 
 class ClockSampler:
@@ -222,7 +231,9 @@ def workload_config(name, B=None):
         cfg["T"] = w["T"]
     if "lo" in w:
         cfg["T_range"] = [w["lo"], w["hi"]]
-    cfg["l2"] = "inputs larger than L2 (no flush needed)"
+    small = w["kind"] == "prefill" and w["T"] <= 1024
+    cfg["l2"] = ("inputs smaller than L2: a 512 MB buffer is written between timed steps"
+                 if small else "inputs larger than L2 (no flush needed)")
     return cfg
 
 
@@ -363,7 +374,38 @@ class IndexWork:
         del self.d, self.idx, self.ws_i
 
 
-WORK_KINDS = {"decode": DecodeWork, "dsa": DsaWork, "index": IndexWork}
+class PrefillWork:
+    """Causal gated MLA prefill (rows a1-a4, a6 on the tensor cores)."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        self.name, self.H, self.B, self.T = name, w["H"], w["B"], w["T"]
+        self.lengths = [w["T"]] * w["B"]
+        self.pf = mi.make_prefill(w["B"], w["H"], w["T"], w["T"], w["gated"], device=dev,
+                                  config=w["config"])
+        self.out = torch.empty((w["B"], w["T"], w["H"] * 128), dtype=torch.bfloat16, device=dev)
+        self.work = acc.prefill_flops(w["B"], w["H"], w["T"], w["T"])
+        self.unit, self.bound, self.scale_unit = "TFLOP/s", "tensor", 1e12
+        self.launches_per_step = 1
+        self.kernels = [(_lib.OP_PREFILL, "mla_prefill_kernel", self.work)]
+        in_bytes = sum(t.numel() * t.element_size() for t in
+                       (self.pf.q, self.pf.k, self.pf.v) + ((self.pf.gate,) if w["gated"] else ()))
+        self.flush_l2 = in_bytes < 4 * (129 << 20)
+
+    def step(self, stream):
+        pf = self.pf
+        self.mla.mla_prefill(pf.q, pf.k, pf.v, pf.gate, out=self.out, scale=pf.scale,
+                             stream=stream)
+
+    def free(self):
+        del self.pf, self.out
+
+
+WORK_KINDS = {"decode": DecodeWork, "dsa": DsaWork, "index": IndexWork,
+              "prefill": PrefillWork}
 
 
 def _time_e2e(one, work, dev, world, steps, h2d, d2h):
@@ -380,32 +422,48 @@ def _time_e2e(one, work, dev, world, steps, h2d, d2h):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+L2_FLUSH_BYTES = 512 << 20   # four times the 129 MB L2
+
+
 def time_work(work, steps, warmup, dev, stream, world, sampler=None):
     """CUDA-event time of `steps` steps (after `warmup`), and each dominant
-    kernel's own event time over the same region."""
+    kernel's own event time over the same region.  Workloads whose inputs fit
+    in L2 (work.flush_l2) are timed step by step with a 512 MB write between
+    steps, outside the timed events."""
     mla = work.mla
     for _ in range(warmup):
         work.step(stream)
     mla.check_device_status(stream)
     torch.cuda.synchronize(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) \
+        if getattr(work, "flush_l2", False) else None
     mla.timing_enable(True)
     for op, _, _ in work.kernels:
         mla.timing_read(op)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps if flush is not None else 1)]
     barrier(world)
     torch.cuda.synchronize(dev)
     if sampler:
         sampler.mark_start()
-    ev0.record(stream)
-    for _ in range(steps):
-        work.step(stream)
-    ev1.record(stream)
+    if flush is None:
+        ev[0][0].record(stream)
+        for _ in range(steps):
+            work.step(stream)
+        ev[0][1].record(stream)
+    else:
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            work.step(stream)
+            ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     if sampler:
         sampler.mark_end()
     barrier(world)
     mla.timing_enable(False)
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world)
+    del flush
     kern = []
     for op, kname, units in work.kernels:
         k_ms, n = mla.timing_read(op)
@@ -414,22 +472,29 @@ def time_work(work, steps, warmup, dev, stream, world, sampler=None):
     return ms, kern
 
 
+def _scale(work):
+    return getattr(work, "scale_unit", 1e9)
+
+
 def roofline(work, kern):
     """Roofline object for the dominant (longest) kernel of a step."""
-    peak, peak_kind = peaks()
+    peak, unit, peak_kind = peaks(work.bound)
+    sc = _scale(work)
     kname, k_ms, units = max(kern, key=lambda x: x[1])
-    achieved = units / (k_ms * 1e-3) / 1e9
-    r = {"bound": work.bound, "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+    achieved = units / (k_ms * 1e-3) / sc
+    nominal = 2250.0 if work.bound == "tensor" else 7900.0
+    per = "flops" if work.bound == "tensor" else "bytes"
+    r = {"bound": work.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
          "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-         "frac_of_nominal_7900": round(achieved / 7900.0, 4), "kernel": kname,
+         f"frac_of_nominal_{int(nominal)}": round(achieved / nominal, 4), "kernel": kname,
          "kernel_ms": round(k_ms, 4), "traffic": traffic_for(kname),
-         "algorithmic_bytes_per_launch": units}
+         f"algorithmic_{per}_per_launch": units}
     others = {}
     for kn, km, ku in kern:
         if kn != kname:
-            a = ku / (km * 1e-3) / 1e9
+            a = ku / (km * 1e-3) / sc
             others[kn] = {"achieved": round(a, 2), "frac": round(a / peak, 4),
-                          "kernel_ms": round(km, 4), "algorithmic_bytes_per_launch": ku}
+                          "kernel_ms": round(km, 4), f"algorithmic_{per}_per_launch": ku}
     if others:
         r["other_kernels"] = others
     return r
@@ -445,7 +510,7 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     ms, kern = time_work(work, args.steps, args.warmup, dev, stream, world, sampler)
     clocks = sampler.finish()
-    value = work.work * world / (ms * 1e-3) / 1e9
+    value = work.work * world / (ms * 1e-3) / _scale(work)
     line = {"metric": METRIC, "value": round(value, 2), "unit": work.unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -468,7 +533,7 @@ def run_ours(args, world, rank, local):
             wk = WORK_KINDS[w["kind"]](other, dev)
             k_steps = max(3, min(args.steps, 20))
             ms_o, kern_o = time_work(wk, k_steps, 3, dev, stream, world)
-            also[other] = {"value": round(wk.work * world / (ms_o * 1e-3) / 1e9, 2),
+            also[other] = {"value": round(wk.work * world / (ms_o * 1e-3) / _scale(wk), 2),
                            "unit": wk.unit, "ms_per_step": round(ms_o, 4), "steps": k_steps,
                            "roofline": roofline(wk, kern_o)}
             line["gpu_launches"] += wk.launches_per_step * (k_steps + 3) * world
@@ -487,8 +552,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=[n for n, w in mi.WORKLOADS.items()
-                             if w["kind"] in ("decode", "dsa", "index")])
+                    choices=list(mi.WORKLOADS))
     ap.add_argument("--only", action="store_true",
                     help="time only --workload (skip the other workloads' short runs)")
     ap.add_argument("--e2e-steps", type=int, default=5)

@@ -86,6 +86,8 @@ def mla_prefill(q, k, v, gate=None, out=None, scale=None, ws=None, stream=None):
         raise ValueError("q must be [B,H,Tq,192]")
     B, H, Tq, _ = q.shape
     Tk = k.shape[2] if k.dim() == 4 else -1
+    if Tk < Tq:
+        raise ValueError(f"the cache must hold the {Tq} new tokens (Tk={Tk} < Tq={Tq})")
     _need(k, "k", torch.bfloat16, (B, H, Tk, DQK), q.device)
     _need(v, "v", torch.bfloat16, (B, H, Tk, DV), q.device)
     if gate is not None:

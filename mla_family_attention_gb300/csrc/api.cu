@@ -261,9 +261,25 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
 mla_status mla_prefill(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
                        const mla_bf16* gate, mla_bf16* out, int B, int H, int Tq, int Tk,
                        float scale, void* ws, size_t ws_bytes, mla_stream stream) {
-    (void)q; (void)k; (void)v; (void)gate; (void)out; (void)B; (void)H; (void)Tq; (void)Tk;
-    (void)scale; (void)ws; (void)ws_bytes; (void)stream;
-    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill is not built yet");
+    (void)ws;
+    (void)ws_bytes;
+    REQUIRE(q && k && v && out, MLA_ERR_INVALID_ARG, "null tensor pointer");
+    REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) &&
+                (gate == nullptr || aligned16(gate)),
+            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    REQUIRE(B >= 1 && H >= 1 && Tq >= 1 && Tk >= Tq, MLA_ERR_INVALID_ARG,
+            "need B >= 1, H >= 1, 1 <= Tq <= Tk (got B=%d H=%d Tq=%d Tk=%d)", B, H, Tq, Tk);
+    REQUIRE(int64_t(B) * H * Tk < (int64_t(1) << 31) &&
+                int64_t(B) * H * ((Tq + 127) / 128) < (int64_t(1) << 31),
+            MLA_ERR_UNSUPPORTED, "B*H*Tk too large for one call");
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    mla::DeviceInfo d;
+    mla_status s = device_info(&d);
+    if (s != MLA_OK) return s;
+    mla::PrefillArgs a{q, k, v, gate, out, B, H, Tq, Tk, scale};
+    cudaError_t e = mla::launch_prefill(a, d, knobs(), take_timer(MLA_OP_PREFILL),
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_prefill launch");
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,

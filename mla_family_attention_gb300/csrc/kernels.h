@@ -85,4 +85,18 @@ IndexPlan plan_index(int B, int max_seqlen);
 cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& p, const DeviceInfo& dev,
                               const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 
+// ------------------------------ prefill -----------------------------------
+struct PrefillArgs {
+    const uint16_t* q;       // [B,H,Tq,192]
+    const uint16_t* k;       // [B,H,Tk,192]
+    const uint16_t* v;       // [B,H,Tk,128]
+    const uint16_t* gate;    // [B,Tq,H*128] or null
+    uint16_t* out;           // [B,Tq,H*128]
+    int B, H, Tq, Tk;
+    float scale;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Knobs& kn,
+                           const KernelTimer& tm, cudaStream_t st);
+
 }  // namespace mla

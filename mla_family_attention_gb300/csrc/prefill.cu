@@ -1,0 +1,394 @@
+// Causal gated MLA prefill on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes (Kimi K3 MLA forward; Kimi K2 "Latent attention > KV
+// cache" score line; K3.1 Gated DSA post eqs. (9), (10)): for every sequence
+// b, head h and new token i (absolute position Tk-Tq+i),
+//   z = sum_{j <= Tk-Tq+i} softmax_j(scale * q_i . k_j) v_j
+//   out[b, i, h*128+d] = z_d * sigmoid(gate[b, i, h*128+d])   (gate optional)
+//
+// Design (one CTA per 128-row query tile of one (b, h); heavy causal tiles
+// are launched first):
+//   * TMEM (512 columns): the query tile (192 bf16 features = 96 columns),
+//     two 128-column score buffers S0/S1, and the 128-column output O.  The
+//     softmax writes P (bf16) back over the first 64 columns of its score
+//     buffer, so both products read their A operand from TMEM: shared
+//     memory only carries K and V, whose bandwidth is the binding limit for
+//     192-feature keys.
+//   * warp 0: TMA producer for a 2-stage key ring (three 64-feature boxes of
+//     128 keys, 128-byte swizzle) and a 2-stage value ring;
+//   * warp 1: owns TMEM; one lane issues S_{j+1} = Q K_{j+1}^T before
+//     O += P_j V_j, so the next scores are computed while the softmax of the
+//     current tile runs; commits signal the other roles through mbarriers;
+//   * warps 2-5: one thread per query row.  Load the row's scores, apply the
+//     causal / length mask on tiles that need it, and update the running
+//     maximum lazily: O (in TMEM) is rescaled only when a row maximum grows by
+//     more than 2^8, otherwise exponentials use the stale maximum (values up
+//     to 2^8 are exact enough in bf16 and fp32).  At the end they normalise
+//     O, apply the sigmoid gate and store bf16 rows.
+// All waits are bounded; a timeout sets MLA_ERR_TIMEOUT, the roles stop, the
+// MMA lane waits for its last commit, and TMEM is released before exit.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kBM = 128;                       // query rows per CTA
+constexpr int kBN = 128;                       // keys per KV tile
+constexpr int kKStages = 2, kVStages = 2;
+constexpr int kBox = kBN * 64 * 2;             // 16 KB: 128 rows x 64 features
+constexpr int kKTile = 3 * kBox;               // 48 KB of keys
+constexpr int kVTile = 2 * kBox;               // 32 KB of values
+constexpr int kPThreads = 6 * 32;
+constexpr uint32_t kCols = 512;
+constexpr uint32_t kColQ = 0, kColS = 128, kColO = 384;
+constexpr float kRescaleLog2 = 8.f;
+constexpr size_t kPrefillSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile + 256;
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
+
+struct PrefillParams {
+    const uint16_t* q;      // [B,H,Tq,192]
+    const uint16_t* gate;   // [B,Tq,H*128] or null
+    uint16_t* out;          // [B,Tq,H*128]
+    int B, H, Tq, Tk, n_qt;
+    float scale_log2;
+    long long wait_ns;
+    int* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    mla_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ksm = smem;                                        // [2][48 KB]
+    uint8_t* vsm = smem + kKStages * kKTile;                    // [2][32 KB]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(vsm + kVStages * kVTile);
+    uint64_t* kfull = bars;                                     // TMA -> MMA
+    uint64_t* kempty = kfull + kKStages;                        // MMA -> TMA
+    uint64_t* vfull = kempty + kKStages;
+    uint64_t* vempty = vfull + kVStages;
+    uint64_t* sfull = vempty + kVStages;                        // [2] MMA -> softmax
+    uint64_t* pfull = sfull + 2;                                // [2] softmax -> MMA
+    uint64_t* odone = pfull + 2;                                // MMA -> softmax (each P.V)
+    uint64_t* ofinal = odone + 1;                               // MMA -> epilogue
+    uint64_t* qready = ofinal + 1;                              // softmax -> MMA
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qready + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbh = p.B * p.H;
+    const int qt = p.n_qt - 1 - int(blockIdx.x) / nbh;         // heavy (late) tiles first
+    const int bh = int(blockIdx.x) % nbh;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int P0 = p.Tk - p.Tq;                                 // cached positions before the new tokens
+    const int q0 = qt * kBM;
+    const int kmax = P0 + min(q0 + kBM - 1, p.Tq - 1);          // last key any row of the tile sees
+    const int n_kv = min((p.Tk + kBN - 1) / kBN, kmax / kBN + 1);
+    const int n_full = min((P0 + q0 + 1) / kBN, p.Tk / kBN);    // tiles visible to every row
+    const int kv_row0 = bh * p.Tk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&vfull[i], 1);
+            mbar_init(&vempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&pfull[i], 4);
+        }
+        mbar_init(odone, 1);
+        mbar_init(ofinal, 1);
+        mbar_init(qready, 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, kCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // --------------------------------- TMA ---------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            int kf[kKStages] = {0, 0}, vf[kVStages] = {0, 0};
+            for (int j = 0; j < n_kv; ++j) {
+                if (*abort_flag) break;
+                const int ks = j % kKStages, kr = j / kKStages;
+                if (kr > 0 && !mbar_wait(&kempty[ks], (kr - 1) & 1, p.wait_ns)) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int y = kv_row0 + j * kBN;
+                mbar_arrive_expect_tx(&kfull[ks], kKTile);
+                for (int c = 0; c < 3; ++c)
+                    tma_load_2d(ksm + ks * kKTile + c * kBox, &kmap, c * 64, y, &kfull[ks]);
+                kf[ks] = kr + 1;
+                const int vs = j % kVStages, vr = j / kVStages;
+                if (vr > 0 && !mbar_wait(&vempty[vs], (vr - 1) & 1, p.wait_ns)) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&vfull[vs], kVTile);
+                for (int c = 0; c < 2; ++c)
+                    tma_load_2d(vsm + vs * kVTile + c * kBox, &vmap, c * 64, y, &vfull[vs]);
+                vf[vs] = vr + 1;
+            }
+            for (int i = 0; i < kKStages; ++i)
+                if (kf[i] > 0 && !mbar_wait(&kfull[i], (kf[i] - 1) & 1, p.wait_ns))
+                    report(p.status, kStTimeout);
+            for (int i = 0; i < kVStages; ++i)
+                if (vf[i] > 0 && !mbar_wait(&vfull[i], (vf[i] - 1) & 1, p.wait_ns))
+                    report(p.status, kStTimeout);
+        }
+    } else if (warp == 1) {
+        // --------------------------------- MMA ---------------------------------
+        if (lane == 0) {
+            bool ok = mbar_wait(qready, 0, p.wait_ns);
+            bool issued = false;
+            // S_j = Q K_j^T into score buffer j&1 (A = queries in TMEM).
+            auto issue_qk = [&](int j) -> bool {
+                const int ks = j % kKStages;
+                if (!mbar_wait(&kfull[ks], (j / kKStages) & 1, p.wait_ns)) return false;
+                tc_fence_after();
+                const uint32_t kb = smem_u32(ksm + ks * kKTile);
+                const uint32_t d = tmem + kColS + uint32_t(j & 1) * 128;
+#pragma unroll
+                for (int kk = 0; kk < 12; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ts(d, tmem + kColQ + kk * 8, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&kempty[ks]);
+                mma_commit(&sfull[j & 1]);
+                issued = true;
+                return true;
+            };
+            if (ok) {
+                tc_fence_after();
+                ok = n_kv > 0 && issue_qk(0);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (*abort_flag) { ok = false; break; }
+                if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
+                const int vs = j % kVStages;
+                if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, p.wait_ns) ||
+                    !mbar_wait(&vfull[vs], (j / kVStages) & 1, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // O += P_j V_j (A = probabilities in TMEM, B = values, MN-major)
+                const uint32_t vb = smem_u32(vsm + vs * kVTile);
+                const uint32_t a = tmem + kColS + uint32_t(j & 1) * 128;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(vb + kk * 2048, kBox, 1024);
+                    mma_bf16_ts(tmem + kColO, a + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&vempty[vs]);
+                mma_commit(odone);
+            }
+            if (!ok) {
+                report(p.status, kStTimeout);
+                *abort_flag = 1;
+            }
+            mma_commit(ofinal);               // also releases the epilogue after an abort
+            if (issued && !mbar_wait(ofinal, 0, p.wait_ns)) report(p.status, kStTimeout);
+        }
+    } else {
+        // ------------------------- softmax / epilogue --------------------------
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                     // row within the tile
+        const int row = q0 + r;                             // query index
+        const int qa = P0 + row;                            // absolute position
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        // queries of this row -> TMEM columns 0..95 (bf16 pairs, feature order)
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.q + ((size_t(bh) * p.Tq + size_t(row < p.Tq ? row : 0)) * kDqk));
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 x = row < p.Tq ? __ldg(src + c * 8 + u) : make_uint4(0, 0, 0, 0);
+                    w[4 * u] = x.x;
+                    w[4 * u + 1] = x.y;
+                    w[4 * u + 2] = x.z;
+                    w[4 * u + 3] = x.w;
+                }
+                tmem_st32(tmem + lane_off + kColQ + c * 32, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qready);
+        }
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const int buf = j & 1;
+            ok = ok && !*abort_flag;
+            if (ok && !mbar_wait(&sfull[buf], (j >> 1) & 1, p.wait_ns)) {
+                report(p.status, kStTimeout);
+                *abort_flag = 1;
+                ok = false;
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sb = tmem + lane_off + kColS + uint32_t(buf) * 128;
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float t[32];
+                tmem_ld32(sb + c * 32, t);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) s[c * 32 + u] = t[u];
+            }
+            tmem_ld_wait();
+            float mt = -INFINITY;
+            const bool masked = j >= n_full;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                float x = s[c] * p.scale_log2;
+                if (masked) {
+                    const int key = j * kBN + c;
+                    if (key > qa || key >= p.Tk) x = -INFINITY;
+                }
+                s[c] = x;
+                mt = fmaxf(mt, x);
+            }
+            // lazy rescale: only when the row maximum grows by more than 2^8
+            const bool need = mt > m_used + kRescaleLog2;
+            const float m_new = need ? mt : m_used;
+            const float factor = need ? ex2(m_used - m_new) : 1.f;     // m_used=-inf -> 0
+            if (__any_sync(0xffffffffu, need && j > 0)) {
+                bool o_ok = mbar_wait(odone, (j - 1) & 1, p.wait_ns);  // P_{j-1} V_{j-1} landed
+                o_ok = __all_sync(0xffffffffu, o_ok);
+                if (!o_ok) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+                    tmem_ld_wait();
+                    uint32_t w[32];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) w[u] = __float_as_uint(o[u] * factor);
+                    tmem_st32(tmem + lane_off + kColO + c * 32, w);
+                }
+            }
+            l *= factor;
+            m_used = m_new;
+            const float me = m_used == -INFINITY ? 0.f : m_used;
+            // P_j (bf16) over the first 64 columns of the score buffer
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float p0 = ex2(s[c * 32 + 2 * u] - me);
+                    const float p1 = ex2(s[c * 32 + 2 * u + 1] - me);
+                    l += p0 + p1;
+                    w[u] = pack_bf16(p0, p1);
+                }
+                tmem_st16(sb + c * 16, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[buf]);
+        }
+        // ---- epilogue: O / l * sigmoid(gate) -> bf16 ----
+        bool fin = ok && mbar_wait(ofinal, 0, p.wait_ns);
+        fin = __all_sync(0xffffffffu, fin);
+        if (!fin) {
+            if (ok) report(p.status, kStTimeout);
+        } else {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const size_t orow = (size_t(b) * p.Tq + size_t(row < p.Tq ? row : 0)) * p.H + h;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDv);
+            const uint4* g = p.gate ? reinterpret_cast<const uint4*>(p.gate + orow * kDv) : nullptr;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float o[32];
+                tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+                tmem_ld_wait();
+                if (row < p.Tq) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float z[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) z[e] = o[u * 8 + e] * inv;
+                        if (g) {
+                            const uint4 gw = __ldg(g + c * 4 + u);
+                            const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                z[2 * e] *= sigmoidf_fast(bf_lo(gg[e]));
+                                z[2 * e + 1] *= sigmoidf_fast(bf_hi(gg[e]));
+                            }
+                        }
+                        dst[c * 4 + u] = make_uint4(pack_bf16(z[0], z[1]), pack_bf16(z[2], z[3]),
+                                                    pack_bf16(z[4], z[5]), pack_bf16(z[6], z[7]));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Knobs& kn,
+                           const KernelTimer& tm, cudaStream_t st) {
+    static_assert(kPrefillSmem <= 227 * 1024, "shared memory budget");
+    CUtensorMap kmap, vmap;
+    const uint64_t rows = uint64_t(a.B) * a.H * a.Tk;
+    cudaError_t e = encode_tmap_2d_bf16(&kmap, a.k, kDqk, rows, kDqk * 2, 64, kBN);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&vmap, a.v, kDv, rows, kDv * 2, 64, kBN);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPrefillSmem));
+    if (e != cudaSuccess) return e;
+    PrefillParams p{a.q, a.gate, a.out, a.B, a.H, a.Tq, a.Tk, (a.Tq + kBM - 1) / kBM,
+                    a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
+    const int grid = p.n_qt * a.B * a.H;
+    if (tm.begin) cudaEventRecord(tm.begin, st);
+    mla_prefill_kernel<<<grid, kPThreads, kPrefillSmem, st>>>(kmap, vmap, p);
+    if (tm.end) cudaEventRecord(tm.end, st);
+    return cudaGetLastError();
+}
+
+}  // namespace mla
