@@ -6,8 +6,8 @@
 //   z = sum_{j <= Tk-Tq+i} softmax_j(scale * q_i . k_j) v_j
 //   out[b, i, h*128+d] = z_d * sigmoid(gate[b, i, h*128+d])   (gate optional)
 //
-// Design (one CTA per 128-row query tile of one (b, h); heavy causal tiles
-// are launched first):
+// Design (one CTA per 128-row query tile of one (b, h); CTAs ordered head by
+// head so concurrent CTAs share K/V in L2, heavy causal tiles first):
 //   * TMEM (512 columns): the query tile (192 bf16 features = 96 columns),
 //     two 128-column score buffers S0/S1, and the 128-column output O.  The
 //     softmax writes P (bf16) back over the first 64 columns of its score
@@ -19,8 +19,10 @@
 //   * warp 1: owns TMEM; one lane issues S_{j+1} = Q K_{j+1}^T before
 //     O += P_j V_j, so the next scores are computed while the softmax of the
 //     current tile runs; commits signal the other roles through mbarriers;
-//   * warps 2-5: one thread per query row.  Load the row's scores, apply the
-//     causal / length mask on tiles that need it, and update the running
+//   * warps 2-9: two threads per query row, each owning 64 of the tile's 128
+//     key columns (and 64 of the 128 output features).  They load their half
+//     of the row's scores, apply the causal / length mask on tiles that need
+//     it, swap partial maxima through shared memory, and update the running
 //     maximum lazily: O (in TMEM) is rescaled only when a row maximum grows by
 //     more than 2^8, otherwise exponentials use the stale maximum (values up
 //     to 2^8 are exact enough in bf16 and fp32).  At the end they normalise
@@ -42,11 +44,16 @@ constexpr int kKStages = 2, kVStages = 2;
 constexpr int kBox = kBN * 64 * 2;             // 16 KB: 128 rows x 64 features
 constexpr int kKTile = 3 * kBox;               // 48 KB of keys
 constexpr int kVTile = 2 * kBox;               // 32 KB of values
-constexpr int kPThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 8;               // two per TMEM lane quadrant
+constexpr int kPThreads = (2 + kSoftmaxWarps) * 32;
 constexpr uint32_t kCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 384;
 constexpr float kRescaleLog2 = 8.f;
-constexpr size_t kPrefillSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile + 256;
+#ifndef MLA_PREFILL_POLY_EXP
+#define MLA_PREFILL_POLY_EXP 0   // 1: odd columns exponentiate on the FMA pipe
+#endif
+constexpr size_t kPrefillSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile + 256 +
+                                (2 * 2 * kBM * 2 + 2 * kBM) * 4;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
 
@@ -59,6 +66,28 @@ struct PrefillParams {
     long long wait_ns;
     int* status;
 };
+
+// 2^t on the FMA and integer pipes, for the share of the exponentials the
+// special-function unit (16 per clock per SM) cannot keep up with.  Range
+// reduction t = k + f with k = round(t), f in [-1/2, 1/2]: adding 1.5*2^23
+// rounds t to an integer in the significand (one FADD, no conversion
+// instruction, which would run on the special-function pipe too); 2^f from a
+// cubic fitted (weighted least squares refined to equal ripple) on
+// [-1/2, 1/2], relative error below 1.5e-4 evaluated in fp32; 2^k added to
+// the exponent field as an integer.  t < -126 gives 0.  The result is
+// rounded to bf16 next, whose step is 2^-9.
+__device__ __forceinline__ float exp2_fma(float t) {
+    const float magic = 12582912.f;                 // 1.5 * 2^23
+    const float tc = fmaxf(t, -127.f);
+    const float y = tc + magic;
+    const float k = y - magic;
+    const float f = tc - k;
+    const float q = fmaf(fmaf(fmaf(0.055171642f, f, 0.24261113f), f, 0.69326097f), f,
+                         0.99992806f);
+    const int ki = __float_as_int(y) - __float_as_int(magic);
+    const float r = __int_as_float(__float_as_int(q) + (ki << 23));
+    return t < -126.f ? 0.f : r;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -85,11 +114,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* qready = ofinal + 1;                              // softmax -> MMA
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qready + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // row-half exchange between the two softmax warps of a quadrant:
+    // [parity][half][row] partial maxima and the halves' ok flags, and a
+    // separate [half][row] slot for the final row sums
+    float* xmax = reinterpret_cast<float*>(smem + kKStages * kKTile + kVStages * kVTile + 256);
+    int* xok = reinterpret_cast<int*>(xmax + 2 * 2 * kBM);
+    float* xsum = reinterpret_cast<float*>(xok + 2 * 2 * kBM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nbh = p.B * p.H;
-    const int qt = p.n_qt - 1 - int(blockIdx.x) / nbh;         // heavy (late) tiles first
-    const int bh = int(blockIdx.x) % nbh;
+    // Head-major order: the CTAs running at one time share one or two heads'
+    // keys and values in L2 (one head's cache is 10 MB at T=16384, all heads'
+    // 1 GB); within a head, heavy (late) causal tiles go first.
+    const int bh = int(blockIdx.x) / p.n_qt;
+    const int qt = p.n_qt - 1 - (int(blockIdx.x) - bh * p.n_qt);
     const int b = bh / p.H, h = bh - b * p.H;
     const int P0 = p.Tk - p.Tq;                                 // cached positions before the new tokens
     const int q0 = qt * kBM;
@@ -109,11 +146,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&pfull[i], 4);
+            mbar_init(&pfull[i], kSoftmaxWarps);
         }
         mbar_init(odone, 1);
         mbar_init(ofinal, 1);
-        mbar_init(qready, 4);
+        mbar_init(qready, kSoftmaxWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -216,27 +253,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else {
         // ------------------------- softmax / epilogue --------------------------
+        // Warps 2..9: warp w serves TMEM lane quadrant w%4 (rows 32*quad..),
+        // and column half `half` of those rows (keys 64*half..64*half+63 of
+        // every tile, output features likewise).  The two warps of a quadrant
+        // swap partial row maxima (and their ok flags, so they stop together)
+        // through shared memory once per tile.
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int bar_id = 1 + quad;                        // named barrier of the pair
         const int r = quad * 32 + lane;                     // row within the tile
         const int row = q0 + r;                             // query index
         const int qa = P0 + row;                            // absolute position
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
-        // queries of this row -> TMEM columns 0..95 (bf16 pairs, feature order)
+        // queries of this row, features 96*half..96*half+95 -> TMEM columns 48*half..
         {
             const uint4* src = reinterpret_cast<const uint4*>(
-                p.q + ((size_t(bh) * p.Tq + size_t(row < p.Tq ? row : 0)) * kDqk));
+                p.q + ((size_t(bh) * p.Tq + size_t(row < p.Tq ? row : 0)) * kDqk)) + half * 12;
+            uint32_t w[16];
 #pragma unroll
             for (int c = 0; c < 3; ++c) {
-                uint32_t w[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 x = row < p.Tq ? __ldg(src + c * 8 + u) : make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < 4; ++u) {
+                    const uint4 x = row < p.Tq ? __ldg(src + c * 4 + u) : make_uint4(0, 0, 0, 0);
                     w[4 * u] = x.x;
                     w[4 * u + 1] = x.y;
                     w[4 * u + 2] = x.z;
                     w[4 * u + 3] = x.w;
                 }
-                tmem_st32(tmem + lane_off + kColQ + c * 32, w);
+                tmem_st16(tmem + lane_off + kColQ + half * 48 + c * 16, w);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -254,30 +298,42 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 ok = false;
             }
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
             const uint32_t sb = tmem + lane_off + kColS + uint32_t(buf) * 128;
-            float s[128];
+            float s[64];
+            float mloc = -INFINITY;
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float t[32];
-                tmem_ld32(sb + c * 32, t);
+                for (int c = 0; c < 2; ++c) {
+                    float t[32];
+                    tmem_ld32(sb + half * 64 + c * 32, t);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) s[c * 32 + u] = t[u];
-            }
-            tmem_ld_wait();
-            float mt = -INFINITY;
-            const bool masked = j >= n_full;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                float x = s[c] * p.scale_log2;
-                if (masked) {
-                    const int key = j * kBN + c;
-                    if (key > qa || key >= p.Tk) x = -INFINITY;
+                    for (int u = 0; u < 32; ++u) s[c * 32 + u] = t[u];
                 }
-                s[c] = x;
-                mt = fmaxf(mt, x);
+                tmem_ld_wait();
+                if (j >= n_full) {                          // causal / length mask
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int key = j * kBN + half * 64 + c;
+                        if (key > qa || key >= p.Tk) s[c] = -INFINITY;
+                    }
+                }
+                float mx[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+                for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+                mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             }
+            // swap with the other half of the row (double-buffered by tile parity)
+            xmax[(buf * 2 + half) * kBM + r] = mloc;
+            xok[(buf * 2 + half) * kBM + r] = ok;
+            named_bar_sync(bar_id, 64);
+            const float mo = xmax[(buf * 2 + (half ^ 1)) * kBM + r];
+            ok = __all_sync(0xffffffffu, ok && xok[(buf * 2 + (half ^ 1)) * kBM + r] != 0);
+            if (!ok) break;                                  // both warps of the pair
+            const float mt = fmaxf(mloc, mo) * p.scale_log2; // scale > 0 keeps the order
             // lazy rescale: only when the row maximum grows by more than 2^8
             const bool need = mt > m_used + kRescaleLog2;
             const float m_new = need ? mt : m_used;
@@ -285,40 +341,41 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (__any_sync(0xffffffffu, need && j > 0)) {
                 bool o_ok = mbar_wait(odone, (j - 1) & 1, p.wait_ns);  // P_{j-1} V_{j-1} landed
                 o_ok = __all_sync(0xffffffffu, o_ok);
-                if (!o_ok) {
+                if (o_ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem + lane_off + kColO + half * 64 + c * 32, o);
+                        tmem_ld_wait();
+                        uint32_t w[32];
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) w[u] = __float_as_uint(o[u] * factor);
+                        tmem_st32(tmem + lane_off + kColO + half * 64 + c * 32, w);
+                    }
+                } else {                                    // both halves stop next tile
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem + lane_off + kColO + c * 32, o);
-                    tmem_ld_wait();
-                    uint32_t w[32];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) w[u] = __float_as_uint(o[u] * factor);
-                    tmem_st32(tmem + lane_off + kColO + c * 32, w);
                 }
             }
             l *= factor;
             m_used = m_new;
-            const float me = m_used == -INFINITY ? 0.f : m_used;
-            // P_j (bf16) over the first 64 columns of the score buffer
+            const float nme = m_used == -INFINITY ? 0.f : -m_used;
+            // P_j (bf16) over columns 32*half.. of the score buffer
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t w[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const float p0 = ex2(s[c * 32 + 2 * u] - me);
-                    const float p1 = ex2(s[c * 32 + 2 * u + 1] - me);
-                    l += p0 + p1;
+                    const float p0 = ex2(fmaf(s[c * 32 + 2 * u], p.scale_log2, nme));
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * u + 1], p.scale_log2, nme));
+                    ls[u & 3] += p0 + p1;
                     w[u] = pack_bf16(p0, p1);
                 }
-                tmem_st16(sb + c * 16, w);
+                tmem_st16(tmem + lane_off + kColS + uint32_t(buf) * 128 + half * 32 + c * 16, w);
             }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -327,18 +384,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ---- epilogue: O / l * sigmoid(gate) -> bf16 ----
         bool fin = ok && mbar_wait(ofinal, 0, p.wait_ns);
         fin = __all_sync(0xffffffffu, fin);
-        if (!fin) {
-            if (ok) report(p.status, kStTimeout);
-        } else {
+        if (!fin && ok) report(p.status, kStTimeout);
+        xsum[half * kBM + r] = l;                           // row sum = both halves
+        named_bar_sync(bar_id, 64);
+        const float lt = l + xsum[(half ^ 1) * kBM + r];
+        if (fin) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const size_t orow = (size_t(b) * p.Tq + size_t(row < p.Tq ? row : 0)) * p.H + h;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDv);
-            const uint4* g = p.gate ? reinterpret_cast<const uint4*>(p.gate + orow * kDv) : nullptr;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDv) + half * 8;
+            const uint4* g = p.gate ? reinterpret_cast<const uint4*>(p.gate + orow * kDv) + half * 8
+                                    : nullptr;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float o[32];
-                tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+                tmem_ld32(tmem + lane_off + kColO + half * 64 + c * 32, o);
                 tmem_ld_wait();
                 if (row < p.Tq) {
 #pragma unroll
