@@ -528,7 +528,7 @@ def run_ours(args, world, rank, local):
     if not args.only and not args.batch:
         also = {}
         for other, w in mi.WORKLOADS.items():
-            if other == name or w["kind"] not in WORK_KINDS:
+            if other == name or w["kind"] not in WORK_KINDS or w.get("profile_only"):
                 continue
             wk = WORK_KINDS[w["kind"]](other, dev)
             k_steps = max(3, min(args.steps, 20))

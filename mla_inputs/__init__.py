@@ -168,6 +168,11 @@ WORKLOADS = {
     "dsa_decode_b8_t131072": dict(kind="dsa", config=4, B=8, H=96, T=131072, topk=2048),
     # the indexer part of the DSA workload alone (same index keys, queries, weights)
     "dsa_index_b8_t131072": dict(kind="index", config=4, B=8, H=96, T=131072, topk=2048),
+    # smaller cases of the same kernels, a few GB on the device, for ncu captures
+    "dsa_decode_b2_t16384": dict(kind="dsa", config=4, B=2, H=96, T=16384, topk=2048,
+                                 profile_only=True),
+    "prefill_b1_h8_t16384": dict(kind="prefill", config=3, B=1, H=8, T=16384, gated=True,
+                                 profile_only=True),
 }
 
 
