@@ -423,6 +423,7 @@ def _time_e2e(one, work, dev, world, steps, h2d, d2h):
 
 
 L2_FLUSH_BYTES = 512 << 20   # four times the 129 MB L2
+E2E_HOST_LIMIT = 24 << 30    # pinned host copies of the inputs for the end-to-end leg
 
 
 def time_work(work, steps, warmup, dev, stream, world, sampler=None):
@@ -518,7 +519,14 @@ def run_ours(args, world, rank, local):
             "roofline": roofline(work, kern),
             "gpu_launches": work.launches_per_step * args.steps * world, "clocks": clocks}
     if hasattr(work, "e2e"):
-        line["e2e"] = work.e2e(dev, stream, world, max(3, min(args.steps, args.e2e_steps)))
+        in_bytes = sum(getattr(work.dec, n).numel() * getattr(work.dec, n).element_size()
+                       for n in ("q", "k", "v", "gate"))
+        if in_bytes <= E2E_HOST_LIMIT:
+            line["e2e"] = work.e2e(dev, stream, world, max(3, min(args.steps, args.e2e_steps)))
+        else:
+            line["e2e"] = {"value": None, "unit": work.unit,
+                           "skipped": f"inputs of {in_bytes / 1e9:.0f} GB exceed the "
+                                      f"{E2E_HOST_LIMIT / 1e9:.0f} GB pinned host budget"}
     if rank == 0 and not args.no_cpu_baseline and hasattr(work, "cpu_sample"):
         line["cpu_baseline"] = work.cpu_sample(args.cpu_seconds)
     work.free()

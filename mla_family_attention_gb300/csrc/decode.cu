@@ -42,33 +42,47 @@ namespace {
 
 constexpr int kKRow = kDqk * 2;                 // 384 bytes
 constexpr int kVRow = kDv * 2;                  // 256 bytes
-constexpr int kSP = 64;                         // positions per pipeline stage
+constexpr int kDenseSP = 64;                    // positions per dense pipeline stage
+#ifndef MLA_SPARSE_COPY
+// How sparse decode gathers rows: 0 = 16-byte cp.async pieces; 1 = one bulk
+// (TMA) copy per key row and per value row; 2 = key rows bulk, value rows
+// cp.async; 3 = key rows cp.async, value rows bulk.
+#define MLA_SPARSE_COPY 0
+#endif
+#ifndef MLA_SPARSE_STAGE_POS
+#define MLA_SPARSE_STAGE_POS 64                 // positions per sparse pipeline stage
+#endif
 constexpr int kConsumerWarps = 8;
 // Dense decode: one producer warp (bulk copies).  Sparse decode: four
 // producer warps (16-byte cp.async gathers), completing on the same barrier.
-// Sparse decode keeps five stages in flight (gathered rows take longer to
-// arrive than streamed ones); dense decode four.
+// Dense decode: four stages of 64 streamed positions (160 KB).  Sparse
+// decode: about 200 KB in smaller stages, because gathered rows take longer
+// to arrive and a stage is only complete when its slowest row has landed.
 template <bool kSparse>
 struct Roles {
     static constexpr int kProducerWarps = kSparse ? 4 : 1;
     static constexpr int kThreads = 32 * (kProducerWarps + kConsumerWarps);
     static constexpr int kFullArrivals = kSparse ? 32 * kProducerWarps : 1;
-    static constexpr int kStages = kSparse ? 5 : 4;
+    static constexpr int kSP = kSparse ? MLA_SPARSE_STAGE_POS : kDenseSP;
+    static constexpr int kStages = kSparse ? (200 * 1024) / (kSP * (kDqk + kDv) * 2) : 4;
+    static constexpr int kKStage = kSP * kDqk * 2;
+    static constexpr int kVStage = kSP * kDv * 2;
+    static constexpr int kPPG = kSP / (kConsumerWarps * 4);    // positions per group per stage
 };
 constexpr int kGroups = kConsumerWarps * 4;     // 8-lane groups
-constexpr int kPPG = kSP / kGroups;             // positions per group per stage
-constexpr int kKStage = kSP * kKRow;            // 24 KB
-constexpr int kVStage = kSP * kVRow;            // 16 KB
+
 constexpr int kMergeFloats = kConsumerWarps * (kDv + 2);
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool kSparse>
 constexpr size_t smem_bytes() {
-    return size_t(Roles<kSparse>::kStages) * (kKStage + kVStage) + kMergeFloats * 4 +
-           2 * Roles<kSparse>::kStages * 8 + 16;
+    return size_t(Roles<kSparse>::kStages) * (Roles<kSparse>::kKStage + Roles<kSparse>::kVStage + kKRow) +
+           kMergeFloats * 4 + 2 * Roles<kSparse>::kStages * 8 + 16;
 }
 
-static_assert(kPPG * kGroups == kSP, "stage must split evenly over groups");
+static_assert(Roles<true>::kPPG * kGroups == Roles<true>::kSP &&
+                  Roles<false>::kPPG * kGroups == Roles<false>::kSP,
+              "stage must split evenly over groups");
 
 struct Params {
     const uint16_t* q;
@@ -94,7 +108,10 @@ struct Item {
     int nst;        // pipeline stages in the item
 };
 
-__device__ __forceinline__ int stage_entry(const Item& w, int k) { return w.e0 + k * kSP; }
+template <bool kSparse>
+__device__ __forceinline__ int stage_entry(const Item& w, int k) {
+    return w.e0 + k * Roles<kSparse>::kSP;
+}
 
 // Work item `it` -> (b, h, chunk).  Dense items come from the prefix table
 // item_start, heads fastest: concurrent CTAs stream different heads'
@@ -115,7 +132,7 @@ __device__ __forceinline__ Item item_of(const Params& p, int it) {
         r.T = static_cast<int>(p.cu[r.b + 1] - r.base);
         r.e0 = r.c * p.chunk;
         r.e1 = min(p.topk, r.e0 + p.chunk);
-        r.nst = (r.e1 - r.e0 + kSP - 1) / kSP;
+        r.nst = (r.e1 - r.e0 + Roles<kSparse>::kSP - 1) / Roles<kSparse>::kSP;
     } else {
         int lo = 0, hi = p.B;   // largest b with item_start[b] <= it
         while (hi - lo > 1) {
@@ -130,7 +147,7 @@ __device__ __forceinline__ Item item_of(const Params& p, int it) {
         r.h = rem - r.c * p.H;
         r.e0 = r.c * p.chunk;
         r.e1 = min(r.T, r.e0 + p.chunk);
-        r.nst = (r.e1 - r.e0 + kSP - 1) / kSP;
+        r.nst = (r.e1 - r.e0 + Roles<kSparse>::kSP - 1) / Roles<kSparse>::kSP;
     }
     return r;
 }
@@ -164,8 +181,10 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
     using R = Roles<kSparse>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* ks = smem;                                        // [stages][64][384]
-    uint8_t* vs = smem + R::kStages * kKStage;                    // [stages][64][256]
-    float* red = reinterpret_cast<float*>(vs + R::kStages * kVStage);   // [8][130]
+    uint8_t* vs = smem + R::kStages * R::kKStage;                    // [stages][64][256]
+    uint8_t* qs = vs + R::kStages * R::kVStage;                // [stages][384]: query row of
+                                                               // the item a stage starts
+    float* red = reinterpret_cast<float*>(qs + R::kStages * kKRow);   // [8][130]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + kMergeFloats);
     uint64_t* empty = full + R::kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + R::kStages);
@@ -194,7 +213,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item w = item_of<kSparse>(p, item);
             for (int st = 0; st < w.nst; ++st, ++it) {
-                const int e = stage_entry(w, st);
+                const int e = stage_entry<kSparse>(w, st);
                 const int slot = it % R::kStages;
                 const int round = it / R::kStages;
                 if (*abort_flag) { ok = false; break; }
@@ -205,13 +224,16 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                     break;
                 }
                 if (it == p.stall_stage) continue;   // test hook: withhold this stage
-                const int n = min(kSP, w.e1 - e);
+                const int n = min(R::kSP, w.e1 - e);
                 if (lane == 0) {
                     const int64_t row = w.base * p.H + int64_t(w.h) * w.T + e;
-                    mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow));
-                    bulk_load(ks + slot * kKStage, p.k + row * kDqk, n * kKRow, &full[slot],
+                    mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow) + (st == 0 ? kKRow : 0));
+                    if (st == 0)                      // the item's query row rides along
+                        bulk_load(qs + slot * kKRow, p.q + (int64_t(w.b) * p.H + w.h) * kDqk,
+                                  kKRow, &full[slot], policy);
+                    bulk_load(ks + slot * R::kKStage, p.k + row * kDqk, n * kKRow, &full[slot],
                               policy);
-                    bulk_load(vs + slot * kVStage, p.v + row * kDv, n * kVRow, &full[slot],
+                    bulk_load(vs + slot * R::kVStage, p.v + row * kDv, n * kVRow, &full[slot],
                               policy);
                 }
                 filled[slot] = round + 1;
@@ -232,30 +254,33 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
         // consecutive pieces of a row.  Each thread's copies complete with one
         // arrival on the stage's barrier (expected count 128).
         const int pt = threadIdx.x;
+        const uint64_t policy = l2_evict_first_policy();
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k);
         const uint8_t* vb = reinterpret_cast<const uint8_t*>(p.v);
         int it = 0;
+        int filled[R::kStages];        // stage count of the last fill per slot (+1)
+        for (int i = 0; i < R::kStages; ++i) filled[i] = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item w = item_of<kSparse>(p, item);
             const int64_t rbase = w.base * p.H + int64_t(w.h) * w.T;
             for (int st = 0; st < w.nst; ++st, ++it) {
-                const int e = stage_entry(w, st);
+                const int e = stage_entry<kSparse>(w, st);
                 const int slot = it % R::kStages;
                 const int round = it / R::kStages;
                 if (*abort_flag) { ok = false; break; }
                 // Selections of this stage are loaded before waiting for the
                 // slot, so their latency hides behind the wait.
-                const int n = min(kSP, w.e1 - e);
+                const int n = min(R::kSP, w.e1 - e);
                 const int32_t* ix = p.idx + int64_t(w.b) * p.topk + e;
-                int selk[kSP * 24 / 128], selv[kSP * 16 / 128];
+                int selk[R::kSP * 24 / 128], selv[R::kSP * 16 / 128];
 #pragma unroll
-                for (int i = 0; i < kSP * 24 / 128; ++i) {
+                for (int i = 0; i < R::kSP * 24 / 128; ++i) {
                     const int j = (pt + 128 * i) / 24;
                     selk[i] = j < n ? ix[j] : -1;
                 }
 #pragma unroll
-                for (int i = 0; i < kSP * 16 / 128; ++i) {
+                for (int i = 0; i < R::kSP * 16 / 128; ++i) {
                     const int j = (pt + 128 * i) >> 4;
                     selv[i] = j < n ? ix[j] : -1;
                 }
@@ -266,26 +291,63 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                     break;
                 }
                 if (it == p.stall_stage) continue;   // test hook: withhold this stage
-#pragma unroll
-                for (int i = 0; i < kSP * 24 / 128; ++i) {
-                    const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
-                    if (valid_pos(selk[i], w.T))
-                        cp_async16(ks + slot * kKStage + j * kKRow + off,
-                                   kb + (rbase + selk[i]) * kKRow + off);
-                    else if (selk[i] < -1 || selk[i] >= w.T)
-                        report(p.status, kStBadIndex);
+                constexpr bool kBulkK = MLA_SPARSE_COPY == 1 || MLA_SPARSE_COPY == 2;
+                constexpr bool kBulkV = MLA_SPARSE_COPY == 1 || MLA_SPARSE_COPY == 3;
+                if (kBulkK || kBulkV) {
+                    // thread t < 64 copies key row t, thread 64 + t value row t; each
+                    // adds its bytes to the stage barrier before its own arrival
+                    const int jr = pt & 63;
+                    const bool is_k = pt < 64;
+                    if (jr < n && (is_k ? kBulkK : kBulkV)) {
+                        const int sidx = ix[jr];
+                        if (valid_pos(sidx, w.T)) {
+                            const uint32_t bytes = is_k ? kKRow : kVRow;
+                            mbar_expect_tx(&full[slot], bytes);
+                            if (is_k)
+                                bulk_load(ks + slot * R::kKStage + jr * kKRow,
+                                          kb + (rbase + sidx) * kKRow, bytes, &full[slot], policy);
+                            else
+                                bulk_load(vs + slot * R::kVStage + jr * kVRow,
+                                          vb + (rbase + sidx) * kVRow, bytes, &full[slot], policy);
+                        } else if (is_k && sidx != -1) {
+                            report(p.status, kStBadIndex);
+                        }
+                    }
                 }
+                if (st == 0 && pt < 24)               // the item's query row rides along
+                    cp_async16(qs + slot * kKRow + pt * 16,
+                               reinterpret_cast<const uint8_t*>(p.q) +
+                                   (int64_t(w.b) * p.H + w.h) * kKRow + pt * 16);
+                if (!kBulkK) {
 #pragma unroll
-                for (int i = 0; i < kSP * 16 / 128; ++i) {
-                    const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
-                    if (valid_pos(selv[i], w.T))
-                        cp_async16(vs + slot * kVStage + j * kVRow + off,
-                                   vb + (rbase + selv[i]) * kVRow + off);
+                    for (int i = 0; i < R::kSP * 24 / 128; ++i) {
+                        const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
+                        if (valid_pos(selk[i], w.T))
+                            cp_async16(ks + slot * R::kKStage + j * kKRow + off,
+                                       kb + (rbase + selk[i]) * kKRow + off);
+                        else if (selk[i] < -1 || selk[i] >= w.T)
+                            report(p.status, kStBadIndex);
+                    }
+                }
+                if (!kBulkV) {
+#pragma unroll
+                    for (int i = 0; i < R::kSP * 16 / 128; ++i) {
+                        const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
+                        if (valid_pos(selv[i], w.T))
+                            cp_async16(vs + slot * R::kVStage + j * kVRow + off,
+                                       vb + (rbase + selv[i]) * kVRow + off);
+                    }
                 }
                 cp_async_arrive_noinc(&full[slot]);
+                filled[slot] = round + 1;
             }
         }
         cp_async_wait_all();   // nothing this thread started is still in flight at exit
+        if (MLA_SPARSE_COPY != 0) {   // bulk copies complete on the stage barriers
+            for (int i = 0; i < R::kStages; ++i)
+                if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, p.wait_ns))
+                    report(p.status, kStTimeout);
+        }
         return;
     }
 
@@ -296,36 +358,23 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
     int it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const Item w = item_of<kSparse>(p, item);
-        // query slices of this lane: features 8j.., 64+8j.., 128+8j..
+        // query slices of this lane (features 8j.., 64+8j.., 128+8j..), read
+        // from the first stage of the item once it has landed
         float qf[24];
-        {
-            const uint4* qp =
-                reinterpret_cast<const uint4*>(p.q + (int64_t(w.b) * p.H + w.h) * kDqk);
-#pragma unroll
-            for (int c = 0; c < 3; ++c) {
-                const uint4 u = __ldg(qp + c * 8 + j);
-                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    qf[c * 8 + 2 * t] = bf_lo(wd[t]) * p.scale_log2;
-                    qf[c * 8 + 2 * t + 1] = bf_hi(wd[t]) * p.scale_log2;
-                }
-            }
-        }
         float m = -INFINITY, l = 0.f, acc[16];
 #pragma unroll
         for (int d = 0; d < 16; ++d) acc[d] = 0.f;
 
         for (int st = 0; st < w.nst; ++st, ++it) {
-            const int e = stage_entry(w, st);
+            const int e = stage_entry<kSparse>(w, st);
             const int slot = it % R::kStages;
             const int round = it / R::kStages;
             // Which of this group's positions hold data: known before the
             // wait (sparse: the selection is read while the copies land).
-            const int n = min(kSP, w.e1 - e);
-            bool ok[kPPG];
+            const int n = min(R::kSP, w.e1 - e);
+            bool ok[R::kPPG];
 #pragma unroll
-            for (int r = 0; r < kPPG; ++r) {
+            for (int r = 0; r < R::kPPG; ++r) {
                 const int pos = g + kGroups * r;
                 ok[r] = pos < n;
                 if (kSparse && ok[r])
@@ -338,12 +387,25 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 have = false;
             }
             have = __all_sync(0xffffffffu, have);
-            if (have) {
-                const uint8_t* kst = ks + slot * kKStage;
-                const uint8_t* vst = vs + slot * kVStage;
-                float s[kPPG];
+            if (have && st == 0) {
+                const uint4* qp = reinterpret_cast<const uint4*>(qs + slot * kKRow);
 #pragma unroll
-                for (int r = 0; r < kPPG; ++r) {
+                for (int c = 0; c < 3; ++c) {
+                    const uint4 u = qp[c * 8 + j];
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        qf[c * 8 + 2 * t] = bf_lo(wd[t]) * p.scale_log2;
+                        qf[c * 8 + 2 * t + 1] = bf_hi(wd[t]) * p.scale_log2;
+                    }
+                }
+            }
+            if (have) {
+                const uint8_t* kst = ks + slot * R::kKStage;
+                const uint8_t* vst = vs + slot * R::kVStage;
+                float s[R::kPPG];
+#pragma unroll
+                for (int r = 0; r < R::kPPG; ++r) {
                     const int pos = g + kGroups * r;
                     float dot = 0.f;
                     if (ok[r]) {
@@ -367,14 +429,14 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 }
                 float mn = m;
 #pragma unroll
-                for (int r = 0; r < kPPG; ++r) mn = fmaxf(mn, s[r]);
+                for (int r = 0; r < R::kPPG; ++r) mn = fmaxf(mn, s[r]);
                 if (mn != -INFINITY) {
                     const float alpha = ex2(m - mn);    // m = -inf -> 0
                     l *= alpha;
 #pragma unroll
                     for (int d = 0; d < 16; ++d) acc[d] *= alpha;
 #pragma unroll
-                    for (int r = 0; r < kPPG; ++r) {
+                    for (int r = 0; r < R::kPPG; ++r) {
                         if (ok[r]) {
                             const float pr = ex2(s[r] - mn);
                             l += pr;
@@ -557,7 +619,7 @@ DecodePlan plan_decode(int B, int H, int max_len, bool sparse, int sparse_chunk)
     DecodePlan pl{};
     int chunk = 1024;
     auto items = [&](int c) { return int64_t(B) * H * ((int64_t(max_len) + c - 1) / c); };
-    while (chunk > kSP && items(chunk) < 2432) chunk >>= 1;
+    while (chunk > kDenseSP && items(chunk) < 2432) chunk >>= 1;
     if (sparse) chunk = sparse_chunk > 0 ? sparse_chunk : 256;
     pl.chunk = chunk;
     pl.max_chunks = int((int64_t(max_len) + chunk - 1) / chunk);
