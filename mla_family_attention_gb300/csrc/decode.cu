@@ -43,12 +43,6 @@ namespace {
 constexpr int kKRow = kDqk * 2;                 // 384 bytes
 constexpr int kVRow = kDv * 2;                  // 256 bytes
 constexpr int kDenseSP = 64;                    // positions per dense pipeline stage
-#ifndef MLA_SPARSE_COPY
-// How sparse decode gathers rows: 0 = 16-byte cp.async pieces; 1 = one bulk
-// (TMA) copy per key row and per value row; 2 = key rows bulk, value rows
-// cp.async; 3 = key rows cp.async, value rows bulk.
-#define MLA_SPARSE_COPY 0
-#endif
 #ifndef MLA_SPARSE_STAGE_POS
 #define MLA_SPARSE_STAGE_POS 64                 // positions per sparse pipeline stage
 #endif
@@ -254,12 +248,9 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
         // consecutive pieces of a row.  Each thread's copies complete with one
         // arrival on the stage's barrier (expected count 128).
         const int pt = threadIdx.x;
-        const uint64_t policy = l2_evict_first_policy();
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k);
         const uint8_t* vb = reinterpret_cast<const uint8_t*>(p.v);
         int it = 0;
-        int filled[R::kStages];        // stage count of the last fill per slot (+1)
-        for (int i = 0; i < R::kStages; ++i) filled[i] = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item w = item_of<kSparse>(p, item);
@@ -291,63 +282,30 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                     break;
                 }
                 if (it == p.stall_stage) continue;   // test hook: withhold this stage
-                constexpr bool kBulkK = MLA_SPARSE_COPY == 1 || MLA_SPARSE_COPY == 2;
-                constexpr bool kBulkV = MLA_SPARSE_COPY == 1 || MLA_SPARSE_COPY == 3;
-                if (kBulkK || kBulkV) {
-                    // thread t < 64 copies key row t, thread 64 + t value row t; each
-                    // adds its bytes to the stage barrier before its own arrival
-                    const int jr = pt & 63;
-                    const bool is_k = pt < 64;
-                    if (jr < n && (is_k ? kBulkK : kBulkV)) {
-                        const int sidx = ix[jr];
-                        if (valid_pos(sidx, w.T)) {
-                            const uint32_t bytes = is_k ? kKRow : kVRow;
-                            mbar_expect_tx(&full[slot], bytes);
-                            if (is_k)
-                                bulk_load(ks + slot * R::kKStage + jr * kKRow,
-                                          kb + (rbase + sidx) * kKRow, bytes, &full[slot], policy);
-                            else
-                                bulk_load(vs + slot * R::kVStage + jr * kVRow,
-                                          vb + (rbase + sidx) * kVRow, bytes, &full[slot], policy);
-                        } else if (is_k && sidx != -1) {
-                            report(p.status, kStBadIndex);
-                        }
-                    }
-                }
                 if (st == 0 && pt < 24)               // the item's query row rides along
                     cp_async16(qs + slot * kKRow + pt * 16,
                                reinterpret_cast<const uint8_t*>(p.q) +
                                    (int64_t(w.b) * p.H + w.h) * kKRow + pt * 16);
-                if (!kBulkK) {
 #pragma unroll
-                    for (int i = 0; i < R::kSP * 24 / 128; ++i) {
-                        const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
-                        if (valid_pos(selk[i], w.T))
-                            cp_async16(ks + slot * R::kKStage + j * kKRow + off,
-                                       kb + (rbase + selk[i]) * kKRow + off);
-                        else if (selk[i] < -1 || selk[i] >= w.T)
-                            report(p.status, kStBadIndex);
-                    }
+                for (int i = 0; i < R::kSP * 24 / 128; ++i) {
+                    const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
+                    if (valid_pos(selk[i], w.T))
+                        cp_async16(ks + slot * R::kKStage + j * kKRow + off,
+                                   kb + (rbase + selk[i]) * kKRow + off);
+                    else if (selk[i] < -1 || selk[i] >= w.T)
+                        report(p.status, kStBadIndex);
                 }
-                if (!kBulkV) {
 #pragma unroll
-                    for (int i = 0; i < R::kSP * 16 / 128; ++i) {
-                        const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
-                        if (valid_pos(selv[i], w.T))
-                            cp_async16(vs + slot * R::kVStage + j * kVRow + off,
-                                       vb + (rbase + selv[i]) * kVRow + off);
-                    }
+                for (int i = 0; i < R::kSP * 16 / 128; ++i) {
+                    const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
+                    if (valid_pos(selv[i], w.T))
+                        cp_async16(vs + slot * R::kVStage + j * kVRow + off,
+                                   vb + (rbase + selv[i]) * kVRow + off);
                 }
                 cp_async_arrive_noinc(&full[slot]);
-                filled[slot] = round + 1;
             }
         }
         cp_async_wait_all();   // nothing this thread started is still in flight at exit
-        if (MLA_SPARSE_COPY != 0) {   // bulk copies complete on the stage barriers
-            for (int i = 0; i < R::kStages; ++i)
-                if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, p.wait_ns))
-                    report(p.status, kStTimeout);
-        }
         return;
     }
 
