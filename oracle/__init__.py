@@ -186,3 +186,74 @@ def dsa_sparse_decode(q, k, v, cu_seqlens, idx, gate, scale: float, lib=None) ->
                                                  topk, B, H, Dqk, Dv, _p(g), _p(out),
                                                  float(scale)), "sparse decode")
     return out
+
+
+# ---------------------------------------------------------------------------
+# KV-cache update and the attention calls that follow it.  The pages' cache
+# grows by concatenation on the sequence axis (Kimi K2 "KV cache" page, the
+# update step: the new keys and values are appended after the cached ones and
+# the full cache is returned for attention).  The library keeps a cache of
+# fixed capacity instead; these functions state what such a cache holds after
+# an append, then run the attention definitions above on the concatenated keys.
+# ---------------------------------------------------------------------------
+def _host(x) -> np.ndarray:
+    """Any torch tensor (bf16 as raw 16-bit patterns) or array -> numpy array."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().to("cpu")
+        if x.dtype == torch.bfloat16:
+            x = x.view(torch.int16)
+        x = x.numpy()
+    return np.asarray(x)
+
+
+def cache_append(k_cache, v_cache, k_new, v_new, start):
+    """Caches [B,H,cap,D] after writing the Tn new rows of every (b, h) at
+    positions start_b .. start_b+Tn-1: for each b, the prefix before start_b,
+    then the new rows, then whatever followed them before.  Works on the raw
+    element patterns, so the result is exact for any dtype.  `start` is an int
+    or a length-B sequence."""
+    kc, vc, kn, vn = (_host(x) for x in (k_cache, v_cache, k_new, v_new))
+    B, Tn = kc.shape[0], kn.shape[2]
+    starts = [int(start)] * B if np.ndim(_host(start)) == 0 else [int(s) for s in _host(start)]
+    k_out, v_out = [], []
+    for b in range(B):
+        s = starts[b]
+        if s < 0 or s + Tn > kc.shape[2]:
+            raise ValueError("append past the cache capacity")
+        k_out.append(np.concatenate([kc[b, :, :s], kn[b], kc[b, :, s + Tn:]], axis=1))
+        v_out.append(np.concatenate([vc[b, :, :s], vn[b], vc[b, :, s + Tn:]], axis=1))
+    return np.stack(k_out), np.stack(v_out)
+
+
+def mla_prefill_chunk(q, k_cache, v_cache, k_new, v_new, P: int, gate, scale: float,
+                      lib=None) -> np.ndarray:
+    """Chunked prefill: Tq new tokens after P cached ones.  The key set is the
+    first P cached positions followed by the new keys (the concatenation), and
+    the queries attend causally with bottom-right alignment (query i sits at
+    absolute position P+i).  Returns out [B,Tq,H*Dv] in float64."""
+    kc, vc = _f64(k_cache), _f64(v_cache)
+    k = np.concatenate([kc[:, :, :P], _f64(k_new)], axis=2)
+    v = np.concatenate([vc[:, :, :P], _f64(v_new)], axis=2)
+    return mla_prefill(q, k, v, gate, scale, lib=lib)
+
+
+def mla_decode_cached(q, k_cache, v_cache, lengths, k_new, v_new, gate, scale: float,
+                      lib=None) -> np.ndarray:
+    """Decode over fixed-capacity caches: sequence b's keys are its first
+    lengths[b] cached positions, followed by the current token's key when
+    k_new is given.  Packs them back to back and runs the decode definition."""
+    kc, vc = _f64(k_cache), _f64(v_cache)
+    kn, vn = _f64(k_new), _f64(v_new)
+    lens = [int(x) for x in _i64(lengths)]
+    ks, vs, cu = [], [], [0]
+    for b, L in enumerate(lens):
+        kb, vb = kc[b, :, :L], vc[b, :, :L]
+        if kn is not None:
+            kb = np.concatenate([kb, kn[b]], axis=1)
+            vb = np.concatenate([vb, vn[b]], axis=1)
+        ks.append(kb.reshape(-1))
+        vs.append(vb.reshape(-1))
+        cu.append(cu[-1] + kb.shape[1])
+    return mla_decode(q, np.concatenate(ks), np.concatenate(vs), np.array(cu, dtype=np.int64),
+                      gate, scale, lib=lib)
