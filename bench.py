@@ -231,6 +231,8 @@ def workload_config(name, B=None):
         cfg["T"] = w["T"]
     if "lo" in w:
         cfg["T_range"] = [w["lo"], w["hi"]]
+    if "chunk" in w:
+        cfg["chunk"] = w["chunk"]
     small = w["kind"] == "prefill" and w["T"] <= 1024
     cfg["l2"] = ("inputs smaller than L2: a 512 MB buffer is written between timed steps"
                  if small else "inputs larger than L2 (no flush needed)")
@@ -404,8 +406,88 @@ class PrefillWork:
         del self.pf, self.out
 
 
+class ChunkedPrefillWork:
+    """A prompt fed through mla_prefill_chunk in equal chunks (the cache-update
+    path): per chunk, an in-place append of its keys and values into a
+    fixed-capacity cache, then causal gated prefill over the cache."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        B, H, T, c = w["B"], w["H"], w["T"], w["chunk"]
+        self.name, self.H, self.B, self.T, self.c = name, H, B, T, c
+        self.lengths = [T] * B
+        pf = mi.make_prefill(B, H, T, T, w["gated"], device=dev, config=w["config"])
+        n = T // c
+        sl = [slice(i * c, (i + 1) * c) for i in range(n)]
+        self.q = [pf.q[:, :, s].contiguous() for s in sl]
+        self.kn = [pf.k[:, :, s].contiguous() for s in sl]
+        self.vn = [pf.v[:, :, s].contiguous() for s in sl]
+        self.g = [pf.gate[:, s].contiguous() if w["gated"] else None for s in sl]
+        self.scale = pf.scale
+        del pf
+        self.kc = mi.nan_filled((B, H, T, 192), dev)
+        self.vc = mi.nan_filled((B, H, T, 128), dev)
+        self.out = [torch.empty((B, c, H * 128), dtype=torch.bfloat16, device=dev)
+                    for _ in range(n)]
+        self.work = sum(acc.prefill_flops(B, H, c, (i + 1) * c) for i in range(n))
+        assert self.work == acc.prefill_flops(B, H, T, T)
+        self.unit, self.bound, self.scale_unit = "TFLOP/s", "tensor", 1e12
+        self.launches_per_step = 2 * n
+        self.kernels = [(_lib.OP_PREFILL, "mla_prefill_kernel", self.work // n),
+                        (_lib.OP_CACHE_APPEND, "cache_append_kernel",
+                         acc.append_bytes(B, H, c), "hbm")]
+
+    def step(self, stream):
+        for i in range(len(self.q)):
+            self.mla.mla_prefill_chunk(self.q[i], self.kn[i], self.vn[i], self.kc, self.vc,
+                                       i * self.c, gate=self.g[i], out=self.out[i],
+                                       scale=self.scale, stream=stream)
+
+    def free(self):
+        del self.q, self.kn, self.vn, self.g, self.kc, self.vc, self.out
+
+
+class DecodeCachedWork:
+    """A decode step over fixed-capacity caches: the current token appended
+    at position T-1 of every sequence, then split-KV gated decode over T."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        B = batch or w["B"]
+        H, T = w["H"], w["T"]
+        self.name, self.H, self.B, self.T = name, H, B, T
+        self.lengths = [T] * B
+        self.cd = mi.make_capacity_decode([T - 1] * B, H, T, w["gated"], device=dev,
+                                          config=w["config"])
+        self.seqlens = torch.full((B,), T - 1, dtype=torch.int64, device=dev)
+        self.out = torch.empty((B, H * 128), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(mla.workspace_size(_lib.OP_DECODE, B, H, T, 0), dtype=torch.uint8,
+                              device=dev)
+        self.work = acc.decode_kv_bytes(self.lengths, H)
+        self.unit, self.bound = "GB/s", "hbm"
+        self.launches_per_step = 4      # append, item prefix, partial, merge
+        self.kernels = [(_lib.OP_DECODE, "decode_partial_kernel", self.work),
+                        (_lib.OP_CACHE_APPEND, "cache_append_kernel", acc.append_bytes(B, H, 1))]
+
+    def step(self, stream):
+        cd = self.cd
+        self.mla.mla_decode_cached(cd.q, cd.k_cache, cd.v_cache, self.seqlens, self.T,
+                                   k_new=cd.k_new, v_new=cd.v_new, gate=cd.gate, out=self.out,
+                                   scale=cd.scale, ws=self.ws, stream=stream)
+
+    def free(self):
+        del self.cd, self.seqlens, self.out, self.ws
+
+
 WORK_KINDS = {"decode": DecodeWork, "dsa": DsaWork, "index": IndexWork,
-              "prefill": PrefillWork}
+              "prefill": PrefillWork, "chunked_prefill": ChunkedPrefillWork,
+              "decode_cached": DecodeCachedWork}
 
 
 def _time_e2e(one, work, dev, world, steps, h2d, d2h):
@@ -439,8 +521,8 @@ def time_work(work, steps, warmup, dev, stream, world, sampler=None):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) \
         if getattr(work, "flush_l2", False) else None
     mla.timing_enable(True)
-    for op, _, _ in work.kernels:
-        mla.timing_read(op)
+    for kd in work.kernels:
+        mla.timing_read(kd[0])
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps if flush is not None else 1)]
     barrier(world)
@@ -466,9 +548,11 @@ def time_work(work, steps, warmup, dev, stream, world, sampler=None):
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world)
     del flush
     kern = []
-    for op, kname, units in work.kernels:
+    for kd in work.kernels:
+        op, kname, units = kd[:3]
         k_ms, n = mla.timing_read(op)
-        kern.append((kname, max_over_ranks(k_ms / max(n, 1), world), units))
+        kern.append((kname, max_over_ranks(k_ms / max(n, 1), world), units,
+                     kd[3] if len(kd) > 3 else work.bound))
     mla.check_device_status(stream)
     return ms, kern
 
@@ -481,7 +565,7 @@ def roofline(work, kern):
     """Roofline object for the dominant (longest) kernel of a step."""
     peak, unit, peak_kind = peaks(work.bound)
     sc = _scale(work)
-    kname, k_ms, units = max(kern, key=lambda x: x[1])
+    kname, k_ms, units, _ = max((k for k in kern if k[3] == work.bound), key=lambda x: x[1])
     achieved = units / (k_ms * 1e-3) / sc
     nominal = 2250.0 if work.bound == "tensor" else 7900.0
     per = "flops" if work.bound == "tensor" else "bytes"
@@ -491,11 +575,13 @@ def roofline(work, kern):
          "kernel_ms": round(k_ms, 4), "traffic": traffic_for(kname),
          f"algorithmic_{per}_per_launch": units}
     others = {}
-    for kn, km, ku in kern:
+    for kn, km, ku, kb in kern:
         if kn != kname:
-            a = ku / (km * 1e-3) / sc
-            others[kn] = {"achieved": round(a, 2), "frac": round(a / peak, 4),
-                          "kernel_ms": round(km, 4), f"algorithmic_{per}_per_launch": ku}
+            pk, pu, _ = peaks(kb)
+            a = ku / (km * 1e-3) / (1e12 if kb == "tensor" else 1e9)
+            others[kn] = {"bound": kb, "achieved": round(a, 2), "unit": pu,
+                          "frac": round(a / pk, 4), "kernel_ms": round(km, 4),
+                          f"algorithmic_{'flops' if kb == 'tensor' else 'bytes'}_per_launch": ku}
     if others:
         r["other_kernels"] = others
     return r

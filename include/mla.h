@@ -60,7 +60,13 @@ typedef enum {
 } mla_status;
 
 /* Operation ids for mla_workspace_size. */
-enum { MLA_OP_PREFILL = 0, MLA_OP_DECODE = 1, MLA_OP_INDEX_TOPK = 2, MLA_OP_SPARSE_DECODE = 3 };
+enum {
+    MLA_OP_PREFILL = 0,
+    MLA_OP_DECODE = 1,
+    MLA_OP_INDEX_TOPK = 2,
+    MLA_OP_SPARSE_DECODE = 3,
+    MLA_OP_CACHE_APPEND = 4
+};
 
 /*
  * Causal gated MLA prefill (Kimi K3 MLA forward; Kimi K2 score line
@@ -132,6 +138,76 @@ mla_status mla_decode_noalloc(const mla_bf16* q, const mla_bf16* k, const mla_bf
                               mla_stream stream);
 
 /*
+ * In-place KV-cache append (the Kimi K2 "KV cache" update: new keys and
+ * values concatenated after the cached ones on the sequence axis, here
+ * written into a cache preallocated with a fixed capacity).
+ *
+ *   k_new   [B,H,Tn,192]        keys of the Tn new tokens
+ *   v_new   [B,H,Tn,128]        their values
+ *   k_cache [B,H,kv_capacity,192]  written in place:
+ *           k_cache[b,h,s_b+t,:] = k_new[b,h,t,:] for t < Tn
+ *   v_cache [B,H,kv_capacity,128]  likewise
+ *   start   [B] int64 on the device (s_b = start[b], per-sequence lengths of
+ *           a ragged batch), or NULL to use s_b = start_all for every b
+ *
+ * Other cache positions are not touched.  Requires B, H, Tn >= 1,
+ * Tn*40 < 2^31, 0 <= start_all and start_all + Tn <= kv_capacity when start
+ * is NULL; a sequence whose device start breaks that bound is skipped and
+ * the device status records MLA_ERR_INVALID_ARG.  The new rows must not
+ * overlap the cache.  No workspace.
+ */
+mla_status mla_cache_append(const mla_bf16* k_new, const mla_bf16* v_new, mla_bf16* k_cache,
+                            mla_bf16* v_cache, const int64_t* start, int64_t start_all, int B,
+                            int H, int Tn, int kv_capacity, mla_stream stream);
+
+/*
+ * Chunked prefill: Tq new tokens after P cached ones (Kimi K3 MLA forward with
+ * a non-empty cache).  Appends k_new/v_new at positions P..P+Tq-1 of the
+ * fixed-capacity caches (as mla_cache_append with start_all = P), then runs
+ * causal gated attention of the Tq queries over cache positions 0..P+Tq-1:
+ * query i (absolute position P+i) sees keys j <= P+i.
+ *
+ *   q       [B,H,Tq,192]     k_new [B,H,Tq,192]    v_new [B,H,Tq,128]
+ *   k_cache [B,H,kv_capacity,192]   v_cache [B,H,kv_capacity,128]
+ *   gate    [B,Tq,H*128] or NULL     out [B,Tq,H*128]
+ *
+ * Feeding a prompt in chunks (P = 0, c, 2c, ...) gives the same rows as one
+ * mla_prefill over the whole prompt.  Cache positions at or past P+Tq are
+ * never read, so the unused capacity may hold anything.  Requires
+ * 0 <= P, 1 <= Tq, P+Tq <= kv_capacity.  No workspace.
+ */
+mla_status mla_prefill_chunk(const mla_bf16* q, const mla_bf16* k_new, const mla_bf16* v_new,
+                             mla_bf16* k_cache, mla_bf16* v_cache, const mla_bf16* gate,
+                             mla_bf16* out, int B, int H, int Tq, int P, int kv_capacity,
+                             float scale, void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
+ * Decode step over fixed-capacity caches [B,H,kv_capacity,D] with a ragged
+ * batch (sequence b holds cache_seqlens[b] positions).
+ *
+ *   q             [B,H,192]
+ *   k_new, v_new  [B,H,1,192] / [B,H,1,128] of the current token, or both
+ *                 NULL.  When given they are first appended at position
+ *                 cache_seqlens[b] (as mla_cache_append) and the query sees
+ *                 T_b = cache_seqlens[b] + 1 positions; when NULL it sees
+ *                 T_b = cache_seqlens[b] (the token is already cached).
+ *   k_cache, v_cache  [B,H,kv_capacity,192] / [B,H,kv_capacity,128]
+ *   cache_seqlens [B] int64 on the device; not modified (the caller
+ *                 advances it after the step)
+ *   gate, out     as in mla_decode
+ *
+ * Same arithmetic, work split and results as mla_decode on the equivalent
+ * packed cache.  Requires 1 <= T_b <= max_seqlen <= kv_capacity; a sequence
+ * outside that is skipped with MLA_ERR_INVALID_ARG in the device status.
+ * Workspace: mla_workspace_size(MLA_OP_DECODE, B, H, max_seqlen, 0).
+ */
+mla_status mla_decode_cached(const mla_bf16* q, const mla_bf16* k_new, const mla_bf16* v_new,
+                             mla_bf16* k_cache, mla_bf16* v_cache, const int64_t* cache_seqlens,
+                             int B, int H, int kv_capacity, int max_seqlen, const mla_bf16* gate,
+                             mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                             mla_stream stream);
+
+/*
  * DSA indexer score and top-k (DSA post eqs. (5) and (6)).
  *
  *   index_q     [B,NH,128]  index queries (NH must be 32)
@@ -178,8 +254,8 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
 /*
  * Bytes of workspace an operation needs (a multiple of 256; 0 if none).
  * `op` is one of MLA_OP_*; arguments an operation does not use are ignored
- * (prefill: none needed; decode: B, H, max_seqlen; index_topk: B,
- * max_seqlen; sparse_decode: B, H, topk).  Returns 0 for invalid arguments.
+ * (prefill and cache_append: none needed; decode: B, H, max_seqlen;
+ * index_topk: B, max_seqlen; sparse_decode: B, H, topk).  Returns 0 for invalid arguments.
  */
 size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk);
 
@@ -217,7 +293,8 @@ mla_status mla_debug_set(int knob, long long value);
  * call records a CUDA event pair on its stream around its dominant kernel
  * (decode: the split-KV partial kernel; sparse decode: the same kernel in
  * gather mode; index_topk: the scoring kernel; prefill: the attention
- * kernel).  mla_timing_read synchronises those events, returns the summed
+ * kernel; cache_append: the copy kernel, also when a chunked prefill or a
+ * cached decode step appends).  mla_timing_read synchronises those events, returns the summed
  * kernel time in milliseconds and the number of launches of operation `op`
  * (MLA_OP_*) since the last read, and resets the count.  Events are created
  * on first use and reused; no device memory is allocated.

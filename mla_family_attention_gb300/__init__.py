@@ -13,6 +13,10 @@ Entry points (names as in the C ABI):
 * ``mla_decode(q, k, v, cu_seqlens, ...)``  split-KV gated MLA decode
 * ``dsa_index_topk(index_q, index_k, w, cu_seqlens, ...)``  DSA indexer + top-k
 * ``dsa_sparse_decode(q, k, v, cu_seqlens, topk_idx, ...)`` gated MLA over a selection
+* ``mla_cache_append(k_new, v_new, k_cache, v_cache, start)``  in-place cache append
+* ``mla_prefill_chunk(q, k_new, v_new, k_cache, v_cache, P)``  append + causal prefill
+* ``mla_decode_cached(q, k_cache, v_cache, cache_seqlens, ...)`` decode step over
+  fixed-capacity caches (optionally appending the current token first)
 """
 from __future__ import annotations
 
@@ -191,6 +195,99 @@ def dsa_sparse_decode(q, k, v, cu_seqlens, topk_idx, gate=None, out=None, scale=
     lib = _lib.load()
     _lib.check(lib.dsa_sparse_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(topk_idx),
                                      topk, B, H, _ptr(gate), _ptr(out),
+                                     float(default_scale() if scale is None else scale),
+                                     _ptr(ws), wsb, _stream(stream)), lib)
+    return out
+
+
+def _check_capacity_cache(k_cache, v_cache, device):
+    torch = _torch()
+    _need(k_cache, "k_cache", torch.bfloat16, None, device)
+    if k_cache.dim() != 4 or k_cache.shape[3] != DQK:
+        raise ValueError("k_cache must be [B,H,capacity,192]")
+    B, H, cap, _ = k_cache.shape
+    _need(v_cache, "v_cache", torch.bfloat16, (B, H, cap, DV), device)
+    return B, H, cap
+
+
+def mla_cache_append(k_new, v_new, k_cache, v_cache, start, stream=None):
+    """Copy k_new [B,H,Tn,192] / v_new [B,H,Tn,128] into positions start_b..start_b+Tn-1
+    of the caches [B,H,capacity,D].  `start` is an int (every sequence) or a device
+    int64 tensor [B] (per sequence)."""
+    torch = _torch()
+    B, H, cap = _check_capacity_cache(k_cache, v_cache, k_cache.device)
+    _need(k_new, "k_new", torch.bfloat16, None, k_cache.device)
+    if k_new.dim() != 4 or tuple(k_new.shape[:2]) != (B, H) or k_new.shape[3] != DQK:
+        raise ValueError(f"k_new must be [{B},{H},Tn,192]")
+    Tn = k_new.shape[2]
+    _need(v_new, "v_new", torch.bfloat16, (B, H, Tn, DV), k_cache.device)
+    if isinstance(start, torch.Tensor):
+        _need(start, "start", torch.int64, (B,), k_cache.device)
+        sp, s_all = _ptr(start), 0
+    else:
+        sp, s_all = None, int(start)
+    lib = _lib.load()
+    _lib.check(lib.mla_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), sp,
+                                    s_all, B, H, Tn, cap, _stream(stream)), lib)
+
+
+def mla_prefill_chunk(q, k_new, v_new, k_cache, v_cache, P: int, gate=None, out=None,
+                      scale=None, stream=None):
+    """Chunked prefill: append the Tq new keys/values at positions P.. of the caches,
+    then causal gated attention of q [B,H,Tq,192] over cache positions 0..P+Tq-1."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4 or q.shape[3] != DQK:
+        raise ValueError("q must be [B,H,Tq,192]")
+    B, H, Tq, _ = q.shape
+    if _check_capacity_cache(k_cache, v_cache, q.device)[:2] != (B, H):
+        raise ValueError("k_cache and q disagree on B or H")
+    cap = k_cache.shape[2]
+    _need(k_new, "k_new", torch.bfloat16, (B, H, Tq, DQK), q.device)
+    _need(v_new, "v_new", torch.bfloat16, (B, H, Tq, DV), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, Tq, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, Tq, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, Tq, H * DV), q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_prefill_chunk(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(gate), _ptr(out), B, H, Tq, int(P), cap,
+                                     float(default_scale() if scale is None else scale), None, 0,
+                                     _stream(stream)), lib)
+    return out
+
+
+def mla_decode_cached(q, k_cache, v_cache, cache_seqlens, max_seqlen: int, k_new=None,
+                      v_new=None, gate=None, out=None, scale=None, ws=None, stream=None):
+    """Decode step over fixed-capacity caches [B,H,capacity,D]: sequence b holds
+    cache_seqlens[b] positions (device int64 [B]).  With k_new/v_new ([B,H,1,D]) the
+    current token is appended at position cache_seqlens[b] first and attended to."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [B,H,192]")
+    B, H, _ = q.shape
+    if _check_capacity_cache(k_cache, v_cache, q.device)[:2] != (B, H):
+        raise ValueError("k_cache and q disagree on B or H")
+    cap = k_cache.shape[2]
+    _need(cache_seqlens, "cache_seqlens", torch.int64, (B,), q.device)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new or neither")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, (B, H, 1, DQK), q.device)
+        _need(v_new, "v_new", torch.bfloat16, (B, H, 1, DV), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_DECODE, B, H, int(max_seqlen), 0)
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_decode_cached(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(cache_seqlens), B, H, cap,
+                                     int(max_seqlen), _ptr(gate), _ptr(out),
                                      float(default_scale() if scale is None else scale),
                                      _ptr(ws), wsb, _stream(stream)), lib)
     return out

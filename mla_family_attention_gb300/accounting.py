@@ -41,6 +41,11 @@ def prefill_flops(B: int, H: int, Tq: int, Tk: int) -> int:
     return B * H * causal_pairs(Tq, Tk) * 2 * (DQK + DV)
 
 
+def append_bytes(B: int, H: int, Tn: int) -> int:
+    """HBM bytes of appending Tn positions to every (b, h): read once, written once."""
+    return 2 * B * Tn * kv_bytes_per_position(H)
+
+
 def index_key_bytes(lengths) -> int:
     return sum(int(t) for t in lengths) * INDEX_DIM * BF16
 

@@ -79,12 +79,13 @@ struct TimerPool {
     std::vector<mla::KernelTimer> ev;
     size_t used = 0;
 };
-TimerPool g_pool[4];
+constexpr int kOps = 5;   // MLA_OP_PREFILL .. MLA_OP_CACHE_APPEND
+TimerPool g_pool[kOps];
 
 // Next event pair for `op` when timing is on, else an empty timer.
 mla::KernelTimer take_timer(int op) {
     mla::KernelTimer t;
-    if (!g_timing.load() || op < 0 || op > 3) return t;
+    if (!g_timing.load() || op < 0 || op >= kOps) return t;
     std::lock_guard<std::mutex> lk(g_tm_mu);
     TimerPool& p = g_pool[op];
     if (p.used == p.ev.size()) {
@@ -155,6 +156,7 @@ mla_status mla_debug_set(int knob, long long value) {
 size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
     switch (op) {
         case MLA_OP_PREFILL:
+        case MLA_OP_CACHE_APPEND:
             return 0;
         case MLA_OP_DECODE:
             if (B < 1 || H < 1 || max_seqlen < 1) return 0;
@@ -176,7 +178,7 @@ mla_status mla_timing_enable(int on) {
 }
 
 mla_status mla_timing_read(int op, double* total_ms, long long* launches) {
-    REQUIRE(op >= 0 && op <= 3 && total_ms && launches, MLA_ERR_INVALID_ARG,
+    REQUIRE(op >= 0 && op < kOps && total_ms && launches, MLA_ERR_INVALID_ARG,
             "mla_timing_read: bad op or null output");
     std::lock_guard<std::mutex> lk(g_tm_mu);
     TimerPool& p = g_pool[op];
@@ -229,7 +231,7 @@ mla_status mla_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
     if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
     mla::DeviceInfo d;
     if ((s = device_info(&d)) != MLA_OK) return s;
-    mla::DecodeArgs a{q, k, v, cu_seqlens, nullptr, gate, out, B, H, max_seqlen, 0, scale,
+    mla::DecodeArgs a{q, k, v, mla::SeqLayout{cu_seqlens}, nullptr, gate, out, B, H, max_seqlen, 0, scale,
                       ws, ws_bytes};
     cudaError_t e = mla::launch_decode(a, pl, false, d, knobs(), take_timer(MLA_OP_DECODE),
                                        static_cast<cudaStream_t>(stream));
@@ -251,7 +253,7 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
     if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
     mla::DeviceInfo d;
     if ((s = device_info(&d)) != MLA_OK) return s;
-    mla::DecodeArgs a{q, k, v, cu_seqlens, topk_idx, gate, out, B, H, 1 << 30, topk, scale,
+    mla::DecodeArgs a{q, k, v, mla::SeqLayout{cu_seqlens}, topk_idx, gate, out, B, H, 1 << 30, topk, scale,
                       ws, ws_bytes};
     cudaError_t e = mla::launch_decode(a, pl, true, d, knobs(), take_timer(MLA_OP_SPARSE_DECODE),
                                        static_cast<cudaStream_t>(stream));
@@ -276,10 +278,110 @@ mla_status mla_prefill(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
     mla::DeviceInfo d;
     mla_status s = device_info(&d);
     if (s != MLA_OK) return s;
-    mla::PrefillArgs a{q, k, v, gate, out, B, H, Tq, Tk, scale};
+    mla::PrefillArgs a{q, k, v, gate, out, B, H, Tq, Tk, Tk, scale};
     cudaError_t e = mla::launch_prefill(a, d, knobs(), take_timer(MLA_OP_PREFILL),
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_prefill launch");
+}
+
+// Host checks of an append of Tn rows per (b, h) into [B,H,cap,D] caches.
+static mla_status check_append(const void* kn, const void* vn, const void* kc, const void* vc,
+                               const void* start, int B, int H, int Tn, int cap) {
+    REQUIRE(kn && vn && kc && vc, MLA_ERR_INVALID_ARG, "null tensor pointer");
+    REQUIRE(aligned16(kn) && aligned16(vn) && aligned16(kc) && aligned16(vc) &&
+                (reinterpret_cast<uintptr_t>(start) & 7u) == 0,
+            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    REQUIRE(B >= 1 && H >= 1 && Tn >= 1 && cap >= 1, MLA_ERR_INVALID_ARG,
+            "need B, H, Tn, kv_capacity >= 1 (got %d, %d, %d, %d)", B, H, Tn, cap);
+    REQUIRE(int64_t(Tn) * 40 < (int64_t(1) << 31) && int64_t(B) * H < (int64_t(1) << 31),
+            MLA_ERR_UNSUPPORTED, "Tn or B*H too large for one call");
+    return MLA_OK;
+}
+
+static mla_status enqueue_append(const mla_bf16* k_new, const mla_bf16* v_new, mla_bf16* k_cache,
+                                 mla_bf16* v_cache, const int64_t* start, int64_t start_all,
+                                 int B, int H, int Tn, int cap, const mla::DeviceInfo& d,
+                                 cudaStream_t st) {
+    mla::AppendArgs a{k_new, v_new, k_cache, v_cache, start, start_all, B, H, Tn, cap};
+    cudaError_t e = mla::launch_cache_append(a, d, take_timer(MLA_OP_CACHE_APPEND), st);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "cache append launch");
+}
+
+mla_status mla_cache_append(const mla_bf16* k_new, const mla_bf16* v_new, mla_bf16* k_cache,
+                            mla_bf16* v_cache, const int64_t* start, int64_t start_all, int B,
+                            int H, int Tn, int kv_capacity, mla_stream stream) {
+    mla_status s = check_append(k_new, v_new, k_cache, v_cache, start, B, H, Tn, kv_capacity);
+    if (s != MLA_OK) return s;
+    REQUIRE(start != nullptr || (start_all >= 0 && start_all + Tn <= kv_capacity),
+            MLA_ERR_INVALID_ARG, "start_all + Tn must lie in [0, kv_capacity] (got %lld + %d, %d)",
+            static_cast<long long>(start_all), Tn, kv_capacity);
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    return enqueue_append(k_new, v_new, k_cache, v_cache, start, start_all, B, H, Tn, kv_capacity,
+                          d, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_prefill_chunk(const mla_bf16* q, const mla_bf16* k_new, const mla_bf16* v_new,
+                             mla_bf16* k_cache, mla_bf16* v_cache, const mla_bf16* gate,
+                             mla_bf16* out, int B, int H, int Tq, int P, int kv_capacity,
+                             float scale, void* ws, size_t ws_bytes, mla_stream stream) {
+    (void)ws;
+    (void)ws_bytes;
+    mla_status s = check_append(k_new, v_new, k_cache, v_cache, nullptr, B, H, Tq, kv_capacity);
+    if (s != MLA_OK) return s;
+    REQUIRE(q && out, MLA_ERR_INVALID_ARG, "null tensor pointer");
+    REQUIRE(aligned16(q) && aligned16(out) && (gate == nullptr || aligned16(gate)),
+            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    REQUIRE(P >= 0 && int64_t(P) + Tq <= kv_capacity, MLA_ERR_INVALID_ARG,
+            "need 0 <= P and P + Tq <= kv_capacity (got P=%d Tq=%d capacity=%d)", P, Tq,
+            kv_capacity);
+    REQUIRE(int64_t(B) * H * ((Tq + 127) / 128) < (int64_t(1) << 31), MLA_ERR_UNSUPPORTED,
+            "B*H*Tq too large for one call");
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((s = enqueue_append(k_new, v_new, k_cache, v_cache, nullptr, P, B, H, Tq, kv_capacity, d,
+                            st)) != MLA_OK)
+        return s;
+    mla::PrefillArgs a{q, k_cache, v_cache, gate, out, B, H, Tq, P + Tq, kv_capacity, scale};
+    cudaError_t e = mla::launch_prefill(a, d, knobs(), take_timer(MLA_OP_PREFILL), st);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_prefill_chunk launch");
+}
+
+mla_status mla_decode_cached(const mla_bf16* q, const mla_bf16* k_new, const mla_bf16* v_new,
+                             mla_bf16* k_cache, mla_bf16* v_cache, const int64_t* cache_seqlens,
+                             int B, int H, int kv_capacity, int max_seqlen, const mla_bf16* gate,
+                             mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                             mla_stream stream) {
+    mla_status s = check_decode_common(q, k_cache, v_cache, cache_seqlens, gate, out, B, H,
+                                       max_seqlen);
+    if (s != MLA_OK) return s;
+    REQUIRE((k_new == nullptr) == (v_new == nullptr), MLA_ERR_INVALID_ARG,
+            "k_new and v_new must both be given or both be NULL");
+    REQUIRE(max_seqlen <= kv_capacity, MLA_ERR_INVALID_ARG,
+            "max_seqlen (%d) exceeds kv_capacity (%d)", max_seqlen, kv_capacity);
+    if (k_new) {
+        s = check_append(k_new, v_new, k_cache, v_cache, cache_seqlens, B, H, 1, kv_capacity);
+        if (s != MLA_OK) return s;
+    }
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    const mla::DecodePlan pl = mla::plan_decode(B, H, max_seqlen, false);
+    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (k_new && (s = enqueue_append(k_new, v_new, k_cache, v_cache, cache_seqlens, 0, B, H, 1,
+                                     kv_capacity, d, st)) != MLA_OK)
+        return s;
+    mla::SeqLayout seq;
+    seq.lens = cache_seqlens;
+    seq.cap = kv_capacity;
+    seq.add = k_new ? 1 : 0;
+    mla::DecodeArgs a{q, k_cache, v_cache, seq, nullptr, gate, out, B, H, max_seqlen, 0, scale,
+                      ws, ws_bytes};
+    cudaError_t e = mla::launch_decode(a, pl, false, d, knobs(), take_timer(MLA_OP_DECODE), st);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode_cached launch");
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,

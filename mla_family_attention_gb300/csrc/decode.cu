@@ -82,7 +82,7 @@ struct Params {
     const uint16_t* q;
     const uint16_t* k;
     const uint16_t* v;
-    const int64_t* cu;
+    SeqLayout seq;
     const int32_t* idx;      // sparse: [B,topk]
     int B, H, chunk, max_chunks, topk, max_seqlen;
     const int* item_start;   // dense: [B+1]
@@ -96,7 +96,7 @@ struct Params {
 
 struct Item {
     int b, h, c;
-    int64_t base;   // first cached position of sequence b (cu[b])
+    int64_t row0;   // cache row of position 0 of (b, h)
     int T;          // T_b
     int e0, e1;     // range of positions (dense) or index entries (sparse)
     int nst;        // pipeline stages in the item
@@ -122,8 +122,8 @@ __device__ __forceinline__ Item item_of(const Params& p, int it) {
         const int rem = it - r.b * p.H * nch;
         r.h = rem / nch;
         r.c = rem - r.h * nch;
-        r.base = p.cu[r.b];
-        r.T = static_cast<int>(p.cu[r.b + 1] - r.base);
+        r.T = static_cast<int>(p.seq.len(r.b));
+        r.row0 = p.seq.row0(r.b, r.h, p.H, r.T);
         r.e0 = r.c * p.chunk;
         r.e1 = min(p.topk, r.e0 + p.chunk);
         r.nst = (r.e1 - r.e0 + Roles<kSparse>::kSP - 1) / Roles<kSparse>::kSP;
@@ -134,11 +134,11 @@ __device__ __forceinline__ Item item_of(const Params& p, int it) {
             if (p.item_start[mid] <= it) lo = mid; else hi = mid;
         }
         r.b = lo;
-        r.base = p.cu[r.b];
-        r.T = static_cast<int>(p.cu[r.b + 1] - r.base);
+        r.T = static_cast<int>(p.seq.len(r.b));
         const int rem = it - p.item_start[r.b];
         r.c = rem / p.H;
         r.h = rem - r.c * p.H;
+        r.row0 = p.seq.row0(r.b, r.h, p.H, r.T);
         r.e0 = r.c * p.chunk;
         r.e1 = min(r.T, r.e0 + p.chunk);
         r.nst = (r.e1 - r.e0 + Roles<kSparse>::kSP - 1) / Roles<kSparse>::kSP;
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 if (it == p.stall_stage) continue;   // test hook: withhold this stage
                 const int n = min(R::kSP, w.e1 - e);
                 if (lane == 0) {
-                    const int64_t row = w.base * p.H + int64_t(w.h) * w.T + e;
+                    const int64_t row = w.row0 + e;
                     mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow) + (st == 0 ? kKRow : 0));
                     if (st == 0)                      // the item's query row rides along
                         bulk_load(qs + slot * kKRow, p.q + (int64_t(w.b) * p.H + w.h) * kDqk,
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Item w = item_of<kSparse>(p, item);
-            const int64_t rbase = w.base * p.H + int64_t(w.h) * w.T;
+            const int64_t rbase = w.row0;
             for (int st = 0; st < w.nst; ++st, ++it) {
                 const int e = stage_entry<kSparse>(w, st);
                 const int slot = it % R::kStages;
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
 
 // Per-sequence work-item prefix: item_start[b] = sum_{b'<b} H*ceil(T_b'/chunk).
 // A sequence with T_b outside [1, max_seqlen] gets no items and is reported.
-__global__ void __launch_bounds__(1024) decode_items_kernel(const int64_t* cu, int B, int H,
+__global__ void __launch_bounds__(1024) decode_items_kernel(const SeqLayout seq, int B, int H,
                                                             int chunk, int max_seqlen,
                                                             int* item_start, int* status) {
     __shared__ int warp_sums[32];
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(1024) decode_items_kernel(const int64_t* cu, i
     const int b0 = min(B, int(threadIdx.x) * per), b1 = min(B, b0 + per);
     int local = 0;
     for (int b = b0; b < b1; ++b) {
-        const int64_t T = cu[b + 1] - cu[b];
+        const int64_t T = seq.len(b);
         if (T < 1 || T > max_seqlen) { report(status, kStInvalid); continue; }
         local += H * int((T + chunk - 1) / chunk);
     }
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(1024) decode_items_kernel(const int64_t* cu, i
     int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
     for (int b = b0; b < b1; ++b) {
         item_start[b] = run;
-        const int64_t T = cu[b + 1] - cu[b];
+        const int64_t T = seq.len(b);
         if (T >= 1 && T <= max_seqlen) run += H * int((T + chunk - 1) / chunk);
     }
     if (threadIdx.x == blockDim.x - 1) item_start[B] = run;
@@ -520,13 +520,13 @@ __global__ void __launch_bounds__(1024) decode_items_kernel(const int64_t* cu, i
 
 // One warp per (b,h): log-sum-exp merge of the chunk partials, then the gate.
 __global__ void __launch_bounds__(256) decode_merge_kernel(
-    const float* part_acc, const float* part_ml, const int64_t* cu, const uint16_t* gate,
+    const float* part_acc, const float* part_ml, const SeqLayout seq, const uint16_t* gate,
     uint16_t* out, int B, int H, int chunk, int max_chunks, int max_seqlen, int sparse_topk) {
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= B * H) return;
     const int b = gw / H;
-    const int64_t T = cu[b + 1] - cu[b];
+    const int64_t T = seq.len(b);
     if (T < 1 || T > max_seqlen) return;        // reported by the item pass
     const int span = sparse_topk > 0 ? sparse_topk : int(T);
     const int nch = (span + chunk - 1) / chunk;
@@ -598,7 +598,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse
     p.q = a.q;
     p.k = a.k;
     p.v = a.v;
-    p.cu = a.cu;
+    p.seq = a.seq;
     p.idx = a.idx;
     p.B = a.B;
     p.H = a.H;
@@ -628,7 +628,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse
         decode_partial_kernel<true><<<grid, Roles<true>::kThreads, smem_bytes<true>(), st>>>(p);
         if (tm.end) cudaEventRecord(tm.end, st);
     } else {
-        decode_items_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.H, pl.chunk, a.max_seqlen,
+        decode_items_kernel<<<1, 1024, 0, st>>>(a.seq, a.B, a.H, pl.chunk, a.max_seqlen,
                                                const_cast<int*>(p.item_start), dev.status);
         e = cudaFuncSetAttribute(decode_partial_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -642,7 +642,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse
     if (e != cudaSuccess) return e;
     const int warps = a.B * a.H;
     decode_merge_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
-        p.part_acc, p.part_ml, a.cu, a.gate, a.out, a.B, a.H, pl.chunk, pl.max_chunks,
+        p.part_acc, p.part_ml, a.seq, a.gate, a.out, a.B, a.H, pl.chunk, pl.max_chunks,
         sparse ? (1 << 30) : a.max_seqlen, sparse ? a.topk : 0);
     return cudaGetLastError();
 }

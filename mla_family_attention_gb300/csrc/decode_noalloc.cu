@@ -75,7 +75,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q, const mla_bf16* k,
     if ((s = mla::current_device(&d)) != MLA_OK) return s;
     void* scratch = nullptr;
     if ((s = scratch_address(&scratch)) != MLA_OK) return s;
-    mla::DecodeArgs a{q, k, v, cu_seqlens, nullptr, gate, out, B, H, max_seqlen, 0, scale,
+    mla::DecodeArgs a{q, k, v, mla::SeqLayout{cu_seqlens}, nullptr, gate, out, B, H, max_seqlen, 0, scale,
                       scratch, MLA_NOALLOC_SCRATCH_BYTES};
     cudaError_t e = mla::launch_decode(a, pl, false, d, mla::current_knobs(), mla::KernelTimer{},
                                        static_cast<cudaStream_t>(stream));

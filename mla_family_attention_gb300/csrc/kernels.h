@@ -33,11 +33,30 @@ struct KernelTimer {
 };
 
 // ------------------------------ decode ------------------------------------
+// Where sequence b's cache lives.  Packed (cap == 0): [H, T_b, D] at
+// position offset cu[b], T_b = cu[b+1] - cu[b].  Fixed capacity (cap > 0):
+// [B, H, cap, D], T_b = lens[b] + add.
+struct SeqLayout {
+    const int64_t* cu = nullptr;
+    const int64_t* lens = nullptr;
+    int64_t cap = 0;
+    int add = 0;
+#ifdef __CUDACC__
+    __device__ __forceinline__ int64_t len(int b) const {
+        return cap > 0 ? lens[b] + add : cu[b + 1] - cu[b];
+    }
+    // Row (in units of one position's features) of position 0 of (b, h).
+    __device__ __forceinline__ int64_t row0(int b, int h, int H, int64_t T) const {
+        return cap > 0 ? (int64_t(b) * H + h) * cap : cu[b] * H + int64_t(h) * T;
+    }
+#endif
+};
+
 struct DecodeArgs {
     const uint16_t* q;       // [B,H,192]
-    const uint16_t* k;       // packed [H,T_b,192] per sequence
-    const uint16_t* v;       // packed [H,T_b,128] per sequence
-    const int64_t* cu;       // [B+1]
+    const uint16_t* k;       // cache keys, laid out as `seq` says
+    const uint16_t* v;       // cache values
+    SeqLayout seq;
     const int32_t* idx;      // sparse only: [B,topk]
     const uint16_t* gate;    // [B,H*128] or null
     uint16_t* out;           // [B,H*128]
@@ -64,6 +83,12 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, bool sparse,
 cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// 3-D bf16 map over [outer][mid][inner] with 128-byte swizzle; rows with
+// mid >= `mid` read as zeros.
+cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
+                                uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
+                                uint32_t box_inner, uint32_t box_mid);
+
 // ---------------------------- DSA indexer --------------------------------
 struct IndexArgs {
     const uint16_t* index_q;   // [B,32,128]
@@ -88,15 +113,30 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& p, const Devi
 // ------------------------------ prefill -----------------------------------
 struct PrefillArgs {
     const uint16_t* q;       // [B,H,Tq,192]
-    const uint16_t* k;       // [B,H,Tk,192]
-    const uint16_t* v;       // [B,H,Tk,128]
+    const uint16_t* k;       // [B,H,kv_cap,192]; positions 0..Tk-1 used
+    const uint16_t* v;       // [B,H,kv_cap,128]
     const uint16_t* gate;    // [B,Tq,H*128] or null
     uint16_t* out;           // [B,Tq,H*128]
-    int B, H, Tq, Tk;
+    int B, H, Tq, Tk, kv_cap;
     float scale;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Knobs& kn,
                            const KernelTimer& tm, cudaStream_t st);
+
+// ---------------------------- cache append --------------------------------
+struct AppendArgs {
+    const uint16_t* k_new;   // [B,H,Tn,192]
+    const uint16_t* v_new;   // [B,H,Tn,128]
+    uint16_t* k_cache;       // [B,H,cap,192]
+    uint16_t* v_cache;       // [B,H,cap,128]
+    const int64_t* start;    // device [B] or null (then `start_all`)
+    int64_t start_all;
+    int B, H, Tn;
+    int64_t cap;
+};
+
+cudaError_t launch_cache_append(const AppendArgs& a, const DeviceInfo& dev, const KernelTimer& tm,
+                                cudaStream_t st);
 
 }  // namespace mla

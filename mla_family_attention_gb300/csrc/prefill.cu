@@ -133,7 +133,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int kmax = P0 + min(q0 + kBM - 1, p.Tq - 1);          // last key any row of the tile sees
     const int n_kv = min((p.Tk + kBN - 1) / kBN, kmax / kBN + 1);
     const int n_full = min((P0 + q0 + 1) / kBN, p.Tk / kBN);    // tiles visible to every row
-    const int kv_row0 = bh * p.Tk;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKStages; ++i) {
@@ -174,10 +173,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                const int y = kv_row0 + j * kBN;
+                // keys j*128.. of (b, h); rows at or past Tk arrive as zeros
+                const int y = j * kBN;
                 mbar_arrive_expect_tx(&kfull[ks], kKTile);
                 for (int c = 0; c < 3; ++c)
-                    tma_load_2d(ksm + ks * kKTile + c * kBox, &kmap, c * 64, y, &kfull[ks]);
+                    tma_load_3d(ksm + ks * kKTile + c * kBox, &kmap, c * 64, y, bh, &kfull[ks]);
                 kf[ks] = kr + 1;
                 const int vs = j % kVStages, vr = j / kVStages;
                 if (vr > 0 && !mbar_wait(&vempty[vs], (vr - 1) & 1, p.wait_ns)) {
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 mbar_arrive_expect_tx(&vfull[vs], kVTile);
                 for (int c = 0; c < 2; ++c)
-                    tma_load_2d(vsm + vs * kVTile + c * kBox, &vmap, c * 64, y, &vfull[vs]);
+                    tma_load_3d(vsm + vs * kVTile + c * kBox, &vmap, c * 64, y, bh, &vfull[vs]);
                 vf[vs] = vr + 1;
             }
             for (int i = 0; i < kKStages; ++i)
@@ -433,11 +433,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
 cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Knobs& kn,
                            const KernelTimer& tm, cudaStream_t st) {
     static_assert(kPrefillSmem <= 227 * 1024, "shared memory budget");
+    // [B*H][Tk][D] views of the [B,H,kv_cap,D] caches: a tile that runs past
+    // Tk reads zeros, never the unused capacity or the next head's rows.
     CUtensorMap kmap, vmap;
-    const uint64_t rows = uint64_t(a.B) * a.H * a.Tk;
-    cudaError_t e = encode_tmap_2d_bf16(&kmap, a.k, kDqk, rows, kDqk * 2, 64, kBN);
+    const uint64_t bhs = uint64_t(a.B) * a.H, cap = uint64_t(a.kv_cap);
+    cudaError_t e = encode_tmap_3d_bf16(&kmap, a.k, kDqk, a.Tk, bhs, kDqk * 2, cap * kDqk * 2, 64,
+                                        kBN);
     if (e != cudaSuccess) return e;
-    e = encode_tmap_2d_bf16(&vmap, a.v, kDv, rows, kDv * 2, 64, kBN);
+    e = encode_tmap_3d_bf16(&vmap, a.v, kDv, a.Tk, bhs, kDv * 2, cap * kDv * 2, 64, kBN);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kPrefillSmem));

@@ -15,8 +15,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 }  // namespace
 
-cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     std::call_once(g_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -25,12 +25,33 @@ cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inn
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode) return cudaErrorNotSupported;
+    return g_encode;
+}
+}  // namespace
+
+cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    if (!encoder()) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {row_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
+                                uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
+                                uint32_t box_inner, uint32_t box_mid) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {inner, mid, outer};
+    const cuuint64_t strides[2] = {mid_bytes, outer_bytes};
+    const cuuint32_t box[3] = {box_inner, box_mid, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

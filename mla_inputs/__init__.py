@@ -140,6 +140,50 @@ def make_decode(lengths, H: int, gated: bool, device="cpu", config: int = 1,
                   default_scale() if scale is None else scale, H)
 
 
+NAN_BF16 = 0x7FC0   # a quiet-NaN bit pattern, used to fill unused cache capacity
+
+
+def nan_filled(shape, device) -> torch.Tensor:
+    """bf16 tensor whose every element is NaN (stands for uninitialised memory)."""
+    return torch.full(shape, NAN_BF16, dtype=torch.int16, device=device).view(torch.bfloat16)
+
+
+@dataclass
+class CapacityDecode:
+    q: torch.Tensor            # [B,H,192]
+    k_cache: torch.Tensor      # [B,H,cap,192]; positions past lengths[b] hold NaN
+    v_cache: torch.Tensor      # [B,H,cap,128]
+    lengths: list[int]         # positions cached per sequence
+    k_new: torch.Tensor | None     # [B,H,1,192]: position lengths[b] of each sequence
+    v_new: torch.Tensor | None
+    gate: torch.Tensor | None
+    scale: float
+    H: int
+
+
+def make_capacity_decode(lengths, H: int, cap: int, gated: bool, device="cpu", config: int = 1,
+                         append: bool = True) -> CapacityDecode:
+    """Fixed-capacity caches holding the same keys and values as
+    make_decode(lengths + [1 if append]) for the same config: sequence b's
+    first lengths[b] positions in the cache, its next position (the current
+    token) in k_new / v_new when `append`, NaN everywhere else."""
+    lengths = [int(t) for t in lengths]
+    B = len(lengths)
+    kc, vc = nan_filled((B, H, cap, DQK), device), nan_filled((B, H, cap, DV), device)
+    extra = 1 if append else 0
+    kn = torch.empty((B, H, 1, DQK), dtype=torch.bfloat16, device=device) if append else None
+    vn = torch.empty((B, H, 1, DV), dtype=torch.bfloat16, device=device) if append else None
+    for b, L in enumerate(lengths):
+        kb, vb = _seq_kv(H, L + extra, device, config, b)
+        kc[b, :, :L], vc[b, :, :L] = kb[:, :L], vb[:, :L]
+        if append:
+            kn[b], vn[b] = kb[:, L:], vb[:, L:]
+        del kb, vb
+    q = _randn((B, H, DQK), seed_of(config, T_Q), device)
+    gate = _randn((B, H * DV), seed_of(config, T_GATE), device) if gated else None
+    return CapacityDecode(q, kc, vc, lengths, kn, vn, gate, default_scale(), H)
+
+
 def make_dsa(lengths, H: int = 96, device="cpu", config: int = 4, with_main=True) -> Dsa:
     lengths = [int(t) for t in lengths]
     B = len(lengths)
@@ -168,6 +212,13 @@ WORKLOADS = {
     "dsa_decode_b8_t131072": dict(kind="dsa", config=4, B=8, H=96, T=131072, topk=2048),
     # the indexer part of the DSA workload alone (same index keys, queries, weights)
     "dsa_index_b8_t131072": dict(kind="index", config=4, B=8, H=96, T=131072, topk=2048),
+    # the cache-update path: a 16384-token prompt fed in four 4096-token chunks
+    # into a 16384-position cache; a decode step that appends the current token
+    # to 8191 cached positions of 32 sequences
+    "chunked_prefill_b1_h96_t16384_c4096": dict(kind="chunked_prefill", config=3, B=1, H=96,
+                                                T=16384, chunk=4096, gated=True),
+    "decode_cached_b32_h96_t8192": dict(kind="decode_cached", config=1, B=32, H=96, T=8192,
+                                        gated=True),
     # smaller cases of the same kernels, a few GB on the device, for ncu captures
     "dsa_decode_b2_t16384": dict(kind="dsa", config=4, B=2, H=96, T=16384, topk=2048,
                                  profile_only=True),
