@@ -40,7 +40,9 @@ INDEX_HEADS = 32   # K3.1 indexer heads
 INDEX_DIM = 128    # K3.1 index key / query features
 
 # tensor ids used in the seed formula
-T_Q, T_K, T_SHARED, T_V, T_GATE, T_IQ, T_IK, T_W = range(8)
+T_Q, T_K, T_SHARED, T_V, T_GATE, T_IQ, T_IK, T_W, T_CKV, T_WK, T_WV = range(11)
+D_LATENT = 512     # normalised KV latent c_s (DSA post, eq. (7))
+D_CKV = D_LATENT + D_SHARED   # cached per position: c_s and the shared key r_s
 
 
 def seed_of(config: int, tensor: int, index: int = 0) -> int:
@@ -140,6 +142,41 @@ def make_decode(lengths, H: int, gated: bool, device="cpu", config: int = 1,
                   default_scale() if scale is None else scale, H)
 
 
+@dataclass
+class LatentDecode:
+    q: torch.Tensor        # [B,H,192] expanded-form queries (128 content ++ 64 shared)
+    ckv: torch.Tensor      # packed [cu[B],576]: latent c_s (512) ++ shared key r_s (64)
+    cu_seqlens: torch.Tensor
+    lengths: list[int]
+    w_kc: torch.Tensor     # [H,128,512] W^K (key up-projection of the latent)
+    w_vc: torch.Tensor     # [H,128,512] W^V (value up-projection)
+    gate: torch.Tensor | None
+    scale: float
+    H: int
+
+
+def make_latent_decode(lengths, H: int, gated: bool = True, device="cpu", config: int = 5,
+                       scale: float | None = None) -> LatentDecode:
+    """Latent cache rows ~N(0,1) (c_s is RMS-normalised on the pages, so unit
+    scale per feature); W^K, W^V entries ~N(0, 1/512), so the expanded keys and
+    values are ~N(0,1) like the expanded-cache workloads."""
+    lengths = [int(t) for t in lengths]
+    B = len(lengths)
+    cu = cu_from_lengths(lengths)
+    ckv = torch.empty((int(cu[-1]), D_CKV), dtype=torch.bfloat16, device=device)
+    for b, T in enumerate(lengths):
+        ckv[int(cu[b]):int(cu[b]) + T] = _randn((T, D_CKV), seed_of(config, T_CKV, b), device)
+    std = D_LATENT ** -0.5
+    w_kc = (_randn((H, D_NOPE, D_LATENT), seed_of(config, T_WK), device, torch.float32)
+            * std).to(torch.bfloat16)
+    w_vc = (_randn((H, DV, D_LATENT), seed_of(config, T_WV), device, torch.float32)
+            * std).to(torch.bfloat16)
+    q = _randn((B, H, DQK), seed_of(config, T_Q), device)
+    gate = _randn((B, H * DV), seed_of(config, T_GATE), device) if gated else None
+    return LatentDecode(q, ckv, cu.to(device), lengths, w_kc, w_vc, gate,
+                        default_scale() if scale is None else scale, H)
+
+
 NAN_BF16 = 0x7FC0   # a quiet-NaN bit pattern, used to fill unused cache capacity
 
 
@@ -218,6 +255,10 @@ WORKLOADS = {
     "chunked_prefill_b1_h96_t16384_c4096": dict(kind="chunked_prefill", config=3, B=1, H=96,
                                                 T=16384, chunk=4096, gated=True),
     "decode_cached_b32_h96_t8192": dict(kind="decode_cached", config=1, B=32, H=96, T=8192,
+                                        gated=True),
+    # decode over the absorbed 576-feature latent cache (1,152 bytes per position
+    # instead of 61,440): the decode workload's batch and length
+    "latent_decode_b32_h96_t8192": dict(kind="latent_decode", config=5, B=32, H=96, T=8192,
                                         gated=True),
     # smaller cases of the same kernels, a few GB on the device, for ncu captures
     "dsa_decode_b2_t16384": dict(kind="dsa", config=4, B=2, H=96, T=16384, topk=2048,

@@ -257,3 +257,40 @@ def mla_decode_cached(q, k_cache, v_cache, lengths, k_new, v_new, gate, scale: f
         cu.append(cu[-1] + kb.shape[1])
     return mla_decode(q, np.concatenate(ks), np.concatenate(vs), np.array(cu, dtype=np.int64),
                       gate, scale, lib=lib)
+
+
+# ---------------------------------------------------------------------------
+# Absorbed-latent MLA (DSA post, eqs. (7)-(8) and the remark after eq. (10)
+# that inference may absorb W^K into the query and apply W^V after attention).
+# The cache holds, per position, the normalised 512-feature latent c_s and the
+# 64-feature shared key r_s (576 values).  Head h's key and value are
+#   k_{s,h} = [W^K_h c_s ; r_s] in R^192,   v_{s,h} = W^V_h c_s in R^128,
+# with W^K_h, W^V_h in R^{128 x 512}.  The oracle expands the cache this way
+# in float64 and runs the plain decode definition on the expanded keys; the
+# absorbed evaluation order is the GPU path's business.
+# ---------------------------------------------------------------------------
+def expand_latent(ckv, w_kc, w_vc):
+    """ckv [N,576], w_kc / w_vc [H,128,512] -> k [H,N,192], v [H,N,128] (float64)."""
+    c, wk, wv = _f64(ckv), _f64(w_kc), _f64(w_vc)
+    lat, rope = c[:, :512], c[:, 512:]
+    H, N = wk.shape[0], c.shape[0]
+    k = np.empty((H, N, 192))
+    k[:, :, :128] = np.einsum("hdj,nj->hnd", wk, lat)
+    k[:, :, 128:] = rope[None]
+    v = np.einsum("hdj,nj->hnd", wv, lat)
+    return k, v
+
+
+def mla_decode_latent(q, ckv, cu_seqlens, w_kc, w_vc, gate, scale: float,
+                      lib=None) -> np.ndarray:
+    """Gated MLA decode over a packed latent cache (sequence b = rows
+    cu[b]..cu[b+1]-1 of ckv [N,576]); q [B,H,192] is the expanded-form query.
+    Returns out [B,H*128] in float64."""
+    cu = _i64(cu_seqlens)
+    c = _f64(ckv)
+    ks, vs = [], []
+    for b in range(cu.size - 1):
+        kb, vb = expand_latent(c[cu[b]:cu[b + 1]], w_kc, w_vc)
+        ks.append(kb.reshape(-1))
+        vs.append(vb.reshape(-1))
+    return mla_decode(q, np.concatenate(ks), np.concatenate(vs), cu, gate, scale, lib=lib)
