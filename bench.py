@@ -485,7 +485,41 @@ class DecodeCachedWork:
         del self.cd, self.seqlens, self.out, self.ws
 
 
-WORK_KINDS = {"decode": DecodeWork, "dsa": DsaWork, "index": IndexWork,
+class LatentDecodeWork:
+    """Gated MLA decode over the absorbed 576-feature latent cache: query
+    absorption, tcgen05 attention over the latent, merge with W^V and gate."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        lengths = mi.workload_lengths(name)
+        if batch:
+            lengths = lengths[:batch]
+        self.name, self.lengths, self.H, self.B = name, lengths, w["H"], len(lengths)
+        self.max_len = max(lengths)
+        self.d = mi.make_latent_decode(lengths, self.H, w["gated"], device=dev,
+                                       config=w["config"])
+        self.out = torch.empty((self.B, self.H * 128), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(mla.workspace_size(_lib.OP_LATENT_DECODE, self.B, self.H,
+                                                 self.max_len, 0), dtype=torch.uint8, device=dev)
+        self.work = acc.latent_kv_bytes(lengths)
+        self.unit, self.bound = "GB/s", "hbm"
+        self.launches_per_step = 4      # absorb, schedule, latent attention, merge
+        self.kernels = [(_lib.OP_LATENT_DECODE, "mla_latent_kernel", self.work)]
+
+    def step(self, stream):
+        d = self.d
+        self.mla.mla_decode_latent(d.q, d.ckv, d.cu_seqlens, self.max_len, d.w_kc, d.w_vc,
+                                   gate=d.gate, out=self.out, scale=d.scale, ws=self.ws,
+                                   stream=stream)
+
+    def free(self):
+        del self.d, self.out, self.ws
+
+
+WORK_KINDS = {"decode": DecodeWork, "latent_decode": LatentDecodeWork, "dsa": DsaWork, "index": IndexWork,
               "prefill": PrefillWork, "chunked_prefill": ChunkedPrefillWork,
               "decode_cached": DecodeCachedWork}
 

@@ -65,7 +65,8 @@ enum {
     MLA_OP_DECODE = 1,
     MLA_OP_INDEX_TOPK = 2,
     MLA_OP_SPARSE_DECODE = 3,
-    MLA_OP_CACHE_APPEND = 4
+    MLA_OP_CACHE_APPEND = 4,
+    MLA_OP_LATENT_DECODE = 5
 };
 
 /*
@@ -208,6 +209,37 @@ mla_status mla_decode_cached(const mla_bf16* q, const mla_bf16* k_new, const mla
                              mla_stream stream);
 
 /*
+ * Gated MLA decode over the absorbed 576-feature latent cache (DSA post,
+ * eqs. (7)-(10), and its remark that inference absorbs W^K into the query
+ * side and applies W^V after attention).  Position s of a sequence caches
+ * c_s (512 normalised latent features) followed by r_s (64 shared key
+ * features); head h's key is [W^K_h c_s ; r_s] and its value W^V_h c_s.
+ *
+ *   q          [B,H,192]  expanded-form queries (128 content ++ 64 shared)
+ *   ckv        packed [total_positions,576]: sequence b is rows
+ *              cu[b]..cu[b+1]-1 (total_positions = rows the allocation holds)
+ *   cu_seqlens [B+1] int64 on the device
+ *   w_kc       [H,128,512] W^K (row d, latent feature j)
+ *   w_vc       [H,128,512] W^V
+ *   gate, out  as in mla_decode
+ *
+ * Result: the same as mla_decode over the expanded keys and values, up to
+ * rounding (the absorbed query W^K_h^T q[0:128] is rounded to bf16).  Reads
+ * 1,152 cache bytes per position instead of 61,440.  Requires H a multiple
+ * of 16 in [16, 96], 1 <= T_b <= max_seqlen (else the sequence is skipped
+ * with MLA_ERR_INVALID_ARG in the device status, output untouched) and
+ * total_positions < 2^31.  Workspace: mla_workspace_size(
+ * MLA_OP_LATENT_DECODE, B, H, max_seqlen, 0) bytes (absorbed queries, the
+ * work split, and per-segment partial results); it depends on the current
+ * device's SM count.
+ */
+mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64_t* cu_seqlens,
+                             int64_t total_positions, int B, int H, int max_seqlen,
+                             const mla_bf16* w_kc, const mla_bf16* w_vc, const mla_bf16* gate,
+                             mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                             mla_stream stream);
+
+/*
  * DSA indexer score and top-k (DSA post eqs. (5) and (6)).
  *
  *   index_q     [B,NH,128]  index queries (NH must be 32)
@@ -255,7 +287,7 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
  * Bytes of workspace an operation needs (a multiple of 256; 0 if none).
  * `op` is one of MLA_OP_*; arguments an operation does not use are ignored
  * (prefill and cache_append: none needed; decode: B, H, max_seqlen;
- * index_topk: B, max_seqlen; sparse_decode: B, H, topk).  Returns 0 for invalid arguments.
+ * index_topk: B, max_seqlen; sparse_decode: B, H, topk; latent_decode: B, H).  Returns 0 for invalid arguments.
  */
 size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk);
 
@@ -294,7 +326,7 @@ mla_status mla_debug_set(int knob, long long value);
  * (decode: the split-KV partial kernel; sparse decode: the same kernel in
  * gather mode; index_topk: the scoring kernel; prefill: the attention
  * kernel; cache_append: the copy kernel, also when a chunked prefill or a
- * cached decode step appends).  mla_timing_read synchronises those events, returns the summed
+ * cached decode step appends; latent_decode: the latent attention kernel).  mla_timing_read synchronises those events, returns the summed
  * kernel time in milliseconds and the number of launches of operation `op`
  * (MLA_OP_*) since the last read, and resets the count.  Events are created
  * on first use and reused; no device memory is allocated.

@@ -17,6 +17,8 @@ Entry points (names as in the C ABI):
 * ``mla_prefill_chunk(q, k_new, v_new, k_cache, v_cache, P)``  append + causal prefill
 * ``mla_decode_cached(q, k_cache, v_cache, cache_seqlens, ...)`` decode step over
   fixed-capacity caches (optionally appending the current token first)
+* ``mla_decode_latent(q, ckv, cu_seqlens, w_kc, w_vc, ...)`` decode over the absorbed
+  576-feature latent cache
 """
 from __future__ import annotations
 
@@ -289,6 +291,38 @@ def mla_decode_cached(q, k_cache, v_cache, cache_seqlens, max_seqlen: int, k_new
                                      _ptr(v_cache), _ptr(cache_seqlens), B, H, cap,
                                      int(max_seqlen), _ptr(gate), _ptr(out),
                                      float(default_scale() if scale is None else scale),
+                                     _ptr(ws), wsb, _stream(stream)), lib)
+    return out
+
+
+def mla_decode_latent(q, ckv, cu_seqlens, max_seqlen: int, w_kc, w_vc, gate=None, out=None,
+                      scale=None, ws=None, stream=None):
+    """Gated MLA decode over a packed latent cache ckv [total,576] (latent c_s ++ shared
+    key r_s per position); q [B,H,192] expanded-form queries; w_kc / w_vc [H,128,512]."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [B,H,192]")
+    B, H, _ = q.shape
+    _need(ckv, "ckv", torch.bfloat16, None, q.device)
+    if ckv.dim() != 2 or ckv.shape[1] != 576:
+        raise ValueError("ckv must be [total,576]")
+    _need(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,), q.device)
+    _need(w_kc, "w_kc", torch.bfloat16, (H, 128, 512), q.device)
+    _need(w_vc, "w_vc", torch.bfloat16, (H, DV, 512), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_LATENT_DECODE, B, H, int(max_seqlen), 0)
+    if nbytes == 0:
+        raise ValueError(f"unsupported latent decode shape B={B} H={H}")
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_decode_latent(_ptr(q), _ptr(ckv), _ptr(cu_seqlens), int(ckv.shape[0]), B,
+                                     H, int(max_seqlen), _ptr(w_kc), _ptr(w_vc), _ptr(gate),
+                                     _ptr(out), float(default_scale() if scale is None else scale),
                                      _ptr(ws), wsb, _stream(stream)), lib)
     return out
 

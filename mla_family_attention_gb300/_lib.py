@@ -17,7 +17,8 @@ MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUD
 STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT",
                 6: "MLA_ERR_BAD_INDEX"}
-OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE, OP_CACHE_APPEND = range(5)
+OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE, OP_CACHE_APPEND, \
+    OP_LATENT_DECODE = range(6)
 DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE, DEBUG_SPARSE_CHUNK = 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -36,6 +37,8 @@ SIGNATURES = {
     "mla_cache_append": (_I, [_P, _P, _P, _P, _P, ctypes.c_int64, _I, _I, _I, _I, _P]),
     "mla_prefill_chunk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "mla_decode_cached": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _F, _P, _Z, _P]),
+    "mla_decode_latent": (_I, [_P, _P, _P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _F, _P,
+                               _Z, _P]),
     "mla_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "mla_check_device_status": (_I, [_P]),
     "mla_last_error": (ctypes.c_char_p, []),

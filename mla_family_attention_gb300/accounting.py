@@ -41,6 +41,12 @@ def prefill_flops(B: int, H: int, Tq: int, Tk: int) -> int:
     return B * H * causal_pairs(Tq, Tk) * 2 * (DQK + DV)
 
 
+def latent_kv_bytes(lengths) -> int:
+    """Bytes of the absorbed latent cache read by a decode step: 576 bf16 values
+    (latent c_s and shared key r_s) per position, shared by every head."""
+    return sum(int(t) for t in lengths) * (512 + 64) * BF16
+
+
 def append_bytes(B: int, H: int, Tn: int) -> int:
     """HBM bytes of appending Tn positions to every (b, h): read once, written once."""
     return 2 * B * Tn * kv_bytes_per_position(H)

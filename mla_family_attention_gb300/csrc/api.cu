@@ -79,7 +79,7 @@ struct TimerPool {
     std::vector<mla::KernelTimer> ev;
     size_t used = 0;
 };
-constexpr int kOps = 5;   // MLA_OP_PREFILL .. MLA_OP_CACHE_APPEND
+constexpr int kOps = 6;   // MLA_OP_PREFILL .. MLA_OP_LATENT_DECODE
 TimerPool g_pool[kOps];
 
 // Next event pair for `op` when timing is on, else an empty timer.
@@ -167,6 +167,12 @@ size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
         case MLA_OP_INDEX_TOPK:
             if (B < 1 || max_seqlen < 1 || max_seqlen > (1 << 24)) return 0;
             return mla::plan_index(B, max_seqlen).total;
+        case MLA_OP_LATENT_DECODE: {
+            if (B < 1 || H < 16 || H > 96 || H % 16 != 0) return 0;
+            mla::DeviceInfo d;
+            if (device_info(&d) != MLA_OK) return 0;
+            return mla::plan_latent(B, H, d.sms).total;
+        }
         default:
             return 0;
     }
@@ -382,6 +388,32 @@ mla_status mla_decode_cached(const mla_bf16* q, const mla_bf16* k_new, const mla
                       ws, ws_bytes};
     cudaError_t e = mla::launch_decode(a, pl, false, d, knobs(), take_timer(MLA_OP_DECODE), st);
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode_cached launch");
+}
+
+mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64_t* cu_seqlens,
+                             int64_t total_positions, int B, int H, int max_seqlen,
+                             const mla_bf16* w_kc, const mla_bf16* w_vc, const mla_bf16* gate,
+                             mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                             mla_stream stream) {
+    mla_status s = check_decode_common(q, ckv, w_kc, cu_seqlens, gate, out, B, H, max_seqlen);
+    if (s != MLA_OK) return s;
+    REQUIRE(w_vc != nullptr && aligned16(w_vc), MLA_ERR_INVALID_ARG,
+            "w_vc must be a 16-byte aligned device pointer");
+    REQUIRE(H >= 16 && H <= 96 && H % 16 == 0, MLA_ERR_UNSUPPORTED,
+            "H must be a multiple of 16 in [16, 96] (got %d)", H);
+    REQUIRE(total_positions >= 0 && total_positions < (int64_t(1) << 31), MLA_ERR_UNSUPPORTED,
+            "total_positions must be in [0, 2^31)");
+    REQUIRE(B <= 65535 * 16, MLA_ERR_UNSUPPORTED, "B too large for one call");
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    const mla::LatentPlan pl = mla::plan_latent(B, H, d.sms);
+    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
+    mla::LatentArgs a{q, ckv, cu_seqlens, w_kc, w_vc, gate, out, B, H, max_seqlen,
+                      total_positions, scale, ws};
+    cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode_latent launch");
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,

@@ -87,7 +87,7 @@ cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inn
 // mid >= `mid` read as zeros.
 cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
                                 uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
-                                uint32_t box_inner, uint32_t box_mid);
+                                uint32_t box_inner, uint32_t box_mid, uint32_t box_outer = 1);
 
 // ---------------------------- DSA indexer --------------------------------
 struct IndexArgs {
@@ -138,5 +138,32 @@ struct AppendArgs {
 
 cudaError_t launch_cache_append(const AppendArgs& a, const DeviceInfo& dev, const KernelTimer& tm,
                                 cudaStream_t st);
+
+// ------------------------ absorbed-latent decode ---------------------------
+constexpr int kLatent = 512;               // latent features c_s
+constexpr int kCkv = kLatent + 64;         // cached per position: c_s ++ r_s
+
+struct LatentArgs {
+    const uint16_t* q;       // [B,H,192] expanded-form queries
+    const uint16_t* ckv;     // packed [total,576]
+    const int64_t* cu;       // [B+1]
+    const uint16_t* w_kc;    // [H,128,512]
+    const uint16_t* w_vc;    // [H,128,512]
+    const uint16_t* gate;    // [B,H*128] or null
+    uint16_t* out;           // [B,H*128]
+    int B, H, max_seqlen;
+    int64_t total;
+    float scale;
+    void* ws;
+};
+
+struct LatentPlan {
+    int ctas;                 // attention CTAs (one per SM)
+    size_t qt_off, sched_off, part_off, ml_off, total;
+};
+
+LatentPlan plan_latent(int B, int H, int sms);
+cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& p, const DeviceInfo& dev,
+                                 const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 
 }  // namespace mla

@@ -1,0 +1,806 @@
+// Absorbed-latent gated MLA decode for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes (K3.1 Gated DSA post, eqs. (7)-(10), and its remark that
+// inference absorbs W^K into the query and applies W^V after attention): the
+// cache holds per position the normalised latent c_s (512 features) and the
+// shared key r_s (64); head h's key is [W^K_h c_s ; r_s] and its value
+// W^V_h c_s.  For the one query of sequence b and head h,
+//   q~_h = [W^K_h^T q_h[0:128] ; q_h[128:192]]                 (576 features)
+//   z~_h = sum_s softmax_s(scale * q~_h . [c_s ; r_s]) c_s     (512 features)
+//   out[b, h*128+d] = (W^V_h z~_h)_d * sigmoid(gate[b, h*128+d])
+// which equals attention over the expanded keys and values exactly (up to
+// rounding) while reading 1,152 cache bytes per position instead of 61,440.
+//
+// Kernels, in launch order:
+//   1. latent_absorb_kernel: q~ = W^K-absorbed queries, bf16, into workspace.
+//   2. latent_sched_kernel: splits the sequences' 64-position tiles evenly over
+//      one CTA per SM (a CTA's range may span sequences); every (CTA,
+//      sequence) piece is a segment with its own partial result.
+//   3. mla_latent_kernel (one CTA per SM):
+//      * S = Q~ K^T on the tensor cores with the heads as the M dimension
+//        (M = 128 rows, rows past H ignored), 64 keys as N, 576 features as K;
+//        Q~ stays in shared memory for the whole segment;
+//      * softmax per head row (two threads per row), lazily rescaled: the
+//        accumulator is rescaled only when a row maximum grows by 2^8;
+//      * O^T += C^T P^T with the latent features as M (four 128-row blocks),
+//        the heads as N and the 64 keys as K; O^T (512 x H fp32) lives in
+//        TMEM next to two 64-column score buffers;
+//      * a six-slot ring of 16 KB slots carries each tile as five TMA units
+//        (the 64 shared-key features, then four 128-feature latent blocks);
+//        the latent blocks stay until P.V has used them, so every cache byte
+//        is read once.  S of the next tile is computed on its first two units
+//        while the softmax of the current tile runs.
+//   4. latent_merge_kernel: per head, log-sum-exp merge of the segments of
+//      every sequence, then z = W^V_h z~ and the sigmoid gate.
+// Every wait is bounded; a timeout records MLA_ERR_TIMEOUT, the roles stop
+// (the softmax warps keep walking their barriers), in-flight copies and MMAs
+// are waited for, and TMEM is released before exit.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kLT = 64;                          // keys per tile
+constexpr int kMaxH = 96;                        // TMEM: 2*64 score + 4*H output columns
+constexpr int kHalf = kLT * 64 * 2;              // 8 KB: 64 keys x 64 features
+constexpr int kSlot = 2 * kHalf;                 // 16 KB ring slot
+constexpr int kSlots = 6;
+constexpr int kFills = 5;                        // ring fills per tile
+constexpr int kQBytes = (8 * kMaxH + 128) * 128; // nine [H x 64] blocks + rows read past them
+constexpr int kPBytes = kMaxH * 128;             // P: [H rows][64 keys] bf16
+constexpr int kThreads = 320;                    // TMA warp, MMA warp, 8 softmax warps
+constexpr int kColO = 2 * kLT;                   // O^T columns start after the score buffers
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kAhead = 4;                        // tiles prefetched into L2 ahead of the ring
+constexpr size_t kExtra = (2 * 2 * 128 + 2 * 128 + 128) * 4 + 256;
+constexpr size_t kLatSmem = 1024 + kQBytes + kPBytes + size_t(kSlots) * kSlot + kExtra;
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kLT, false, false);
+
+struct LatParams {
+    const int* sched;        // n, per, ts[B+1], seg[B+1]
+    const int64_t* cu;
+    const uint16_t* ckv;     // for L2 prefetches ahead of the ring
+    int64_t total;           // rows of ckv
+    float* part;             // [slots][H][512] unnormalised O
+    float* ml;               // [slots][H][2]: max (log2 units), sum
+    int B, H;
+    float scale_log2;
+    long long wait_ns;
+    int* status;
+};
+
+__device__ __forceinline__ bool bar_or(int id, int threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Walks a CTA's tile range [t0, t1) sequence by sequence.
+struct Cursor {
+    const int* ts;
+    int b = 0;
+    __device__ void seek(int t, int B) {
+        int lo = 0, hi = B;                      // largest b with ts[b] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (ts[mid] <= t) lo = mid; else hi = mid;
+        }
+        b = lo;
+    }
+    __device__ void advance(int t) {
+        while (t >= ts[b + 1]) ++b;
+    }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_latent_kernel(const __grid_constant__ CUtensorMap cmap,
+                      const __grid_constant__ CUtensorMap qmap, const LatParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* qs = smem;                                  // Q~: block kb at kb*H*128
+    uint8_t* ps = qs + kQBytes;                          // P (B operand of P.V)
+    uint8_t* ring = ps + kPBytes;
+    float* xmax = reinterpret_cast<float*>(ring + kSlots * kSlot);   // [2][2][128]
+    float* xsum = xmax + 2 * 2 * 128;                                // [2][128]
+    float* fsm = xsum + 2 * 128;                                     // [128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(fsm + 128);
+    uint64_t* empty = full + kSlots;
+    uint64_t* sfull = empty + kSlots;      // [2] MMA -> softmax
+    uint64_t* sfree = sfull + 2;           // [2] softmax -> MMA
+    uint64_t* pfull = sfree + 2;           // softmax -> MMA
+    uint64_t* qfull = pfull + 1;           // TMA -> MMA (Q~ of a segment)
+    uint64_t* qfree = qfull + 1;           // MMA -> TMA (a segment's Q.K^T done)
+    uint64_t* ofinal = qfree + 1;          // MMA -> epilogue (a segment's P.V done)
+    uint64_t* oread = ofinal + 1;          // epilogue -> MMA (O^T read out)
+    uint64_t* mdone = oread + 1;           // MMA drain before TMEM release
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mdone + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, B = p.B;
+    const int n = p.sched[0], per = p.sched[1];
+    const int* ts = p.sched + 2;
+    const int* seg = ts + B + 1;
+    const int c = blockIdx.x;
+    const int t0 = min(n, c * per), t1 = min(n, t0 + per);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sfree[i], 8);
+        }
+        mbar_init(pfull, 8);
+        mbar_init(qfull, 1);
+        mbar_init(qfree, 1);
+        mbar_init(ofinal, 1);
+        mbar_init(oread, 8);
+        mbar_init(mdone, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    auto fail = [&]() {
+        report(p.status, kStTimeout);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------- TMA -------------------------------
+        if (lane == 0 && t0 < t1) {
+            tma_prefetch_desc(&cmap);
+            tma_prefetch_desc(&qmap);
+            const uint64_t policy = l2_evict_first_policy();
+            int filled[kSlots];
+            for (int s = 0; s < kSlots; ++s) filled[s] = 0;
+            int nseg = 0, fill = 0;
+            Cursor cur{ts}, ahead{ts};
+            cur.seek(t0, B);
+            ahead.seek(t0, B);
+            // The ring holds little more than one tile, so HBM latency is
+            // covered by prefetching the tiles kAhead ahead into L2.
+            auto prefetch_tile = [&](int t) {
+                ahead.advance(t);
+                const int64_t r0 = p.cu[ahead.b] + int64_t(t - ts[ahead.b]) * kLT;
+                const int64_t r1 = min(r0 + kLT, p.total);
+                if (r1 > r0)
+                    prefetch_l2(p.ckv + r0 * kCkv, uint32_t((r1 - r0) * kCkv * 2));
+            };
+            for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
+            bool ok = true;
+            for (int t = t0; t < t1 && ok; ++t) {
+                if (t + kAhead < t1) prefetch_tile(t + kAhead);
+                cur.advance(t);
+                const int b = cur.b;
+                if (t == t0 || t == ts[b]) {
+                    // Q~ of sequence b, once the previous segment's Q.K^T is done
+                    if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
+                        fail();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(qfull, 9 * H * 128);
+                    for (int kb = 0; kb < 9; ++kb)
+                        tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                    ++nseg;
+                }
+                const int row = int(p.cu[b]) + (t - ts[b]) * kLT;
+                for (int i = 0; i < kFills; ++i, ++fill) {
+                    const int slot = fill % kSlots, round = fill / kSlots;
+                    if (*abort_flag) { ok = false; break; }
+                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = ring + slot * kSlot;
+                    if (i == 0) {              // shared-key features 512..575
+                        mbar_arrive_expect_tx(&full[slot], kHalf);
+                        tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
+                    } else {                   // latent features 128*(i-1) .. +127
+                        mbar_arrive_expect_tx(&full[slot], kSlot);
+                        tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot], policy);
+                        tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row, &full[slot],
+                                         policy);
+                    }
+                    filled[slot] = round + 1;
+                }
+            }
+            for (int s = 0; s < kSlots; ++s)
+                if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
+                    report(p.status, kStTimeout);
+            if (nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
+                report(p.status, kStTimeout);
+        }
+    } else if (warp == 1) {
+        // ------------------------------- MMA -------------------------------
+        if (lane == 0 && t0 < t1) {
+            const uint32_t idesc_pv = idesc_bf16_f32(128, H, true, false);
+            const uint32_t qa = smem_u32(qs), pa = smem_u32(ps), ra = smem_u32(ring);
+            bool ok = true;
+            // Fill i (0 = shared key, 1..4 = latent block i-1) of local tile j.
+            auto qk = [&](int j, int i) -> bool {
+                const int f = j * kFills + i, slot = f % kSlots;
+                if (*abort_flag || !mbar_wait(&full[slot], (f / kSlots) & 1, p.wait_ns))
+                    return false;
+                tc_fence_after();
+                const uint32_t d = tmem + uint32_t(j & 1) * kLT;
+                const int halves = i == 0 ? 1 : 2;
+                for (int hf = 0; hf < halves; ++hf) {
+                    const int kb = i == 0 ? 8 : 2 * (i - 1) + hf;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(qa + kb * H * 128 + kk * 32, 16, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(ra + slot * kSlot + hf * kHalf + kk * 32, 16, 1024);
+                        mma_bf16_ss(d, ad, bd, kIdescQK, (i > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                if (i == 0) mma_commit(&empty[slot]);
+                return true;
+            };
+            int pv_seg = 0;      // segments whose first P.V has been issued
+            // O^T += C^T P^T for local tile j (first = first tile of its segment).
+            auto pv = [&](int j, bool first) -> bool {
+                if (*abort_flag || !mbar_wait(pfull, j & 1, p.wait_ns)) return false;
+                if (first) {
+                    if (pv_seg > 0 && !mbar_wait(oread, (pv_seg - 1) & 1, p.wait_ns)) return false;
+                    ++pv_seg;
+                }
+                tc_fence_after();
+                for (int u = 0; u < 4; ++u) {
+                    const int slot = (j * kFills + 1 + u) % kSlots;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = smem_desc_sw128(ra + slot * kSlot + k * 2048, kHalf, 1024);
+                        const uint64_t bd = smem_desc_sw128(pa + k * 32, 16, 1024);
+                        mma_bf16_ss(tmem + kColO + u * H, ad, bd, idesc_pv,
+                                    (first && k == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&empty[slot]);
+                }
+                return true;
+            };
+            Cursor cur{ts};
+            cur.seek(t0, B);
+            int nseg = 0;
+            bool prev_first = false;
+            for (int t = t0; t < t1 && ok; ++t) {
+                const int j = t - t0;
+                cur.advance(t);
+                const int b = cur.b;
+                const bool first = (t == t0 || t == ts[b]);
+                const bool last = (t + 1 == t1 || t + 1 == ts[b + 1]);
+                if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (first) {
+                    if (j > 0) {
+                        if (!pv(j - 1, prev_first)) { ok = false; break; }
+                        mma_commit(ofinal);
+                    }
+                    if (!mbar_wait(qfull, nseg & 1, p.wait_ns)) { ok = false; break; }
+                    ++nseg;
+                    for (int i = 0; i < kFills && ok; ++i) ok = qk(j, i);
+                } else {
+                    ok = qk(j, 0) && qk(j, 1) && pv(j - 1, prev_first);
+                    for (int i = 2; i < kFills && ok; ++i) ok = qk(j, i);
+                }
+                if (!ok) break;
+                if (last) mma_commit(qfree);
+                mma_commit(&sfull[j & 1]);
+                prev_first = first;
+            }
+            if (ok) {
+                ok = pv(t1 - 1 - t0, prev_first);
+                mma_commit(ofinal);
+            }
+            if (!ok) {
+                fail();
+                mma_commit(ofinal);
+            }
+            mma_commit(mdone);
+            if (!mbar_wait(mdone, 0, p.wait_ns)) report(p.status, kStTimeout);
+        }
+    } else {
+        // ------------------------- softmax / epilogue ------------------------
+        // Warp w serves TMEM lane quadrant w%4 (head rows 32*quad..) and key
+        // columns 32*half.. of each tile; for O^T it serves the same lanes
+        // (latent features) of output blocks 2*half and 2*half+1.
+        const int quad = warp & 3, half = (warp - 2) >> 2;
+        const int r = quad * 32 + lane;
+        const bool real = r < H;
+        const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
+        float m = 0.f, l = 0.f;
+        int nseg = -1;
+        Cursor cur{ts};
+        if (t0 < t1) cur.seek(t0, B);
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (*abort_flag) return;
+            if (!mbar_wait(bar, parity, p.wait_ns)) fail();
+        };
+        for (int t = t0; t < t1; ++t) {
+            const int j = t - t0;
+            cur.advance(t);
+            const int b = cur.b;
+            const bool first = (t == t0 || t == ts[b]);
+            const bool last = (t + 1 == t1 || t + 1 == ts[b + 1]);
+            if (first) ++nseg;
+            const int T = int(p.cu[b + 1] - p.cu[b]);
+            const int key0 = (t - ts[b]) * kLT + half * 32;
+            const int sb = j & 1;
+            wait(&sfull[sb], (j >> 1) & 1);
+            tc_fence_after();
+            float s[32];
+            tmem_ld32(lane_base + sb * kLT + half * 32, s);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree[sb]);
+            float lm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x = key0 + i < T ? s[i] * p.scale_log2 : -INFINITY;
+                s[i] = x;
+                lm = fmaxf(lm, x);
+            }
+            xmax[(sb * 2 + half) * 128 + r] = lm;
+            named_bar_sync(1, 256);
+            const float rm = fmaxf(xmax[(sb * 2) * 128 + r], xmax[(sb * 2 + 1) * 128 + r]);
+            bool need = false;
+            if (first) {
+                m = real ? rm : 0.f;
+                l = 0.f;
+            } else if (real && rm > m + kRescaleLog2) {
+                need = true;
+            }
+            if (bar_or(2, 256, need)) {
+                // a row maximum grew past the slack: rescale O^T columns (heads)
+                float f = 1.f;
+                if (need) {
+                    f = ex2(m - rm);
+                    m = rm;
+                    l *= f;
+                }
+                if (half == 0) fsm[r] = f;
+                named_bar_sync(1, 256);
+                for (int uu = 0; uu < 2; ++uu) {
+                    const uint32_t base = lane_base + kColO + (2 * half + uu) * H;
+                    for (int c0 = 0; c0 < H; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(base + c0, v);
+                        tmem_ld_wait();
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * fsm[c0 + i]);
+                        tmem_st16(base + c0, w);
+                    }
+                }
+                tmem_st_wait();
+            }
+            // probabilities, bf16, into P row r (128-byte swizzled K-major rows)
+            uint32_t w[16];
+            float ps_sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a = ex2(s[2 * i] - m), bq = ex2(s[2 * i + 1] - m);
+                ps_sum += a + bq;
+                w[i] = pack2(a, bq);
+            }
+            l += ps_sum;
+            if (real) {
+                uint8_t* row = ps + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4*>(row + (((half * 4 + q4) ^ (r & 7)) << 4)) =
+                        make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull);
+            if (last) {
+                // segment done: row sums, then O^T and (m, l) to the partial slot
+                xsum[half * 128 + r] = l;
+                named_bar_sync(1, 256);
+                const int slot = seg[b] + (c - ts[b] / per);
+                if (half == 0 && real) {
+                    p.ml[(int64_t(slot) * H + r) * 2] = m;
+                    p.ml[(int64_t(slot) * H + r) * 2 + 1] = xsum[r] + xsum[128 + r];
+                }
+                wait(ofinal, nseg & 1);
+                tc_fence_after();
+                for (int uu = 0; uu < 2; ++uu) {
+                    const int u = 2 * half + uu;
+                    float* dst = p.part + int64_t(slot) * H * kLatent + u * 128 + quad * 32 + lane;
+                    for (int c0 = 0; c0 < H; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(lane_base + kColO + u * H + c0, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) dst[int64_t(c0 + i) * kLatent] = v[i];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(oread);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// q~[b,h,0:512] = W^K_h^T q[b,h,0:128] and q~[b,h,512:576] = q[b,h,128:192],
+// as one small tensor-core GEMM per (head, 128 latent features, up to 128
+// sequences): D[j, b] = sum_d W^K_h[d, j] q[b, h, d] with the latent features
+// as M (A = W^K block, MN-major), the sequences as N (B = queries, K-major)
+// and K = 128.  Bound by the 12.6 MB read of W^K (H = 96).
+constexpr int kAbsorbN = 128;      // sequences per CTA at most
+constexpr size_t kAbsorbSmem = 1024 + 2 * 16384 + 2 * kAbsorbN * 128 + 64;
+
+__global__ void __launch_bounds__(128) latent_absorb_kernel(
+    const __grid_constant__ CUtensorMap wkmap, const __grid_constant__ CUtensorMap qmap,
+    const uint16_t* q, uint16_t* qt, int B, int H, int nbox, long long wait_ns, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 2 * 16384 + 2 * kAbsorbN * 128);
+    uint32_t& tmem_holder = *reinterpret_cast<uint32_t*>(bars + 2);
+    const int jb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * nbox;
+    const int nb = min(nbox, B - b0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* wsm = sm;                       // [2 halves][128 d][64 j]
+    uint8_t* qsm = sm + 2 * 16384;           // [2 halves][nbox b][64 d]
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_holder, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_holder;
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bars[0], 2 * 16384 + 2 * nbox * 128);
+        for (int hf = 0; hf < 2; ++hf) {
+            tma_load_2d(wsm + hf * 16384, &wkmap, jb * 128 + hf * 64, h * 128, &bars[0]);
+            tma_load_3d(qsm + hf * nbox * 128, &qmap, hf * 64, h, b0, &bars[0]);
+        }
+        ok = mbar_wait(&bars[0], 0, wait_ns);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(128, nbox, true, false);
+            const uint32_t wa = smem_u32(wsm), qa = smem_u32(qsm);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad = smem_desc_sw128(wa + kk * 2048, 16384, 1024);
+                const uint64_t bd =
+                    smem_desc_sw128(qa + (kk >> 2) * nbox * 128 + (kk & 3) * 32, 16, 1024);
+                mma_bf16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+        } else {
+            report(status, kStTimeout);
+        }
+        mma_commit(&bars[1]);
+    }
+    __syncwarp();
+    if (!mbar_wait(&bars[1], 0, wait_ns) && lane == 0) report(status, kStTimeout);
+    tc_fence_after();
+    const int j = jb * 128 + warp * 32 + lane;
+    for (int c0 = 0; c0 < nb; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (c0 + i < nb) {
+                const __nv_bfloat16 x = __float2bfloat16_rn(v[i]);
+                qt[(int64_t(b0 + c0 + i) * H + h) * kCkv + j] =
+                    *reinterpret_cast<const uint16_t*>(&x);
+            }
+    }
+    if (jb == 0)
+        for (int i = threadIdx.x; i < nb * 64; i += 128) {
+            const int64_t bh = int64_t(b0 + (i >> 6)) * H + h;
+            qt[bh * kCkv + kLatent + (i & 63)] = q[bh * kDqk + 128 + (i & 63)];
+        }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the
+// exclusive prefix and writes the total to *total.
+__device__ int block_scan_excl(int v, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int s = lane < int(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    *total = warp_sums[31];
+    __syncthreads();
+    return excl;
+}
+
+// Tile prefix ts[b] (64-position tiles per sequence), n = ts[B], per =
+// ceil(n / G) tiles per CTA, and segment prefix seg[b] (number of CTA ranges
+// sequence b overlaps).  A sequence with T_b outside [1, max_seqlen] gets no
+// tiles and is reported.
+__global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, int B,
+                                                            int max_seqlen, int G, int* sched,
+                                                            int* status) {
+    __shared__ int warp_sums[32];
+    int* ts = sched + 2;
+    int* seg = ts + B + 1;
+    const int per_thr = (B + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(B, int(threadIdx.x) * per_thr), b1 = min(B, b0 + per_thr);
+    auto tiles = [&](int b) -> int {
+        const int64_t T = cu[b + 1] - cu[b];
+        return (T >= 1 && T <= max_seqlen) ? int((T + kLT - 1) / kLT) : 0;
+    };
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int64_t T = cu[b + 1] - cu[b];
+        if (T < 1 || T > max_seqlen) report(status, kStInvalid);
+        local += tiles(b);
+    }
+    int n;
+    int run = block_scan_excl(local, warp_sums, &n);
+    for (int b = b0; b < b1; ++b) {
+        ts[b] = run;
+        run += tiles(b);
+    }
+    if (threadIdx.x == 0) ts[B] = n;
+    const int per = max(1, (n + G - 1) / G);
+    __syncthreads();
+    local = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int nt = ts[b + 1] - ts[b];
+        if (nt > 0) local += (ts[b] + nt - 1) / per - ts[b] / per + 1;
+    }
+    int nseg;
+    run = block_scan_excl(local, warp_sums, &nseg);
+    for (int b = b0; b < b1; ++b) {
+        seg[b] = run;
+        const int nt = ts[b + 1] - ts[b];
+        if (nt > 0) run += (ts[b] + nt - 1) / per - ts[b] / per + 1;
+    }
+    if (threadIdx.x == 0) {
+        seg[B] = nseg;
+        sched[0] = n;
+        sched[1] = per;
+    }
+}
+
+// Per head h and up to 64 sequences: merge the segments' (O, m, l) by
+// log-sum-exp into z~ (bf16, in shared memory), then z = W^V_h z~ as one
+// tensor-core GEMM (M = 128 output features, N = sequences, K = 512 latent
+// features; A = W^V_h by TMA, B = z~) and the sigmoid gate.
+constexpr int kMergeN = 64;        // sequences per CTA at most
+constexpr size_t kMergeSmem = 1024 + 8 * 16384 + size_t(8) * kMergeN * 128 + 64;
+
+__global__ void __launch_bounds__(256) latent_merge_kernel(
+    const __grid_constant__ CUtensorMap wvmap, const float* part, const float* ml,
+    const int* sched, const uint16_t* gate, uint16_t* out, int B, int H, int nbox,
+    long long wait_ns, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* wsm = sm;                                   // [8 blocks][128 d][64 j]
+    uint8_t* zsm = sm + 8 * 16384;                       // [8 blocks][nbox b][64 j]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(zsm + 8 * kMergeN * 128);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
+    const int h = blockIdx.x, b0 = blockIdx.y * nbox;
+    const int nb = min(nbox, B - b0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per = sched[1];
+    const int* ts = sched + 2;
+    const int* seg = ts + B + 1;
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_holder, 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bars[0], 8 * 16384);
+        for (int kb = 0; kb < 8; ++kb)
+            tma_load_2d(wsm + kb * 16384, &wvmap, kb * 64, h * kDv, &bars[0]);
+    }
+    // z~ rows: thread handles latent features 2*tid, 2*tid+1 of every sequence
+    const int j = 2 * threadIdx.x, kb = j >> 6, jc = (j & 63) * 2;
+    for (int bb = 0; bb < nbox; ++bb) {
+        const int b = b0 + bb;
+        const int nt = bb < nb ? ts[b + 1] - ts[b] : 0;
+        float z0 = 0.f, z1 = 0.f;
+        if (nt > 0) {
+            const int s0 = seg[b], ns = (ts[b] + nt - 1) / per - ts[b] / per + 1;
+            float M = -INFINITY;
+            for (int i = 0; i < ns; ++i) M = fmaxf(M, ml[(int64_t(s0 + i) * H + h) * 2]);
+            float L = 0.f;
+            for (int i = 0; i < ns; ++i) {
+                const float* mi = ml + (int64_t(s0 + i) * H + h) * 2;
+                const float wgt = ex2(mi[0] - M);
+                L += wgt * mi[1];
+                const float2 pv =
+                    *reinterpret_cast<const float2*>(part + (int64_t(s0 + i) * H + h) * kLatent + j);
+                z0 = fmaf(wgt, pv.x, z0);
+                z1 = fmaf(wgt, pv.y, z1);
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            z0 *= inv;
+            z1 *= inv;
+        }
+        uint8_t* row = zsm + kb * nbox * 128 + (bb >> 3) * 1024 + (bb & 7) * 128;
+        *reinterpret_cast<uint32_t*>(row + ((((jc >> 4) ^ (bb & 7)) << 4) | (jc & 15))) =
+            pack2(z0, z1);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (mbar_wait(&bars[0], 0, wait_ns)) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(128, nbox, false, false);
+            const uint32_t wa = smem_u32(wsm), za = smem_u32(zsm);
+            for (int kk = 0; kk < 32; ++kk) {
+                const uint64_t ad = smem_desc_sw128(wa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd =
+                    smem_desc_sw128(za + (kk >> 2) * nbox * 128 + (kk & 3) * 32, 16, 1024);
+                mma_bf16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+        } else {
+            report(status, kStTimeout);
+        }
+        mma_commit(&bars[1]);
+    }
+    __syncwarp();
+    if (warp < 4) {
+        if (!mbar_wait(&bars[1], 0, wait_ns) && lane == 0) report(status, kStTimeout);
+        tc_fence_after();
+        const int d = warp * 32 + lane;
+        for (int c0 = 0; c0 < nb; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int b = b0 + c0 + i;
+                if (c0 + i >= nb || ts[b + 1] == ts[b]) continue;
+                const int64_t o = (int64_t(b) * H + h) * kDv + d;
+                float z = v[i];
+                if (gate) z *= sigmoidf_fast(__uint_as_float(uint32_t(gate[o]) << 16));
+                const __nv_bfloat16 x = __float2bfloat16_rn(z);
+                out[o] = *reinterpret_cast<const uint16_t*>(&x);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+LatentPlan plan_latent(int B, int H, int sms) {
+    LatentPlan pl{};
+    pl.ctas = sms;
+    const size_t slots = size_t(sms) + B;
+    pl.qt_off = 0;
+    pl.sched_off = align256(size_t(B) * H * kCkv * 2);
+    pl.part_off = pl.sched_off + align256((2 + 2 * size_t(B + 1)) * 4);
+    pl.ml_off = pl.part_off + align256(slots * H * kLatent * 4);
+    pl.total = pl.ml_off + align256(slots * H * 2 * 4);
+    return pl;
+}
+
+cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, const DeviceInfo& dev,
+                                 const Knobs& kn, const KernelTimer& tm, cudaStream_t st) {
+    static_assert(kLatSmem <= 227 * 1024, "shared memory budget");
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    uint16_t* qt = reinterpret_cast<uint16_t*>(ws + pl.qt_off);
+    int* sched = reinterpret_cast<int*>(ws + pl.sched_off);
+    float* part = reinterpret_cast<float*>(ws + pl.part_off);
+    float* ml = reinterpret_cast<float*>(ws + pl.ml_off);
+
+    // W^K as [H*128 rows (h, d)][512], W^V likewise; queries as [B][H][192]
+    const int nabs = a.B < kAbsorbN ? (a.B + 15) / 16 * 16 : kAbsorbN;
+    const int nmrg = a.B < kMergeN ? (a.B + 15) / 16 * 16 : kMergeN;
+    CUtensorMap wkmap, wvmap, q3map, cmap, qmap;
+    cudaError_t e = encode_tmap_2d_bf16(&wkmap, a.w_kc, kLatent, uint64_t(a.H) * 128, kLatent * 2,
+                                        64, 128);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&wvmap, a.w_vc, kLatent, uint64_t(a.H) * kDv, kLatent * 2, 64, 128);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_3d_bf16(&q3map, a.q, kDqk, a.H, a.B, kDqk * 2, uint64_t(a.H) * kDqk * 2, 64,
+                            1, nabs);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kAbsorbSmem));
+    if (e != cudaSuccess) return e;
+    latent_absorb_kernel<<<dim3(4, a.H, (a.B + nabs - 1) / nabs), 128, kAbsorbSmem, st>>>(
+        wkmap, q3map, a.q, qt, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
+    latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.max_seqlen, pl.ctas, sched, dev.status);
+    e = encode_tmap_2d_bf16(&cmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, kLT);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&qmap, qt, kCkv, uint64_t(a.B) * a.H, kCkv * 2, 64, a.H);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mla_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kLatSmem));
+    if (e != cudaSuccess) return e;
+    LatParams p{sched, a.cu, a.ckv, a.total, part, ml, a.B, a.H, a.scale * 1.4426950408889634f, kn.wait_limit_ns,
+                dev.status};
+    if (tm.begin) cudaEventRecord(tm.begin, st);
+    mla_latent_kernel<<<pl.ctas, kThreads, kLatSmem, st>>>(cmap, qmap, p);
+    if (tm.end) cudaEventRecord(tm.end, st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(latent_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kMergeSmem));
+    if (e != cudaSuccess) return e;
+    latent_merge_kernel<<<dim3(a.H, (a.B + nmrg - 1) / nmrg), 256, kMergeSmem, st>>>(
+        wvmap, part, ml, sched, a.gate, a.out, a.B, a.H, nmrg, kn.wait_limit_ns, dev.status);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -45,11 +45,11 @@ cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inn
 
 cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
                                 uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
-                                uint32_t box_inner, uint32_t box_mid) {
+                                uint32_t box_inner, uint32_t box_mid, uint32_t box_outer) {
     if (!encoder()) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {inner, mid, outer};
     const cuuint64_t strides[2] = {mid_bytes, outer_bytes};
-    const cuuint32_t box[3] = {box_inner, box_mid, 1};
+    const cuuint32_t box[3] = {box_inner, box_mid, box_outer};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
