@@ -538,11 +538,25 @@ __global__ void __launch_bounds__(128) latent_absorb_kernel(
                     *reinterpret_cast<const uint16_t*>(&x);
             }
     }
-    if (jb == 0)
-        for (int i = threadIdx.x; i < nb * 64; i += 128) {
-            const int64_t bh = int64_t(b0 + (i >> 6)) * H + h;
-            qt[bh * kCkv + kLatent + (i & 63)] = q[bh * kDqk + 128 + (i & 63)];
+    if (jb == 0) {
+        // the 64 shared-key features pass through: eight 16-byte pieces per
+        // sequence, all loads issued before the stores
+        uint4 x[kAbsorbN * 8 / 128];
+#pragma unroll
+        for (int k = 0; k < kAbsorbN * 8 / 128; ++k) {
+            const int i = threadIdx.x + 128 * k;
+            if (i < nb * 8)
+                x[k] = *reinterpret_cast<const uint4*>(
+                    q + (int64_t(b0 + (i >> 3)) * H + h) * kDqk + 128 + (i & 7) * 8);
         }
+#pragma unroll
+        for (int k = 0; k < kAbsorbN * 8 / 128; ++k) {
+            const int i = threadIdx.x + 128 * k;
+            if (i < nb * 8)
+                *reinterpret_cast<uint4*>(qt + (int64_t(b0 + (i >> 3)) * H + h) * kCkv + kLatent +
+                                          (i & 7) * 8) = x[k];
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
@@ -631,9 +645,10 @@ __global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, i
 // tensor-core GEMM (M = 128 output features, N = sequences, K = 512 latent
 // features; A = W^V_h by TMA, B = z~) and the sigmoid gate.
 constexpr int kMergeN = 64;        // sequences per CTA at most
-constexpr size_t kMergeSmem = 1024 + 8 * 16384 + size_t(8) * kMergeN * 128 + 64;
+constexpr int kMergeWarps = 32;
+constexpr size_t kMergeSmem = 1024 + 8 * 16384 + size_t(8) * kMergeN * 128 + 32 + 4 * kMergeN;
 
-__global__ void __launch_bounds__(256) latent_merge_kernel(
+__global__ void __launch_bounds__(kMergeWarps * 32) latent_merge_kernel(
     const __grid_constant__ CUtensorMap wvmap, const float* part, const float* ml,
     const int* sched, const uint16_t* gate, uint16_t* out, int B, int H, int nbox,
     long long wait_ns, int* status) {
@@ -644,6 +659,7 @@ __global__ void __launch_bounds__(256) latent_merge_kernel(
     uint8_t* zsm = sm + 8 * 16384;                       // [8 blocks][nbox b][64 j]
     uint64_t* bars = reinterpret_cast<uint64_t*>(zsm + 8 * kMergeN * 128);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
+    int* vld = reinterpret_cast<int*>(tmem_holder + 1);   // [nbox] sequence has output
     const int h = blockIdx.x, b0 = blockIdx.y * nbox;
     const int nb = min(nbox, B - b0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -665,33 +681,63 @@ __global__ void __launch_bounds__(256) latent_merge_kernel(
         for (int kb = 0; kb < 8; ++kb)
             tma_load_2d(wsm + kb * 16384, &wvmap, kb * 64, h * kDv, &bars[0]);
     }
-    // z~ rows: thread handles latent features 2*tid, 2*tid+1 of every sequence
-    const int j = 2 * threadIdx.x, kb = j >> 6, jc = (j & 63) * 2;
-    for (int bb = 0; bb < nbox; ++bb) {
+    // z~ rows: warp w merges sequence w (and w+32, ...); lane holds latent
+    // features 2*lane + 64*k (k < 8), so each float2 load of a partial row is
+    // one coalesced 256-byte access.  The lanes read the segments' (max, sum)
+    // pairs in parallel; the partial rows are then independent weighted sums,
+    // loaded two segments at a time.
+    for (int bb = warp; bb < nbox; bb += kMergeWarps) {
         const int b = b0 + bb;
         const int nt = bb < nb ? ts[b + 1] - ts[b] : 0;
-        float z0 = 0.f, z1 = 0.f;
+        if (lane == 0) vld[bb] = nt > 0;
+        float z[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) z[k] = 0.f;
         if (nt > 0) {
             const int s0 = seg[b], ns = (ts[b] + nt - 1) / per - ts[b] / per + 1;
-            float M = -INFINITY;
-            for (int i = 0; i < ns; ++i) M = fmaxf(M, ml[(int64_t(s0 + i) * H + h) * 2]);
-            float L = 0.f;
-            for (int i = 0; i < ns; ++i) {
-                const float* mi = ml + (int64_t(s0 + i) * H + h) * 2;
-                const float wgt = ex2(mi[0] - M);
-                L += wgt * mi[1];
-                const float2 pv =
-                    *reinterpret_cast<const float2*>(part + (int64_t(s0 + i) * H + h) * kLatent + j);
-                z0 = fmaf(wgt, pv.x, z0);
-                z1 = fmaf(wgt, pv.y, z1);
+            float M = -INFINITY, L = 0.f;       // lane-local over segments lane, lane+32, ...
+            for (int i = lane; i < ns; i += 32) {
+                const float2 v = *reinterpret_cast<const float2*>(ml + (int64_t(s0 + i) * H + h) * 2);
+                const float Mn = fmaxf(M, v.x);
+                L = L * ex2(M - Mn) + v.y * ex2(v.x - Mn);
+                M = Mn;
             }
+            float Mw = M;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
+            L = M == -INFINITY ? 0.f : L * ex2(M - Mw);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            z0 *= inv;
-            z1 *= inv;
+            for (int i0 = 0; i0 < ns; i0 += 2) {
+                float2 pv[2][8];
+                float wgt[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int i = min(i0 + q, ns - 1);
+                    const float* row = part + (int64_t(s0 + i) * H + h) * kLatent + 2 * lane;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        pv[q][k] = *reinterpret_cast<const float2*>(row + 64 * k);
+                    wgt[q] = i0 + q < ns ? ex2(ml[(int64_t(s0 + i) * H + h) * 2] - Mw) * inv : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        z[2 * k] = fmaf(wgt[q], pv[q][k].x, z[2 * k]);
+                        z[2 * k + 1] = fmaf(wgt[q], pv[q][k].y, z[2 * k + 1]);
+                    }
+            }
         }
-        uint8_t* row = zsm + kb * nbox * 128 + (bb >> 3) * 1024 + (bb & 7) * 128;
-        *reinterpret_cast<uint32_t*>(row + ((((jc >> 4) ^ (bb & 7)) << 4) | (jc & 15))) =
-            pack2(z0, z1);
+        // bf16 pairs into row bb of the eight K-major [nbox x 64] blocks
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int jc = lane * 4;                       // byte offset within the 128-byte row
+            uint8_t* row = zsm + k * nbox * 128 + (bb >> 3) * 1024 + (bb & 7) * 128;
+            *reinterpret_cast<uint32_t*>(row + ((((jc >> 4) ^ (bb & 7)) << 4) | (jc & 15))) =
+                pack2(z[2 * k], z[2 * k + 1]);
+        }
     }
     fence_async_smem();
     tc_fence_before();
@@ -713,24 +759,32 @@ __global__ void __launch_bounds__(256) latent_merge_kernel(
         mma_commit(&bars[1]);
     }
     __syncwarp();
-    if (warp < 4) {
+    // epilogue: warp w reads TMEM lane quadrant w%4 (output features) and
+    // columns 16*(w/4).. (sequences); gate logits are loaded before the
+    // accumulators so their latency overlaps
+    if (warp < 4 * (nbox / 16)) {
+        const int quad = warp & 3, c0 = (warp >> 2) * 16;
+        const int d = quad * 32 + lane;
+        float g[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const bool ok = c0 + i < nb && vld[c0 + i];
+            g[i] = (ok && gate) ? __uint_as_float(uint32_t(
+                                      gate[(int64_t(b0 + c0 + i) * H + h) * kDv + d]) << 16)
+                                : 0.f;
+        }
         if (!mbar_wait(&bars[1], 0, wait_ns) && lane == 0) report(status, kStTimeout);
         tc_fence_after();
-        const int d = warp * 32 + lane;
-        for (int c0 = 0; c0 < nb; c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + c0, v);
-            tmem_ld_wait();
+        float v[16];
+        tmem_ld16(tmem + (uint32_t(quad * 32) << 16) + c0, v);
+        tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int b = b0 + c0 + i;
-                if (c0 + i >= nb || ts[b + 1] == ts[b]) continue;
-                const int64_t o = (int64_t(b) * H + h) * kDv + d;
-                float z = v[i];
-                if (gate) z *= sigmoidf_fast(__uint_as_float(uint32_t(gate[o]) << 16));
-                const __nv_bfloat16 x = __float2bfloat16_rn(z);
-                out[o] = *reinterpret_cast<const uint16_t*>(&x);
-            }
+        for (int i = 0; i < 16; ++i) {
+            if (c0 + i >= nb || !vld[c0 + i]) continue;
+            float z = v[i];
+            if (gate) z *= sigmoidf_fast(g[i]);
+            const __nv_bfloat16 x = __float2bfloat16_rn(z);
+            out[(int64_t(b0 + c0 + i) * H + h) * kDv + d] = *reinterpret_cast<const uint16_t*>(&x);
         }
     }
     tc_fence_before();
@@ -798,7 +852,7 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     e = cudaFuncSetAttribute(latent_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kMergeSmem));
     if (e != cudaSuccess) return e;
-    latent_merge_kernel<<<dim3(a.H, (a.B + nmrg - 1) / nmrg), 256, kMergeSmem, st>>>(
+    latent_merge_kernel<<<dim3(a.H, (a.B + nmrg - 1) / nmrg), kMergeWarps * 32, kMergeSmem, st>>>(
         wvmap, part, ml, sched, a.gate, a.out, a.B, a.H, nmrg, kn.wait_limit_ns, dev.status);
     return cudaGetLastError();
 }
