@@ -177,6 +177,34 @@ def make_latent_decode(lengths, H: int, gated: bool = True, device="cpu", config
                         default_scale() if scale is None else scale, H)
 
 
+@dataclass
+class DsaPrefill:
+    index_q: torch.Tensor  # [Tq,32,128]
+    index_k: torch.Tensor  # [Tk,128]
+    w: torch.Tensor        # [Tq,32] fp32
+    q: torch.Tensor        # [Tq,H,192] expanded-form queries
+    ckv: torch.Tensor      # [Tk,576] latent cache
+    w_kc: torch.Tensor     # [H,128,512]
+    w_vc: torch.Tensor     # [H,128,512]
+    gate: torch.Tensor | None  # [Tq,H*128]
+    scale: float
+    H: int
+
+
+def make_dsa_prefill(Tq: int, Tk: int, H: int = 96, gated: bool = True, device="cpu",
+                     config: int = 6) -> DsaPrefill:
+    """One prompt of Tq tokens after Tk - Tq cached positions: index queries,
+    keys and head weights as in make_dsa, the main cache as in
+    make_latent_decode (one sequence)."""
+    iq = _randn((Tq, INDEX_HEADS, INDEX_DIM), seed_of(config, T_IQ), device)
+    ik = _randn((Tk, INDEX_DIM), seed_of(config, T_IK), device)
+    w = _randn((Tq, INDEX_HEADS), seed_of(config, T_W), device, dtype=torch.float32)
+    lat = make_latent_decode([Tk], H, False, device, config)
+    q = _randn((Tq, H, DQK), seed_of(config, T_Q), device)
+    gate = _randn((Tq, H * DV), seed_of(config, T_GATE), device) if gated else None
+    return DsaPrefill(iq, ik, w, q, lat.ckv, lat.w_kc, lat.w_vc, gate, default_scale(), H)
+
+
 NAN_BF16 = 0x7FC0   # a quiet-NaN bit pattern, used to fill unused cache capacity
 
 
@@ -260,6 +288,10 @@ WORKLOADS = {
     # instead of 61,440): the decode workload's batch and length
     "latent_decode_b32_h96_t8192": dict(kind="latent_decode", config=5, B=32, H=96, T=8192,
                                         gated=True),
+    # DSA prefill: a 16384-token prompt, every token scoring its whole visible
+    # history and attending over its own top-2048 of the latent cache
+    "dsa_prefill_t16384": dict(kind="dsa_prefill", config=6, B=1, H=96, T=16384, topk=2048,
+                               gated=True),
     # smaller cases of the same kernels, a few GB on the device, for ncu captures
     "dsa_decode_b2_t16384": dict(kind="dsa", config=4, B=2, H=96, T=16384, topk=2048,
                                  profile_only=True),

@@ -294,3 +294,55 @@ def mla_decode_latent(q, ckv, cu_seqlens, w_kc, w_vc, gate, scale: float,
         ks.append(kb.reshape(-1))
         vs.append(vb.reshape(-1))
     return mla_decode(q, np.concatenate(ks), np.concatenate(vs), cu, gate, scale, lib=lib)
+
+
+# ---------------------------------------------------------------------------
+# DSA prefill (DSA post, eqs. (5), (6), (9), (10) for every new token, and the
+# complexity section: each token of a prompt scores its whole visible history
+# and keeps its own top-k).  A prompt of Tq tokens follows P = Tk - Tq cached
+# positions; token i sits at position P + i and sees positions 0..P+i.
+# ---------------------------------------------------------------------------
+def dsa_prefill_index_scores(index_q, index_k, w) -> np.ndarray:
+    """scores [Tq, Tk] in float64: sum_h w[i,h] * max(0, q^I[i,h] . k^I[s]) for
+    s <= P+i (eq. (5), the constant folded into w), -inf where s > P+i."""
+    iq, ik, ww = _f64(index_q), _f64(index_k), _f64(w)
+    Tq, Tk = iq.shape[0], ik.shape[0]
+    dots = np.einsum("ihd,sd->ihs", iq, ik)
+    scores = np.einsum("ih,ihs->is", ww, np.maximum(dots, 0.0))
+    P = Tk - Tq
+    mask = np.arange(Tk)[None, :] > (P + np.arange(Tq))[:, None]
+    scores[mask] = -np.inf
+    return scores
+
+
+def dsa_prefill_topk(scores, topk: int, lib=None) -> np.ndarray:
+    """Per token i, the top min(topk, P+i+1) visible positions (eq. (6)) by the
+    same ranking as dsa_topk: int32 [Tq, topk], ascending, -1 padded."""
+    s = _f64(scores)
+    Tq, Tk = s.shape
+    P = Tk - Tq
+    out = np.empty((Tq, topk), dtype=np.int32)
+    for i in range(Tq):
+        n = P + i + 1
+        out[i] = dsa_topk(s[i, :n], np.array([0, n], dtype=np.int64), topk, lib=lib)[0]
+    return out
+
+
+def dsa_prefill_latent(q, ckv, w_kc, w_vc, idx, gate, scale: float, lib=None) -> np.ndarray:
+    """Gated MLA of every prompt token over its own selection (eq. (9) on S_i,
+    then eq. (10)), with the keys and values expanded from the latent cache
+    (eq. (8)).  q [Tq,H,192], ckv [Tk,576], idx [Tq,topk] (-1 entries skipped).
+    Returns out [Tq,H*128] in float64."""
+    qq = _f64(q)
+    c = _f64(ckv)
+    ix = _i32(idx)
+    g = _f64(gate)
+    Tq, H = qq.shape[0], qq.shape[1]
+    out = np.empty((Tq, H * 128))
+    for i in range(Tq):
+        sel = ix[i][ix[i] >= 0]
+        k, v = expand_latent(c[sel], w_kc, w_vc)
+        cu = np.array([0, sel.size], dtype=np.int64)
+        out[i] = mla_decode(qq[i:i + 1], k.reshape(-1), v.reshape(-1), cu,
+                            None if g is None else g[i:i + 1], scale, lib=lib)[0]
+    return out
