@@ -519,7 +519,48 @@ class LatentDecodeWork:
         del self.d, self.out, self.ws
 
 
-WORK_KINDS = {"decode": DecodeWork, "latent_decode": LatentDecodeWork, "dsa": DsaWork, "index": IndexWork,
+class DsaPrefillWork:
+    """K3.1 Gated DSA prefill of one prompt: every token's index scores and
+    top-k, then every token's gated MLA over its own selection of the latent
+    cache (rows f2 and f3 of the scope)."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        T, H, K = w["T"], w["H"], w["topk"]
+        self.name, self.H, self.B, self.T, self.K = name, H, 1, T, K
+        self.lengths = [T]
+        self.d = mi.make_dsa_prefill(T, T, H, w["gated"], device=dev, config=w["config"])
+        self.idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        self.out = torch.empty((T, H * 128), dtype=torch.bfloat16, device=dev)
+        self.ws_i = torch.empty(mla.workspace_size(_lib.OP_PREFILL_INDEX_TOPK, T, 0, T, K),
+                                dtype=torch.uint8, device=dev)
+        self.ws_a = torch.empty(mla.workspace_size(_lib.OP_SPARSE_PREFILL_LATENT, T, H, T, K),
+                                dtype=torch.uint8, device=dev)
+        fi = acc.dsa_prefill_index_flops(T, T)
+        fa = acc.sparse_latent_attention_flops(T, T, H, K)
+        self.work = fi + fa
+        self.unit, self.bound, self.scale_unit = "TFLOP/s", "tensor", 1e12
+        self.launches_per_step = 7      # score, top-k, absorb, schedule, attention, fixup, out
+        self.kernels = [(_lib.OP_LATENT_DECODE, "mla_latent_kernel", fa),
+                        (_lib.OP_PREFILL_INDEX_TOPK, "dsa_prefill_score_kernel", fi)]
+
+    def step(self, stream):
+        d = self.d
+        self.mla.dsa_prefill_index_topk(d.index_q, d.index_k, d.w, self.K, topk_idx=self.idx,
+                                        ws=self.ws_i, stream=stream)
+        self.mla.mla_sparse_prefill_latent(d.q, d.ckv, self.idx, d.w_kc, d.w_vc, gate=d.gate,
+                                           out=self.out, scale=d.scale, ws=self.ws_a,
+                                           stream=stream)
+
+    def free(self):
+        del self.d, self.idx, self.out, self.ws_i, self.ws_a
+
+
+WORK_KINDS = {"decode": DecodeWork, "latent_decode": LatentDecodeWork,
+              "dsa_prefill": DsaPrefillWork, "dsa": DsaWork, "index": IndexWork,
               "prefill": PrefillWork, "chunked_prefill": ChunkedPrefillWork,
               "decode_cached": DecodeCachedWork}
 

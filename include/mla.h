@@ -66,7 +66,9 @@ enum {
     MLA_OP_INDEX_TOPK = 2,
     MLA_OP_SPARSE_DECODE = 3,
     MLA_OP_CACHE_APPEND = 4,
-    MLA_OP_LATENT_DECODE = 5
+    MLA_OP_LATENT_DECODE = 5,
+    MLA_OP_PREFILL_INDEX_TOPK = 6,
+    MLA_OP_SPARSE_PREFILL_LATENT = 7
 };
 
 /*
@@ -268,6 +270,54 @@ mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, cons
                           void* ws, size_t ws_bytes, mla_stream stream);
 
 /*
+ * DSA prefill indexer: index score and top-k for every token of a prompt
+ * (DSA post, eqs. (5) and (6) applied per token; its complexity section:
+ * every token scores its whole visible history).  Token i of the Tq new
+ * tokens sits at position Tk-Tq+i and sees positions 0..Tk-Tq+i.
+ *
+ *   index_q     [Tq,NH,128] index queries (NH must be 32)
+ *   index_k     [Tk,128]    index keys of the sequence (cached ones first)
+ *   w           [Tq,NH]     fp32 head weights (eq. (5) constant folded in)
+ *   topk_idx    [Tq,topk]   int32 out: per token, the min(topk, visible)
+ *               positions of largest score ranked by (score descending,
+ *               position ascending), ascending, -1 padded
+ *   topk_scores [Tq,topk]   fp32 out or NULL (-inf on padding and on rows
+ *               that keep every visible position)
+ *
+ * Requires 1 <= Tq <= Tk < 2^24, 1 <= topk <= 2048, NH == 32.  Workspace:
+ * mla_workspace_size(MLA_OP_PREFILL_INDEX_TOPK, Tq, 0, Tk, topk) bytes (the
+ * fp32 score rows, Tq x Tk rounded up).
+ */
+mla_status dsa_prefill_index_topk(const mla_bf16* index_q, const mla_bf16* index_k,
+                                  const float* w, int Tq, int Tk, int NH, int topk,
+                                  int32_t* topk_idx, float* topk_scores, void* ws,
+                                  size_t ws_bytes, mla_stream stream);
+
+/*
+ * DSA sparse prefill over the absorbed latent cache: every prompt token
+ * attends over its own selection (DSA post, eqs. (9), (10) on S_t, with the
+ * keys and values of eq. (8) absorbed as in mla_decode_latent).  Token i of
+ * the Tq new tokens sits at position Tk-Tq+i.
+ *
+ *   q        [Tq,H,192]  expanded-form queries
+ *   ckv      [Tk,576]    latent cache of the sequence (c_s ++ r_s per position)
+ *   topk_idx [Tq,topk]   int32 selections (dsa_prefill_index_topk's output):
+ *            token i uses its first min(topk, Tk-Tq+i+1) entries; -1 entries
+ *            are skipped; an entry outside [0, Tk-Tq+i] is skipped and
+ *            recorded as MLA_ERR_BAD_INDEX in the device status
+ *   w_kc, w_vc [H,128,512]; gate [Tq,H*128] or NULL; out [Tq,H*128]
+ *
+ * Requires H a multiple of 16 in [16, 96], 1 <= Tq <= Tk < 2^31,
+ * 1 <= topk <= 2048.  Workspace: mla_workspace_size(
+ * MLA_OP_SPARSE_PREFILL_LATENT, Tq, H, Tk, topk) bytes.
+ */
+mla_status mla_sparse_prefill_latent(const mla_bf16* q, const mla_bf16* ckv,
+                                     const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
+                                     const mla_bf16* w_kc, const mla_bf16* w_vc,
+                                     const mla_bf16* gate, mla_bf16* out, float scale, void* ws,
+                                     size_t ws_bytes, mla_stream stream);
+
+/*
  * Gated MLA over the selected positions only (DSA post eqs. (9), (10)); all
  * H heads of a sequence share its selection.
  *
@@ -287,7 +337,8 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
  * Bytes of workspace an operation needs (a multiple of 256; 0 if none).
  * `op` is one of MLA_OP_*; arguments an operation does not use are ignored
  * (prefill and cache_append: none needed; decode: B, H, max_seqlen;
- * index_topk: B, max_seqlen; sparse_decode: B, H, topk; latent_decode: B, H).  Returns 0 for invalid arguments.
+ * index_topk: B, max_seqlen; sparse_decode: B, H, topk; latent_decode: B, H;
+ * prefill_index_topk: B = Tq, max_seqlen = Tk; sparse_prefill_latent: B = Tq, H).  Returns 0 for invalid arguments.
  */
 size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk);
 
@@ -326,7 +377,9 @@ mla_status mla_debug_set(int knob, long long value);
  * (decode: the split-KV partial kernel; sparse decode: the same kernel in
  * gather mode; index_topk: the scoring kernel; prefill: the attention
  * kernel; cache_append: the copy kernel, also when a chunked prefill or a
- * cached decode step appends; latent_decode: the latent attention kernel).  mla_timing_read synchronises those events, returns the summed
+ * cached decode step appends; latent_decode: the latent attention kernel;
+ * prefill_index_topk: the prefill scoring kernel; sparse_prefill_latent: the
+ * latent attention kernel, counted under MLA_OP_LATENT_DECODE).  mla_timing_read synchronises those events, returns the summed
  * kernel time in milliseconds and the number of launches of operation `op`
  * (MLA_OP_*) since the last read, and resets the count.  Events are created
  * on first use and reused; no device memory is allocated.

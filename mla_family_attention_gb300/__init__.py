@@ -19,6 +19,9 @@ Entry points (names as in the C ABI):
   fixed-capacity caches (optionally appending the current token first)
 * ``mla_decode_latent(q, ckv, cu_seqlens, w_kc, w_vc, ...)`` decode over the absorbed
   576-feature latent cache
+* ``dsa_prefill_index_topk(index_q, index_k, w, ...)``  per-token DSA index + top-k
+* ``mla_sparse_prefill_latent(q, ckv, topk_idx, w_kc, w_vc, ...)`` every prompt token
+  over its own selection of the latent cache
 """
 from __future__ import annotations
 
@@ -324,6 +327,70 @@ def mla_decode_latent(q, ckv, cu_seqlens, max_seqlen: int, w_kc, w_vc, gate=None
                                      H, int(max_seqlen), _ptr(w_kc), _ptr(w_vc), _ptr(gate),
                                      _ptr(out), float(default_scale() if scale is None else scale),
                                      _ptr(ws), wsb, _stream(stream)), lib)
+    return out
+
+
+def dsa_prefill_index_topk(index_q, index_k, w, topk: int = MAX_TOPK, topk_idx=None,
+                           topk_scores=None, ws=None, stream=None):
+    """Per-token DSA index score + top-k for a prompt: index_q [Tq,32,128], index_k
+    [Tk,128] (token i sees positions 0..Tk-Tq+i), w [Tq,32] fp32 -> [Tq,topk] int32."""
+    torch = _torch()
+    _need(index_q, "index_q", torch.bfloat16)
+    if index_q.dim() != 3 or index_q.shape[2] != INDEX_DIM:
+        raise ValueError("index_q must be [Tq,NH,128]")
+    Tq, NH, _ = index_q.shape
+    _need(index_k, "index_k", torch.bfloat16, None, index_q.device)
+    if index_k.dim() != 2 or index_k.shape[1] != INDEX_DIM:
+        raise ValueError("index_k must be [Tk,128]")
+    Tk = index_k.shape[0]
+    _need(w, "w", torch.float32, (Tq, NH), index_q.device)
+    if topk_idx is None:
+        topk_idx = torch.empty((Tq, topk), dtype=torch.int32, device=index_q.device)
+    _need(topk_idx, "topk_idx", torch.int32, (Tq, topk), index_q.device)
+    if topk_scores is not None:
+        _need(topk_scores, "topk_scores", torch.float32, (Tq, topk), index_q.device)
+    nbytes = workspace_size(_lib.OP_PREFILL_INDEX_TOPK, Tq, 0, Tk, topk)
+    ws, wsb = _workspace(ws, nbytes, index_q.device)
+    lib = _lib.load()
+    _lib.check(lib.dsa_prefill_index_topk(_ptr(index_q), _ptr(index_k), _ptr(w), Tq, Tk, NH,
+                                          int(topk), _ptr(topk_idx), _ptr(topk_scores), _ptr(ws),
+                                          wsb, _stream(stream)), lib)
+    return topk_idx
+
+
+def mla_sparse_prefill_latent(q, ckv, topk_idx, w_kc, w_vc, gate=None, out=None, scale=None,
+                              ws=None, stream=None):
+    """DSA sparse prefill over the latent cache: q [Tq,H,192], ckv [Tk,576], topk_idx
+    [Tq,topk] int32 (token i at position Tk-Tq+i), w_kc / w_vc [H,128,512]."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [Tq,H,192]")
+    Tq, H, _ = q.shape
+    _need(ckv, "ckv", torch.bfloat16, None, q.device)
+    if ckv.dim() != 2 or ckv.shape[1] != 576:
+        raise ValueError("ckv must be [Tk,576]")
+    Tk = ckv.shape[0]
+    _need(topk_idx, "topk_idx", torch.int32, None, q.device)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != Tq:
+        raise ValueError("topk_idx must be [Tq,topk]")
+    topk = topk_idx.shape[1]
+    _need(w_kc, "w_kc", torch.bfloat16, (H, 128, 512), q.device)
+    _need(w_vc, "w_vc", torch.bfloat16, (H, DV, 512), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (Tq, H * DV), q.device)
+    if out is None:
+        out = torch.empty((Tq, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (Tq, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_SPARSE_PREFILL_LATENT, Tq, H, Tk, topk)
+    if nbytes == 0:
+        raise ValueError(f"unsupported sparse prefill shape Tq={Tq} H={H}")
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_sparse_prefill_latent(_ptr(q), _ptr(ckv), _ptr(topk_idx), Tq, Tk, topk, H,
+                                             _ptr(w_kc), _ptr(w_vc), _ptr(gate), _ptr(out),
+                                             float(default_scale() if scale is None else scale),
+                                             _ptr(ws), wsb, _stream(stream)), lib)
     return out
 
 

@@ -47,6 +47,21 @@ def latent_kv_bytes(lengths) -> int:
     return sum(int(t) for t in lengths) * (512 + 64) * BF16
 
 
+def dsa_prefill_index_flops(Tq: int, Tk: int) -> int:
+    """Index scoring of a prompt: 2*32*128 flops per visible (token, position) pair."""
+    return 2 * INDEX_HEADS * INDEX_DIM * causal_pairs(Tq, Tk)
+
+
+def sparse_latent_attention_flops(Tq: int, Tk: int, H: int, topk: int) -> int:
+    """Attention of every prompt token over its min(topk, visible) selected
+    positions in the absorbed latent form: 2*(576 + 512) flops per selected
+    (token, position, head), plus the W^K absorption and the W^V projection,
+    2*128*512 flops each per (token, head)."""
+    P = Tk - Tq
+    sel = sum(min(topk, P + i + 1) for i in range(Tq))
+    return sel * H * 2 * (576 + 512) + Tq * H * 2 * 2 * 128 * 512
+
+
 def append_bytes(B: int, H: int, Tn: int) -> int:
     """HBM bytes of appending Tn positions to every (b, h): read once, written once."""
     return 2 * B * Tn * kv_bytes_per_position(H)

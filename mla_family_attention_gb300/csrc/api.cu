@@ -79,7 +79,7 @@ struct TimerPool {
     std::vector<mla::KernelTimer> ev;
     size_t used = 0;
 };
-constexpr int kOps = 6;   // MLA_OP_PREFILL .. MLA_OP_LATENT_DECODE
+constexpr int kOps = 7;   // MLA_OP_PREFILL .. MLA_OP_PREFILL_INDEX_TOPK
 TimerPool g_pool[kOps];
 
 // Next event pair for `op` when timing is on, else an empty timer.
@@ -167,6 +167,10 @@ size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
         case MLA_OP_INDEX_TOPK:
             if (B < 1 || max_seqlen < 1 || max_seqlen > (1 << 24)) return 0;
             return mla::plan_index(B, max_seqlen).total;
+        case MLA_OP_PREFILL_INDEX_TOPK:
+            if (B < 1 || max_seqlen < B || max_seqlen >= (1 << 24)) return 0;
+            return mla::prefill_index_ws(B, max_seqlen);
+        case MLA_OP_SPARSE_PREFILL_LATENT:
         case MLA_OP_LATENT_DECODE: {
             if (B < 1 || H < 16 || H > 96 || H % 16 != 0) return 0;
             mla::DeviceInfo d;
@@ -414,6 +418,68 @@ mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64
     cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
                                               static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode_latent launch");
+}
+
+mla_status dsa_prefill_index_topk(const mla_bf16* index_q, const mla_bf16* index_k,
+                                  const float* w, int Tq, int Tk, int NH, int topk,
+                                  int32_t* topk_idx, float* topk_scores, void* ws,
+                                  size_t ws_bytes, mla_stream stream) {
+    REQUIRE(index_q && index_k && w && topk_idx, MLA_ERR_INVALID_ARG, "null pointer");
+    REQUIRE(aligned16(index_q) && aligned16(index_k), MLA_ERR_INVALID_ARG,
+            "index_q and index_k must be 16-byte aligned");
+    REQUIRE((reinterpret_cast<uintptr_t>(w) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(topk_scores) & 3u) == 0,
+            MLA_ERR_INVALID_ARG, "misaligned w or outputs");
+    REQUIRE(NH == mla::kIndexHeads, MLA_ERR_UNSUPPORTED, "NH must be 32 (got %d)", NH);
+    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
+            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
+    REQUIRE(Tq >= 1 && Tk >= Tq && Tk < (1 << 24), MLA_ERR_INVALID_ARG,
+            "need 1 <= Tq <= Tk < 2^24 (got Tq=%d Tk=%d)", Tq, Tk);
+    REQUIRE(int64_t(Tq) * mla::kIndexHeads < (int64_t(1) << 31), MLA_ERR_UNSUPPORTED,
+            "Tq too large for one call");
+    mla_status s = check_ws(ws, ws_bytes, mla::prefill_index_ws(Tq, Tk));
+    if (s != MLA_OK) return s;
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    mla::PrefillIndexArgs a{index_q, index_k, w, Tq, Tk, topk, topk_idx, topk_scores, ws};
+    cudaError_t e = mla::launch_prefill_index_topk(a, d, knobs(),
+                                                   take_timer(MLA_OP_PREFILL_INDEX_TOPK),
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_prefill_index_topk launch");
+}
+
+mla_status mla_sparse_prefill_latent(const mla_bf16* q, const mla_bf16* ckv,
+                                     const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
+                                     const mla_bf16* w_kc, const mla_bf16* w_vc,
+                                     const mla_bf16* gate, mla_bf16* out, float scale, void* ws,
+                                     size_t ws_bytes, mla_stream stream) {
+    REQUIRE(q && ckv && topk_idx && w_kc && w_vc && out, MLA_ERR_INVALID_ARG, "null pointer");
+    REQUIRE(aligned16(q) && aligned16(ckv) && aligned16(w_kc) && aligned16(w_vc) &&
+                aligned16(out) && (gate == nullptr || aligned16(gate)) &&
+                (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0,
+            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    REQUIRE(H >= 16 && H <= 96 && H % 16 == 0, MLA_ERR_UNSUPPORTED,
+            "H must be a multiple of 16 in [16, 96] (got %d)", H);
+    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
+            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
+    REQUIRE(Tq >= 1 && Tk >= Tq, MLA_ERR_INVALID_ARG, "need 1 <= Tq <= Tk (got Tq=%d Tk=%d)",
+            Tq, Tk);
+    REQUIRE(int64_t(Tq) * H < (int64_t(1) << 31) && Tq <= 65535 * 128, MLA_ERR_UNSUPPORTED,
+            "Tq too large for one call");
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    mla::DeviceInfo d;
+    mla_status s = device_info(&d);
+    if (s != MLA_OK) return s;
+    const mla::LatentPlan pl = mla::plan_latent(Tq, H, d.sms);
+    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
+    mla::LatentArgs a{q, ckv, nullptr, w_kc, w_vc, gate, out, Tq, H, Tk, Tk, scale, ws};
+    a.idx = topk_idx;
+    a.topk = topk;
+    a.P = Tk - Tq;
+    cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_sparse_prefill_latent launch");
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,

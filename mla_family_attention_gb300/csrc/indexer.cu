@@ -657,6 +657,307 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
     }
 }
 
+// ---------------------------------------------------------------------------
+// DSA prefill: every token of a prompt scores its own visible history and
+// keeps its own top-k (DSA post, eqs. (5), (6) per token; complexity section).
+// Token i (position P+i, P = Tk - Tq) sees positions 0..P+i.
+//
+// Scoring (dsa_prefill_score_kernel): one CTA per block of 8 tokens, heavy
+// (late) blocks first.  The block's 8 x 32 index queries are the N = 256
+// columns of a tcgen05 tile (B operand, resident), 128 index keys the M rows
+// (A operand, streamed by TMA through a 4-stage ring); two 256-column TMEM
+// accumulators alternate.  Eight epilogue warps each take 32 keys x 4 tokens:
+// ReLU per head, the token's head weights, the sum over the 32 heads, and a
+// coalesced store of the visible scores.
+// ---------------------------------------------------------------------------
+constexpr int kPQ = 8;                               // tokens per CTA
+constexpr int kPN = kPQ * kIndexHeads;               // 256 MMA columns
+constexpr int kPStages = 4;
+constexpr int kPQHalf = kPN * 64 * 2;                // 32 KB: 256 rows x 128 B
+constexpr int kPThreads = 10 * 32;
+constexpr size_t kPScoreSmem =
+    1024 + 2 * size_t(kPQHalf) + size_t(kPStages) * kStageBytes + kPN * 4 + 256;
+constexpr uint32_t kPIdesc = idesc_bf16_f32(128, kPN, false, false);
+
+struct PrefillScoreParams {
+    const float* w;          // [Tq][32]
+    float* scores;           // [Tq][stride]
+    int Tq, Tk, stride;
+    long long wait_ns;
+    int* status;
+};
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    dsa_prefill_score_kernel(const __grid_constant__ CUtensorMap kmap,
+                             const __grid_constant__ CUtensorMap qmap,
+                             const PrefillScoreParams p) {
+    extern __shared__ uint8_t psm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(psm_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* qsm = sm;                                        // [2][256 rows][64]
+    uint8_t* ring = sm + 2 * kPQHalf;                         // [stages][2][128 rows][64]
+    float* wsm = reinterpret_cast<float*>(ring + kPStages * kStageBytes);   // [8][32]
+    uint64_t* full = reinterpret_cast<uint64_t*>(wsm + kPN);
+    uint64_t* empty = full + kPStages;
+    uint64_t* afull = empty + kPStages;                       // [2] MMA -> epilogue
+    uint64_t* aempty = afull + 2;                             // [2] epilogue -> MMA
+    uint64_t* qfull = aempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qfull + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nqb = (p.Tq + kPQ - 1) / kPQ;
+    const int qb = nqb - 1 - int(blockIdx.x);                 // heavy blocks first
+    const int i0 = qb * kPQ;
+    const int P = p.Tk - p.Tq;
+    const int last_key = P + min(i0 + kPQ - 1, p.Tq - 1);
+    const int ntiles = last_key / kTile + 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&afull[i], 1);
+            mbar_init(&aempty[i], 8);
+        }
+        mbar_init(qfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < kPN; i += blockDim.x) {
+        const int t = i0 + i / kIndexHeads;
+        wsm[i] = t < p.Tq ? p.w[int64_t(t) * kIndexHeads + (i % kIndexHeads)] : 0.f;
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&qmap);
+            mbar_arrive_expect_tx(qfull, 2 * kPQHalf);
+            for (int hf = 0; hf < 2; ++hf)
+                tma_load_2d(qsm + hf * kPQHalf, &qmap, hf * 64, i0 * kIndexHeads, qfull);
+            int filled[kPStages] = {0, 0, 0, 0};
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j % kPStages, r = j / kPStages;
+                if (*abort_flag) break;
+                if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, p.wait_ns)) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[st], kStageBytes);
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_2d(ring + st * kStageBytes + hf * kAHalf, &kmap, hf * 64, j * kTile,
+                                &full[st]);
+                filled[st] = r + 1;
+            }
+            for (int i = 0; i < kPStages; ++i)
+                if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, p.wait_ns))
+                    report(p.status, kStTimeout);
+            if (!mbar_wait(qfull, 0, p.wait_ns)) report(p.status, kStTimeout);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait(qfull, 0, p.wait_ns);
+            const uint32_t qa = smem_u32(qsm), ra = smem_u32(ring);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int st = j % kPStages, acc = j & 1;
+                if (*abort_flag) { ok = false; break; }
+                if (j >= 2 && !mbar_wait(&aempty[acc], ((j - 2) >> 1) & 1, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(&full[st], (j / kPStages) & 1, p.wait_ns)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(
+                        ra + st * kStageBytes + (kk >> 2) * kAHalf + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd =
+                        smem_desc_sw128(qa + (kk >> 2) * kPQHalf + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ss(tmem + acc * kPN, ad, bd, kPIdesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&empty[st]);
+                mma_commit(&afull[acc]);
+            }
+            if (!ok) {
+                report(p.status, kStTimeout);
+                *abort_flag = 1;
+            }
+            // drain: wait for the last tile's MMAs before TMEM is released
+            if (ntiles > 0) mbar_wait(&afull[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, p.wait_ns);
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes of quadrant w%4 (keys) and the
+        // columns of tokens 4*half..4*half+3 of the block
+        const int quad = warp & 3, half = (warp - 2) >> 2;
+        for (int j = 0; j < ntiles; ++j) {
+            const int acc = j & 1;
+            if (!*abort_flag && !mbar_wait(&afull[acc], (j >> 1) & 1, p.wait_ns)) {
+                report(p.status, kStTimeout);
+                *abort_flag = 1;
+            }
+            tc_fence_after();
+            const int key = j * kTile + quad * 32 + lane;
+            float sc[4];
+#pragma unroll
+            for (int tq = 0; tq < 4; ++tq) {
+                const int col = (half * 4 + tq) * kIndexHeads;
+                float v[32];
+                tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + acc * kPN + col, v);
+                tmem_ld_wait();
+                float a = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < kIndexHeads; ++hh) a = fmaf(wsm[col + hh], fmaxf(v[hh], 0.f), a);
+                sc[tq] = a;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[acc]);
+#pragma unroll
+            for (int tq = 0; tq < 4; ++tq) {
+                const int i = i0 + half * 4 + tq;
+                if (i < p.Tq && key <= P + i) p.scores[int64_t(i) * p.stride + key] = sc[tq];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// Per-token top-k (dsa_prefill_topk_kernel): one CTA of 1024 threads per
+// token row, rows walked heavy-first by a persistent grid.  The same exact
+// radix select as the decode top-k (11 + 11 + 10 key bits, then a pass in
+// position order keeping the keys above the k-th and the lowest positions
+// among keys equal to it), on one CTA: the row's visible scores stay in
+// shared memory when they fit (16,384 positions), else each pass re-reads
+// them from L2.
+struct PrefillTopkParams {
+    const float* scores;     // [Tq][stride]
+    int Tq, Tk, stride, topk;
+    int32_t* out_idx;        // [Tq][topk]
+    float* out_scores;       // [Tq][topk] or null
+    int* status;
+};
+
+constexpr size_t kPTopkSmem = size_t(kStep) * 4 + kBins * 4;
+
+__global__ void __launch_bounds__(1024) dsa_prefill_topk_kernel(const PrefillTopkParams p) {
+    extern __shared__ float4 ptopk_dyn[];
+    float* vals = reinterpret_cast<float*>(ptopk_dyn);      // vals[u*1024 + tid]
+    unsigned* hist = reinterpret_cast<unsigned*>(vals + kStep);
+    __shared__ int sh[40];
+    const int tid = threadIdx.x;
+    const int P = p.Tk - p.Tq;
+    const int K = p.topk;
+    for (int rr = blockIdx.x; rr < p.Tq; rr += gridDim.x) {
+        const int row = p.Tq - 1 - rr;
+        const int n = P + row + 1;                           // visible positions
+        int32_t* oi = p.out_idx + size_t(row) * K;
+        float* os = p.out_scores ? p.out_scores + size_t(row) * K : nullptr;
+        if (n <= K) {                                        // every position is kept
+            for (int i = tid; i < K; i += blockDim.x) {
+                oi[i] = i < n ? i : -1;
+                if (os) os[i] = -INFINITY;
+            }
+            continue;
+        }
+        const float* s = p.scores + size_t(row) * p.stride;
+        const bool resident = n <= kStep;
+        auto stage = [&](int t0) {
+            float v[kSelPer];
+            load16(s, t0 + tid * kSelPer, n, v);
+#pragma unroll
+            for (int u = 0; u < kSelPer; ++u) vals[u * 1024 + tid] = v[u];
+        };
+        __syncthreads();                                    // previous row fully consumed
+        if (resident) stage(0);
+        // histogram over the keys whose bits above `shift + width` equal `pre`
+        auto level = [&](int shift, int nb, int width, uint32_t pre, bool all) {
+            for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+            __syncthreads();
+            for (int t0 = 0; t0 < n; t0 += kStep) {
+                if (!resident) {
+                    stage(t0);
+                    __syncthreads();
+                }
+                const int i0 = t0 + tid * kSelPer;
+#pragma unroll
+                for (int u = 0; u < kSelPer; ++u)
+                    if (i0 + u < n) {
+                        const uint32_t k = okey(vals[u * 1024 + tid]);
+                        if (all || (k >> (shift + width)) == pre)
+                            atomicAdd(&hist[(k >> shift) & uint32_t(nb - 1)], 1u);
+                    }
+                if (!resident) __syncthreads();
+            }
+            __syncthreads();
+        };
+        level(21, kBins, 11, 0, true);
+        int bin1, above1;
+        find_bin(hist, kBins, K, sh, &bin1, &above1);
+        level(10, kBins, 11, uint32_t(bin1), false);
+        int bin2, above2;
+        find_bin(hist, kBins, K - above1, sh, &bin2, &above2);
+        const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
+        level(0, 1024, 10, pre, false);
+        int bin3, above3;
+        find_bin(hist, 1024, K - above1 - above2, sh, &bin3, &above3);
+        const uint32_t kth = (pre << 10) | uint32_t(bin3);
+        const int need_eq = K - above1 - above2 - above3;
+        const bool all_eq = int(hist[bin3]) == need_eq;
+        // emit in position order
+        int out = 0, eq_seen = 0;
+        for (int t0 = 0; t0 < n; t0 += kStep) {
+            if (!resident) {
+                __syncthreads();
+                stage(t0);
+                __syncthreads();
+            }
+            const int i0 = t0 + tid * kSelPer;
+            uint32_t g = 0, e = 0;
+#pragma unroll
+            for (int u = 0; u < kSelPer; ++u)
+                if (i0 + u < n) {
+                    const uint32_t k = okey(vals[u * 1024 + tid]);
+                    g |= uint32_t(k > kth) << u;
+                    e |= uint32_t(k == kth) << u;
+                }
+            uint32_t keep = e;
+            if (!all_eq) {
+                int e_total;
+                int r = eq_seen + block_excl_scan(__popc(e), sh, &e_total);
+                keep = 0;
+                for (uint32_t m = e; m; m &= m - 1, ++r)
+                    if (r < need_eq) keep |= m & (~m + 1);
+                eq_seen += e_total;
+            }
+            const uint32_t take = g | keep;
+            int total;
+            int o = out + block_excl_scan(__popc(take), sh, &total);
+            for (uint32_t m = take; m; m &= m - 1, ++o) {
+                const int u = __ffs(m) - 1;
+                if (o < K) {
+                    oi[o] = i0 + u;
+                    if (os) os[o] = vals[u * 1024 + tid];
+                } else {
+                    report(p.status, kStInvalid);
+                }
+            }
+            out += total;
+        }
+    }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Score rows start on 16-byte boundaries so the top-k passes can load float4.
@@ -711,6 +1012,42 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
                              int(kTopkSmem));
     if (e != cudaSuccess) return e;
     dsa_topk_cluster_kernel<<<dim3(kCluster, a.B), 1024, kTopkSmem, st>>>(tp);
+    return cudaGetLastError();
+}
+
+size_t prefill_index_ws(int Tq, int Tk) {
+    return align256(size_t(Tq) * score_stride(Tk) * 4);
+}
+
+cudaError_t launch_prefill_index_topk(const PrefillIndexArgs& a, const DeviceInfo& dev,
+                                      const Knobs& kn, const KernelTimer& tm, cudaStream_t st) {
+    static_assert(kPScoreSmem <= 227 * 1024, "shared memory budget");
+    float* scores = static_cast<float*>(a.ws);
+    CUtensorMap kmap, qmap;
+    cudaError_t e = encode_tmap_2d_bf16(&kmap, a.index_k, kIndexDim, uint64_t(a.Tk),
+                                        kIndexDim * 2, 64, kTile);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&qmap, a.index_q, kIndexDim, uint64_t(a.Tq) * kIndexHeads,
+                            kIndexDim * 2, 64, kPN);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dsa_prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPScoreSmem));
+    if (e != cudaSuccess) return e;
+    PrefillScoreParams sp{a.w, scores, a.Tq, a.Tk, score_stride(a.Tk), kn.wait_limit_ns,
+                          dev.status};
+    if (tm.begin) cudaEventRecord(tm.begin, st);
+    dsa_prefill_score_kernel<<<(a.Tq + kPQ - 1) / kPQ, kPThreads, kPScoreSmem, st>>>(kmap, qmap,
+                                                                                   sp);
+    if (tm.end) cudaEventRecord(tm.end, st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dsa_prefill_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPTopkSmem));
+    if (e != cudaSuccess) return e;
+    PrefillTopkParams tp{scores, a.Tq, a.Tk, score_stride(a.Tk), a.topk, a.topk_idx, a.topk_scores,
+                         dev.status};
+    const int grid = a.Tq < 2 * dev.sms ? a.Tq : 2 * dev.sms;
+    dsa_prefill_topk_kernel<<<grid, 1024, kPTopkSmem, st>>>(tp);
     return cudaGetLastError();
 }
 

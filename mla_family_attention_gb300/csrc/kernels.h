@@ -110,6 +110,21 @@ IndexPlan plan_index(int B, int max_seqlen);
 cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& p, const DeviceInfo& dev,
                               const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 
+// ----------------------------- DSA prefill ---------------------------------
+struct PrefillIndexArgs {
+    const uint16_t* index_q;   // [Tq,32,128]
+    const uint16_t* index_k;   // [Tk,128]
+    const float* w;            // [Tq,32]
+    int Tq, Tk, topk;
+    int32_t* topk_idx;         // [Tq,topk]
+    float* topk_scores;        // [Tq,topk] or null
+    void* ws;                  // prefill_index_ws(Tq, Tk) bytes: fp32 score rows
+};
+
+size_t prefill_index_ws(int Tq, int Tk);
+cudaError_t launch_prefill_index_topk(const PrefillIndexArgs& a, const DeviceInfo& dev,
+                                      const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
+
 // ------------------------------ prefill -----------------------------------
 struct PrefillArgs {
     const uint16_t* q;       // [B,H,Tq,192]
@@ -144,9 +159,9 @@ constexpr int kLatent = 512;               // latent features c_s
 constexpr int kCkv = kLatent + 64;         // cached per position: c_s ++ r_s
 
 struct LatentArgs {
-    const uint16_t* q;       // [B,H,192] expanded-form queries
+    const uint16_t* q;       // [B,H,192] expanded-form queries (sparse prefill: B = tokens)
     const uint16_t* ckv;     // packed [total,576]
-    const int64_t* cu;       // [B+1]
+    const int64_t* cu;       // decode: [B+1]; null for sparse prefill
     const uint16_t* w_kc;    // [H,128,512]
     const uint16_t* w_vc;    // [H,128,512]
     const uint16_t* gate;    // [B,H*128] or null
@@ -155,11 +170,13 @@ struct LatentArgs {
     int64_t total;
     float scale;
     void* ws;
+    const int32_t* idx = nullptr;   // sparse prefill: [B][topk] selections
+    int topk = 0, P = 0;            // sparse prefill: selection width, cached positions
 };
 
 struct LatentPlan {
     int ctas;                 // attention CTAs (one per SM)
-    size_t qt_off, sched_off, part_off, ml_off, total;
+    size_t qt_off, sched_off, part_off, ml_off, z_off, total;
 };
 
 LatentPlan plan_latent(int B, int H, int sms);

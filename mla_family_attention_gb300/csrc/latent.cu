@@ -56,17 +56,33 @@ constexpr int kThreads = 320;                    // TMA warp, MMA warp, 8 softma
 constexpr int kColO = 2 * kLT;                   // O^T columns start after the score buffers
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kAhead = 4;                        // tiles prefetched into L2 ahead of the ring
-constexpr size_t kExtra = (2 * 2 * 128 + 2 * 128 + 128) * 4 + 256;
+constexpr size_t kExtra = (2 * 2 * 128 + 2 * 128 + 128 + 128) * 4 + 256;
 constexpr size_t kLatSmem = 1024 + kQBytes + kPBytes + size_t(kSlots) * kSlot + kExtra;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kLT, false, false);
 
+// Work split written by latent_sched_kernel: n tiles in all, `per` tiles
+// per CTA, the number of sequences that span CTAs, the tile prefix, the
+// partial-slot prefix (nonzero only for spanning sequences), and their list.
+struct Sched {
+    const int* base;
+    __device__ int n() const { return base[0]; }
+    __device__ int per() const { return base[1]; }
+    __device__ int nmulti() const { return base[2]; }
+    __device__ const int* ts() const { return base + 3; }
+    __device__ const int* seg(int B) const { return base + 3 + (B + 1); }
+    __device__ const int* mlist(int B) const { return base + 3 + 2 * (B + 1); }
+};
+
 struct LatParams {
-    const int* sched;        // n, per, ts[B+1], seg[B+1]
-    const int64_t* cu;
+    const int* sched;
+    const int64_t* cu;       // decode: [B+1] packed positions of each sequence
+    const int32_t* idx;      // sparse prefill: [B][topk] selections, else null
+    int topk, P;             // sparse prefill: selection width; cached positions before token 0
     const uint16_t* ckv;     // for L2 prefetches ahead of the ring
     int64_t total;           // rows of ckv
-    float* part;             // [slots][H][512] unnormalised O
+    float* part;             // [slots][H][512] unnormalised O of segments of spanning sequences
     float* ml;               // [slots][H][2]: max (log2 units), sum
+    uint16_t* zbuf;          // [B][H][512] bf16 normalised latent outputs
     int B, H;
     float scale_log2;
     long long wait_ns;
@@ -100,6 +116,48 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// A "sequence" of the latent kernel: a decode sequence (rows row0..row0+T-1
+// of the cache) or one prompt token of a sparse prefill (the first T entries
+// of its selection, positions below vis).
+struct SeqDesc {
+    int64_t row0;
+    int T, vis;
+};
+
+__device__ __forceinline__ SeqDesc seq_desc(const LatParams& p, int b) {
+    if (p.idx) {
+        const int vis = p.P + b + 1;
+        return SeqDesc{0, min(p.topk, vis), vis};
+    }
+    const int64_t r0 = p.cu[b];
+    return SeqDesc{r0, int(p.cu[b + 1] - r0), 0};
+}
+
+// Selection entry e of token b (sparse prefill), -1 past the token's count.
+__device__ __forceinline__ int sel_raw(const LatParams& p, int b, const SeqDesc& sd, int e) {
+    return e < sd.T ? __ldg(p.idx + int64_t(b) * p.topk + e) : -1;
+}
+
+// Cache row of a selection entry and whether it names a visible position;
+// padding and invalid entries read row 0 and are masked by the softmax.
+__device__ __forceinline__ int sel_row(const LatParams& p, const SeqDesc& sd, int v, bool* valid) {
+    *valid = v >= 0 && v < sd.vis;
+    if (!*valid && (v < -1 || v >= sd.vis)) report(p.status, kStBadIndex);
+    return *valid ? v : 0;
+}
+
+// TMA gather of four 64-feature rows (one 128-byte row each) into shared
+// memory; the tensor map's box is one row high.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Walks a CTA's tile range [t0, t1) sequence by sequence.
 struct Cursor {
     const int* ts;
@@ -119,6 +177,7 @@ struct Cursor {
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_latent_kernel(const __grid_constant__ CUtensorMap cmap,
+                      const __grid_constant__ CUtensorMap gmap,
                       const __grid_constant__ CUtensorMap qmap, const LatParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -129,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xmax = reinterpret_cast<float*>(ring + kSlots * kSlot);   // [2][2][128]
     float* xsum = xmax + 2 * 2 * 128;                                // [2][128]
     float* fsm = xsum + 2 * 128;                                     // [128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(fsm + 128);
+    float* inv_l = fsm + 128;                                        // [128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(inv_l + 128);
     uint64_t* empty = full + kSlots;
     uint64_t* sfull = empty + kSlots;      // [2] MMA -> softmax
     uint64_t* sfree = sfull + 2;           // [2] softmax -> MMA
@@ -144,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, B = p.B;
-    const int n = p.sched[0], per = p.sched[1];
-    const int* ts = p.sched + 2;
-    const int* seg = ts + B + 1;
+    const Sched sch{p.sched};
+    const int n = sch.n(), per = sch.per();
+    const int* ts = sch.ts();
+    const int* seg = sch.seg(B);
+    const bool sparse = p.idx != nullptr;
     const int c = blockIdx.x;
     const int t0 = min(n, c * per), t1 = min(n, t0 + per);
 
@@ -181,9 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------- TMA -------------------------------
-        if (lane == 0 && t0 < t1) {
-            tma_prefetch_desc(&cmap);
-            tma_prefetch_desc(&qmap);
+        // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.
+        // Sparse prefill: the lanes read the tile's 64 selection entries and
+        // each issues gather4 loads of four selected rows.
+        if (t0 < t1) {
+            if (lane == 0) {
+                tma_prefetch_desc(sparse ? &gmap : &cmap);
+                tma_prefetch_desc(&qmap);
+            }
             const uint64_t policy = l2_evict_first_policy();
             int filled[kSlots];
             for (int s = 0; s < kSlots; ++s) filled[s] = 0;
@@ -200,50 +267,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (r1 > r0)
                     prefetch_l2(p.ckv + r0 * kCkv, uint32_t((r1 - r0) * kCkv * 2));
             };
-            for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
+            if (!sparse && lane == 0)
+                for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
             bool ok = true;
+            // sparse prefill: the next tile's selection entries are loaded one
+            // tile ahead, so their latency is off the gather path
+            Cursor nxt{ts};
+            nxt.seek(t0, B);
+            int na = -1, nb = -1;
+            if (sparse) {
+                const SeqDesc s0 = seq_desc(p, nxt.b);
+                const int e = (t0 - ts[nxt.b]) * kLT + 2 * lane;
+                na = sel_raw(p, nxt.b, s0, e);
+                nb = sel_raw(p, nxt.b, s0, e + 1);
+            }
             for (int t = t0; t < t1 && ok; ++t) {
-                if (t + kAhead < t1) prefetch_tile(t + kAhead);
+                if (!sparse && lane == 0 && t + kAhead < t1) prefetch_tile(t + kAhead);
                 cur.advance(t);
                 const int b = cur.b;
+                const SeqDesc sd = seq_desc(p, b);
+                const int va = na, vb = nb;
+                if (sparse && t + 1 < t1) {
+                    nxt.advance(t + 1);
+                    const SeqDesc s1 = seq_desc(p, nxt.b);
+                    const int e = (t + 1 - ts[nxt.b]) * kLT + 2 * lane;
+                    na = sel_raw(p, nxt.b, s1, e);
+                    nb = sel_raw(p, nxt.b, s1, e + 1);
+                }
                 if (t == t0 || t == ts[b]) {
-                    // Q~ of sequence b, once the previous segment's Q.K^T is done
-                    if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
-                        fail();
-                        break;
+                    // q~ of sequence b, once the previous segment's Q.K^T is done
+                    bool go = true;
+                    if (lane == 0) {
+                        if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
+                            fail();
+                            go = false;
+                        } else {
+                            mbar_arrive_expect_tx(qfull, 9 * H * 128);
+                            for (int kb = 0; kb < 9; ++kb)
+                                tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                        }
                     }
-                    mbar_arrive_expect_tx(qfull, 9 * H * 128);
-                    for (int kb = 0; kb < 9; ++kb)
-                        tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                    if (!__shfl_sync(0xffffffffu, go, 0)) break;
                     ++nseg;
                 }
-                const int row = int(p.cu[b]) + (t - ts[b]) * kLT;
+                const int e0 = (t - ts[b]) * kLT;
+                int ra = 0, rb = 0;
+                if (sparse) {
+                    bool ua, ub;
+                    ra = sel_row(p, sd, va, &ua);
+                    rb = sel_row(p, sd, vb, &ub);
+                }
+                const int row = int(sd.row0) + e0;
+                const int g = lane & 15, hfl = lane >> 4;
+                const int g0 = __shfl_sync(0xffffffffu, ra, 2 * g);
+                const int g1 = __shfl_sync(0xffffffffu, rb, 2 * g);
+                const int g2 = __shfl_sync(0xffffffffu, ra, 2 * g + 1);
+                const int g3 = __shfl_sync(0xffffffffu, rb, 2 * g + 1);
                 for (int i = 0; i < kFills; ++i, ++fill) {
                     const int slot = fill % kSlots, round = fill / kSlots;
-                    if (*abort_flag) { ok = false; break; }
-                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
-                        fail();
-                        ok = false;
-                        break;
+                    bool go = true;
+                    if (lane == 0) {
+                        if (*abort_flag) {
+                            go = false;
+                        } else if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                            fail();
+                            go = false;
+                        } else {
+                            mbar_arrive_expect_tx(&full[slot], i == 0 ? kHalf : kSlot);
+                            filled[slot] = round + 1;
+                        }
                     }
+                    if (!__shfl_sync(0xffffffffu, go, 0)) { ok = false; break; }
                     uint8_t* dst = ring + slot * kSlot;
-                    if (i == 0) {              // shared-key features 512..575
-                        mbar_arrive_expect_tx(&full[slot], kHalf);
-                        tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
-                    } else {                   // latent features 128*(i-1) .. +127
-                        mbar_arrive_expect_tx(&full[slot], kSlot);
-                        tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot], policy);
-                        tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row, &full[slot],
-                                         policy);
+                    if (!sparse) {
+                        if (lane == 0) {
+                            if (i == 0) {              // shared-key features 512..575
+                                tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
+                            } else {                   // latent features 128*(i-1) .. +127
+                                tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot],
+                                                 policy);
+                                tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
+                                                 &full[slot], policy);
+                            }
+                        }
+                    } else if (hfl < (i == 0 ? 1 : 2)) {
+                        const int x = i == 0 ? kLatent : 128 * (i - 1) + 64 * hfl;
+                        tma_gather4(dst + hfl * kHalf + g * 512, &gmap, x, g0, g1, g2, g3,
+                                    &full[slot]);
                     }
-                    filled[slot] = round + 1;
                 }
             }
-            for (int s = 0; s < kSlots; ++s)
-                if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
+            if (lane == 0) {
+                for (int s = 0; s < kSlots; ++s)
+                    if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
+                        report(p.status, kStTimeout);
+                if (nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
-            if (nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
-                report(p.status, kStTimeout);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------- MMA -------------------------------
@@ -347,8 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
         float m = 0.f, l = 0.f;
         int nseg = -1;
-        Cursor cur{ts};
-        if (t0 < t1) cur.seek(t0, B);
+        Cursor cur{ts}, nxt{ts};
+        int nraw = -1;                        // sparse: this lane's entry of the next tile
+        if (t0 < t1) {
+            cur.seek(t0, B);
+            nxt.seek(t0, B);
+            if (sparse)
+                nraw = sel_raw(p, nxt.b, seq_desc(p, nxt.b), (t0 - ts[nxt.b]) * kLT + half * 32 + lane);
+        }
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (*abort_flag) return;
             if (!mbar_wait(bar, parity, p.wait_ns)) fail();
@@ -357,11 +483,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = t - t0;
             cur.advance(t);
             const int b = cur.b;
+            const int raw = nraw;
+            if (sparse && t + 1 < t1) {
+                nxt.advance(t + 1);
+                nraw = sel_raw(p, nxt.b, seq_desc(p, nxt.b),
+                               (t + 1 - ts[nxt.b]) * kLT + half * 32 + lane);
+            }
             const bool first = (t == t0 || t == ts[b]);
             const bool last = (t + 1 == t1 || t + 1 == ts[b + 1]);
             if (first) ++nseg;
-            const int T = int(p.cu[b + 1] - p.cu[b]);
+            const SeqDesc sd = seq_desc(p, b);
             const int key0 = (t - ts[b]) * kLT + half * 32;
+            // keys of this warp's 32 columns that take part in the softmax
+            uint32_t valid;
+            if (sparse) {
+                bool v;
+                sel_row(p, sd, raw, &v);
+                valid = __ballot_sync(0xffffffffu, v);
+            } else {
+                const int nk = sd.T - key0;
+                valid = nk >= 32 ? 0xffffffffu : (nk <= 0 ? 0u : (1u << nk) - 1u);
+            }
             const int sb = j & 1;
             wait(&sfull[sb], (j >> 1) & 1);
             tc_fence_after();
@@ -374,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float lm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float x = key0 + i < T ? s[i] * p.scale_log2 : -INFINITY;
+                const float x = (valid >> i) & 1u ? s[i] * p.scale_log2 : -INFINITY;
                 s[i] = x;
                 lm = fmaxf(lm, x);
             }
@@ -434,25 +576,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull);
             if (last) {
-                // segment done: row sums, then O^T and (m, l) to the partial slot
+                // segment done: row sums; a sequence wholly inside this CTA
+                // writes its normalised output z~ (bf16), a spanning one its
+                // partial (O^T, m, l) for the fixup pass
                 xsum[half * 128 + r] = l;
                 named_bar_sync(1, 256);
-                const int slot = seg[b] + (c - ts[b] / per);
-                if (half == 0 && real) {
-                    p.ml[(int64_t(slot) * H + r) * 2] = m;
-                    p.ml[(int64_t(slot) * H + r) * 2 + 1] = xsum[r] + xsum[128 + r];
+                const float L = xsum[r] + xsum[128 + r];
+                const bool single = seg[b + 1] == seg[b];
+                const int slot = single ? 0 : seg[b] + (c - ts[b] / per);
+                if (half == 0) {
+                    inv_l[r] = L > 0.f ? 1.f / L : 0.f;
+                    if (!single && real) {
+                        p.ml[(int64_t(slot) * H + r) * 2] = m;
+                        p.ml[(int64_t(slot) * H + r) * 2 + 1] = L;
+                    }
                 }
+                named_bar_sync(1, 256);
                 wait(ofinal, nseg & 1);
                 tc_fence_after();
                 for (int uu = 0; uu < 2; ++uu) {
-                    const int u = 2 * half + uu;
-                    float* dst = p.part + int64_t(slot) * H * kLatent + u * 128 + quad * 32 + lane;
+                    const int u = 2 * half + uu, dim = u * 128 + quad * 32 + lane;
                     for (int c0 = 0; c0 < H; c0 += 16) {
                         float v[16];
                         tmem_ld16(lane_base + kColO + u * H + c0, v);
                         tmem_ld_wait();
+                        if (single) {
+                            uint16_t* dst = p.zbuf + int64_t(b) * H * kLatent + dim;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) dst[int64_t(c0 + i) * kLatent] = v[i];
+                            for (int i = 0; i < 16; ++i) {
+                                const __nv_bfloat16 x = __float2bfloat16_rn(v[i] * inv_l[c0 + i]);
+                                dst[int64_t(c0 + i) * kLatent] = *reinterpret_cast<const uint16_t*>(&x);
+                            }
+                        } else {
+                            float* dst = p.part + int64_t(slot) * H * kLatent + dim;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) dst[int64_t(c0 + i) * kLatent] = v[i];
+                        }
                     }
                 }
                 tc_fence_before();
@@ -590,26 +749,32 @@ __device__ int block_scan_excl(int v, int* warp_sums, int* total) {
     return excl;
 }
 
-// Tile prefix ts[b] (64-position tiles per sequence), n = ts[B], per =
-// ceil(n / G) tiles per CTA, and segment prefix seg[b] (number of CTA ranges
-// sequence b overlaps).  A sequence with T_b outside [1, max_seqlen] gets no
-// tiles and is reported.
-__global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, int B,
+// The work split.  Tiles per sequence: ceil(T_b / 64) (decode: T_b from the
+// packed lengths, 0 when outside [1, max_seqlen], which is reported; sparse
+// prefill: T_b = min(topk, P+b+1) selection entries).  n tiles in all, `per`
+// = ceil(n / G) per CTA; a sequence whose tiles span several CTAs gets one
+// partial slot per CTA (seg prefix) and a place in the fixup list.
+__global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, const int32_t* idx,
+                                                            int topk, int P, int B,
                                                             int max_seqlen, int G, int* sched,
                                                             int* status) {
     __shared__ int warp_sums[32];
-    int* ts = sched + 2;
+    int* ts = sched + 3;
     int* seg = ts + B + 1;
+    int* mlist = seg + B + 1;
     const int per_thr = (B + blockDim.x - 1) / blockDim.x;
     const int b0 = min(B, int(threadIdx.x) * per_thr), b1 = min(B, b0 + per_thr);
     auto tiles = [&](int b) -> int {
+        if (idx) return (min(topk, P + b + 1) + kLT - 1) / kLT;
         const int64_t T = cu[b + 1] - cu[b];
         return (T >= 1 && T <= max_seqlen) ? int((T + kLT - 1) / kLT) : 0;
     };
     int local = 0;
     for (int b = b0; b < b1; ++b) {
-        const int64_t T = cu[b + 1] - cu[b];
-        if (T < 1 || T > max_seqlen) report(status, kStInvalid);
+        if (!idx) {
+            const int64_t T = cu[b + 1] - cu[b];
+            if (T < 1 || T > max_seqlen) report(status, kStInvalid);
+        }
         local += tiles(b);
     }
     int n;
@@ -621,175 +786,202 @@ __global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, i
     if (threadIdx.x == 0) ts[B] = n;
     const int per = max(1, (n + G - 1) / G);
     __syncthreads();
-    local = 0;
-    for (int b = b0; b < b1; ++b) {
+    auto nseg = [&](int b) -> int {
         const int nt = ts[b + 1] - ts[b];
-        if (nt > 0) local += (ts[b] + nt - 1) / per - ts[b] / per + 1;
+        if (nt == 0) return 0;
+        const int clo = ts[b] / per, chi = (ts[b] + nt - 1) / per;
+        return chi > clo ? chi - clo + 1 : 0;
+    };
+    local = 0;
+    int lm = 0;
+    for (int b = b0; b < b1; ++b) {
+        local += nseg(b);
+        lm += nseg(b) > 0;
     }
-    int nseg;
-    run = block_scan_excl(local, warp_sums, &nseg);
+    int nslots;
+    run = block_scan_excl(local, warp_sums, &nslots);
+    int nmulti;
+    int mrun = block_scan_excl(lm, warp_sums, &nmulti);
     for (int b = b0; b < b1; ++b) {
         seg[b] = run;
-        const int nt = ts[b + 1] - ts[b];
-        if (nt > 0) run += (ts[b] + nt - 1) / per - ts[b] / per + 1;
+        const int k = nseg(b);
+        run += k;
+        if (k > 0) mlist[mrun++] = b;
     }
     if (threadIdx.x == 0) {
-        seg[B] = nseg;
+        seg[B] = nslots;
         sched[0] = n;
         sched[1] = per;
+        sched[2] = nmulti;
     }
 }
 
-// Per head h and up to 64 sequences: merge the segments' (O, m, l) by
-// log-sum-exp into z~ (bf16, in shared memory), then z = W^V_h z~ as one
-// tensor-core GEMM (M = 128 output features, N = sequences, K = 512 latent
-// features; A = W^V_h by TMA, B = z~) and the sigmoid gate.
-constexpr int kMergeN = 64;        // sequences per CTA at most
-constexpr int kMergeWarps = 32;
-constexpr size_t kMergeSmem = 1024 + 8 * 16384 + size_t(8) * kMergeN * 128 + 32 + 4 * kMergeN;
+// Fixup: the sequences whose tiles spanned several CTAs.  Warp w of CTA
+// (h, y) takes list entry 8y+w, merges its segments' (O, m, l) by
+// log-sum-exp and writes the normalised z~ (bf16) like a single-CTA
+// sequence.  Lane holds latent features 2*lane + 64*k (k < 8); the segments'
+// maxima and sums are read by the lanes in parallel, then the partial rows
+// are independent weighted sums, loaded two segments at a time.
+__global__ void __launch_bounds__(256) latent_fixup_kernel(const float* part, const float* ml,
+                                                           const int* sched_base, uint16_t* zbuf,
+                                                           int B, int H) {
+    const Sched sch{sched_base};
+    const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = blockIdx.y * 8 + warp;
+    if (k >= sch.nmulti()) return;
+    const int b = sch.mlist(B)[k];
+    const int* seg = sch.seg(B);
+    const int s0 = seg[b], ns = seg[b + 1] - s0;
+    float M = -INFINITY, L = 0.f;                // lane-local over segments lane, lane+32, ...
+    for (int i = lane; i < ns; i += 32) {
+        const float2 v = *reinterpret_cast<const float2*>(ml + (int64_t(s0 + i) * H + h) * 2);
+        const float Mn = fmaxf(M, v.x);
+        L = L * ex2(M - Mn) + v.y * ex2(v.x - Mn);
+        M = Mn;
+    }
+    float Mw = M;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
+    L = M == -INFINITY ? 0.f : L * ex2(M - Mw);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float z[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) z[q] = 0.f;
+    for (int i0 = 0; i0 < ns; i0 += 2) {
+        float2 pv[2][8];
+        float wgt[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = min(i0 + q, ns - 1);
+            const float* row = part + (int64_t(s0 + i) * H + h) * kLatent + 2 * lane;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) pv[q][kk] = *reinterpret_cast<const float2*>(row + 64 * kk);
+            wgt[q] = i0 + q < ns ? ex2(ml[(int64_t(s0 + i) * H + h) * 2] - Mw) * inv : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                z[2 * kk] = fmaf(wgt[q], pv[q][kk].x, z[2 * kk]);
+                z[2 * kk + 1] = fmaf(wgt[q], pv[q][kk].y, z[2 * kk + 1]);
+            }
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(zbuf + (int64_t(b) * H + h) * kLatent + 2 * lane);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) dst[32 * kk] = pack2(z[2 * kk], z[2 * kk + 1]);
+}
 
-__global__ void __launch_bounds__(kMergeWarps * 32) latent_merge_kernel(
-    const __grid_constant__ CUtensorMap wvmap, const float* part, const float* ml,
-    const int* sched, const uint16_t* gate, uint16_t* out, int B, int H, int nbox,
-    long long wait_ns, int* status) {
+// Output projection and gate: for head h and 128 sequences (rows),
+//   out[b, h*128+d] = sigmoid(gate[b, h*128+d]) * sum_j z~[b,h,j] W^V_h[d,j]
+// as a tensor-core GEMM with the sequences as M (A = z~ rows, K-major), the
+// 128 output features as N (B = W^V_h, K-major) and K = 512 latent features,
+// streamed in eight 64-feature blocks through a four-stage ring.
+constexpr int kOutStages = 4;
+constexpr int kOutStage = 2 * 16384;             // z~ block + W^V block
+constexpr size_t kOutSmem = 1024 + size_t(kOutStages) * kOutStage + 128;
+constexpr uint32_t kIdescOut = idesc_bf16_f32(128, 128, false, false);
+
+__global__ void __launch_bounds__(192) latent_out_kernel(
+    const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wvmap,
+    const int* sched_base, const uint16_t* gate, uint16_t* out, int B, int H, long long wait_ns,
+    int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* wsm = sm;                                   // [8 blocks][128 d][64 j]
-    uint8_t* zsm = sm + 8 * 16384;                       // [8 blocks][nbox b][64 j]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(zsm + 8 * kMergeN * 128);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2);
-    int* vld = reinterpret_cast<int*>(tmem_holder + 1);   // [nbox] sequence has output
-    const int h = blockIdx.x, b0 = blockIdx.y * nbox;
-    const int nb = min(nbox, B - b0);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOutStages * kOutStage);
+    uint64_t* empty = full + kOutStages;
+    uint64_t* done = empty + kOutStages;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+    const int h = blockIdx.x, b0 = blockIdx.y * 128;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int per = sched[1];
-    const int* ts = sched + 2;
-    const int* seg = ts + B + 1;
+    const int* ts = Sched{sched_base}.ts();
     if (threadIdx.x == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < kOutStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(done, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_holder, 64);
+    if (warp == 1) tmem_alloc(tmem_holder, 128);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bars[0], 8 * 16384);
-        for (int kb = 0; kb < 8; ++kb)
-            tma_load_2d(wsm + kb * 16384, &wvmap, kb * 64, h * kDv, &bars[0]);
-    }
-    // z~ rows: warp w merges sequence w (and w+32, ...); lane holds latent
-    // features 2*lane + 64*k (k < 8), so each float2 load of a partial row is
-    // one coalesced 256-byte access.  The lanes read the segments' (max, sum)
-    // pairs in parallel; the partial rows are then independent weighted sums,
-    // loaded two segments at a time.
-    for (int bb = warp; bb < nbox; bb += kMergeWarps) {
-        const int b = b0 + bb;
-        const int nt = bb < nb ? ts[b + 1] - ts[b] : 0;
-        if (lane == 0) vld[bb] = nt > 0;
-        float z[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) z[k] = 0.f;
-        if (nt > 0) {
-            const int s0 = seg[b], ns = (ts[b] + nt - 1) / per - ts[b] / per + 1;
-            float M = -INFINITY, L = 0.f;       // lane-local over segments lane, lane+32, ...
-            for (int i = lane; i < ns; i += 32) {
-                const float2 v = *reinterpret_cast<const float2*>(ml + (int64_t(s0 + i) * H + h) * 2);
-                const float Mn = fmaxf(M, v.x);
-                L = L * ex2(M - Mn) + v.y * ex2(v.x - Mn);
-                M = Mn;
+    if (warp == 0 && lane == 0) {
+        int filled[kOutStages] = {0, 0, 0, 0};
+        for (int kb = 0; kb < 8; ++kb) {
+            const int st = kb % kOutStages, r = kb / kOutStages;
+            if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, wait_ns)) {
+                report(status, kStTimeout);
+                break;
             }
-            float Mw = M;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
-            L = M == -INFINITY ? 0.f : L * ex2(M - Mw);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            for (int i0 = 0; i0 < ns; i0 += 2) {
-                float2 pv[2][8];
-                float wgt[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int i = min(i0 + q, ns - 1);
-                    const float* row = part + (int64_t(s0 + i) * H + h) * kLatent + 2 * lane;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        pv[q][k] = *reinterpret_cast<const float2*>(row + 64 * k);
-                    wgt[q] = i0 + q < ns ? ex2(ml[(int64_t(s0 + i) * H + h) * 2] - Mw) * inv : 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        z[2 * k] = fmaf(wgt[q], pv[q][k].x, z[2 * k]);
-                        z[2 * k + 1] = fmaf(wgt[q], pv[q][k].y, z[2 * k + 1]);
-                    }
+            mbar_arrive_expect_tx(&full[st], kOutStage);
+            tma_load_3d(sm + st * kOutStage, &zmap, kb * 64, h, b0, &full[st]);
+            tma_load_2d(sm + st * kOutStage + 16384, &wvmap, kb * 64, h * kDv, &full[st]);
+            filled[st] = r + 1;
+        }
+        for (int i = 0; i < kOutStages; ++i)
+            if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, wait_ns))
+                report(status, kStTimeout);
+    } else if (warp == 1 && lane == 0) {
+        const uint32_t sa = smem_u32(sm);
+        bool ok = true;
+        for (int kb = 0; kb < 8 && ok; ++kb) {
+            const int st = kb % kOutStages;
+            if (!mbar_wait(&full[st], (kb / kOutStages) & 1, wait_ns)) {
+                report(status, kStTimeout);
+                ok = false;
+                break;
             }
-        }
-        // bf16 pairs into row bb of the eight K-major [nbox x 64] blocks
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int jc = lane * 4;                       // byte offset within the 128-byte row
-            uint8_t* row = zsm + k * nbox * 128 + (bb >> 3) * 1024 + (bb & 7) * 128;
-            *reinterpret_cast<uint32_t*>(row + ((((jc >> 4) ^ (bb & 7)) << 4) | (jc & 15))) =
-                pack2(z[2 * k], z[2 * k + 1]);
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (mbar_wait(&bars[0], 0, wait_ns)) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16_f32(128, nbox, false, false);
-            const uint32_t wa = smem_u32(wsm), za = smem_u32(zsm);
-            for (int kk = 0; kk < 32; ++kk) {
-                const uint64_t ad = smem_desc_sw128(wa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                const uint64_t bd =
-                    smem_desc_sw128(za + (kk >> 2) * nbox * 128 + (kk & 3) * 32, 16, 1024);
-                mma_bf16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc_sw128(sa + st * kOutStage + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(sa + st * kOutStage + 16384 + kk * 32, 16, 1024);
+                mma_bf16_ss(tmem, ad, bd, kIdescOut, (kb > 0 || kk > 0) ? 1u : 0u);
             }
-        } else {
-            report(status, kStTimeout);
+            mma_commit(&empty[st]);
         }
-        mma_commit(&bars[1]);
-    }
-    __syncwarp();
-    // epilogue: warp w reads TMEM lane quadrant w%4 (output features) and
-    // columns 16*(w/4).. (sequences); gate logits are loaded before the
-    // accumulators so their latency overlaps
-    if (warp < 4 * (nbox / 16)) {
-        const int quad = warp & 3, c0 = (warp >> 2) * 16;
-        const int d = quad * 32 + lane;
-        float g[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const bool ok = c0 + i < nb && vld[c0 + i];
-            g[i] = (ok && gate) ? __uint_as_float(uint32_t(
-                                      gate[(int64_t(b0 + c0 + i) * H + h) * kDv + d]) << 16)
-                                : 0.f;
-        }
-        if (!mbar_wait(&bars[1], 0, wait_ns) && lane == 0) report(status, kStTimeout);
+        mma_commit(done);
+    } else if (warp >= 2) {
+        // thread = sequence row (TMEM lane), 128 output features
+        const int quad = warp & 3, b = b0 + quad * 32 + lane;
+        if (!mbar_wait(done, 0, wait_ns) && lane == 0) report(status, kStTimeout);
         tc_fence_after();
-        float v[16];
-        tmem_ld16(tmem + (uint32_t(quad * 32) << 16) + c0, v);
-        tmem_ld_wait();
+        const bool live = b < B && ts[b + 1] > ts[b];
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + c0, v);
+            tmem_ld_wait();
+            if (!live) continue;
+            const int64_t o = (int64_t(b) * H + h) * kDv + c0;
+            uint32_t w[16];
+            if (gate) {
+                const uint4* g4 = reinterpret_cast<const uint4*>(gate + o);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (c0 + i >= nb || !vld[c0 + i]) continue;
-            float z = v[i];
-            if (gate) z *= sigmoidf_fast(g[i]);
-            const __nv_bfloat16 x = __float2bfloat16_rn(z);
-            out[(int64_t(b0 + c0 + i) * H + h) * kDv + d] = *reinterpret_cast<const uint16_t*>(&x);
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 gq = __ldg(g4 + q);
+                    const uint32_t gg[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[4 * q + e] = pack2(v[8 * q + 2 * e] * sigmoidf_fast(bf_lo(gg[e])),
+                                             v[8 * q + 2 * e + 1] * sigmoidf_fast(bf_hi(gg[e])));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = pack2(v[2 * e], v[2 * e + 1]);
+            }
+            uint4* o4 = reinterpret_cast<uint4*>(out + o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -799,12 +991,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 LatentPlan plan_latent(int B, int H, int sms) {
     LatentPlan pl{};
     pl.ctas = sms;
-    const size_t slots = size_t(sms) + B;
+    const size_t slots = 2 * size_t(sms);        // segments of sequences spanning CTAs
     pl.qt_off = 0;
-    pl.sched_off = align256(size_t(B) * H * kCkv * 2);
-    pl.part_off = pl.sched_off + align256((2 + 2 * size_t(B + 1)) * 4);
+    pl.sched_off = pl.qt_off + align256(size_t(B) * H * kCkv * 2);
+    pl.part_off = pl.sched_off + align256((3 + 2 * size_t(B + 1) + sms) * 4);
     pl.ml_off = pl.part_off + align256(slots * H * kLatent * 4);
-    pl.total = pl.ml_off + align256(slots * H * 2 * 4);
+    pl.z_off = pl.ml_off + align256(slots * H * 2 * 4);
+    pl.total = pl.z_off + align256(size_t(B) * H * kLatent * 2);
     return pl;
 }
 
@@ -816,11 +1009,11 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     int* sched = reinterpret_cast<int*>(ws + pl.sched_off);
     float* part = reinterpret_cast<float*>(ws + pl.part_off);
     float* ml = reinterpret_cast<float*>(ws + pl.ml_off);
+    uint16_t* zbuf = reinterpret_cast<uint16_t*>(ws + pl.z_off);
 
     // W^K as [H*128 rows (h, d)][512], W^V likewise; queries as [B][H][192]
     const int nabs = a.B < kAbsorbN ? (a.B + 15) / 16 * 16 : kAbsorbN;
-    const int nmrg = a.B < kMergeN ? (a.B + 15) / 16 * 16 : kMergeN;
-    CUtensorMap wkmap, wvmap, q3map, cmap, qmap;
+    CUtensorMap wkmap, wvmap, q3map, cmap, gmap, qmap, zmap;
     cudaError_t e = encode_tmap_2d_bf16(&wkmap, a.w_kc, kLatent, uint64_t(a.H) * 128, kLatent * 2,
                                         64, 128);
     if (e != cudaSuccess) return e;
@@ -829,31 +1022,40 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     e = encode_tmap_3d_bf16(&q3map, a.q, kDqk, a.H, a.B, kDqk * 2, uint64_t(a.H) * kDqk * 2, 64,
                             1, nabs);
     if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&cmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, kLT);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&gmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, 1);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_bf16(&qmap, qt, kCkv, uint64_t(a.B) * a.H, kCkv * 2, 64, a.H);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_3d_bf16(&zmap, zbuf, kLatent, a.H, a.B, kLatent * 2,
+                            uint64_t(a.H) * kLatent * 2, 64, 1, 128);
+    if (e != cudaSuccess) return e;
+
     e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kAbsorbSmem));
     if (e != cudaSuccess) return e;
     latent_absorb_kernel<<<dim3(4, a.H, (a.B + nabs - 1) / nabs), 128, kAbsorbSmem, st>>>(
         wkmap, q3map, a.q, qt, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
-    latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.max_seqlen, pl.ctas, sched, dev.status);
-    e = encode_tmap_2d_bf16(&cmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, kLT);
-    if (e != cudaSuccess) return e;
-    e = encode_tmap_2d_bf16(&qmap, qt, kCkv, uint64_t(a.B) * a.H, kCkv * 2, 64, a.H);
-    if (e != cudaSuccess) return e;
+    latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.idx, a.topk, a.P, a.B, a.max_seqlen, pl.ctas,
+                                           sched, dev.status);
     e = cudaFuncSetAttribute(mla_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kLatSmem));
     if (e != cudaSuccess) return e;
-    LatParams p{sched, a.cu, a.ckv, a.total, part, ml, a.B, a.H, a.scale * 1.4426950408889634f, kn.wait_limit_ns,
-                dev.status};
+    LatParams p{sched, a.cu, a.idx, a.topk, a.P, a.ckv, a.total, part, ml, zbuf, a.B, a.H,
+                a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
     if (tm.begin) cudaEventRecord(tm.begin, st);
-    mla_latent_kernel<<<pl.ctas, kThreads, kLatSmem, st>>>(cmap, qmap, p);
+    mla_latent_kernel<<<pl.ctas, kThreads, kLatSmem, st>>>(cmap, gmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(latent_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kMergeSmem));
+    latent_fixup_kernel<<<dim3(a.H, (pl.ctas + 7) / 8), 256, 0, st>>>(part, ml, sched, zbuf, a.B,
+                                                                      a.H);
+    e = cudaFuncSetAttribute(latent_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kOutSmem));
     if (e != cudaSuccess) return e;
-    latent_merge_kernel<<<dim3(a.H, (a.B + nmrg - 1) / nmrg), kMergeWarps * 32, kMergeSmem, st>>>(
-        wvmap, part, ml, sched, a.gate, a.out, a.B, a.H, nmrg, kn.wait_limit_ns, dev.status);
+    latent_out_kernel<<<dim3(a.H, (a.B + 127) / 128), 192, kOutSmem, st>>>(
+        zmap, wvmap, sched, a.gate, a.out, a.B, a.H, kn.wait_limit_ns, dev.status);
     return cudaGetLastError();
 }
 
