@@ -323,6 +323,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int g1 = __shfl_sync(0xffffffffu, rb, 2 * g);
                 const int g2 = __shfl_sync(0xffffffffu, ra, 2 * g + 1);
                 const int g3 = __shfl_sync(0xffffffffu, rb, 2 * g + 1);
+                if (!sparse) {
+                    // decode: one lane issues the tiled loads, no warp-wide sync
+                    if (lane == 0) {
+                        for (int i = 0; i < kFills; ++i, ++fill) {
+                            const int slot = fill % kSlots, round = fill / kSlots;
+                            if (*abort_flag) { ok = false; break; }
+                            if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                                fail();
+                                ok = false;
+                                break;
+                            }
+                            uint8_t* dst = ring + slot * kSlot;
+                            if (i == 0) {              // shared-key features 512..575
+                                mbar_arrive_expect_tx(&full[slot], kHalf);
+                                tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
+                            } else {                   // latent features 128*(i-1) .. +127
+                                mbar_arrive_expect_tx(&full[slot], kSlot);
+                                tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot],
+                                                 policy);
+                                tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
+                                                 &full[slot], policy);
+                            }
+                            filled[slot] = round + 1;
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    fill = __shfl_sync(0xffffffffu, fill, 0);
+                    continue;
+                }
                 for (int i = 0; i < kFills; ++i, ++fill) {
                     const int slot = fill % kSlots, round = fill / kSlots;
                     bool go = true;
@@ -636,7 +665,8 @@ constexpr size_t kAbsorbSmem = 1024 + 2 * 16384 + 2 * kAbsorbN * 128 + 64;
 
 __global__ void __launch_bounds__(128) latent_absorb_kernel(
     const __grid_constant__ CUtensorMap wkmap, const __grid_constant__ CUtensorMap qmap,
-    const uint16_t* q, uint16_t* qt, int B, int H, int nbox, long long wait_ns, int* status) {
+    const uint16_t* q, uint16_t* qt, const uint16_t* wv, int B, int H, int nbox,
+    long long wait_ns, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -658,6 +688,8 @@ __global__ void __launch_bounds__(128) latent_absorb_kernel(
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
     bool ok = true;
+    if (threadIdx.x == 32 && blockIdx.z == 0)   // W^V rows of this head's quarter, into L2
+        prefetch_l2(wv + (int64_t(h) * kDv + jb * 32) * kLatent, 32 * kLatent * 2);
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(&bars[0], 2 * 16384 + 2 * nbox * 128);
         for (int hf = 0; hf < 2; ++hf) {
@@ -885,8 +917,8 @@ constexpr uint32_t kIdescOut = idesc_bf16_f32(128, 128, false, false);
 
 __global__ void __launch_bounds__(192) latent_out_kernel(
     const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wvmap,
-    const int* sched_base, const uint16_t* gate, uint16_t* out, int B, int H, long long wait_ns,
-    int* status) {
+    const int* sched_base, const uint16_t* gate, uint16_t* out, int B, int H, int zrows,
+    long long wait_ns, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -918,7 +950,7 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
                 report(status, kStTimeout);
                 break;
             }
-            mbar_arrive_expect_tx(&full[st], kOutStage);
+            mbar_arrive_expect_tx(&full[st], 16384 + zrows * 128);
             tma_load_3d(sm + st * kOutStage, &zmap, kb * 64, h, b0, &full[st]);
             tma_load_2d(sm + st * kOutStage + 16384, &wvmap, kb * 64, h * kDv, &full[st]);
             filled[st] = r + 1;
@@ -947,34 +979,36 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
         }
         mma_commit(done);
     } else if (warp >= 2) {
-        // thread = sequence row (TMEM lane), 128 output features
+        // thread = sequence row (TMEM lane), 128 output features; the gate
+        // logits are loaded first so their latency overlaps the GEMM
         const int quad = warp & 3, b = b0 + quad * 32 + lane;
+        const bool live = b < B && ts[b + 1] > ts[b];
+        uint4 g[16];
+        const uint4* g4 = reinterpret_cast<const uint4*>(gate + (int64_t(b) * H + h) * kDv);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) g[q] = (live && gate) ? __ldg(g4 + q) : make_uint4(0, 0, 0, 0);
         if (!mbar_wait(done, 0, wait_ns) && lane == 0) report(status, kStTimeout);
         tc_fence_after();
-        const bool live = b < B && ts[b + 1] > ts[b];
+#pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
             float v[32];
             tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + c0, v);
             tmem_ld_wait();
             if (!live) continue;
-            const int64_t o = (int64_t(b) * H + h) * kDv + c0;
             uint32_t w[16];
-            if (gate) {
-                const uint4* g4 = reinterpret_cast<const uint4*>(gate + o);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 gq = __ldg(g4 + q);
-                    const uint32_t gg[4] = {gq.x, gq.y, gq.z, gq.w};
+            for (int q = 0; q < 4; ++q) {
+                const uint4 gq = g[c0 / 8 + q];
+                const uint32_t gg[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[4 * q + e] = pack2(v[8 * q + 2 * e] * sigmoidf_fast(bf_lo(gg[e])),
-                                             v[8 * q + 2 * e + 1] * sigmoidf_fast(bf_hi(gg[e])));
+                for (int e = 0; e < 4; ++e) {
+                    const float a = v[8 * q + 2 * e], c = v[8 * q + 2 * e + 1];
+                    w[4 * q + e] = gate ? pack2(a * sigmoidf_fast(bf_lo(gg[e])),
+                                                c * sigmoidf_fast(bf_hi(gg[e])))
+                                        : pack2(a, c);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = pack2(v[2 * e], v[2 * e + 1]);
             }
-            uint4* o4 = reinterpret_cast<uint4*>(out + o);
+            uint4* o4 = reinterpret_cast<uint4*>(out + (int64_t(b) * H + h) * kDv + c0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) o4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
@@ -1028,15 +1062,16 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     if (e != cudaSuccess) return e;
     e = encode_tmap_2d_bf16(&qmap, qt, kCkv, uint64_t(a.B) * a.H, kCkv * 2, 64, a.H);
     if (e != cudaSuccess) return e;
+    const int zrows = a.B < 128 ? (a.B + 15) / 16 * 16 : 128;   // rows a z~ box carries
     e = encode_tmap_3d_bf16(&zmap, zbuf, kLatent, a.H, a.B, kLatent * 2,
-                            uint64_t(a.H) * kLatent * 2, 64, 1, 128);
+                            uint64_t(a.H) * kLatent * 2, 64, 1, zrows);
     if (e != cudaSuccess) return e;
 
     e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kAbsorbSmem));
     if (e != cudaSuccess) return e;
     latent_absorb_kernel<<<dim3(4, a.H, (a.B + nabs - 1) / nabs), 128, kAbsorbSmem, st>>>(
-        wkmap, q3map, a.q, qt, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
+        wkmap, q3map, a.q, qt, a.w_vc, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
     latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.idx, a.topk, a.P, a.B, a.max_seqlen, pl.ctas,
                                            sched, dev.status);
     e = cudaFuncSetAttribute(mla_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1055,7 +1090,7 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
                              int(kOutSmem));
     if (e != cudaSuccess) return e;
     latent_out_kernel<<<dim3(a.H, (a.B + 127) / 128), 192, kOutSmem, st>>>(
-        zmap, wvmap, sched, a.gate, a.out, a.B, a.H, kn.wait_limit_ns, dev.status);
+        zmap, wvmap, sched, a.gate, a.out, a.B, a.H, zrows, kn.wait_limit_ns, dev.status);
     return cudaGetLastError();
 }
 
