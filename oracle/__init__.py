@@ -346,3 +346,47 @@ def dsa_prefill_latent(q, ckv, w_kc, w_vc, idx, gate, scale: float, lib=None) ->
         out[i] = mla_decode(qq[i:i + 1], k.reshape(-1), v.reshape(-1), cu,
                             None if g is None else g[i:i + 1], scale, lib=lib)[0]
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 caches (DSA post, cache section): the index key of a position is 128
+# one-byte FP8 features plus one fp32 scale (132 B); the main cache record is
+# 512 FP8 latent features, four fp32 scales (one per 128 features) and the 64
+# bf16 shared-key features (656 B).  The pages fix the byte counts, not the
+# encoding; the reading taken: e4m3 (the "fn" variant, largest finite 448),
+# scale = amax/448 per group in fp32, code = e4m3(x * (448/amax)) computed in
+# fp32 and rounded to nearest even; an all-zero group has scale 0 and zero
+# codes.  torch's float8_e4m3fn conversion is the rounding step.
+# ---------------------------------------------------------------------------
+def quantize_e4m3_rows(x):
+    """Rows of x -> (codes uint8 [rows, cols], scale float32 [rows])."""
+    import torch
+    xf = _f64(x).astype(np.float32)
+    xf = xf.reshape(-1, xf.shape[-1])
+    amax = np.abs(xf).max(axis=1).astype(np.float32)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(amax > 0, np.float32(448.0) / amax, np.float32(0.0)).astype(np.float32)
+    y = (xf * inv[:, None]).astype(np.float32)
+    codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    codes[amax == 0] = 0
+    return codes, scale
+
+
+def e4m3_values(codes) -> np.ndarray:
+    """The real values of e4m3 codes (float64, exact)."""
+    import torch
+    c = np.ascontiguousarray(_host(codes), dtype=np.uint8)
+    return torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def dsa_index_scores_fp8(index_q, k8, kscale, w, cu_seqlens, lib=None) -> np.ndarray:
+    """Index scores (eq. (5)) over FP8 index keys: the keys are the codes times
+    their scale, the queries are quantised per (sequence, head) the same way
+    and dequantised; the score is then computed in float64."""
+    iq = _f64(index_q)
+    B, NH, D = iq.shape
+    qc, qs = quantize_e4m3_rows(iq.reshape(B * NH, D))
+    q_deq = (e4m3_values(qc) * qs.astype(np.float64)[:, None]).reshape(B, NH, D)
+    k_deq = e4m3_values(k8) * _f64(kscale)[:, None]
+    return dsa_index_scores(q_deq, k_deq, w, cu_seqlens, lib=lib)
