@@ -376,6 +376,30 @@ class IndexWork:
         del self.d, self.idx, self.ws_i
 
 
+class IndexFp8Work(IndexWork):
+    """The DSA indexer over FP8 index keys (132 B per position)."""
+
+    def __init__(self, name, dev, batch=0):
+        super().__init__(name, dev, batch)
+        mla, _lib = self.mla, self.lib
+        self.k8, self.ks = mla.dsa_quantize_index_keys(self.d.index_k)
+        self.ws_i = torch.empty(mla.workspace_size(_lib.OP_INDEX_TOPK_FP8, self.B, 0,
+                                                   self.max_len, self.topk),
+                                dtype=torch.uint8, device=dev)
+        self.work = acc.index_key_bytes_fp8(self.lengths)
+        self.launches_per_step = 7      # query quantisation, tiles, score, 4 top-k passes
+        self.kernels = [(_lib.OP_INDEX_TOPK_FP8, "dsa_score_kernel<fp8>", self.work)]
+
+    def step(self, stream):
+        d = self.d
+        self.mla.dsa_index_topk_fp8(d.index_q, self.k8, self.ks, d.w, self.cu, self.max_len,
+                                    self.topk, topk_idx=self.idx, ws=self.ws_i, stream=stream)
+
+    def free(self):
+        del self.k8, self.ks
+        super().free()
+
+
 class PrefillWork:
     """Causal gated MLA prefill (rows a1-a4, a6 on the tensor cores)."""
 
@@ -560,7 +584,7 @@ class DsaPrefillWork:
 
 
 WORK_KINDS = {"decode": DecodeWork, "latent_decode": LatentDecodeWork,
-              "dsa_prefill": DsaPrefillWork, "dsa": DsaWork, "index": IndexWork,
+              "dsa_prefill": DsaPrefillWork, "index_fp8": IndexFp8Work, "dsa": DsaWork, "index": IndexWork,
               "prefill": PrefillWork, "chunked_prefill": ChunkedPrefillWork,
               "decode_cached": DecodeCachedWork}
 

@@ -68,7 +68,8 @@ enum {
     MLA_OP_CACHE_APPEND = 4,
     MLA_OP_LATENT_DECODE = 5,
     MLA_OP_PREFILL_INDEX_TOPK = 6,
-    MLA_OP_SPARSE_PREFILL_LATENT = 7
+    MLA_OP_SPARSE_PREFILL_LATENT = 7,
+    MLA_OP_INDEX_TOPK_FP8 = 8
 };
 
 /*
@@ -318,6 +319,30 @@ mla_status mla_sparse_prefill_latent(const mla_bf16* q, const mla_bf16* ckv,
                                      size_t ws_bytes, mla_stream stream);
 
 /*
+ * FP8 index keys (DSA post, cache section: the default FP8 index key is 128
+ * bytes of data plus a 4-byte scale per position).  The two parts are kept
+ * as separate arrays so every 128-byte row stays 16-byte aligned.
+ *
+ * dsa_quantize_index_keys writes, for each of the N rows of index_k
+ * [N,128] bf16, the e4m3 codes k8 [N,128] and the fp32 scale kscale [N]:
+ *   scale = amax / 448, code = e4m3(x * (448 / amax)) rounded to nearest
+ *   even with saturation (computed in fp32); an all-zero row gets scale 0.
+ * dsa_index_topk_fp8 is dsa_index_topk over such keys: the index queries are
+ * quantised the same way per (sequence, head) inside and their scales folded
+ * into the head weights, the 32-head dot products run as e4m3 x e4m3
+ * tensor-core products with fp32 accumulation, and each position's score is
+ * multiplied by its key scale.  Same outputs, tie rule and status behaviour
+ * as dsa_index_topk.  Workspace: mla_workspace_size(MLA_OP_INDEX_TOPK_FP8,
+ * B, 0, max_seqlen, topk) bytes.
+ */
+mla_status dsa_quantize_index_keys(const mla_bf16* index_k, uint8_t* k8, float* kscale, int64_t N,
+                                   mla_stream stream);
+mla_status dsa_index_topk_fp8(const mla_bf16* index_q, const uint8_t* k8, const float* kscale,
+                              const float* w, const int64_t* cu_seqlens, int B, int NH,
+                              int64_t total_keys, int max_seqlen, int topk, int32_t* topk_idx,
+                              float* topk_scores, void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
  * Gated MLA over the selected positions only (DSA post eqs. (9), (10)); all
  * H heads of a sequence share its selection.
  *
@@ -338,7 +363,8 @@ mla_status dsa_sparse_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf1
  * `op` is one of MLA_OP_*; arguments an operation does not use are ignored
  * (prefill and cache_append: none needed; decode: B, H, max_seqlen;
  * index_topk: B, max_seqlen; sparse_decode: B, H, topk; latent_decode: B, H;
- * prefill_index_topk: B = Tq, max_seqlen = Tk; sparse_prefill_latent: B = Tq, H).  Returns 0 for invalid arguments.
+ * prefill_index_topk: B = Tq, max_seqlen = Tk; sparse_prefill_latent: B = Tq, H;
+ * index_topk_fp8: B, max_seqlen).  Returns 0 for invalid arguments.
  */
 size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk);
 
@@ -379,7 +405,8 @@ mla_status mla_debug_set(int knob, long long value);
  * kernel; cache_append: the copy kernel, also when a chunked prefill or a
  * cached decode step appends; latent_decode: the latent attention kernel;
  * prefill_index_topk: the prefill scoring kernel; sparse_prefill_latent: the
- * latent attention kernel, counted under MLA_OP_LATENT_DECODE).  mla_timing_read synchronises those events, returns the summed
+ * latent attention kernel, counted under MLA_OP_LATENT_DECODE; index_topk_fp8:
+ * the FP8 scoring kernel).  mla_timing_read synchronises those events, returns the summed
  * kernel time in milliseconds and the number of launches of operation `op`
  * (MLA_OP_*) since the last read, and resets the count.  Events are created
  * on first use and reused; no device memory is allocated.

@@ -22,6 +22,7 @@ Entry points (names as in the C ABI):
 * ``dsa_prefill_index_topk(index_q, index_k, w, ...)``  per-token DSA index + top-k
 * ``mla_sparse_prefill_latent(q, ckv, topk_idx, w_kc, w_vc, ...)`` every prompt token
   over its own selection of the latent cache
+* ``dsa_quantize_index_keys(index_k)`` / ``dsa_index_topk_fp8(...)``  FP8 index keys
 """
 from __future__ import annotations
 
@@ -392,6 +393,54 @@ def mla_sparse_prefill_latent(q, ckv, topk_idx, w_kc, w_vc, gate=None, out=None,
                                              float(default_scale() if scale is None else scale),
                                              _ptr(ws), wsb, _stream(stream)), lib)
     return out
+
+
+def dsa_quantize_index_keys(index_k, k8=None, kscale=None, stream=None):
+    """bf16 index keys [N,128] -> (e4m3 codes uint8 [N,128], fp32 scales [N])."""
+    torch = _torch()
+    _need(index_k, "index_k", torch.bfloat16)
+    if index_k.dim() != 2 or index_k.shape[1] != INDEX_DIM:
+        raise ValueError("index_k must be [N,128]")
+    N = index_k.shape[0]
+    if k8 is None:
+        k8 = torch.empty((N, INDEX_DIM), dtype=torch.uint8, device=index_k.device)
+    if kscale is None:
+        kscale = torch.empty((N,), dtype=torch.float32, device=index_k.device)
+    _need(k8, "k8", torch.uint8, (N, INDEX_DIM), index_k.device)
+    _need(kscale, "kscale", torch.float32, (N,), index_k.device)
+    lib = _lib.load()
+    _lib.check(lib.dsa_quantize_index_keys(_ptr(index_k), _ptr(k8), _ptr(kscale), N,
+                                           _stream(stream)), lib)
+    return k8, kscale
+
+
+def dsa_index_topk_fp8(index_q, k8, kscale, w, cu_seqlens, max_seqlen: int, topk: int = MAX_TOPK,
+                       topk_idx=None, topk_scores=None, ws=None, stream=None):
+    """dsa_index_topk over FP8 index keys (k8 [total,128] uint8, kscale [total] fp32)."""
+    torch = _torch()
+    _need(index_q, "index_q", torch.bfloat16)
+    if index_q.dim() != 3 or index_q.shape[2] != INDEX_DIM:
+        raise ValueError("index_q must be [B,NH,128]")
+    B, NH, _ = index_q.shape
+    _need(k8, "k8", torch.uint8, None, index_q.device)
+    if k8.dim() != 2 or k8.shape[1] != INDEX_DIM:
+        raise ValueError("k8 must be [total,128]")
+    _need(kscale, "kscale", torch.float32, (k8.shape[0],), index_q.device)
+    _need(w, "w", torch.float32, (B, NH), index_q.device)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,), index_q.device)
+    if topk_idx is None:
+        topk_idx = torch.empty((B, topk), dtype=torch.int32, device=index_q.device)
+    _need(topk_idx, "topk_idx", torch.int32, (B, topk), index_q.device)
+    if topk_scores is not None:
+        _need(topk_scores, "topk_scores", torch.float32, (B, topk), index_q.device)
+    nbytes = workspace_size(_lib.OP_INDEX_TOPK_FP8, B, NH, int(max_seqlen), topk)
+    ws, wsb = _workspace(ws, nbytes, index_q.device)
+    lib = _lib.load()
+    _lib.check(lib.dsa_index_topk_fp8(_ptr(index_q), _ptr(k8), _ptr(kscale), _ptr(w),
+                                      _ptr(cu_seqlens), B, NH, int(k8.shape[0]), int(max_seqlen),
+                                      int(topk), _ptr(topk_idx), _ptr(topk_scores), _ptr(ws), wsb,
+                                      _stream(stream)), lib)
+    return topk_idx
 
 
 def check_device_status(stream=None) -> None:

@@ -18,7 +18,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT",
                 6: "MLA_ERR_BAD_INDEX"}
 OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE, OP_CACHE_APPEND, \
-    OP_LATENT_DECODE, OP_PREFILL_INDEX_TOPK, OP_SPARSE_PREFILL_LATENT = range(8)
+    OP_LATENT_DECODE, OP_PREFILL_INDEX_TOPK, OP_SPARSE_PREFILL_LATENT, OP_INDEX_TOPK_FP8 = range(9)
 DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE, DEBUG_SPARSE_CHUNK = 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -42,6 +42,9 @@ SIGNATURES = {
     "dsa_prefill_index_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "mla_sparse_prefill_latent": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _F, _P, _Z,
                                        _P]),
+    "dsa_quantize_index_keys": (_I, [_P, _P, _P, ctypes.c_int64, _P]),
+    "dsa_index_topk_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, ctypes.c_int64, _I, _I, _P, _P, _P,
+                                _Z, _P]),
     "mla_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "mla_check_device_status": (_I, [_P]),
     "mla_last_error": (ctypes.c_char_p, []),

@@ -71,6 +71,11 @@ def index_key_bytes(lengths) -> int:
     return sum(int(t) for t in lengths) * INDEX_DIM * BF16
 
 
+def index_key_bytes_fp8(lengths) -> int:
+    """FP8 index keys: 128 one-byte features and one fp32 scale per position."""
+    return sum(int(t) for t in lengths) * (INDEX_DIM + 4)
+
+
 def index_flops(lengths) -> int:
     return sum(int(t) for t in lengths) * 2 * INDEX_HEADS * INDEX_DIM
 

@@ -79,7 +79,7 @@ struct TimerPool {
     std::vector<mla::KernelTimer> ev;
     size_t used = 0;
 };
-constexpr int kOps = 7;   // MLA_OP_PREFILL .. MLA_OP_PREFILL_INDEX_TOPK
+constexpr int kOps = 9;   // MLA_OP_PREFILL .. MLA_OP_INDEX_TOPK_FP8
 TimerPool g_pool[kOps];
 
 // Next event pair for `op` when timing is on, else an empty timer.
@@ -167,6 +167,9 @@ size_t mla_workspace_size(int op, int B, int H, int max_seqlen, int topk) {
         case MLA_OP_INDEX_TOPK:
             if (B < 1 || max_seqlen < 1 || max_seqlen > (1 << 24)) return 0;
             return mla::plan_index(B, max_seqlen).total;
+        case MLA_OP_INDEX_TOPK_FP8:
+            if (B < 1 || max_seqlen < 1 || max_seqlen > (1 << 24)) return 0;
+            return mla::plan_index(B, max_seqlen, true).total;
         case MLA_OP_PREFILL_INDEX_TOPK:
             if (B < 1 || max_seqlen < B || max_seqlen >= (1 << 24)) return 0;
             return mla::prefill_index_ws(B, max_seqlen);
@@ -480,6 +483,55 @@ mla_status mla_sparse_prefill_latent(const mla_bf16* q, const mla_bf16* ckv,
     cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
                                               static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_sparse_prefill_latent launch");
+}
+
+mla_status dsa_quantize_index_keys(const mla_bf16* index_k, uint8_t* k8, float* kscale, int64_t N,
+                                   mla_stream stream) {
+    REQUIRE(N >= 0, MLA_ERR_INVALID_ARG, "N must be >= 0");
+    if (N == 0) return MLA_OK;
+    REQUIRE(index_k && k8 && kscale, MLA_ERR_INVALID_ARG, "null pointer");
+    REQUIRE(aligned16(index_k) && aligned16(k8) && (reinterpret_cast<uintptr_t>(kscale) & 3u) == 0,
+            MLA_ERR_INVALID_ARG, "misaligned pointer");
+    REQUIRE(N < (int64_t(1) << 34), MLA_ERR_UNSUPPORTED, "N too large for one call");
+    cudaError_t e = mla::launch_quantize_rows_e4m3(index_k, k8, kscale, N, mla::kIndexDim,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_quantize_index_keys launch");
+}
+
+mla_status dsa_index_topk_fp8(const mla_bf16* index_q, const uint8_t* k8, const float* kscale,
+                              const float* w, const int64_t* cu_seqlens, int B, int NH,
+                              int64_t total_keys, int max_seqlen, int topk, int32_t* topk_idx,
+                              float* topk_scores, void* ws, size_t ws_bytes, mla_stream stream) {
+    REQUIRE(index_q && k8 && kscale && w && cu_seqlens && topk_idx, MLA_ERR_INVALID_ARG,
+            "null pointer");
+    REQUIRE(aligned16(index_q) && aligned16(k8), MLA_ERR_INVALID_ARG,
+            "index_q and k8 must be 16-byte aligned");
+    REQUIRE((reinterpret_cast<uintptr_t>(w) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(kscale) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(topk_scores) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(cu_seqlens) & 7u) == 0,
+            MLA_ERR_INVALID_ARG, "misaligned w, kscale, cu_seqlens or outputs");
+    REQUIRE(NH == mla::kIndexHeads, MLA_ERR_UNSUPPORTED, "NH must be 32 (got %d)", NH);
+    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
+            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
+    REQUIRE(B >= 1 && B <= 65535, MLA_ERR_INVALID_ARG, "B must be in [1, 65535]");
+    REQUIRE(max_seqlen >= 1 && max_seqlen <= (1 << 24), MLA_ERR_UNSUPPORTED,
+            "max_seqlen must be in [1, 2^24]");
+    REQUIRE(total_keys >= 0 && total_keys < (int64_t(1) << 31), MLA_ERR_UNSUPPORTED,
+            "total_keys must be in [0, 2^31)");
+    const mla::IndexPlan pl = mla::plan_index(B, max_seqlen, true);
+    mla_status s = check_ws(ws, ws_bytes, pl.total);
+    if (s != MLA_OK) return s;
+    mla::DeviceInfo d;
+    if ((s = device_info(&d)) != MLA_OK) return s;
+    mla::IndexArgs a{index_q, nullptr, w, cu_seqlens, B, max_seqlen, topk, total_keys,
+                     topk_idx, topk_scores, ws};
+    mla::IndexFp8Args f{k8, kscale};
+    cudaError_t e = mla::launch_index_topk_fp8(a, f, pl, d, knobs(),
+                                               take_timer(MLA_OP_INDEX_TOPK_FP8),
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_index_topk_fp8 launch");
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,

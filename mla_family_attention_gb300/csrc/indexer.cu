@@ -31,6 +31,7 @@
 // order keeps every key above it plus the lowest positions among keys equal
 // to it, writing the output in ascending position order directly.
 #include <cuda.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -49,15 +50,32 @@ constexpr int kBHalf = kIndexHeads * 64 * 2;                 // 4 KB: 32 rows x 
 constexpr int kStageBytes = 2 * kAHalf;                      // 32 KB of index keys
 constexpr int kQBytes = 2 * kBHalf;                          // 8 KB: one sequence's queries
 constexpr int kBins = 2048;
-constexpr int kScoreThreads = 6 * 32;
+constexpr int kEpiGroups = 4;                               // epilogue groups of four warps (one per accumulator)
+constexpr int kScoreThreads = (2 + 4 * kEpiGroups) * 32;
+constexpr int kEpiThreads = 128 * kEpiGroups;
 constexpr int kAcc = 4;                                      // TMEM accumulators (32 columns each)
 constexpr uint32_t kTmemCols = 32 * kAcc;
-constexpr size_t kScoreSmem =
-    1024 + size_t(kIStages) * kStageBytes + 2 * kQBytes + kBins * 4 + 256;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kIndexHeads, false, false);
+constexpr uint32_t kIdescF8 = idesc_e4m3_f32(128, kIndexHeads);
+
+// Per-variant tile sizes: bf16 keys are two 64-feature boxes (256 B per
+// position), e4m3 keys one 128-byte box (128 B per position).
+// FP8 tiles are half the size, so the FP8 ring has twice the stages (the
+// same bytes in flight, which is what keeps HBM busy).
+template <bool kFp8>
+struct ScoreCfg {
+    static constexpr int kStage = kFp8 ? kTile * 128 : kStageBytes;
+    static constexpr int kStages = kFp8 ? 2 * kIStages : kIStages;
+    static constexpr int kQ = kFp8 ? kIndexHeads * 128 : kQBytes;
+    // barriers: 2*kStages ring + 2*kAcc accumulator + 2 query, then the TMEM
+    // address and the abort flag
+    static constexpr size_t kBarBytes = (2 * kStages + 2 * kAcc + 2) * 8 + 16;
+    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStage + 2 * kQ + kBins * 4 + kBarBytes;
+};
 
 struct ScoreParams {
-    const float* w;
+    const float* w;          // head weights (FP8: with the query scales folded in)
+    const float* kscale;     // FP8: per-position key scale, else null
     const int64_t* cu;
     const int* tile_start;   // [B+1]
     float* scores;           // [B][stride]
@@ -97,17 +115,19 @@ struct SeqCursor {
     }
 };
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     dsa_score_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap qmap, const ScoreParams p) {
+    using C = ScoreCfg<kFp8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* qbuf = smem + kIStages * kStageBytes;            // [2][8 KB] query tiles
-    unsigned* hist = reinterpret_cast<unsigned*>(qbuf + 2 * kQBytes);
+    uint8_t* qbuf = smem + C::kStages * C::kStage;              // [2] query tiles
+    unsigned* hist = reinterpret_cast<unsigned*>(qbuf + 2 * C::kQ);
     uint64_t* full = reinterpret_cast<uint64_t*>(hist + kBins);
-    uint64_t* empty = full + kIStages;
-    uint64_t* tfull = empty + kIStages;
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + kAcc;
     uint64_t* qfull = tempty + kAcc;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qfull + 2);
@@ -119,7 +139,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int t_end = int((int64_t(n_tiles) * (blockIdx.x + 1)) / gridDim.x);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kIStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -148,14 +168,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             // Queries are loaded once per sequence into one of two buffers; a
             // buffer is refilled only after the MMAs of the last tile that read
             // it have completed (the commit of that tile's stage).
-            int filled[kIStages];
-            for (int i = 0; i < kIStages; ++i) filled[i] = 0;
+            int filled[C::kStages];
+            for (int i = 0; i < C::kStages; ++i) filled[i] = 0;
             int qfilled[2] = {0, 0}, last_use[2] = {-1, -1};
-            int cur_b = -1, seg = 0;
+            int cur_b = -1, seg = 0, row0 = 0;   // row0: first key row of sequence cur_b
             SeqCursor cs;
             if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
             for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
-                const int slot = j % kIStages, round = j / kIStages;
+                const int slot = j % C::kStages, round = j / C::kStages;
                 if (*abort_flag) break;
                 if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
                     report(p.status, kStTimeout);
@@ -167,29 +187,32 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (b != cur_b) {
                     const int qb = seg & 1;
                     const int lu = last_use[qb];
-                    if (lu >= 0 && j - lu < kIStages &&
-                        !mbar_wait(&empty[lu % kIStages], (lu / kIStages) & 1, p.wait_ns)) {
+                    if (lu >= 0 && j - lu < C::kStages &&
+                        !mbar_wait(&empty[lu % C::kStages], (lu / C::kStages) & 1, p.wait_ns)) {
                         report(p.status, kStTimeout);
                         *abort_flag = 1;
                         break;
                     }
-                    mbar_arrive_expect_tx(&qfull[qb], kQBytes);
-                    tma_load_2d(qbuf + qb * kQBytes, &qmap, 0, b * kIndexHeads, &qfull[qb]);
-                    tma_load_2d(qbuf + qb * kQBytes + kBHalf, &qmap, 64, b * kIndexHeads,
-                                &qfull[qb]);
+                    mbar_arrive_expect_tx(&qfull[qb], C::kQ);
+                    tma_load_2d(qbuf + qb * C::kQ, &qmap, 0, b * kIndexHeads, &qfull[qb]);
+                    if (!kFp8)
+                        tma_load_2d(qbuf + qb * C::kQ + kBHalf, &qmap, 64, b * kIndexHeads,
+                                    &qfull[qb]);
                     qfilled[qb] = (seg >> 1) + 1;
                     cur_b = b;
+                    row0 = int(p.cu[b]) - p.tile_start[b] * kTile;
                     ++seg;
                 }
                 last_use[(seg - 1) & 1] = j;
-                const int row = int(p.cu[b]) + (t - p.tile_start[b]) * kTile;
-                uint8_t* st = smem + slot * kStageBytes;
-                mbar_arrive_expect_tx(&full[slot], kStageBytes);
+                const int row = row0 + t * kTile;
+                uint8_t* st = smem + slot * C::kStage;
+                mbar_arrive_expect_tx(&full[slot], C::kStage);
                 tma_load_2d_hint(st, &kmap, 0, row, &full[slot], stream_policy);
-                tma_load_2d_hint(st + kAHalf, &kmap, 64, row, &full[slot], stream_policy);
+                if (!kFp8)
+                    tma_load_2d_hint(st + kAHalf, &kmap, 64, row, &full[slot], stream_policy);
                 filled[slot] = round + 1;
             }
-            for (int i = 0; i < kIStages; ++i)
+            for (int i = 0; i < C::kStages; ++i)
                 if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
             for (int i = 0; i < 2; ++i)
@@ -204,7 +227,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             SeqCursor cs;
             if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
             for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
-                const int slot = j % kIStages, acc = j % kAcc;
+                const int slot = j % C::kStages, acc = j % kAcc;
                 if (*abort_flag) break;
                 cs.advance(p.tile_start, t);
                 const int b = cs.b;
@@ -214,20 +237,32 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     cur_b = b;
                     ++seg;
                 }
-                if (!ok || !mbar_wait(&full[slot], (j / kIStages) & 1, p.wait_ns) ||
+                if (!ok || !mbar_wait(&full[slot], (j / C::kStages) & 1, p.wait_ns) ||
                     (j >= kAcc && !mbar_wait(&tempty[acc], ((j / kAcc) - 1) & 1, p.wait_ns))) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(smem + slot * kStageBytes);
-                const uint32_t b0 = smem_u32(qbuf + ((seg - 1) & 1) * kQBytes);
+                const uint32_t a0 = smem_u32(smem + slot * C::kStage);
+                const uint32_t b0 = smem_u32(qbuf + ((seg - 1) & 1) * C::kQ);
+                if (kFp8) {
+                    // one 128-byte row per position: four K = 32 steps of 32 bytes
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a0 + (kk >> 2) * kAHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(b0 + (kk >> 2) * kBHalf + (kk & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tmem + acc * 32, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                        mma_f8_ss(tmem + acc * 32, ad, bd, kIdescF8, kk > 0 ? 1u : 0u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad =
+                            smem_desc_sw128(a0 + (kk >> 2) * kAHalf + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(b0 + (kk >> 2) * kBHalf + (kk & 3) * 32, 16, 1024);
+                        mma_bf16_ss(tmem + acc * 32, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(&empty[slot]);
                 mma_commit(&tfull[acc]);
@@ -240,9 +275,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
     } else {
         // ------------------------------- epilogue --------------------------------
+        // kEpiGroups groups of four warps take turns (group g the tiles with
+        // j % kEpiGroups == g, i.e. TMEM accumulator g); every group walks
+        // every tile's sequence bookkeeping so all meet the same
+        // histogram-flush barriers.
+        const int grp = (warp - 2) >> 2;
         const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
         const int r = quad * 32 + lane;            // position within the tile
         int cur_b = -1, T = 0, tstart = 0;
+        int64_t kbase = 0;                         // first key row of the current sequence
         float wr[kIndexHeads];                     // head weights of the current sequence
         SeqCursor cs;
         if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
@@ -252,22 +293,29 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const int b = cs.b;
             if (b != cur_b) {
                 if (cur_b >= 0) {                  // flush the previous sequence's bins
-                    named_bar_sync(1, 128);
-                    for (int i = threadIdx.x - 64; i < kBins; i += 128) {
+                    named_bar_sync(1, kEpiThreads);
+                    for (int i = threadIdx.x - 64; i < kBins; i += kEpiThreads) {
                         const unsigned c = hist[i];
                         if (c) {
                             atomicAdd(&p.hist[size_t(cur_b) * kBins + i], c);
                             hist[i] = 0;
                         }
                     }
-                    named_bar_sync(1, 128);
+                    named_bar_sync(1, kEpiThreads);
                 }
                 cur_b = b;
-                T = int(p.cu[b + 1] - p.cu[b]);
+                kbase = p.cu[b];
+                T = int(p.cu[b + 1] - kbase);
                 tstart = p.tile_start[b];
 #pragma unroll
                 for (int h = 0; h < kIndexHeads; ++h) wr[h] = __ldg(p.w + size_t(b) * kIndexHeads + h);
             }
+            if (j % kEpiGroups != grp) continue;   // another group's tile
+            const int pos = (t - tstart) * kTile + r;
+            const bool in = pos < T;
+            // FP8: the key scale is loaded before the accumulator wait so its
+            // latency overlaps it
+            const float ksc = (kFp8 && in) ? __ldg(p.kscale + kbase + pos) : 1.f;
             // After a timeout every warp keeps walking the tile list without
             // touching TMEM, so all four warps meet the same named barriers.
             bool ok = !*abort_flag;
@@ -277,7 +325,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 ok = false;
             }
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) continue;
+            if (!ok) continue;                     // (no barrier inside a tile's work)
             tc_fence_after();
             float d[32];
             tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + acc * 32, d);
@@ -289,9 +337,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             float s = 0.f;
 #pragma unroll
             for (int h = 0; h < kIndexHeads; ++h) s = fmaf(wr[h], fmaxf(d[h], 0.f), s);
+            if (kFp8) s *= ksc;
             s += 0.0f;                             // -0 -> +0: equal scores compare equal
-            const int pos = (t - tstart) * kTile + r;
-            const bool in = pos < T;
             if (in) p.scores[size_t(b) * p.stride + pos] = s;
             // histogram of the top 11 key bits, one atomic per distinct bin per warp
             const unsigned mask = __ballot_sync(0xffffffffu, in);
@@ -301,9 +348,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], unsigned(__popc(peers)));
             }
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         if (cur_b >= 0) {
-            for (int i = threadIdx.x - 64; i < kBins; i += 128) {
+            for (int i = threadIdx.x - 64; i < kBins; i += kEpiThreads) {
                 const unsigned c = hist[i];
                 if (c) atomicAdd(&p.hist[size_t(cur_b) * kBins + i], c);
             }
@@ -958,6 +1005,47 @@ __global__ void __launch_bounds__(1024) dsa_prefill_topk_kernel(const PrefillTop
     }
 }
 
+// ---------------------------------------------------------------------------
+// E4M3 quantisation (the FP8 index key of the DSA post's cache section: 128
+// one-byte features and one fp32 scale per position).  One warp per row of
+// 128 values, four per lane: amax by shuffles, scale = amax/448, codes =
+// e4m3(x * (448/amax)) rounded to nearest even with saturation.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                                              __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE,
+                                                              __NV_E4M3);
+    return uint32_t(lo) | (uint32_t(hi) << 16);
+}
+
+// codes [rows][128], scale [rows]; `wq`/`w`: when given, wq[row] = w[row] * scale
+// (the index queries' scales folded into the head weights).
+__global__ void __launch_bounds__(256) quantize_rows128_kernel(const uint16_t* x, uint8_t* codes,
+                                                               float* scale, int64_t rows,
+                                                               const float* w, float* wq) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const uint2 v = *reinterpret_cast<const uint2*>(x + row * 128 + lane * 4);
+    const float f0 = bf_lo(v.x), f1 = bf_hi(v.x), f2 = bf_lo(v.y), f3 = bf_hi(v.y);
+    float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    uint32_t c = 0;
+    float sc = 0.f;
+    if (amax > 0.f) {
+        const float inv = 448.0f / amax;
+        sc = amax / 448.0f;
+        c = e4m3x4(f0 * inv, f1 * inv, f2 * inv, f3 * inv);
+    }
+    *reinterpret_cast<uint32_t*>(codes + row * 128 + lane * 4) = c;
+    if (lane == 0) {
+        scale[row] = sc;
+        if (wq) wq[row] = w[row] * sc;
+    }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Score rows start on 16-byte boundaries so the top-k passes can load float4.
@@ -965,20 +1053,36 @@ int score_stride(int max_seqlen) { return (max_seqlen + 3) & ~3; }
 
 }  // namespace
 
-IndexPlan plan_index(int B, int max_seqlen) {
-    // scores | level-1 histograms | tile table
+IndexPlan plan_index(int B, int max_seqlen, bool fp8) {
+    // scores | level-1 histograms | tile table | FP8: query codes, scales, folded weights
     IndexPlan p{};
     p.scores_off = 0;
     p.hist_off = align256(size_t(B) * score_stride(max_seqlen) * 4);
     p.counts_off = p.hist_off + align256(size_t(B) * kBins * 4);
     p.tiles_off = p.counts_off;
     p.total = p.tiles_off + align256(size_t(B + 1) * 4);
+    if (fp8) {
+        p.q8_off = p.total;
+        p.qs_off = p.q8_off + align256(size_t(B) * kIndexHeads * 128);
+        p.wq_off = p.qs_off + align256(size_t(B) * kIndexHeads * 4);
+        p.total = p.wq_off + align256(size_t(B) * kIndexHeads * 4);
+    }
     return p;
+}
+
+cudaError_t launch_quantize_rows_e4m3(const uint16_t* x, uint8_t* codes, float* scale,
+                                      int64_t rows, int cols, cudaStream_t st) {
+    if (cols != 128) return cudaErrorInvalidValue;
+    if (rows == 0) return cudaSuccess;
+    quantize_rows128_kernel<<<unsigned((rows + 7) / 8), 256, 0, st>>>(x, codes, scale, rows,
+                                                                       nullptr, nullptr);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const DeviceInfo& dev,
                               const Knobs& kn, const KernelTimer& tm, cudaStream_t st) {
-    static_assert(kScoreSmem <= 227 * 1024, "shared memory budget");
+    static_assert(ScoreCfg<false>::kSmem <= 227 * 1024 && ScoreCfg<true>::kSmem <= 227 * 1024,
+                  "shared memory budget");
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     float* scores = reinterpret_cast<float*>(ws + pl.scores_off);
     unsigned* hist = reinterpret_cast<unsigned*>(ws + pl.hist_off);
@@ -996,13 +1100,13 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
     if (e != cudaSuccess) return e;
     dsa_tiles_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.max_seqlen, a.total_keys, a.topk, tiles,
                                          dev.status);
-    e = cudaFuncSetAttribute(dsa_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kScoreSmem));
+    e = cudaFuncSetAttribute(dsa_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(ScoreCfg<false>::kSmem));
     if (e != cudaSuccess) return e;
-    ScoreParams p{a.w, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
+    ScoreParams p{a.w, nullptr, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
                   kn.wait_limit_ns, dev.status};
     if (tm.begin) cudaEventRecord(tm.begin, st);
-    dsa_score_kernel<<<dev.sms, kScoreThreads, kScoreSmem, st>>>(kmap, qmap, p);
+    dsa_score_kernel<false><<<dev.sms, kScoreThreads, ScoreCfg<false>::kSmem, st>>>(kmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1048,6 +1152,49 @@ cudaError_t launch_prefill_index_topk(const PrefillIndexArgs& a, const DeviceInf
                          dev.status};
     const int grid = a.Tq < 2 * dev.sms ? a.Tq : 2 * dev.sms;
     dsa_prefill_topk_kernel<<<grid, 1024, kPTopkSmem, st>>>(tp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_index_topk_fp8(const IndexArgs& a, const IndexFp8Args& f, const IndexPlan& pl,
+                                  const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
+                                  cudaStream_t st) {
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    float* scores = reinterpret_cast<float*>(ws + pl.scores_off);
+    unsigned* hist = reinterpret_cast<unsigned*>(ws + pl.hist_off);
+    int* tiles = reinterpret_cast<int*>(ws + pl.tiles_off);
+    uint8_t* q8 = ws + pl.q8_off;
+    float* qs = reinterpret_cast<float*>(ws + pl.qs_off);
+    float* wq = reinterpret_cast<float*>(ws + pl.wq_off);
+    // queries: one scale per (sequence, head), folded into that head's weight
+    const int64_t qrows = int64_t(a.B) * kIndexHeads;
+    quantize_rows128_kernel<<<unsigned((qrows + 7) / 8), 256, 0, st>>>(a.index_q, q8, qs, qrows,
+                                                                        a.w, wq);
+    CUtensorMap kmap, qmap;
+    const uint64_t rows = a.total_keys > 0 ? uint64_t(a.total_keys) : 1;
+    cudaError_t e = encode_tmap_2d_u8(&kmap, f.k8, 128, rows, 128, 128, kTile);
+    if (e != cudaSuccess) return e;
+    e = encode_tmap_2d_u8(&qmap, q8, 128, uint64_t(qrows), 128, 128, kIndexHeads);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(hist, 0, size_t(a.B) * kBins * 4, st);
+    if (e != cudaSuccess) return e;
+    dsa_tiles_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.max_seqlen, a.total_keys, a.topk, tiles,
+                                         dev.status);
+    e = cudaFuncSetAttribute(dsa_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(ScoreCfg<true>::kSmem));
+    if (e != cudaSuccess) return e;
+    ScoreParams p{wq, f.kscale, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
+                  kn.wait_limit_ns, dev.status};
+    if (tm.begin) cudaEventRecord(tm.begin, st);
+    dsa_score_kernel<true><<<dev.sms, kScoreThreads, ScoreCfg<true>::kSmem, st>>>(kmap, qmap, p);
+    if (tm.end) cudaEventRecord(tm.end, st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    TopkParams tp{scores, hist, a.cu, a.max_seqlen, score_stride(a.max_seqlen), a.topk,
+                  a.total_keys, a.topk_idx, a.topk_scores, dev.status};
+    e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTopkSmem));
+    if (e != cudaSuccess) return e;
+    dsa_topk_cluster_kernel<<<dim3(kCluster, a.B), 1024, kTopkSmem, st>>>(tp);
     return cudaGetLastError();
 }
 

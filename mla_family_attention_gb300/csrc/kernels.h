@@ -89,6 +89,10 @@ cudaError_t encode_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inn
                                 uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
                                 uint32_t box_inner, uint32_t box_mid, uint32_t box_outer = 1);
 
+// 2-D 8-bit map over a row-major [outer][inner] byte array, 128-byte swizzle.
+cudaError_t encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
 // ---------------------------- DSA indexer --------------------------------
 struct IndexArgs {
     const uint16_t* index_q;   // [B,32,128]
@@ -104,9 +108,25 @@ struct IndexArgs {
 
 struct IndexPlan {
     size_t scores_off, hist_off, counts_off, tiles_off, total;
+    size_t q8_off = 0, qs_off = 0, wq_off = 0;   // FP8 variant only
 };
 
-IndexPlan plan_index(int B, int max_seqlen);
+IndexPlan plan_index(int B, int max_seqlen, bool fp8 = false);
+// FP8 index keys: k8 [total_keys,128] e4m3 codes and kscale [total_keys]
+// fp32 (132 bytes per position); the queries are quantised per (b, head)
+// inside, their scales folded into the head weights.
+struct IndexFp8Args {
+    const uint8_t* k8;
+    const float* kscale;
+};
+cudaError_t launch_index_topk_fp8(const IndexArgs& a, const IndexFp8Args& f, const IndexPlan& p,
+                                  const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
+                                  cudaStream_t st);
+// Quantise rows of `cols` bf16 values to e4m3 codes with one fp32 scale per
+// row: scale = amax/448, code = e4m3(x * (448/amax)) (round to nearest even,
+// saturating); an all-zero row gets scale 0 and zero codes.
+cudaError_t launch_quantize_rows_e4m3(const uint16_t* x, uint8_t* codes, float* scale,
+                                      int64_t rows, int cols, cudaStream_t st);
 cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& p, const DeviceInfo& dev,
                               const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 
