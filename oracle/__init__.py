@@ -390,3 +390,45 @@ def dsa_index_scores_fp8(index_q, k8, kscale, w, cu_seqlens, lib=None) -> np.nda
     q_deq = (e4m3_values(qc) * qs.astype(np.float64)[:, None]).reshape(B, NH, D)
     k_deq = e4m3_values(k8) * _f64(kscale)[:, None]
     return dsa_index_scores(q_deq, k_deq, w, cu_seqlens, lib=lib)
+
+
+LATENT_RECORD_BYTES = 656   # 512 e4m3 codes + 4 fp32 scales + 64 bf16 shared-key features
+
+
+def quantize_latent_records(ckv) -> np.ndarray:
+    """Latent cache rows [N,576] (bf16) -> FP8 records uint8 [N,656] in the
+    order the DSA post lists them: the 512 latent features as e4m3 codes in
+    four groups of 128 (quantised like quantize_e4m3_rows), the four fp32
+    group scales, then the 64 shared-key features unchanged (bf16)."""
+    import torch
+    c = _f64(ckv)
+    N = c.shape[0]
+    codes, scale = quantize_e4m3_rows(c[:, :512].reshape(N * 4, 128))
+    rec = np.zeros((N, LATENT_RECORD_BYTES), dtype=np.uint8)
+    rec[:, :512] = codes.reshape(N, 512)
+    rec[:, 512:528] = scale.astype("<f4").reshape(N, 4).view(np.uint8)
+    rope = torch.from_numpy(c[:, 512:].astype(np.float32)).to(torch.bfloat16)
+    rec[:, 528:] = rope.view(torch.uint8).numpy().reshape(N, 128)
+    return rec
+
+
+def dequantize_latent_records(rec) -> np.ndarray:
+    """FP8 records [N,656] -> the latent rows they stand for, [N,576] float64."""
+    import torch
+    r = np.ascontiguousarray(_host(rec), dtype=np.uint8)
+    N = r.shape[0]
+    codes = e4m3_values(r[:, :512]).reshape(N, 4, 128)
+    scale = r[:, 512:528].copy().view("<f4").astype(np.float64).reshape(N, 4, 1)
+    out = np.empty((N, 576))
+    out[:, :512] = (codes * scale).reshape(N, 512)
+    rope = torch.from_numpy(r[:, 528:].copy()).view(torch.bfloat16).to(torch.float64)
+    out[:, 512:] = rope.numpy().reshape(N, 64)
+    return out
+
+
+def mla_decode_latent_fp8(q, rec, cu_seqlens, w_kc, w_vc, gate, scale: float,
+                          lib=None) -> np.ndarray:
+    """Latent decode over FP8 records: the records' latent rows, then the
+    latent decode definition."""
+    return mla_decode_latent(q, dequantize_latent_records(rec), cu_seqlens, w_kc, w_vc, gate,
+                             scale, lib=lib)

@@ -66,3 +66,45 @@ def test_fp8_scores_equal_bf16_scores_on_representable_inputs():
     got = oracle.dsa_index_scores_fp8(q, k8, ks, w, cu)
     ref = oracle.dsa_index_scores(q, k, w, cu)
     np.testing.assert_array_equal(got, ref)
+
+
+def test_latent_record_layout():
+    """Byte layout of the 656-byte record: codes of features 0..511 first,
+    then the four group scales (little-endian fp32), then the 64 bf16
+    shared-key features, bit for bit."""
+    import torch
+    x = bf16_like((3, 576), RNG)
+    x[1, 128:256] = 0.0                            # a zero group: scale 0, codes 0
+    rec = oracle.quantize_latent_records(x)
+    assert rec.shape == (3, 656)
+    codes, scale = oracle.quantize_e4m3_rows(x[:, :512].reshape(12, 128))
+    np.testing.assert_array_equal(rec[:, :512], codes.reshape(3, 512))
+    np.testing.assert_array_equal(rec[:, 512:528].copy().view("<f4").reshape(12), scale)
+    assert scale[5] == 0 and not rec[1, 128:256].any()
+    rope = torch.from_numpy(x[:, 512:].astype(np.float32)).to(torch.bfloat16)
+    np.testing.assert_array_equal(rec[:, 528:], rope.view(torch.uint8).numpy())
+    deq = oracle.dequantize_latent_records(rec)
+    np.testing.assert_array_equal(deq[:, 512:], x[:, 512:])
+    rel = np.abs(deq[:, :512] - x[:, :512]) / np.maximum(np.abs(x[:, :512]), 1e-30)
+    big = np.abs(x[:, :512]) >= 2.0 ** -6 * np.repeat(scale.reshape(3, 4), 128, axis=1)
+    assert rel[big].max() <= 2.0 ** -4 * (1 + 1e-6)
+
+
+def test_fp8_latent_decode_equals_bf16_on_representable_cache():
+    grid = oracle.e4m3_values(np.arange(0, 0x7E, dtype=np.uint8).reshape(1, -1))[0]
+    grid = np.concatenate([grid, -grid])
+    lengths, H = [5, 9], 2
+    N = sum(lengths)
+    ckv = bf16_like((N, 576), RNG)
+    ckv[:, :512] = RNG.choice(grid, size=(N, 512))
+    ckv[:, :512:128] = 448.0                       # every group's maximum is 448: scale 1
+    wk = bf16_like((H, 128, 512), RNG) / 64
+    wv = bf16_like((H, 128, 512), RNG) / 64
+    q = bf16_like((2, H, 192), RNG)
+    g = bf16_like((2, H * 128), RNG)
+    cu = np.array([0, 5, 14], dtype=np.int64)
+    rec = oracle.quantize_latent_records(ckv)
+    np.testing.assert_array_equal(oracle.dequantize_latent_records(rec), ckv)
+    got = oracle.mla_decode_latent_fp8(q, rec, cu, wk, wv, g, 192 ** -0.5)
+    ref = oracle.mla_decode_latent(q, ckv, cu, wk, wv, g, 192 ** -0.5)
+    np.testing.assert_array_equal(got, ref)
