@@ -543,6 +543,26 @@ class LatentDecodeWork:
         del self.d, self.out, self.ws
 
 
+class LatentDecodeFp8Work(LatentDecodeWork):
+    """The latent decode over 656-byte FP8 records of the same cache."""
+
+    def __init__(self, name, dev, batch=0):
+        super().__init__(name, dev, batch)
+        self.rec = self.mla.mla_quantize_latent_cache(self.d.ckv)
+        self.work = acc.latent_kv_bytes_fp8(self.lengths)
+        self.kernels = [(self.lib.OP_LATENT_DECODE, "mla_latent_kernel<fp8>", self.work)]
+
+    def step(self, stream):
+        d = self.d
+        self.mla.mla_decode_latent_fp8(d.q, self.rec, d.cu_seqlens, self.max_len, d.w_kc, d.w_vc,
+                                       gate=d.gate, out=self.out, scale=d.scale, ws=self.ws,
+                                       stream=stream)
+
+    def free(self):
+        del self.rec
+        super().free()
+
+
 class DsaPrefillWork:
     """K3.1 Gated DSA prefill of one prompt: every token's index scores and
     top-k, then every token's gated MLA over its own selection of the latent
@@ -584,7 +604,8 @@ class DsaPrefillWork:
 
 
 WORK_KINDS = {"decode": DecodeWork, "latent_decode": LatentDecodeWork,
-              "dsa_prefill": DsaPrefillWork, "index_fp8": IndexFp8Work, "dsa": DsaWork, "index": IndexWork,
+              "dsa_prefill": DsaPrefillWork, "index_fp8": IndexFp8Work,
+              "latent_decode_fp8": LatentDecodeFp8Work, "dsa": DsaWork, "index": IndexWork,
               "prefill": PrefillWork, "chunked_prefill": ChunkedPrefillWork,
               "decode_cached": DecodeCachedWork}
 

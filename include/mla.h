@@ -243,6 +243,35 @@ mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64
                              mla_stream stream);
 
 /*
+ * FP8 latent cache (DSA post, cache section: the fp8_ds_mla record is 512
+ * bytes of FP8 latent, 4 fp32 scales and 64 bf16 shared-key features, 656
+ * bytes per position).  Record layout: bytes 0..511 the e4m3 codes of latent
+ * features 0..511, in four groups of 128 with one scale each (scale =
+ * amax/448, code = e4m3(x * 448/amax) rounded to nearest even, saturating,
+ * computed in fp32; a zero group has scale 0); bytes 512..527 the four fp32
+ * scales; bytes 528..655 the 64 bf16 shared-key features unchanged.
+ *
+ * mla_quantize_latent_cache writes the records rec [N,656] of N latent rows
+ * ckv [N,576] bf16.  mla_decode_latent_fp8 and mla_sparse_prefill_latent_fp8
+ * are mla_decode_latent and mla_sparse_prefill_latent over such records (the
+ * row arguments count records); the kernels convert each record back to
+ * bf16 features (code x scale, rounded to bf16) on the way into shared
+ * memory, so the arithmetic after that is the bf16 path's.
+ */
+mla_status mla_quantize_latent_cache(const mla_bf16* ckv, uint8_t* rec, int64_t N,
+                                     mla_stream stream);
+mla_status mla_decode_latent_fp8(const mla_bf16* q, const uint8_t* rec, const int64_t* cu_seqlens,
+                                 int64_t total_positions, int B, int H, int max_seqlen,
+                                 const mla_bf16* w_kc, const mla_bf16* w_vc, const mla_bf16* gate,
+                                 mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                                 mla_stream stream);
+mla_status mla_sparse_prefill_latent_fp8(const mla_bf16* q, const uint8_t* rec,
+                                         const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
+                                         const mla_bf16* w_kc, const mla_bf16* w_vc,
+                                         const mla_bf16* gate, mla_bf16* out, float scale,
+                                         void* ws, size_t ws_bytes, mla_stream stream);
+
+/*
  * DSA indexer score and top-k (DSA post eqs. (5) and (6)).
  *
  *   index_q     [B,NH,128]  index queries (NH must be 32)

@@ -23,6 +23,8 @@ Entry points (names as in the C ABI):
 * ``mla_sparse_prefill_latent(q, ckv, topk_idx, w_kc, w_vc, ...)`` every prompt token
   over its own selection of the latent cache
 * ``dsa_quantize_index_keys(index_k)`` / ``dsa_index_topk_fp8(...)``  FP8 index keys
+* ``mla_quantize_latent_cache(ckv)`` / ``mla_decode_latent_fp8(...)`` /
+  ``mla_sparse_prefill_latent_fp8(...)``  656-byte FP8 latent cache records
 """
 from __future__ import annotations
 
@@ -441,6 +443,91 @@ def dsa_index_topk_fp8(index_q, k8, kscale, w, cu_seqlens, max_seqlen: int, topk
                                       int(topk), _ptr(topk_idx), _ptr(topk_scores), _ptr(ws), wsb,
                                       _stream(stream)), lib)
     return topk_idx
+
+
+RECORD_BYTES = 656
+
+
+def mla_quantize_latent_cache(ckv, rec=None, stream=None):
+    """Latent rows [N,576] bf16 -> FP8 records [N,656] uint8."""
+    torch = _torch()
+    _need(ckv, "ckv", torch.bfloat16)
+    if ckv.dim() != 2 or ckv.shape[1] != 576:
+        raise ValueError("ckv must be [N,576]")
+    N = ckv.shape[0]
+    if rec is None:
+        rec = torch.empty((N, RECORD_BYTES), dtype=torch.uint8, device=ckv.device)
+    _need(rec, "rec", torch.uint8, (N, RECORD_BYTES), ckv.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_quantize_latent_cache(_ptr(ckv), _ptr(rec), N, _stream(stream)), lib)
+    return rec
+
+
+def mla_decode_latent_fp8(q, rec, cu_seqlens, max_seqlen: int, w_kc, w_vc, gate=None, out=None,
+                          scale=None, ws=None, stream=None):
+    """mla_decode_latent over FP8 records rec [total,656] uint8."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [B,H,192]")
+    B, H, _ = q.shape
+    _need(rec, "rec", torch.uint8, None, q.device)
+    if rec.dim() != 2 or rec.shape[1] != RECORD_BYTES:
+        raise ValueError("rec must be [total,656]")
+    _need(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,), q.device)
+    _need(w_kc, "w_kc", torch.bfloat16, (H, 128, 512), q.device)
+    _need(w_vc, "w_vc", torch.bfloat16, (H, DV, 512), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (B, H * DV), q.device)
+    if out is None:
+        out = torch.empty((B, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_LATENT_DECODE, B, H, int(max_seqlen), 0)
+    if nbytes == 0:
+        raise ValueError(f"unsupported latent decode shape B={B} H={H}")
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_decode_latent_fp8(_ptr(q), _ptr(rec), _ptr(cu_seqlens), int(rec.shape[0]),
+                                         B, H, int(max_seqlen), _ptr(w_kc), _ptr(w_vc),
+                                         _ptr(gate), _ptr(out),
+                                         float(default_scale() if scale is None else scale),
+                                         _ptr(ws), wsb, _stream(stream)), lib)
+    return out
+
+
+def mla_sparse_prefill_latent_fp8(q, rec, topk_idx, w_kc, w_vc, gate=None, out=None, scale=None,
+                                  ws=None, stream=None):
+    """mla_sparse_prefill_latent over FP8 records rec [Tk,656] uint8."""
+    torch = _torch()
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != DQK:
+        raise ValueError("q must be [Tq,H,192]")
+    Tq, H, _ = q.shape
+    _need(rec, "rec", torch.uint8, None, q.device)
+    if rec.dim() != 2 or rec.shape[1] != RECORD_BYTES:
+        raise ValueError("rec must be [Tk,656]")
+    Tk = rec.shape[0]
+    _need(topk_idx, "topk_idx", torch.int32, None, q.device)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != Tq:
+        raise ValueError("topk_idx must be [Tq,topk]")
+    topk = topk_idx.shape[1]
+    _need(w_kc, "w_kc", torch.bfloat16, (H, 128, 512), q.device)
+    _need(w_vc, "w_vc", torch.bfloat16, (H, DV, 512), q.device)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, (Tq, H * DV), q.device)
+    if out is None:
+        out = torch.empty((Tq, H * DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (Tq, H * DV), q.device)
+    nbytes = workspace_size(_lib.OP_SPARSE_PREFILL_LATENT, Tq, H, Tk, topk)
+    if nbytes == 0:
+        raise ValueError(f"unsupported sparse prefill shape Tq={Tq} H={H}")
+    ws, wsb = _workspace(ws, nbytes, q.device)
+    lib = _lib.load()
+    _lib.check(lib.mla_sparse_prefill_latent_fp8(_ptr(q), _ptr(rec), _ptr(topk_idx), Tq, Tk, topk,
+                                                 H, _ptr(w_kc), _ptr(w_vc), _ptr(gate), _ptr(out),
+                                                 float(default_scale() if scale is None else scale),
+                                                 _ptr(ws), wsb, _stream(stream)), lib)
+    return out
 
 
 def check_device_status(stream=None) -> None:

@@ -45,6 +45,11 @@ SIGNATURES = {
     "dsa_quantize_index_keys": (_I, [_P, _P, _P, ctypes.c_int64, _P]),
     "dsa_index_topk_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, ctypes.c_int64, _I, _I, _P, _P, _P,
                                 _Z, _P]),
+    "mla_quantize_latent_cache": (_I, [_P, _P, ctypes.c_int64, _P]),
+    "mla_decode_latent_fp8": (_I, [_P, _P, _P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _F,
+                                   _P, _Z, _P]),
+    "mla_sparse_prefill_latent_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _F, _P,
+                                           _Z, _P]),
     "mla_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "mla_check_device_status": (_I, [_P]),
     "mla_last_error": (ctypes.c_char_p, []),

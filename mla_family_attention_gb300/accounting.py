@@ -62,6 +62,12 @@ def sparse_latent_attention_flops(Tq: int, Tk: int, H: int, topk: int) -> int:
     return sel * H * 2 * (576 + 512) + Tq * H * 2 * 2 * 128 * 512
 
 
+def latent_kv_bytes_fp8(lengths) -> int:
+    """Bytes of the FP8 latent cache read by a decode step: one 656-byte record
+    (512 e4m3 codes, 4 fp32 scales, 64 bf16 shared-key features) per position."""
+    return sum(int(t) for t in lengths) * 656
+
+
 def append_bytes(B: int, H: int, Tn: int) -> int:
     """HBM bytes of appending Tn positions to every (b, h): read once, written once."""
     return 2 * B * Tn * kv_bytes_per_position(H)

@@ -397,12 +397,14 @@ mla_status mla_decode_cached(const mla_bf16* q, const mla_bf16* k_new, const mla
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode_cached launch");
 }
 
-mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64_t* cu_seqlens,
-                             int64_t total_positions, int B, int H, int max_seqlen,
-                             const mla_bf16* w_kc, const mla_bf16* w_vc, const mla_bf16* gate,
-                             mla_bf16* out, float scale, void* ws, size_t ws_bytes,
-                             mla_stream stream) {
-    mla_status s = check_decode_common(q, ckv, w_kc, cu_seqlens, gate, out, B, H, max_seqlen);
+// Shared body of the bf16 and FP8 latent decode entry points.
+static mla_status latent_decode_common(const mla_bf16* q, const mla_bf16* ckv, const uint8_t* rec,
+                                       const int64_t* cu_seqlens, int64_t total_positions, int B,
+                                       int H, int max_seqlen, const mla_bf16* w_kc,
+                                       const mla_bf16* w_vc, const mla_bf16* gate, mla_bf16* out,
+                                       float scale, void* ws, size_t ws_bytes, mla_stream stream) {
+    const void* cache = rec ? static_cast<const void*>(rec) : static_cast<const void*>(ckv);
+    mla_status s = check_decode_common(q, cache, w_kc, cu_seqlens, gate, out, B, H, max_seqlen);
     if (s != MLA_OK) return s;
     REQUIRE(w_vc != nullptr && aligned16(w_vc), MLA_ERR_INVALID_ARG,
             "w_vc must be a 16-byte aligned device pointer");
@@ -418,9 +420,75 @@ mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64
     if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
     mla::LatentArgs a{q, ckv, cu_seqlens, w_kc, w_vc, gate, out, B, H, max_seqlen,
                       total_positions, scale, ws};
+    a.rec = rec;
     cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
                                               static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_decode_latent launch");
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "latent decode launch");
+}
+
+mla_status mla_decode_latent(const mla_bf16* q, const mla_bf16* ckv, const int64_t* cu_seqlens,
+                             int64_t total_positions, int B, int H, int max_seqlen,
+                             const mla_bf16* w_kc, const mla_bf16* w_vc, const mla_bf16* gate,
+                             mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                             mla_stream stream) {
+    return latent_decode_common(q, ckv, nullptr, cu_seqlens, total_positions, B, H, max_seqlen,
+                                w_kc, w_vc, gate, out, scale, ws, ws_bytes, stream);
+}
+
+mla_status mla_decode_latent_fp8(const mla_bf16* q, const uint8_t* rec, const int64_t* cu_seqlens,
+                                 int64_t total_positions, int B, int H, int max_seqlen,
+                                 const mla_bf16* w_kc, const mla_bf16* w_vc, const mla_bf16* gate,
+                                 mla_bf16* out, float scale, void* ws, size_t ws_bytes,
+                                 mla_stream stream) {
+    REQUIRE(rec != nullptr, MLA_ERR_INVALID_ARG, "null record pointer");
+    return latent_decode_common(q, nullptr, rec, cu_seqlens, total_positions, B, H, max_seqlen,
+                                w_kc, w_vc, gate, out, scale, ws, ws_bytes, stream);
+}
+
+mla_status mla_quantize_latent_cache(const mla_bf16* ckv, uint8_t* rec, int64_t N,
+                                     mla_stream stream) {
+    REQUIRE(N >= 0, MLA_ERR_INVALID_ARG, "N must be >= 0");
+    if (N == 0) return MLA_OK;
+    REQUIRE(ckv && rec, MLA_ERR_INVALID_ARG, "null pointer");
+    REQUIRE(aligned16(ckv) && aligned16(rec), MLA_ERR_INVALID_ARG, "misaligned pointer");
+    REQUIRE(N < (int64_t(1) << 31), MLA_ERR_UNSUPPORTED, "N too large for one call");
+    cudaError_t e = mla::launch_quantize_latent(ckv, rec, N, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_quantize_latent_cache launch");
+}
+
+static mla_status sparse_prefill_common(const mla_bf16* q, const mla_bf16* ckv, const uint8_t* rec,
+                                        const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
+                                        const mla_bf16* w_kc, const mla_bf16* w_vc,
+                                        const mla_bf16* gate, mla_bf16* out, float scale, void* ws,
+                                        size_t ws_bytes, mla_stream stream) {
+    const void* cache = rec ? static_cast<const void*>(rec) : static_cast<const void*>(ckv);
+    REQUIRE(q && cache && topk_idx && w_kc && w_vc && out, MLA_ERR_INVALID_ARG, "null pointer");
+    REQUIRE(aligned16(q) && aligned16(cache) && aligned16(w_kc) && aligned16(w_vc) &&
+                aligned16(out) && (gate == nullptr || aligned16(gate)) &&
+                (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0,
+            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    REQUIRE(H >= 16 && H <= 96 && H % 16 == 0, MLA_ERR_UNSUPPORTED,
+            "H must be a multiple of 16 in [16, 96] (got %d)", H);
+    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
+            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
+    REQUIRE(Tq >= 1 && Tk >= Tq, MLA_ERR_INVALID_ARG, "need 1 <= Tq <= Tk (got Tq=%d Tk=%d)",
+            Tq, Tk);
+    REQUIRE(int64_t(Tq) * H < (int64_t(1) << 31) && Tq <= 65535 * 128, MLA_ERR_UNSUPPORTED,
+            "Tq too large for one call");
+    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
+    mla::DeviceInfo d;
+    mla_status s = device_info(&d);
+    if (s != MLA_OK) return s;
+    const mla::LatentPlan pl = mla::plan_latent(Tq, H, d.sms);
+    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
+    mla::LatentArgs a{q, ckv, nullptr, w_kc, w_vc, gate, out, Tq, H, Tk, Tk, scale, ws};
+    a.idx = topk_idx;
+    a.topk = topk;
+    a.P = Tk - Tq;
+    a.rec = rec;
+    cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_sparse_prefill_latent launch");
 }
 
 mla_status dsa_prefill_index_topk(const mla_bf16* index_q, const mla_bf16* index_k,
@@ -450,39 +518,6 @@ mla_status dsa_prefill_index_topk(const mla_bf16* index_q, const mla_bf16* index
                                                    take_timer(MLA_OP_PREFILL_INDEX_TOPK),
                                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_prefill_index_topk launch");
-}
-
-mla_status mla_sparse_prefill_latent(const mla_bf16* q, const mla_bf16* ckv,
-                                     const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
-                                     const mla_bf16* w_kc, const mla_bf16* w_vc,
-                                     const mla_bf16* gate, mla_bf16* out, float scale, void* ws,
-                                     size_t ws_bytes, mla_stream stream) {
-    REQUIRE(q && ckv && topk_idx && w_kc && w_vc && out, MLA_ERR_INVALID_ARG, "null pointer");
-    REQUIRE(aligned16(q) && aligned16(ckv) && aligned16(w_kc) && aligned16(w_vc) &&
-                aligned16(out) && (gate == nullptr || aligned16(gate)) &&
-                (reinterpret_cast<uintptr_t>(topk_idx) & 3u) == 0,
-            MLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-    REQUIRE(H >= 16 && H <= 96 && H % 16 == 0, MLA_ERR_UNSUPPORTED,
-            "H must be a multiple of 16 in [16, 96] (got %d)", H);
-    REQUIRE(topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_UNSUPPORTED,
-            "topk must be in [1, %d] (got %d)", mla::kMaxTopk, topk);
-    REQUIRE(Tq >= 1 && Tk >= Tq, MLA_ERR_INVALID_ARG, "need 1 <= Tq <= Tk (got Tq=%d Tk=%d)",
-            Tq, Tk);
-    REQUIRE(int64_t(Tq) * H < (int64_t(1) << 31) && Tq <= 65535 * 128, MLA_ERR_UNSUPPORTED,
-            "Tq too large for one call");
-    REQUIRE(scale > 0.f && scale < 1e30f, MLA_ERR_INVALID_ARG, "scale must be positive finite");
-    mla::DeviceInfo d;
-    mla_status s = device_info(&d);
-    if (s != MLA_OK) return s;
-    const mla::LatentPlan pl = mla::plan_latent(Tq, H, d.sms);
-    if ((s = check_ws(ws, ws_bytes, pl.total)) != MLA_OK) return s;
-    mla::LatentArgs a{q, ckv, nullptr, w_kc, w_vc, gate, out, Tq, H, Tk, Tk, scale, ws};
-    a.idx = topk_idx;
-    a.topk = topk;
-    a.P = Tk - Tq;
-    cudaError_t e = mla::launch_latent_decode(a, pl, d, knobs(), take_timer(MLA_OP_LATENT_DECODE),
-                                              static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_sparse_prefill_latent launch");
 }
 
 mla_status dsa_quantize_index_keys(const mla_bf16* index_k, uint8_t* k8, float* kscale, int64_t N,
@@ -532,6 +567,25 @@ mla_status dsa_index_topk_fp8(const mla_bf16* index_q, const uint8_t* k8, const 
                                                take_timer(MLA_OP_INDEX_TOPK_FP8),
                                                static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "dsa_index_topk_fp8 launch");
+}
+
+mla_status mla_sparse_prefill_latent(const mla_bf16* q, const mla_bf16* ckv,
+                                     const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
+                                     const mla_bf16* w_kc, const mla_bf16* w_vc,
+                                     const mla_bf16* gate, mla_bf16* out, float scale, void* ws,
+                                     size_t ws_bytes, mla_stream stream) {
+    return sparse_prefill_common(q, ckv, nullptr, topk_idx, Tq, Tk, topk, H, w_kc, w_vc, gate, out,
+                                 scale, ws, ws_bytes, stream);
+}
+
+mla_status mla_sparse_prefill_latent_fp8(const mla_bf16* q, const uint8_t* rec,
+                                         const int32_t* topk_idx, int Tq, int Tk, int topk, int H,
+                                         const mla_bf16* w_kc, const mla_bf16* w_vc,
+                                         const mla_bf16* gate, mla_bf16* out, float scale,
+                                         void* ws, size_t ws_bytes, mla_stream stream) {
+    REQUIRE(rec != nullptr, MLA_ERR_INVALID_ARG, "null record pointer");
+    return sparse_prefill_common(q, nullptr, rec, topk_idx, Tq, Tk, topk, H, w_kc, w_vc, gate, out,
+                                 scale, ws, ws_bytes, stream);
 }
 
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,

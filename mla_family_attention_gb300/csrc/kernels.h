@@ -192,6 +192,7 @@ struct LatentArgs {
     void* ws;
     const int32_t* idx = nullptr;   // sparse prefill: [B][topk] selections
     int topk = 0, P = 0;            // sparse prefill: selection width, cached positions
+    const uint8_t* rec = nullptr;   // FP8 cache: [total][656] records instead of ckv
 };
 
 struct LatentPlan {
@@ -200,6 +201,9 @@ struct LatentPlan {
 };
 
 LatentPlan plan_latent(int B, int H, int sms);
+// FP8 latent records [rows][656] from bf16 latent rows [rows][576].
+cudaError_t launch_quantize_latent(const uint16_t* ckv, uint8_t* rec, int64_t rows,
+                                   cudaStream_t st);
 cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& p, const DeviceInfo& dev,
                                  const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 

@@ -36,6 +36,8 @@
 // (the softmax warps keep walking their barriers), in-flight copies and MMAs
 // are waited for, and TMEM is released before exit.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -52,7 +54,11 @@ constexpr int kSlots = 6;
 constexpr int kFills = 5;                        // ring fills per tile
 constexpr int kQBytes = (8 * kMaxH + 128) * 128; // nine [H x 64] blocks + rows read past them
 constexpr int kPBytes = kMaxH * 128;             // P: [H rows][64 keys] bf16
-constexpr int kThreads = 320;                    // TMA warp, MMA warp, 8 softmax warps
+// TMA warp, MMA warp, 8 softmax warps; the FP8-cache variant has 3 more
+// producer warps (warp 0 and warps 10-12 convert records to bf16)
+template <bool kFp8>
+constexpr int kThreadsOf = kFp8 ? 416 : 320;
+constexpr int kRec = 656;                        // FP8 record: 512 codes, 4 fp32 scales, 64 bf16
 constexpr int kColO = 2 * kLT;                   // O^T columns start after the score buffers
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kAhead = 4;                        // tiles prefetched into L2 ahead of the ring
@@ -83,6 +89,7 @@ struct LatParams {
     float* part;             // [slots][H][512] unnormalised O of segments of spanning sequences
     float* ml;               // [slots][H][2]: max (log2 units), sum
     uint16_t* zbuf;          // [B][H][512] bf16 normalised latent outputs
+    const uint8_t* rec;      // FP8 cache: [total][656] records, else null
     int B, H;
     float scale_log2;
     long long wait_ns;
@@ -175,7 +182,8 @@ struct Cursor {
     }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
     mla_latent_kernel(const __grid_constant__ CUtensorMap cmap,
                       const __grid_constant__ CUtensorMap gmap,
                       const __grid_constant__ CUtensorMap qmap, const LatParams p) {
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], kFp8 ? 128 : 1);      // FP8: every producer thread arrives
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -241,7 +249,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
     };
 
-    if (warp == 0) {
+    if (kFp8 && (warp == 0 || warp >= 10)) {
+        // -------------------- FP8 producer (128 threads) --------------------
+        // Thread ptid converts row ptid/2 of each fill, half ptid&1: 64 e4m3
+        // codes times their group scale into 64 bf16 features (or 32 bf16
+        // shared-key features), stored in the same 128-byte swizzled layout
+        // the TMA boxes have; every thread arrives on the fill's barrier.
+        const int ptid = warp == 0 ? lane : (warp - 9) * 32 + lane;
+        const int r = ptid >> 1, hf = ptid & 1;
+        if (t0 < t1) {
+            int nseg = 0, fill = 0;
+            Cursor cur{ts}, ahead{ts};
+            cur.seek(t0, B);
+            ahead.seek(t0, B);
+            auto prefetch_tile = [&](int t) {
+                ahead.advance(t);
+                const int64_t r0 = p.cu[ahead.b] + int64_t(t - ts[ahead.b]) * kLT;
+                const int64_t r1 = min(r0 + kLT, p.total);
+                if (r1 > r0) prefetch_l2(p.rec + r0 * kRec, uint32_t((r1 - r0) * kRec));
+            };
+            if (!sparse && ptid == 0)
+                for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
+            bool ok = true;
+            for (int t = t0; t < t1 && ok; ++t) {
+                if (!sparse && ptid == 0 && t + kAhead < t1) prefetch_tile(t + kAhead);
+                cur.advance(t);
+                const int b = cur.b;
+                const SeqDesc sd = seq_desc(p, b);
+                if (t == t0 || t == ts[b]) {
+                    if (ptid == 0) {
+                        if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
+                            fail();
+                        } else {
+                            mbar_arrive_expect_tx(qfull, 9 * H * 128);
+                            for (int kb = 0; kb < 9; ++kb)
+                                tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                        }
+                    }
+                    ++nseg;
+                }
+                const int e0 = (t - ts[b]) * kLT;
+                int64_t grow;
+                if (sparse) {
+                    bool v;
+                    grow = sel_row(p, sd, sel_raw(p, b, sd, e0 + r), &v);
+                } else {
+                    grow = sd.row0 + e0 + r;
+                }
+                const bool inb = grow < p.total;
+                const uint8_t* src = p.rec + (inb ? grow : 0) * kRec;
+                const uint32_t rowoff = (r >> 3) * 1024 + (r & 7) * 128;
+                // this thread's 320 bytes of the tile (shared key, 4 x 64 codes)
+                // and the 4 group scales, loaded together so one latency covers
+                // the tile's five fills
+                uint4 v[kFills][4];
+                float4 sc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < kFills; ++i) {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(
+                        i == 0 ? src + 512 + 16 + hf * 64 : src + 128 * (i - 1) + 64 * hf);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[i][q] = inb ? __ldg(s4 + q) : make_uint4(0, 0, 0, 0);
+                }
+                if (inb) sc4 = __ldg(reinterpret_cast<const float4*>(src + 512));
+                const float scs[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+                for (int i = 0; i < kFills; ++i, ++fill) {
+                    const int slot = fill % kSlots, round = fill / kSlots;
+                    if (*abort_flag) { ok = false; break; }
+                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = ring + slot * kSlot;
+                    if (i == 0) {                      // shared key: bf16 copy, 64 bytes
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(dst + rowoff + (((hf * 4 + q) ^ (r & 7)) << 4)) =
+                                v[0][q];
+                    } else {                           // latent features 128u + 64hf ..
+                        const float sc = scs[i - 1];
+                        uint8_t* hrow = dst + hf * kHalf + rowoff;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t cw[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
+                            uint32_t o[8];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                                    __nv_fp8x2_storage_t(cw[k] & 0xffffu), __NV_E4M3);
+                                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                                    __nv_fp8x2_storage_t(cw[k] >> 16), __NV_E4M3);
+                                const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+                                const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+                                o[2 * k] = pack2(fl.x * sc, fl.y * sc);
+                                o[2 * k + 1] = pack2(fh.x * sc, fh.y * sc);
+                            }
+                            *reinterpret_cast<uint4*>(hrow + (((2 * q) ^ (r & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4*>(hrow + (((2 * q + 1) ^ (r & 7)) << 4)) =
+                                make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                    fence_async_smem();
+                    mbar_arrive(&full[slot]);
+                }
+            }
+            if (ptid == 0 && nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
+                report(p.status, kStTimeout);
+        }
+    } else if (warp >= 10) {
+        // idle unless the cache is FP8
+    } else if (warp == 0) {
         // ------------------------------- TMA -------------------------------
         // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.
         // Sparse prefill: the lanes read the tile's 64 selection entries and
@@ -1018,6 +1138,43 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
     if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
+// FP8 latent records: one warp per cache row.  Group g (features 128g..) is
+// quantised like the index keys (scale = amax/448, codes e4m3(x * 448/amax),
+// nearest even, saturating; a zero group has scale 0); record bytes: codes
+// 0..511, scales 512..527, the 64 bf16 shared-key features 528..655.
+__global__ void __launch_bounds__(256) quantize_latent_kernel(const uint16_t* ckv, uint8_t* rec,
+                                                              int64_t rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const uint16_t* x = ckv + row * kCkv;
+    uint8_t* o = rec + row * kRec;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint2 v = *reinterpret_cast<const uint2*>(x + g * 128 + lane * 4);
+        const float f0 = bf_lo(v.x), f1 = bf_hi(v.x), f2 = bf_lo(v.y), f3 = bf_hi(v.y);
+        float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        uint32_t c = 0;
+        float sc = 0.f;
+        if (amax > 0.f) {
+            const float inv = 448.0f / amax;
+            sc = amax / 448.0f;
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(f0 * inv, f1 * inv), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(f2 * inv, f3 * inv), __NV_SATFINITE, __NV_E4M3);
+            c = uint32_t(lo) | (uint32_t(hi) << 16);
+        }
+        *reinterpret_cast<uint32_t*>(o + g * 128 + lane * 4) = c;
+        if (lane == 0) *reinterpret_cast<float*>(o + 512 + 4 * g) = sc;
+    }
+    *reinterpret_cast<uint32_t*>(o + 528 + lane * 4) =
+        *reinterpret_cast<const uint32_t*>(x + 512 + lane * 2);
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -1056,10 +1213,15 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     e = encode_tmap_3d_bf16(&q3map, a.q, kDqk, a.H, a.B, kDqk * 2, uint64_t(a.H) * kDqk * 2, 64,
                             1, nabs);
     if (e != cudaSuccess) return e;
-    e = encode_tmap_2d_bf16(&cmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, kLT);
-    if (e != cudaSuccess) return e;
-    e = encode_tmap_2d_bf16(&gmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, 1);
-    if (e != cudaSuccess) return e;
+    if (a.rec == nullptr) {
+        e = encode_tmap_2d_bf16(&cmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, kLT);
+        if (e != cudaSuccess) return e;
+        e = encode_tmap_2d_bf16(&gmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, 1);
+        if (e != cudaSuccess) return e;
+    } else {                                  // FP8 cache: read by the producer threads
+        cmap = wkmap;
+        gmap = wkmap;
+    }
     e = encode_tmap_2d_bf16(&qmap, qt, kCkv, uint64_t(a.B) * a.H, kCkv * 2, 64, a.H);
     if (e != cudaSuccess) return e;
     const int zrows = a.B < 128 ? (a.B + 15) / 16 * 16 : 128;   // rows a z~ box carries
@@ -1074,13 +1236,19 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
         wkmap, q3map, a.q, qt, a.w_vc, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
     latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.idx, a.topk, a.P, a.B, a.max_seqlen, pl.ctas,
                                            sched, dev.status);
-    e = cudaFuncSetAttribute(mla_latent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(mla_latent_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kLatSmem));
     if (e != cudaSuccess) return e;
-    LatParams p{sched, a.cu, a.idx, a.topk, a.P, a.ckv, a.total, part, ml, zbuf, a.B, a.H,
+    e = cudaFuncSetAttribute(mla_latent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kLatSmem));
+    if (e != cudaSuccess) return e;
+    LatParams p{sched, a.cu, a.idx, a.topk, a.P, a.ckv, a.total, part, ml, zbuf, a.rec, a.B, a.H,
                 a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
     if (tm.begin) cudaEventRecord(tm.begin, st);
-    mla_latent_kernel<<<pl.ctas, kThreads, kLatSmem, st>>>(cmap, gmap, qmap, p);
+    if (a.rec)
+        mla_latent_kernel<true><<<pl.ctas, kThreadsOf<true>, kLatSmem, st>>>(cmap, gmap, qmap, p);
+    else
+        mla_latent_kernel<false><<<pl.ctas, kThreadsOf<false>, kLatSmem, st>>>(cmap, gmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1091,6 +1259,13 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     if (e != cudaSuccess) return e;
     latent_out_kernel<<<dim3(a.H, (a.B + 127) / 128), 192, kOutSmem, st>>>(
         zmap, wvmap, sched, a.gate, a.out, a.B, a.H, zrows, kn.wait_limit_ns, dev.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_latent(const uint16_t* ckv, uint8_t* rec, int64_t rows,
+                                   cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    quantize_latent_kernel<<<unsigned((rows + 7) / 8), 256, 0, st>>>(ckv, rec, rows);
     return cudaGetLastError();
 }
 

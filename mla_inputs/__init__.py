@@ -290,6 +290,9 @@ WORKLOADS = {
                                         gated=True),
     # the indexer of the DSA decode workload over FP8 index keys (132 B/position)
     "dsa_index_fp8_b8_t131072": dict(kind="index_fp8", config=4, B=8, H=96, T=131072, topk=2048),
+    # the latent decode over 656-byte FP8 records (the same cache, quantised)
+    "latent_decode_fp8_b32_h96_t8192": dict(kind="latent_decode_fp8", config=5, B=32, H=96,
+                                            T=8192, gated=True),
     # DSA prefill: a 16384-token prompt, every token scoring its whole visible
     # history and attending over its own top-2048 of the latent cache
     "dsa_prefill_t16384": dict(kind="dsa_prefill", config=6, B=1, H=96, T=16384, topk=2048,

@@ -81,3 +81,66 @@ def test_fp8_index_full_size_sampled():
         check_selection(idx[b:b + 1], sc[b:b + 1], s64, [T], w["topk"])
     del d, k8, ks
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# FP8 latent cache records (656 bytes per position)
+# ---------------------------------------------------------------------------
+def test_quantize_latent_cache_is_bit_exact():
+    d = mi.make_latent_decode([300, 77], 16, True, device=DEV, config=103)
+    ckv = d.ckv.clone()
+    ckv[5, 128:256] = 0                                  # a zero group
+    rec = mla.mla_quantize_latent_cache(ckv)
+    mla.check_device_status()
+    assert np.array_equal(rec.cpu().numpy(), oracle.quantize_latent_records(ckv))
+
+
+@pytest.mark.parametrize("lengths,H", [([1, 63, 64, 65, 700], 96), ([2000], 16),
+                                       (mi.ragged_lengths(40, 1, 3000, 104), 96)])
+def test_fp8_latent_decode_matches_oracle(lengths, H):
+    from parity import assert_close
+    d = mi.make_latent_decode(lengths, H, True, device=DEV, config=104)
+    rec = mla.mla_quantize_latent_cache(d.ckv)
+    out = mla.mla_decode_latent_fp8(d.q, rec, d.cu_seqlens, max(lengths), d.w_kc, d.w_vc,
+                                    gate=d.gate, scale=d.scale)
+    mla.check_device_status()
+    heads = list(range(H)) if len(lengths) < 10 else [0, 41, 95]
+    cols = np.concatenate([np.arange(h * 128, (h + 1) * 128) for h in heads])
+    ref = oracle.mla_decode_latent_fp8(d.q[:, heads], rec, d.cu_seqlens, d.w_kc[heads],
+                                       d.w_vc[heads], d.gate[:, cols], d.scale)
+    assert_close(out[:, cols], ref, what=f"fp8 latent decode {len(lengths)} seqs H{H}")
+
+
+def test_fp8_sparse_prefill_matches_oracle():
+    from parity import assert_close
+    Tq, Tk, H, topk = 120, 600, 32, 128
+    d = mi.make_dsa_prefill(Tq, Tk, H, device=DEV, config=105)
+    idx = oracle.dsa_prefill_topk(oracle.dsa_prefill_index_scores(d.index_q, d.index_k, d.w),
+                                  topk)
+    rec = mla.mla_quantize_latent_cache(d.ckv)
+    out = mla.mla_sparse_prefill_latent_fp8(d.q, rec, torch.from_numpy(idx).to(DEV), d.w_kc,
+                                            d.w_vc, gate=d.gate, scale=d.scale)
+    mla.check_device_status()
+    ref = oracle.dsa_prefill_latent(d.q, oracle.dequantize_latent_records(rec), d.w_kc, d.w_vc,
+                                    idx, d.gate, d.scale)
+    assert_close(out, ref, what="fp8 sparse prefill")
+
+
+def test_fp8_latent_decode_full_size_sampled():
+    from parity import assert_close
+    w = mi.WORKLOADS["latent_decode_fp8_b32_h96_t8192"]
+    T, B = w["T"], w["B"]
+    d = mi.make_latent_decode([T] * B, w["H"], True, device=DEV, config=w["config"])
+    rec = mla.mla_quantize_latent_cache(d.ckv)
+    out = mla.mla_decode_latent_fp8(d.q, rec, d.cu_seqlens, T, d.w_kc, d.w_vc, gate=d.gate,
+                                    scale=d.scale)
+    mla.check_device_status()
+    heads = [0, 48, 95]
+    cols = np.concatenate([np.arange(h * 128, (h + 1) * 128) for h in heads])
+    for b in (0, B - 1):
+        ref = oracle.mla_decode_latent_fp8(d.q[b:b + 1, heads], rec[b * T:(b + 1) * T],
+                                           torch.tensor([0, T]), d.w_kc[heads], d.w_vc[heads],
+                                           d.gate[b:b + 1, cols], d.scale)
+        assert_close(out[b:b + 1, cols], ref, what=f"fp8 latent full b{b}")
+    del d, rec, out
+    torch.cuda.empty_cache()
