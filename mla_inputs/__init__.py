@@ -302,6 +302,8 @@ WORKLOADS = {
                                  profile_only=True),
     "prefill_b1_h8_t16384": dict(kind="prefill", config=3, B=1, H=8, T=16384, gated=True,
                                  profile_only=True),
+    "dsa_prefill_t4096": dict(kind="dsa_prefill", config=6, B=1, H=96, T=4096, topk=2048,
+                              gated=True, profile_only=True),
 }
 
 
