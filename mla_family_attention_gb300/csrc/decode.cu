@@ -154,21 +154,6 @@ __device__ __forceinline__ int total_items(const Params& p) {
 
 __device__ __forceinline__ bool valid_pos(int s, int T) { return s >= 0 && s < T; }
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
-                 : "memory");
-}
-
-// One arrival on `bar` once every cp.async this thread issued so far has landed.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 template <bool kSparse>
 __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
     decode_partial_kernel(const Params p) {

@@ -25,13 +25,18 @@
 //      * O^T += C^T P^T with the latent features as M (four 128-row blocks),
 //        the heads as N and the 64 keys as K; O^T (512 x H fp32) lives in
 //        TMEM next to two 64-column score buffers;
-//      * a six-slot ring of 16 KB slots carries each tile as five TMA units
-//        (the 64 shared-key features, then four 128-feature latent blocks);
-//        the latent blocks stay until P.V has used them, so every cache byte
-//        is read once.  S of the next tile is computed on its first two units
-//        while the softmax of the current tile runs.
-//   4. latent_merge_kernel: per head, log-sum-exp merge of the segments of
-//      every sequence, then z = W^V_h z~ and the sigmoid gate.
+//      * a six-slot ring of 16 KB slots carries each tile as five units
+//        (the 64 shared-key features, then four 128-feature latent blocks),
+//        filled by TMA tile loads of a decode sequence's contiguous rows, by
+//        16-byte cp.async copies of a prompt token's selected rows (sparse
+//        prefill) or by producer threads converting FP8 records; the latent
+//        blocks stay until P.V has used them, so every cache byte is read
+//        once.  S of the next tile is computed on its first two units while
+//        the softmax of the current tile runs.
+//   4. latent_fixup_kernel: per head, log-sum-exp merge of the segments of
+//      the sequences that span CTAs, into the normalised z~.
+//   5. latent_out_kernel: out = (W^V_h z~) * sigmoid(gate), a tensor-core
+//      GEMM per head over all sequences.
 // Every wait is bounded; a timeout records MLA_ERR_TIMEOUT, the roles stop
 // (the softmax warps keep walking their barriers), in-flight copies and MMAs
 // are waited for, and TMEM is released before exit.
@@ -54,10 +59,14 @@ constexpr int kSlots = 6;
 constexpr int kFills = 5;                        // ring fills per tile
 constexpr int kQBytes = (8 * kMaxH + 128) * 128; // nine [H x 64] blocks + rows read past them
 constexpr int kPBytes = kMaxH * 128;             // P: [H rows][64 keys] bf16
-// TMA warp, MMA warp, 8 softmax warps; the FP8-cache variant has 3 more
-// producer warps (warp 0 and warps 10-12 convert records to bf16)
-template <bool kFp8>
-constexpr int kThreadsOf = kFp8 ? 416 : 320;
+// Where a tile's rows come from: tiled TMA loads of 64 contiguous cache rows
+// (decode), 16-byte cp.async copies of the selected rows (sparse prefill), or
+// FP8 records converted to bf16 by the producer threads.
+enum Src { kSrcTma = 0, kSrcGather = 1, kSrcFp8 = 2 };
+// TMA warp, MMA warp, 8 softmax warps; the gather and FP8 variants have 128
+// producer threads instead of the TMA warp (warp 0 and warps 10-12)
+template <int kSrc>
+constexpr int kThreadsOf = kSrc == kSrcTma ? 320 : 416;
 constexpr int kRec = 656;                        // FP8 record: 512 codes, 4 fp32 scales, 64 bf16
 constexpr int kColO = 2 * kLT;                   // O^T columns start after the score buffers
 constexpr float kRescaleLog2 = 8.f;
@@ -153,18 +162,6 @@ __device__ __forceinline__ int sel_row(const LatParams& p, const SeqDesc& sd, in
     return *valid ? v : 0;
 }
 
-// TMA gather of four 64-feature rows (one 128-byte row each) into shared
-// memory; the tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int r0,
-                                            int r1, int r2, int r3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Walks a CTA's tile range [t0, t1) sequence by sequence.
 struct Cursor {
     const int* ts;
@@ -182,10 +179,9 @@ struct Cursor {
     }
 };
 
-template <bool kFp8>
-__global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
+template <int kSrc>
+__global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
     mla_latent_kernel(const __grid_constant__ CUtensorMap cmap,
-                      const __grid_constant__ CUtensorMap gmap,
                       const __grid_constant__ CUtensorMap qmap, const LatParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -222,7 +218,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&full[i], kFp8 ? 128 : 1);      // FP8: every producer thread arrives
+            mbar_init(&full[i], kSrc == kSrcTma ? 1 : 128);   // else every producer thread arrives
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -249,7 +245,7 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
         *abort_flag = 1;
     };
 
-    if (kFp8 && (warp == 0 || warp >= 10)) {
+    if (kSrc == kSrcFp8 && (warp == 0 || warp >= 10)) {
         // -------------------- FP8 producer (128 threads) --------------------
         // Thread ptid converts row ptid/2 of each fill, half ptid&1: 64 e4m3
         // codes times their group scale into 64 bf16 features (or 32 bf16
@@ -359,18 +355,92 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             if (ptid == 0 && nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
                 report(p.status, kStTimeout);
         }
-    } else if (warp >= 10) {
-        // idle unless the cache is FP8
+    } else if (kSrc == kSrcGather && (warp == 0 || warp >= 10)) {
+        // ------------------- cp.async gather (128 threads) -------------------
+        // Thread ptid copies 16-byte chunk ptid&7 of tile rows 8k + ptid/16:
+        // of feature half (ptid/8)&1 of a latent block (k = 0..7), or of the
+        // shared key for the rows whose k%2 is that half.  Eight lanes cover
+        // one 128-byte row segment, so a warp request reads whole lines.  A
+        // thread's copies arrive on the fill's barrier as they land; nothing
+        // waits for them here but the drain at exit.  The selection entries
+        // of the next tile are loaded while the current one is copied.
+        const int ptid = warp == 0 ? lane : (warp - 9) * 32 + lane;
+        const int rr = ptid >> 4, hf = (ptid >> 3) & 1, ch = ptid & 7;
+        const uint32_t sw = uint32_t(rr * 128 + ((ch ^ rr) << 4));   // row 8k+rr, swizzled chunk
+        if (t0 < t1) {
+            int nseg = 0, fill = 0;
+            Cursor cur{ts}, nxt{ts};
+            cur.seek(t0, B);
+            nxt.seek(t0, B);
+            int nraw[8];
+            auto load_sel = [&](int t) {
+                nxt.advance(t);
+                const SeqDesc s1 = seq_desc(p, nxt.b);
+                const int e = (t - ts[nxt.b]) * kLT + rr;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) nraw[k] = sel_raw(p, nxt.b, s1, e + 8 * k);
+            };
+            load_sel(t0);
+            const uint8_t* base = reinterpret_cast<const uint8_t*>(p.ckv) + ch * 16;
+            bool ok = true;
+            for (int t = t0; t < t1 && ok; ++t) {
+                cur.advance(t);
+                const int b = cur.b;
+                const SeqDesc sd = seq_desc(p, b);
+                int grow[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    bool v;
+                    grow[k] = sel_row(p, sd, nraw[k], &v);
+                }
+                if (t + 1 < t1) load_sel(t + 1);
+                if (t == t0 || t == ts[b]) {
+                    if (ptid == 0) {
+                        if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
+                            fail();
+                        } else {
+                            mbar_arrive_expect_tx(qfull, 9 * H * 128);
+                            for (int kb = 0; kb < 9; ++kb)
+                                tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                        }
+                    }
+                    ++nseg;
+                }
+                for (int i = 0; i < kFills; ++i, ++fill) {
+                    const int slot = fill % kSlots, round = fill / kSlots;
+                    if (*abort_flag) { ok = false; break; }
+                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = ring + slot * kSlot + sw;
+                    if (i == 0) {                      // shared-key features 512..575
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            cp_async16(dst + (2 * m + hf) * 1024,
+                                       base + int64_t(grow[2 * m + hf]) * (kCkv * 2) + kLatent * 2);
+                    } else {                           // latent features 128(i-1) + 64hf ..
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            cp_async16(dst + hf * kHalf + k * 1024,
+                                       base + int64_t(grow[k]) * (kCkv * 2) + (128 * (i - 1) + 64 * hf) * 2);
+                    }
+                    cp_async_arrive_noinc(&full[slot]);
+                }
+            }
+            cp_async_wait_all();   // nothing this thread started is still in flight at exit
+            if (ptid == 0 && nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
+                report(p.status, kStTimeout);
+        }
     } else if (warp == 0) {
         // ------------------------------- TMA -------------------------------
-        // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.
-        // Sparse prefill: the lanes read the tile's 64 selection entries and
-        // each issues gather4 loads of four selected rows.
-        if (t0 < t1) {
-            if (lane == 0) {
-                tma_prefetch_desc(sparse ? &gmap : &cmap);
-                tma_prefetch_desc(&qmap);
-            }
+        // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.  The
+        // ring holds little more than one tile, so HBM latency is covered by
+        // prefetching the tiles kAhead ahead into L2.
+        if (t0 < t1 && lane == 0) {
+            tma_prefetch_desc(&cmap);
+            tma_prefetch_desc(&qmap);
             const uint64_t policy = l2_evict_first_policy();
             int filled[kSlots];
             for (int s = 0; s < kSlots; ++s) filled[s] = 0;
@@ -378,8 +448,6 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
             Cursor cur{ts}, ahead{ts};
             cur.seek(t0, B);
             ahead.seek(t0, B);
-            // The ring holds little more than one tile, so HBM latency is
-            // covered by prefetching the tiles kAhead ahead into L2.
             auto prefetch_tile = [&](int t) {
                 ahead.advance(t);
                 const int64_t r0 = p.cu[ahead.b] + int64_t(t - ts[ahead.b]) * kLT;
@@ -387,132 +455,50 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                 if (r1 > r0)
                     prefetch_l2(p.ckv + r0 * kCkv, uint32_t((r1 - r0) * kCkv * 2));
             };
-            if (!sparse && lane == 0)
-                for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
+            for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
             bool ok = true;
-            // sparse prefill: the next tile's selection entries are loaded one
-            // tile ahead, so their latency is off the gather path
-            Cursor nxt{ts};
-            nxt.seek(t0, B);
-            int na = -1, nb = -1;
-            if (sparse) {
-                const SeqDesc s0 = seq_desc(p, nxt.b);
-                const int e = (t0 - ts[nxt.b]) * kLT + 2 * lane;
-                na = sel_raw(p, nxt.b, s0, e);
-                nb = sel_raw(p, nxt.b, s0, e + 1);
-            }
             for (int t = t0; t < t1 && ok; ++t) {
-                if (!sparse && lane == 0 && t + kAhead < t1) prefetch_tile(t + kAhead);
+                if (t + kAhead < t1) prefetch_tile(t + kAhead);
                 cur.advance(t);
                 const int b = cur.b;
-                const SeqDesc sd = seq_desc(p, b);
-                const int va = na, vb = nb;
-                if (sparse && t + 1 < t1) {
-                    nxt.advance(t + 1);
-                    const SeqDesc s1 = seq_desc(p, nxt.b);
-                    const int e = (t + 1 - ts[nxt.b]) * kLT + 2 * lane;
-                    na = sel_raw(p, nxt.b, s1, e);
-                    nb = sel_raw(p, nxt.b, s1, e + 1);
-                }
                 if (t == t0 || t == ts[b]) {
                     // q~ of sequence b, once the previous segment's Q.K^T is done
-                    bool go = true;
-                    if (lane == 0) {
-                        if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
-                            fail();
-                            go = false;
-                        } else {
-                            mbar_arrive_expect_tx(qfull, 9 * H * 128);
-                            for (int kb = 0; kb < 9; ++kb)
-                                tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
-                        }
+                    if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
+                        fail();
+                        break;
                     }
-                    if (!__shfl_sync(0xffffffffu, go, 0)) break;
+                    mbar_arrive_expect_tx(qfull, 9 * H * 128);
+                    for (int kb = 0; kb < 9; ++kb)
+                        tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
                     ++nseg;
                 }
-                const int e0 = (t - ts[b]) * kLT;
-                int ra = 0, rb = 0;
-                if (sparse) {
-                    bool ua, ub;
-                    ra = sel_row(p, sd, va, &ua);
-                    rb = sel_row(p, sd, vb, &ub);
-                }
-                const int row = int(sd.row0) + e0;
-                const int g = lane & 15, hfl = lane >> 4;
-                const int g0 = __shfl_sync(0xffffffffu, ra, 2 * g);
-                const int g1 = __shfl_sync(0xffffffffu, rb, 2 * g);
-                const int g2 = __shfl_sync(0xffffffffu, ra, 2 * g + 1);
-                const int g3 = __shfl_sync(0xffffffffu, rb, 2 * g + 1);
-                if (!sparse) {
-                    // decode: one lane issues the tiled loads, no warp-wide sync
-                    if (lane == 0) {
-                        for (int i = 0; i < kFills; ++i, ++fill) {
-                            const int slot = fill % kSlots, round = fill / kSlots;
-                            if (*abort_flag) { ok = false; break; }
-                            if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
-                                fail();
-                                ok = false;
-                                break;
-                            }
-                            uint8_t* dst = ring + slot * kSlot;
-                            if (i == 0) {              // shared-key features 512..575
-                                mbar_arrive_expect_tx(&full[slot], kHalf);
-                                tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
-                            } else {                   // latent features 128*(i-1) .. +127
-                                mbar_arrive_expect_tx(&full[slot], kSlot);
-                                tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot],
-                                                 policy);
-                                tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
-                                                 &full[slot], policy);
-                            }
-                            filled[slot] = round + 1;
-                        }
-                    }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    fill = __shfl_sync(0xffffffffu, fill, 0);
-                    continue;
-                }
+                const int row = int(p.cu[b]) + (t - ts[b]) * kLT;
                 for (int i = 0; i < kFills; ++i, ++fill) {
                     const int slot = fill % kSlots, round = fill / kSlots;
-                    bool go = true;
-                    if (lane == 0) {
-                        if (*abort_flag) {
-                            go = false;
-                        } else if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
-                            fail();
-                            go = false;
-                        } else {
-                            mbar_arrive_expect_tx(&full[slot], i == 0 ? kHalf : kSlot);
-                            filled[slot] = round + 1;
-                        }
+                    if (*abort_flag) { ok = false; break; }
+                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                        fail();
+                        ok = false;
+                        break;
                     }
-                    if (!__shfl_sync(0xffffffffu, go, 0)) { ok = false; break; }
                     uint8_t* dst = ring + slot * kSlot;
-                    if (!sparse) {
-                        if (lane == 0) {
-                            if (i == 0) {              // shared-key features 512..575
-                                tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
-                            } else {                   // latent features 128*(i-1) .. +127
-                                tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot],
-                                                 policy);
-                                tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
-                                                 &full[slot], policy);
-                            }
-                        }
-                    } else if (hfl < (i == 0 ? 1 : 2)) {
-                        const int x = i == 0 ? kLatent : 128 * (i - 1) + 64 * hfl;
-                        tma_gather4(dst + hfl * kHalf + g * 512, &gmap, x, g0, g1, g2, g3,
-                                    &full[slot]);
+                    if (i == 0) {              // shared-key features 512..575
+                        mbar_arrive_expect_tx(&full[slot], kHalf);
+                        tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
+                    } else {                   // latent features 128*(i-1) .. +127
+                        mbar_arrive_expect_tx(&full[slot], kSlot);
+                        tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot], policy);
+                        tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
+                                         &full[slot], policy);
                     }
+                    filled[slot] = round + 1;
                 }
             }
-            if (lane == 0) {
-                for (int s = 0; s < kSlots; ++s)
-                    if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
-                        report(p.status, kStTimeout);
-                if (nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
+            for (int s = 0; s < kSlots; ++s)
+                if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
-            }
+            if (nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
+                report(p.status, kStTimeout);
         }
     } else if (warp == 1) {
         // ------------------------------- MMA -------------------------------
@@ -525,6 +511,9 @@ __global__ void __launch_bounds__(kThreadsOf<kFp8>, 1)
                 const int f = j * kFills + i, slot = f % kSlots;
                 if (*abort_flag || !mbar_wait(&full[slot], (f / kSlots) & 1, p.wait_ns))
                     return false;
+                // cp.async writes come through the generic proxy: order them
+                // before the tensor core's reads of the slot
+                if (kSrc == kSrcGather) fence_async_smem();
                 tc_fence_after();
                 const uint32_t d = tmem + uint32_t(j & 1) * kLT;
                 const int halves = i == 0 ? 1 : 2;
@@ -1204,7 +1193,7 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
 
     // W^K as [H*128 rows (h, d)][512], W^V likewise; queries as [B][H][192]
     const int nabs = a.B < kAbsorbN ? (a.B + 15) / 16 * 16 : kAbsorbN;
-    CUtensorMap wkmap, wvmap, q3map, cmap, gmap, qmap, zmap;
+    CUtensorMap wkmap, wvmap, q3map, cmap, qmap, zmap;
     cudaError_t e = encode_tmap_2d_bf16(&wkmap, a.w_kc, kLatent, uint64_t(a.H) * 128, kLatent * 2,
                                         64, 128);
     if (e != cudaSuccess) return e;
@@ -1213,14 +1202,12 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     e = encode_tmap_3d_bf16(&q3map, a.q, kDqk, a.H, a.B, kDqk * 2, uint64_t(a.H) * kDqk * 2, 64,
                             1, nabs);
     if (e != cudaSuccess) return e;
-    if (a.rec == nullptr) {
+    const int src = a.rec ? kSrcFp8 : a.idx ? kSrcGather : kSrcTma;
+    if (src == kSrcTma) {
         e = encode_tmap_2d_bf16(&cmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, kLT);
         if (e != cudaSuccess) return e;
-        e = encode_tmap_2d_bf16(&gmap, a.ckv, kCkv, uint64_t(a.total), kCkv * 2, 64, 1);
-        if (e != cudaSuccess) return e;
-    } else {                                  // FP8 cache: read by the producer threads
+    } else {                                  // rows are read by the producer threads
         cmap = wkmap;
-        gmap = wkmap;
     }
     e = encode_tmap_2d_bf16(&qmap, qt, kCkv, uint64_t(a.B) * a.H, kCkv * 2, 64, a.H);
     if (e != cudaSuccess) return e;
@@ -1236,19 +1223,21 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
         wkmap, q3map, a.q, qt, a.w_vc, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
     latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.idx, a.topk, a.P, a.B, a.max_seqlen, pl.ctas,
                                            sched, dev.status);
-    e = cudaFuncSetAttribute(mla_latent_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kLatSmem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mla_latent_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kLatSmem));
+    const void* kern = src == kSrcFp8      ? reinterpret_cast<const void*>(mla_latent_kernel<kSrcFp8>)
+                       : src == kSrcGather ? reinterpret_cast<const void*>(mla_latent_kernel<kSrcGather>)
+                                           : reinterpret_cast<const void*>(mla_latent_kernel<kSrcTma>);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kLatSmem));
     if (e != cudaSuccess) return e;
     LatParams p{sched, a.cu, a.idx, a.topk, a.P, a.ckv, a.total, part, ml, zbuf, a.rec, a.B, a.H,
                 a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
     if (tm.begin) cudaEventRecord(tm.begin, st);
-    if (a.rec)
-        mla_latent_kernel<true><<<pl.ctas, kThreadsOf<true>, kLatSmem, st>>>(cmap, gmap, qmap, p);
+    if (src == kSrcFp8)
+        mla_latent_kernel<kSrcFp8><<<pl.ctas, kThreadsOf<kSrcFp8>, kLatSmem, st>>>(cmap, qmap, p);
+    else if (src == kSrcGather)
+        mla_latent_kernel<kSrcGather><<<pl.ctas, kThreadsOf<kSrcGather>, kLatSmem, st>>>(cmap, qmap,
+                                                                                      p);
     else
-        mla_latent_kernel<false><<<pl.ctas, kThreadsOf<false>, kLatSmem, st>>>(cmap, gmap, qmap, p);
+        mla_latent_kernel<kSrcTma><<<pl.ctas, kThreadsOf<kSrcTma>, kLatSmem, st>>>(cmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
