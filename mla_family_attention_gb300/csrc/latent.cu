@@ -63,10 +63,16 @@ constexpr int kPBytes = kMaxH * 128;             // P: [H rows][64 keys] bf16
 // (decode), 16-byte cp.async copies of the selected rows (sparse prefill), or
 // FP8 records converted to bf16 by the producer threads.
 enum Src { kSrcTma = 0, kSrcGather = 1, kSrcFp8 = 2 };
-// TMA warp, MMA warp, 8 softmax warps; the gather and FP8 variants have 128
-// producer threads instead of the TMA warp (warp 0 and warps 10-12)
+// Warp roles: 0 TMA producer, 1 Q.K^T MMA issue, 2-9 softmax and epilogue,
+// then the P.V MMA issue warp; the gather and FP8 variants have 128 producer
+// threads instead of the TMA warp (warp 0 and warps 10-12), so their P.V
+// warp is warp 13.  tcgen05.mma issue blocks the issuing thread until the
+// tensor pipe takes the instruction, so every barrier wait or commit of an
+// issuing thread idles the pipe; two issuing warps hide each other's waits.
 template <int kSrc>
-constexpr int kThreadsOf = kSrc == kSrcTma ? 320 : 416;
+constexpr int kPvWarp = kSrc == kSrcTma ? 10 : 13;
+template <int kSrc>
+constexpr int kThreadsOf = (kPvWarp<kSrc> + 1) * 32;
 constexpr int kRec = 656;                        // FP8 record: 512 codes, 4 fp32 scales, 64 bf16
 constexpr int kColO = 2 * kLT;                   // O^T columns start after the score buffers
 constexpr float kRescaleLog2 = 8.f;
@@ -202,8 +208,9 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
     uint64_t* qfree = qfull + 1;           // MMA -> TMA (a segment's Q.K^T done)
     uint64_t* ofinal = qfree + 1;          // MMA -> epilogue (a segment's P.V done)
     uint64_t* oread = ofinal + 1;          // epilogue -> MMA (O^T read out)
-    uint64_t* mdone = oread + 1;           // MMA drain before TMEM release
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mdone + 1);
+    uint64_t* pfree = oread + 1;           // P.V of a tile done: P and O^T free
+    uint64_t* mdone = pfree + 1;           // [2] each issuing warp's drain before TMEM release
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mdone + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -230,7 +237,9 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
         mbar_init(qfree, 1);
         mbar_init(ofinal, 1);
         mbar_init(oread, 8);
-        mbar_init(mdone, 1);
+        mbar_init(pfree, 1);
+        mbar_init(&mdone[0], 1);
+        mbar_init(&mdone[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -245,7 +254,8 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
         *abort_flag = 1;
     };
 
-    if (kSrc == kSrcFp8 && (warp == 0 || warp >= 10)) {
+    const bool producer_warp = warp == 0 || (warp >= 10 && warp < 13);
+    if (kSrc == kSrcFp8 && producer_warp) {
         // -------------------- FP8 producer (128 threads) --------------------
         // Thread ptid converts row ptid/2 of each fill, half ptid&1: 64 e4m3
         // codes times their group scale into 64 bf16 features (or 32 bf16
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
             if (ptid == 0 && nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
                 report(p.status, kStTimeout);
         }
-    } else if (kSrc == kSrcGather && (warp == 0 || warp >= 10)) {
+    } else if (kSrc == kSrcGather && producer_warp) {
         // ------------------- cp.async gather (128 threads) -------------------
         // Thread ptid copies 16-byte chunk ptid&7 of tile rows 8k + ptid/16:
         // of feature half (ptid/8)&1 of a latent block (k = 0..7), or of the
@@ -501,98 +511,133 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 report(p.status, kStTimeout);
         }
     } else if (warp == 1) {
-        // ------------------------------- MMA -------------------------------
+        // ---------------------------- Q.K^T MMAs ----------------------------
+        // One thread, in order: for each tile, the five fills' S (+)= Q~ K^T
+        // into the tile's score buffer.  Descriptors are built once and
+        // advanced by their 16-byte address units; the ring slot and phase
+        // advance with the fills.
         if (lane == 0 && t0 < t1) {
-            const uint32_t idesc_pv = idesc_bf16_f32(128, H, true, false);
-            const uint32_t qa = smem_u32(qs), pa = smem_u32(ps), ra = smem_u32(ring);
+            const uint64_t qdesc = smem_desc_sw128(smem_u32(qs), 16, 1024);     // Q~, K-major
+            const uint64_t kdesc = smem_desc_sw128(smem_u32(ring), 16, 1024);   // keys, K-major
+            const uint32_t qblk = uint32_t(H) * 8;       // one [H x 64] block of Q~
+            constexpr uint32_t kSlotU = kSlot >> 4, kHalfU = kHalf >> 4;
             bool ok = true;
-            // Fill i (0 = shared key, 1..4 = latent block i-1) of local tile j.
-            auto qk = [&](int j, int i) -> bool {
-                const int f = j * kFills + i, slot = f % kSlots;
-                if (*abort_flag || !mbar_wait(&full[slot], (f / kSlots) & 1, p.wait_ns))
-                    return false;
-                // cp.async writes come through the generic proxy: order them
-                // before the tensor core's reads of the slot
-                if (kSrc == kSrcGather) fence_async_smem();
-                tc_fence_after();
-                const uint32_t d = tmem + uint32_t(j & 1) * kLT;
-                const int halves = i == 0 ? 1 : 2;
-                for (int hf = 0; hf < halves; ++hf) {
-                    const int kb = i == 0 ? 8 : 2 * (i - 1) + hf;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(qa + kb * H * 128 + kk * 32, 16, 1024);
-                        const uint64_t bd =
-                            smem_desc_sw128(ra + slot * kSlot + hf * kHalf + kk * 32, 16, 1024);
-                        mma_bf16_ss(d, ad, bd, kIdescQK, (i > 0 || hf > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                if (i == 0) mma_commit(&empty[slot]);
-                return true;
-            };
-            int pv_seg = 0;      // segments whose first P.V has been issued
-            // O^T += C^T P^T for local tile j (first = first tile of its segment).
-            auto pv = [&](int j, bool first) -> bool {
-                if (*abort_flag || !mbar_wait(pfull, j & 1, p.wait_ns)) return false;
-                if (first) {
-                    if (pv_seg > 0 && !mbar_wait(oread, (pv_seg - 1) & 1, p.wait_ns)) return false;
-                    ++pv_seg;
-                }
-                tc_fence_after();
-                for (int u = 0; u < 4; ++u) {
-                    const int slot = (j * kFills + 1 + u) % kSlots;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t ad = smem_desc_sw128(ra + slot * kSlot + k * 2048, kHalf, 1024);
-                        const uint64_t bd = smem_desc_sw128(pa + k * 32, 16, 1024);
-                        mma_bf16_ss(tmem + kColO + u * H, ad, bd, idesc_pv,
-                                    (first && k == 0) ? 0u : 1u);
-                    }
-                    mma_commit(&empty[slot]);
-                }
-                return true;
+            int slot = 0;                                // ring slot of the next fill
+            uint32_t phase = 0;                          // and the parity of its phase
+            auto wait_bar = [&](uint64_t* bar, uint32_t par) -> bool {
+                if (mbar_test(bar, par)) return true;
+                return !*abort_flag && mbar_wait(bar, par, p.wait_ns);
             };
             Cursor cur{ts};
             cur.seek(t0, B);
             int nseg = 0;
-            bool prev_first = false;
             for (int t = t0; t < t1 && ok; ++t) {
                 const int j = t - t0;
                 cur.advance(t);
                 const int b = cur.b;
                 const bool first = (t == t0 || t == ts[b]);
                 const bool last = (t + 1 == t1 || t + 1 == ts[b + 1]);
-                if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.wait_ns)) {
+                if (j >= 2 && !wait_bar(&sfree[j & 1], ((j - 2) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
                 if (first) {
-                    if (j > 0) {
-                        if (!pv(j - 1, prev_first)) { ok = false; break; }
-                        mma_commit(ofinal);
-                    }
-                    if (!mbar_wait(qfull, nseg & 1, p.wait_ns)) { ok = false; break; }
+                    if (!wait_bar(qfull, nseg & 1)) { ok = false; break; }
                     ++nseg;
-                    for (int i = 0; i < kFills && ok; ++i) ok = qk(j, i);
-                } else {
-                    ok = qk(j, 0) && qk(j, 1) && pv(j - 1, prev_first);
-                    for (int i = 2; i < kFills && ok; ++i) ok = qk(j, i);
+                }
+                const uint32_t d = tmem + uint32_t(j & 1) * kLT;
+                for (int i = 0; i < kFills; ++i) {
+                    if (!wait_bar(&full[slot], phase)) { ok = false; break; }
+                    // cp.async writes come through the generic proxy: order
+                    // them before the tensor core's reads of the slot
+                    if (kSrc == kSrcGather) fence_async_smem();
+                    tc_fence_after();
+                    const uint64_t b0 = kdesc + uint32_t(slot) * kSlotU;
+                    if (i == 0) {                        // shared-key features
+                        const uint64_t a0 = qdesc + 8 * qblk;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(d, a0 + 2 * kk, b0 + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
+                        mma_commit(&empty[slot]);
+                    } else {                             // latent block i-1
+                        const uint64_t a0 = qdesc + uint32_t(2 * (i - 1)) * qblk;
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss(d, a0 + hf * qblk + 2 * kk, b0 + hf * kHalfU + 2 * kk,
+                                            kIdescQK, 1u);
+                    }
+                    if (++slot == kSlots) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 if (last) mma_commit(qfree);
                 mma_commit(&sfull[j & 1]);
-                prev_first = first;
             }
-            if (ok) {
-                ok = pv(t1 - 1 - t0, prev_first);
-                mma_commit(ofinal);
+            if (!ok) fail();
+            mma_commit(&mdone[0]);
+            if (!mbar_wait(&mdone[0], 0, p.wait_ns)) report(p.status, kStTimeout);
+        }
+    } else if (warp == kPvWarp<kSrc>) {
+        // ----------------------------- P.V MMAs -----------------------------
+        // O^T += C^T P^T for each tile once its probabilities are written;
+        // the latent blocks' ring slots are released as their MMAs finish.
+        // A tile's P.V follows its softmax, which followed its Q.K^T, so the
+        // slots' Q.K^T reads are complete when these commits free them.
+        if (lane == 0 && t0 < t1) {
+            const uint32_t idesc_pv = idesc_bf16_f32(128, H, true, false);
+            const uint64_t cdesc = smem_desc_sw128(smem_u32(ring), kHalf, 1024);  // C^T, MN-major
+            const uint64_t pdesc = smem_desc_sw128(smem_u32(ps), 16, 1024);     // P, K-major
+            constexpr uint32_t kSlotU = kSlot >> 4;
+            bool ok = true;
+            auto wait_bar = [&](uint64_t* bar, uint32_t par) -> bool {
+                if (mbar_test(bar, par)) return true;
+                return !*abort_flag && mbar_wait(bar, par, p.wait_ns);
+            };
+            Cursor cur{ts};
+            cur.seek(t0, B);
+            int s1 = 1;          // ring slot of the current tile's first latent block
+            int pv_seg = 0;      // segments whose first P.V has been issued
+            for (int t = t0; t < t1 && ok; ++t) {
+                const int j = t - t0;
+                cur.advance(t);
+                const int b = cur.b;
+                const bool first = (t == t0 || t == ts[b]);
+                const bool last = (t + 1 == t1 || t + 1 == ts[b + 1]);
+                if (!wait_bar(pfull, j & 1)) { ok = false; break; }
+                if (first) {
+                    // the previous segment's O^T has been read out
+                    if (pv_seg > 0 && !wait_bar(oread, (pv_seg - 1) & 1)) { ok = false; break; }
+                    ++pv_seg;
+                }
+                if (kSrc == kSrcGather) fence_async_smem();
+                tc_fence_after();
+                int sl = s1;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint64_t a0 = cdesc + uint32_t(sl) * kSlotU;
+                    const uint32_t d = tmem + kColO + uint32_t(u * H);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16_ss(d, a0 + 128 * k, pdesc + 2 * k, idesc_pv,
+                                    (first && k == 0) ? 0u : 1u);
+                    mma_commit(&empty[sl]);
+                    if (++sl == kSlots) sl = 0;
+                }
+                mma_commit(pfree);
+                if (last) mma_commit(ofinal);
+                s1 += kFills;
+                if (s1 >= kSlots) s1 -= kSlots;
             }
             if (!ok) {
                 fail();
                 mma_commit(ofinal);
             }
-            mma_commit(mdone);
-            if (!mbar_wait(mdone, 0, p.wait_ns)) report(p.status, kStTimeout);
+            mma_commit(&mdone[1]);
+            if (!mbar_wait(&mdone[1], 0, p.wait_ns)) report(p.status, kStTimeout);
         }
     } else {
         // ------------------------- softmax / epilogue ------------------------
@@ -614,7 +659,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 nraw = sel_raw(p, nxt.b, seq_desc(p, nxt.b), (t0 - ts[nxt.b]) * kLT + half * 32 + lane);
         }
         auto wait = [&](uint64_t* bar, uint32_t parity) {
-            if (*abort_flag) return;
+            if (mbar_test(bar, parity) || *abort_flag) return;
             if (!mbar_wait(bar, parity, p.wait_ns)) fail();
         };
         for (int t = t0; t < t1; ++t) {
@@ -668,6 +713,9 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
             } else if (real && rm > m + kRescaleLog2) {
                 need = true;
             }
+            // the previous tile's P.V is done before O^T is rescaled or P rewritten
+            if (j > 0) wait(pfree, (j - 1) & 1);
+            tc_fence_after();
             if (bar_or(2, 256, need)) {
                 // a row maximum grew past the slack: rescale O^T columns (heads)
                 float f = 1.f;
