@@ -703,42 +703,45 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 s[i] = x;
                 lm = fmaxf(lm, x);
             }
-            xmax[(sb * 2 + half) * 128 + r] = lm;
-            named_bar_sync(1, 256);
-            const float rm = fmaxf(xmax[(sb * 2) * 128 + r], xmax[(sb * 2 + 1) * 128 + r]);
-            bool need = false;
-            if (first) {
-                m = real ? rm : 0.f;
-                l = 0.f;
-            } else if (real && rm > m + kRescaleLog2) {
-                need = true;
-            }
+            // A segment's first tile sets the running maxima; later tiles
+            // rescale only when a row maximum grows past the slack, which a
+            // thread can see from its own half of the row, so the halves'
+            // maxima are exchanged only on those tiles.
+            const bool need = first || (real && lm > m + kRescaleLog2);
             // the previous tile's P.V is done before O^T is rescaled or P rewritten
             if (j > 0) wait(pfree, (j - 1) & 1);
             tc_fence_after();
             if (bar_or(2, 256, need)) {
-                // a row maximum grew past the slack: rescale O^T columns (heads)
-                float f = 1.f;
-                if (need) {
-                    f = ex2(m - rm);
-                    m = rm;
-                    l *= f;
-                }
-                if (half == 0) fsm[r] = f;
+                xmax[(sb * 2 + half) * 128 + r] = lm;
                 named_bar_sync(1, 256);
-                for (int uu = 0; uu < 2; ++uu) {
-                    const uint32_t base = lane_base + kColO + (2 * half + uu) * H;
-                    for (int c0 = 0; c0 < H; c0 += 16) {
-                        float v[16];
-                        tmem_ld16(base + c0, v);
-                        tmem_ld_wait();
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * fsm[c0 + i]);
-                        tmem_st16(base + c0, w);
+                const float rm = fmaxf(xmax[(sb * 2) * 128 + r], xmax[(sb * 2 + 1) * 128 + r]);
+                if (first) {
+                    m = real ? rm : 0.f;
+                    l = 0.f;
+                } else {
+                    // rescale O^T columns (heads) of the rows whose maximum grew
+                    float f = 1.f;
+                    if (real && rm > m + kRescaleLog2) {
+                        f = ex2(m - rm);
+                        m = rm;
+                        l *= f;
                     }
+                    if (half == 0) fsm[r] = f;
+                    named_bar_sync(1, 256);
+                    for (int uu = 0; uu < 2; ++uu) {
+                        const uint32_t base = lane_base + kColO + (2 * half + uu) * H;
+                        for (int c0 = 0; c0 < H; c0 += 16) {
+                            float v[16];
+                            tmem_ld16(base + c0, v);
+                            tmem_ld_wait();
+                            uint32_t w[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * fsm[c0 + i]);
+                            tmem_st16(base + c0, w);
+                        }
+                    }
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
             }
             // probabilities, bf16, into P row r (128-byte swizzled K-major rows)
             uint32_t w[16];
