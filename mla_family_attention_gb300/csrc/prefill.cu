@@ -16,9 +16,12 @@
 //     192-feature keys.
 //   * warp 0: TMA producer for a 2-stage key ring (three 64-feature boxes of
 //     128 keys, 128-byte swizzle) and a 2-stage value ring;
-//   * warp 1: owns TMEM; one lane issues S_{j+1} = Q K_{j+1}^T before
-//     O += P_j V_j, so the next scores are computed while the softmax of the
-//     current tile runs; commits signal the other roles through mbarriers;
+//   * warp 1: owns TMEM; one lane issues S_j = Q K_j^T; warp 10: one lane
+//     issues O += P_j V_j.  tcgen05.mma blocks the issuing thread until the
+//     pipe accepts it, so with two issuing threads one's barrier waits and
+//     commits overlap the other's MMAs; the next scores are computed while
+//     the softmax of the current tile runs.  S_{j+2} reuses the buffer whose
+//     P_j the P.V of tile j reads, so it waits for that P.V to complete;
 //   * warps 2-9: two threads per query row, each owning 64 of the tile's 128
 //     key columns (and 64 of the 128 output features).  They load their half
 //     of the row's scores, apply the causal / length mask on tiles that need
@@ -45,7 +48,8 @@ constexpr int kBox = kBN * 64 * 2;             // 16 KB: 128 rows x 64 features
 constexpr int kKTile = 3 * kBox;               // 48 KB of keys
 constexpr int kVTile = 2 * kBox;               // 32 KB of values
 constexpr int kSoftmaxWarps = 8;               // two per TMEM lane quadrant
-constexpr int kPThreads = (2 + kSoftmaxWarps) * 32;
+constexpr int kPvWarp = 2 + kSoftmaxWarps;     // the P.V issuing warp, after the softmax warps
+constexpr int kPThreads = (kPvWarp + 1) * 32;
 constexpr uint32_t kCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 384;
 constexpr float kRescaleLog2 = 8.f;
@@ -112,7 +116,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint64_t* odone = pfull + 2;                                // MMA -> softmax (each P.V)
     uint64_t* ofinal = odone + 1;                               // MMA -> epilogue
     uint64_t* qready = ofinal + 1;                              // softmax -> MMA
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qready + 1);
+    uint64_t* qkdone = qready + 1;                              // Q.K^T lane's drain
+    uint64_t* sfree = qkdone + 1;                               // [2] P.V -> Q.K^T (buffer's P read)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sfree + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     // row-half exchange between the two softmax warps of a quadrant:
     // [parity][half][row] partial maxima and the halves' ok flags, and a
@@ -150,6 +156,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(odone, 1);
         mbar_init(ofinal, 1);
         mbar_init(qready, kSoftmaxWarps);
+        mbar_init(qkdone, 1);
+        mbar_init(&sfree[0], 1);
+        mbar_init(&sfree[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -198,14 +207,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     report(p.status, kStTimeout);
         }
     } else if (warp == 1) {
-        // --------------------------------- MMA ---------------------------------
+        // ------------------------------ Q.K^T MMAs ------------------------------
         if (lane == 0) {
             bool ok = mbar_wait(qready, 0, p.wait_ns);
             bool issued = false;
-            // S_j = Q K_j^T into score buffer j&1 (A = queries in TMEM).
-            auto issue_qk = [&](int j) -> bool {
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (*abort_flag) { ok = false; break; }
                 const int ks = j % kKStages;
-                if (!mbar_wait(&kfull[ks], (j / kKStages) & 1, p.wait_ns)) return false;
+                // S_j = Q K_j^T into score buffer j&1 (A = queries in TMEM), once
+                // the keys landed and P_{j-2}, in that buffer, has been consumed
+                // (a barrier per buffer: its next phase needs S_j, so the
+                // parity cannot run two phases ahead of this wait)
+                if (!mbar_wait(&kfull[ks], (j / kKStages) & 1, p.wait_ns) ||
+                    (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.wait_ns))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t kb = smem_u32(ksm + ks * kKTile);
                 const uint32_t d = tmem + kColS + uint32_t(j & 1) * 128;
@@ -217,15 +234,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 mma_commit(&kempty[ks]);
                 mma_commit(&sfull[j & 1]);
                 issued = true;
-                return true;
-            };
-            if (ok) {
-                tc_fence_after();
-                ok = n_kv > 0 && issue_qk(0);
             }
+            if (!ok) {
+                report(p.status, kStTimeout);
+                *abort_flag = 1;
+            }
+            mma_commit(qkdone);
+            if (issued && !mbar_wait(qkdone, 0, p.wait_ns)) report(p.status, kStTimeout);
+        }
+    } else if (warp == kPvWarp) {
+        // ------------------------------- P.V MMAs -------------------------------
+        if (lane == 0) {
+            bool ok = true, issued = false;
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
-                if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
                 const int vs = j % kVStages;
                 if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, p.wait_ns) ||
                     !mbar_wait(&vfull[vs], (j / kVStages) & 1, p.wait_ns)) {
@@ -242,7 +264,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     mma_bf16_ts(tmem + kColO, a + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&vempty[vs]);
+                mma_commit(&sfree[j & 1]);
                 mma_commit(odone);
+                issued = true;
             }
             if (!ok) {
                 report(p.status, kStTimeout);
