@@ -54,7 +54,7 @@ constexpr uint32_t kCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 384;
 constexpr float kRescaleLog2 = 8.f;
 #ifndef MLA_PREFILL_POLY_EXP
-#define MLA_PREFILL_POLY_EXP 0   // 1: odd columns exponentiate on the FMA pipe
+#define MLA_PREFILL_POLY_EXP 0   // 1: odd columns exponentiate on the FMA pipe, 2: one in four
 #endif
 constexpr size_t kPrefillSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile + 256 +
                                 (2 * 2 * kBM * 2 + 2 * kBM) * 4;
@@ -393,7 +393,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const float p0 = ex2(fmaf(s[c * 32 + 2 * u], p.scale_log2, nme));
-                    const float p1 = ex2(fmaf(s[c * 32 + 2 * u + 1], p.scale_log2, nme));
+                    const float t1 = fmaf(s[c * 32 + 2 * u + 1], p.scale_log2, nme);
+                    const bool poly = MLA_PREFILL_POLY_EXP == 1 || (MLA_PREFILL_POLY_EXP == 2 && (u & 1));
+                    const float p1 = poly ? exp2_fma(t1) : ex2(t1);
                     ls[u & 3] += p0 + p1;
                     w[u] = pack_bf16(p0, p1);
                 }
