@@ -129,4 +129,16 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start while the previous kernel of the stream
+// finishes; grid_dep_wait blocks until that grid has completed and its
+// writes are visible (a no-op under a normal launch), so it precedes every
+// read of the previous kernel's results.  grid_dep_trigger, issued once a
+// CTA's work is done, lets the next kernel start launching early; its own
+// grid_dep_wait still waits for this grid to complete.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace mla

@@ -32,6 +32,27 @@ struct KernelTimer {
     cudaEvent_t begin = nullptr, end = nullptr;
 };
 
+#ifdef __CUDACC__
+// Launch with programmatic stream serialization: the kernel may begin while
+// the previous kernel of the stream finishes, so it calls grid_dep_wait
+// before it reads that kernel's results.
+template <typename... P, typename... A>
+inline cudaError_t launch_after_prev(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, A&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+#endif
+
 // ------------------------------ decode ------------------------------------
 // Where sequence b's cache lives.  Packed (cap == 0): [H, T_b, D] at
 // position offset cu[b], T_b = cu[b+1] - cu[b].  Fixed capacity (cap > 0):

@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    grid_dep_wait();                                     // the work split and absorbed queries
 
     auto fail = [&]() {
         report(p.status, kStTimeout);
@@ -813,6 +814,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) grid_dep_trigger();
 }
 
 // q~[b,h,0:512] = W^K_h^T q[b,h,0:128] and q~[b,h,512:576] = q[b,h,128:192],
@@ -827,6 +829,8 @@ __global__ void __launch_bounds__(128) latent_absorb_kernel(
     const __grid_constant__ CUtensorMap wkmap, const __grid_constant__ CUtensorMap qmap,
     const uint16_t* q, uint16_t* qt, const uint16_t* wv, int B, int H, int nbox,
     long long wait_ns, int* status) {
+    // the work split launched next reads none of this kernel's output
+    if (threadIdx.x == 0) grid_dep_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -912,6 +916,7 @@ __global__ void __launch_bounds__(128) latent_absorb_kernel(
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
+
 
 // Block-wide exclusive scan of one int per thread (1024 threads); returns the
 // exclusive prefix and writes the total to *total.
@@ -1006,6 +1011,10 @@ __global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, c
         sched[1] = per;
         sched[2] = nmulti;
     }
+    // runs beside the absorption (it reads none of its output); finishing
+    // only after it lets the attention kernel's wait cover both
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_trigger();
 }
 
 // Fixup: the sequences whose tiles spanned several CTAs.  Warp w of CTA
@@ -1017,6 +1026,7 @@ __global__ void __launch_bounds__(1024) latent_sched_kernel(const int64_t* cu, c
 __global__ void __launch_bounds__(256) latent_fixup_kernel(const float* part, const float* ml,
                                                            const int* sched_base, uint16_t* zbuf,
                                                            int B, int H) {
+    grid_dep_wait();                             // the attention kernel's partials
     const Sched sch{sched_base};
     const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = blockIdx.y * 8 + warp;
@@ -1063,6 +1073,7 @@ __global__ void __launch_bounds__(256) latent_fixup_kernel(const float* part, co
     uint32_t* dst = reinterpret_cast<uint32_t*>(zbuf + (int64_t(b) * H + h) * kLatent + 2 * lane);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) dst[32 * kk] = pack2(z[2 * kk], z[2 * kk + 1]);
+    if (lane == 0) grid_dep_trigger();
 }
 
 // Output projection and gate: for head h and 128 sequences (rows),
@@ -1070,11 +1081,16 @@ __global__ void __launch_bounds__(256) latent_fixup_kernel(const float* part, co
 // as a tensor-core GEMM with the sequences as M (A = z~ rows, K-major), the
 // 128 output features as N (B = W^V_h, K-major) and K = 512 latent features,
 // streamed in eight 64-feature blocks through a four-stage ring.
+// kN output features per CTA: 128 (a head's all) for large batches; for a
+// batch of at most 128 sequences the head's features are split over two
+// CTAs (N = 64) so twice as many SMs stream W^V.
 constexpr int kOutStages = 4;
-constexpr int kOutStage = 2 * 16384;             // z~ block + W^V block
-constexpr size_t kOutSmem = 1024 + size_t(kOutStages) * kOutStage + 128;
-constexpr uint32_t kIdescOut = idesc_bf16_f32(128, 128, false, false);
+template <int kN>
+constexpr int kOutStageOf = 16384 + kN * 128;    // z~ block (128 rows) + W^V block
+template <int kN>
+constexpr size_t kOutSmemOf = 1024 + size_t(kOutStages) * kOutStageOf<kN> + 128;
 
+template <int kN>
 __global__ void __launch_bounds__(192) latent_out_kernel(
     const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap wvmap,
     const int* sched_base, const uint16_t* gate, uint16_t* out, int B, int H, int zrows,
@@ -1082,11 +1098,13 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kOutStage = kOutStageOf<kN>;
+    constexpr uint32_t kIdescOut = idesc_bf16_f32(128, kN, false, false);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOutStages * kOutStage);
     uint64_t* empty = full + kOutStages;
     uint64_t* done = empty + kOutStages;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
-    const int h = blockIdx.x, b0 = blockIdx.y * 128;
+    const int h = blockIdx.x, b0 = blockIdx.y * 128, n0 = blockIdx.z * kN;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int* ts = Sched{sched_base}.ts();
     if (threadIdx.x == 0) {
@@ -1097,11 +1115,12 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
         mbar_init(done, 1);
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_holder, 128);
+    if (warp == 1) tmem_alloc(tmem_holder, kN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    grid_dep_wait();                                     // z~ from the attention and fixup kernels
     if (warp == 0 && lane == 0) {
         int filled[kOutStages] = {0, 0, 0, 0};
         for (int kb = 0; kb < 8; ++kb) {
@@ -1110,9 +1129,9 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
                 report(status, kStTimeout);
                 break;
             }
-            mbar_arrive_expect_tx(&full[st], 16384 + zrows * 128);
+            mbar_arrive_expect_tx(&full[st], kN * 128 + zrows * 128);
             tma_load_3d(sm + st * kOutStage, &zmap, kb * 64, h, b0, &full[st]);
-            tma_load_2d(sm + st * kOutStage + 16384, &wvmap, kb * 64, h * kDv, &full[st]);
+            tma_load_2d(sm + st * kOutStage + 16384, &wvmap, kb * 64, h * kDv + n0, &full[st]);
             filled[st] = r + 1;
         }
         for (int i = 0; i < kOutStages; ++i)
@@ -1139,18 +1158,18 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
         }
         mma_commit(done);
     } else if (warp >= 2) {
-        // thread = sequence row (TMEM lane), 128 output features; the gate
+        // thread = sequence row (TMEM lane), kN output features; the gate
         // logits are loaded first so their latency overlaps the GEMM
         const int quad = warp & 3, b = b0 + quad * 32 + lane;
         const bool live = b < B && ts[b + 1] > ts[b];
-        uint4 g[16];
-        const uint4* g4 = reinterpret_cast<const uint4*>(gate + (int64_t(b) * H + h) * kDv);
+        uint4 g[kN / 8];
+        const uint4* g4 = reinterpret_cast<const uint4*>(gate + (int64_t(b) * H + h) * kDv + n0);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) g[q] = (live && gate) ? __ldg(g4 + q) : make_uint4(0, 0, 0, 0);
+        for (int q = 0; q < kN / 8; ++q) g[q] = (live && gate) ? __ldg(g4 + q) : make_uint4(0, 0, 0, 0);
         if (!mbar_wait(done, 0, wait_ns) && lane == 0) report(status, kStTimeout);
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < kN; c0 += 32) {
             float v[32];
             tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + c0, v);
             tmem_ld_wait();
@@ -1168,14 +1187,14 @@ __global__ void __launch_bounds__(192) latent_out_kernel(
                                         : pack2(a, c);
                 }
             }
-            uint4* o4 = reinterpret_cast<uint4*>(out + (int64_t(b) * H + h) * kDv + c0);
+            uint4* o4 = reinterpret_cast<uint4*>(out + (int64_t(b) * H + h) * kDv + n0 + c0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) o4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 128);
+    if (warp == 1) tmem_dealloc(tmem, kN);
 }
 
 // FP8 latent records: one warp per cache row.  Group g (features 128g..) is
@@ -1248,7 +1267,9 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     cudaError_t e = encode_tmap_2d_bf16(&wkmap, a.w_kc, kLatent, uint64_t(a.H) * 128, kLatent * 2,
                                         64, 128);
     if (e != cudaSuccess) return e;
-    e = encode_tmap_2d_bf16(&wvmap, a.w_vc, kLatent, uint64_t(a.H) * kDv, kLatent * 2, 64, 128);
+    const bool small = a.B <= 128;               // one sequence block: split each head's features
+    e = encode_tmap_2d_bf16(&wvmap, a.w_vc, kLatent, uint64_t(a.H) * kDv, kLatent * 2, 64,
+                            small ? 64 : 128);
     if (e != cudaSuccess) return e;
     e = encode_tmap_3d_bf16(&q3map, a.q, kDqk, a.H, a.B, kDqk * 2, uint64_t(a.H) * kDqk * 2, 64,
                             1, nabs);
@@ -1272,8 +1293,12 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     if (e != cudaSuccess) return e;
     latent_absorb_kernel<<<dim3(4, a.H, (a.B + nabs - 1) / nabs), 128, kAbsorbSmem, st>>>(
         wkmap, q3map, a.q, qt, a.w_vc, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
-    latent_sched_kernel<<<1, 1024, 0, st>>>(a.cu, a.idx, a.topk, a.P, a.B, a.max_seqlen, pl.ctas,
-                                           sched, dev.status);
+    // the four kernels after the absorption are launched programmatically
+    // dependent: each may start while its predecessor finishes and waits on
+    // the device for that predecessor's results
+    e = launch_after_prev(latent_sched_kernel, dim3(1), dim3(1024), 0, st, a.cu, a.idx, a.topk, a.P,
+                          a.B, a.max_seqlen, pl.ctas, sched, dev.status);
+    if (e != cudaSuccess) return e;
     const void* kern = src == kSrcFp8      ? reinterpret_cast<const void*>(mla_latent_kernel<kSrcFp8>)
                        : src == kSrcGather ? reinterpret_cast<const void*>(mla_latent_kernel<kSrcGather>)
                                            : reinterpret_cast<const void*>(mla_latent_kernel<kSrcTma>);
@@ -1283,22 +1308,37 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
                 a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
     if (tm.begin) cudaEventRecord(tm.begin, st);
     if (src == kSrcFp8)
-        mla_latent_kernel<kSrcFp8><<<pl.ctas, kThreadsOf<kSrcFp8>, kLatSmem, st>>>(cmap, qmap, p);
+        e = launch_after_prev(mla_latent_kernel<kSrcFp8>, dim3(pl.ctas), dim3(kThreadsOf<kSrcFp8>),
+                              kLatSmem, st, cmap, qmap, p);
     else if (src == kSrcGather)
-        mla_latent_kernel<kSrcGather><<<pl.ctas, kThreadsOf<kSrcGather>, kLatSmem, st>>>(cmap, qmap,
-                                                                                      p);
+        e = launch_after_prev(mla_latent_kernel<kSrcGather>, dim3(pl.ctas),
+                              dim3(kThreadsOf<kSrcGather>), kLatSmem, st, cmap, qmap, p);
     else
-        mla_latent_kernel<kSrcTma><<<pl.ctas, kThreadsOf<kSrcTma>, kLatSmem, st>>>(cmap, qmap, p);
+        e = launch_after_prev(mla_latent_kernel<kSrcTma>, dim3(pl.ctas), dim3(kThreadsOf<kSrcTma>),
+                              kLatSmem, st, cmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    latent_fixup_kernel<<<dim3(a.H, (pl.ctas + 7) / 8), 256, 0, st>>>(part, ml, sched, zbuf, a.B,
-                                                                      a.H);
-    e = cudaFuncSetAttribute(latent_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kOutSmem));
+    // the fixup list holds at most min(B, CTAs) sequences
+    e = launch_after_prev(latent_fixup_kernel, dim3(a.H, (min(a.B, pl.ctas) + 7) / 8), dim3(256), 0,
+                          st, static_cast<const float*>(part), static_cast<const float*>(ml),
+                          static_cast<const int*>(sched), zbuf, a.B, a.H);
     if (e != cudaSuccess) return e;
-    latent_out_kernel<<<dim3(a.H, (a.B + 127) / 128), 192, kOutSmem, st>>>(
-        zmap, wvmap, sched, a.gate, a.out, a.B, a.H, zrows, kn.wait_limit_ns, dev.status);
+    if (small) {
+        e = cudaFuncSetAttribute(latent_out_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kOutSmemOf<64>));
+        if (e != cudaSuccess) return e;
+        e = launch_after_prev(latent_out_kernel<64>, dim3(a.H, 1, 2), dim3(192), kOutSmemOf<64>, st,
+                              zmap, wvmap, static_cast<const int*>(sched), a.gate, a.out, a.B, a.H,
+                              zrows, kn.wait_limit_ns, dev.status);
+    } else {
+        e = cudaFuncSetAttribute(latent_out_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kOutSmemOf<128>));
+        if (e != cudaSuccess) return e;
+        e = launch_after_prev(latent_out_kernel<128>, dim3(a.H, (a.B + 127) / 128, 1), dim3(192),
+                              kOutSmemOf<128>, st, zmap, wvmap, static_cast<const int*>(sched),
+                              a.gate, a.out, a.B, a.H, zrows, kn.wait_limit_ns, dev.status);
+    }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
