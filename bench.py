@@ -328,7 +328,7 @@ class DsaWork:
         sb = acc.sparse_kv_bytes(lengths, self.H, self.topk)
         self.work = ib + sb
         self.unit, self.bound = "GB/s", "hbm"
-        self.launches_per_step = 8      # tiles, score, 4 top-k passes, sparse partial, merge
+        self.launches_per_step = 5      # tiles, score, top-k, sparse partial, merge
         self.kernels = [(_lib.OP_INDEX_TOPK, "dsa_score_kernel", ib),
                         (_lib.OP_SPARSE_DECODE, "decode_partial_kernel<sparse>", sb)]
 
@@ -364,7 +364,7 @@ class IndexWork:
                                                    self.topk), dtype=torch.uint8, device=dev)
         self.work = acc.index_key_bytes(lengths)
         self.unit, self.bound = "GB/s", "hbm"
-        self.launches_per_step = 6      # tiles, score, 4 top-k passes
+        self.launches_per_step = 3      # tiles, score, top-k
         self.kernels = [(_lib.OP_INDEX_TOPK, "dsa_score_kernel", self.work)]
 
     def step(self, stream):
@@ -387,7 +387,7 @@ class IndexFp8Work(IndexWork):
                                                    self.max_len, self.topk),
                                 dtype=torch.uint8, device=dev)
         self.work = acc.index_key_bytes_fp8(self.lengths)
-        self.launches_per_step = 7      # query quantisation, tiles, score, 4 top-k passes
+        self.launches_per_step = 4      # query quantisation, tiles, score, top-k
         self.kernels = [(_lib.OP_INDEX_TOPK_FP8, "dsa_score_kernel<fp8>", self.work)]
 
     def step(self, stream):
@@ -530,7 +530,7 @@ class LatentDecodeWork:
                                                  self.max_len, 0), dtype=torch.uint8, device=dev)
         self.work = acc.latent_kv_bytes(lengths)
         self.unit, self.bound = "GB/s", "hbm"
-        self.launches_per_step = 4      # absorb, schedule, latent attention, merge
+        self.launches_per_step = 5      # absorb, schedule, latent attention, fixup, W^V output
         self.kernels = [(_lib.OP_LATENT_DECODE, "mla_latent_kernel", self.work)]
 
     def step(self, stream):
@@ -629,9 +629,12 @@ E2E_HOST_LIMIT = 24 << 30    # pinned host copies of the inputs for the end-to-e
 
 
 def time_work(work, steps, warmup, dev, stream, world, sampler=None):
-    """CUDA-event time of `steps` steps (after `warmup`), and each dominant
-    kernel's own event time over the same region.  Workloads whose inputs fit
-    in L2 (work.flush_l2) are timed step by step with a 512 MB write between
+    """CUDA-event time of `steps` steps (after `warmup`), then each dominant
+    kernel's own event time over a second run of `steps` steps.  The step
+    time is taken with the library's per-kernel events off (an event recorded
+    between two kernels keeps the later one from being placed on the SMs
+    while the earlier one finishes).  Workloads whose inputs fit in L2
+    (work.flush_l2) are timed step by step with a 512 MB write between
     steps, outside the timed events."""
     mla = work.mla
     for _ in range(warmup):
@@ -640,32 +643,40 @@ def time_work(work, steps, warmup, dev, stream, world, sampler=None):
     torch.cuda.synchronize(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) \
         if getattr(work, "flush_l2", False) else None
+
+    def region(evs):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        if flush is None:
+            evs[0][0].record(stream)
+            for _ in range(steps):
+                work.step(stream)
+            evs[0][1].record(stream)
+        else:
+            for i in range(steps):
+                flush.fill_(i & 0xFF)
+                evs[i][0].record(stream)
+                work.step(stream)
+                evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+
+    def events():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(steps if flush is not None else 1)]
+
+    ev = events()
+    if sampler:
+        sampler.mark_start()
+    region(ev)
+    if sampler:
+        sampler.mark_end()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world)
     mla.timing_enable(True)
     for kd in work.kernels:
         mla.timing_read(kd[0])
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps if flush is not None else 1)]
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_start()
-    if flush is None:
-        ev[0][0].record(stream)
-        for _ in range(steps):
-            work.step(stream)
-        ev[0][1].record(stream)
-    else:
-        for i in range(steps):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            work.step(stream)
-            ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.mark_end()
-    barrier(world)
+    region(events())
     mla.timing_enable(False)
-    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world)
     del flush
     kern = []
     for kd in work.kernels:
@@ -750,7 +761,7 @@ def run_ours(args, world, rank, local):
             also[other] = {"value": round(wk.work * world / (ms_o * 1e-3) / _scale(wk), 2),
                            "unit": wk.unit, "ms_per_step": round(ms_o, 4), "steps": k_steps,
                            "roofline": roofline(wk, kern_o)}
-            line["gpu_launches"] += wk.launches_per_step * (k_steps + 3) * world
+            line["gpu_launches"] += wk.launches_per_step * (2 * k_steps + 3) * world
             wk.free()
             del wk
             torch.cuda.empty_cache()

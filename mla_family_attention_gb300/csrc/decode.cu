@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
         }
         *abort_flag = 0;
         fence_mbar_init();
+        grid_dep_trigger();
     }
+    grid_dep_wait();   // the item table (dense) or the selections (sparse) of earlier kernels
     __syncthreads();
 
     const int n_items = total_items<kSparse>(p);
@@ -467,6 +469,8 @@ __global__ void __launch_bounds__(1024) decode_items_kernel(const SeqLayout seq,
                                                             int chunk, int max_seqlen,
                                                             int* item_start, int* status) {
     __shared__ int warp_sums[32];
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();
     const int per = (B + blockDim.x - 1) / blockDim.x;
     const int b0 = min(B, int(threadIdx.x) * per), b1 = min(B, b0 + per);
     int local = 0;
@@ -507,6 +511,8 @@ __global__ void __launch_bounds__(1024) decode_items_kernel(const SeqLayout seq,
 __global__ void __launch_bounds__(256) decode_merge_kernel(
     const float* part_acc, const float* part_ml, const SeqLayout seq, const uint16_t* gate,
     uint16_t* out, int B, int H, int chunk, int max_chunks, int max_seqlen, int sparse_topk) {
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();                           // the partial kernel's chunk states
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= B * H) return;
@@ -516,21 +522,35 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(
     const int span = sparse_topk > 0 ? sparse_topk : int(T);
     const int nch = (span + chunk - 1) / chunk;
     const int64_t s0 = int64_t(gw) * max_chunks;
+    // Chunks go 32 at a time: lane c holds chunk c's (max, sum), and every
+    // lane's accumulator loads of the 32 chunks are issued together.
     float mx = -INFINITY;
     for (int c = lane; c < nch; c += 32) mx = fmaxf(mx, part_ml[(s0 + c) * 2]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float a[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
     if (mx != -INFINITY) {
-        for (int c = 0; c < nch; ++c) {
-            const float wgt = ex2(part_ml[(s0 + c) * 2] - mx);
-            L += wgt * part_ml[(s0 + c) * 2 + 1];
-            const float4 pa = *reinterpret_cast<const float4*>(part_acc + (s0 + c) * kDv + lane * 4);
-            a[0] += wgt * pa.x;
-            a[1] += wgt * pa.y;
-            a[2] += wgt * pa.z;
-            a[3] += wgt * pa.w;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int cnt = min(32, nch - c0);
+            float wl = 0.f;
+            if (lane < cnt) {
+                const float2 ml = *reinterpret_cast<const float2*>(part_ml + (s0 + c0 + lane) * 2);
+                wl = ex2(ml.x - mx);
+                L += wl * ml.y;
+            }
+            const float* base = part_acc + (s0 + c0) * kDv + lane * 4;
+#pragma unroll 8
+            for (int u = 0; u < cnt; ++u) {
+                const float wgt = __shfl_sync(0xffffffffu, wl, u);
+                const float4 pa = *reinterpret_cast<const float4*>(base + u * kDv);
+                a[0] += wgt * pa.x;
+                a[1] += wgt * pa.y;
+                a[2] += wgt * pa.z;
+                a[3] += wgt * pa.w;
+            }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     }
     const float inv = L > 0.f ? 1.0f / L : 0.f;
     const int64_t o = int64_t(gw) * kDv + lane * 4;
@@ -610,25 +630,31 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse
                                  int(smem_bytes<true>()));
         if (e != cudaSuccess) return e;
         if (tm.begin) cudaEventRecord(tm.begin, st);
-        decode_partial_kernel<true><<<grid, Roles<true>::kThreads, smem_bytes<true>(), st>>>(p);
+        e = launch_after_prev(decode_partial_kernel<true>, dim3(grid), dim3(Roles<true>::kThreads),
+                              smem_bytes<true>(), st, p);
         if (tm.end) cudaEventRecord(tm.end, st);
     } else {
-        decode_items_kernel<<<1, 1024, 0, st>>>(a.seq, a.B, a.H, pl.chunk, a.max_seqlen,
-                                               const_cast<int*>(p.item_start), dev.status);
+        e = launch_after_prev(decode_items_kernel, dim3(1), dim3(1024), 0, st, a.seq, a.B, a.H,
+                              pl.chunk, a.max_seqlen, const_cast<int*>(p.item_start), dev.status);
+        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(decode_partial_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem_bytes<false>()));
         if (e != cudaSuccess) return e;
         if (tm.begin) cudaEventRecord(tm.begin, st);
-        decode_partial_kernel<false><<<grid, Roles<false>::kThreads, smem_bytes<false>(), st>>>(p);
+        e = launch_after_prev(decode_partial_kernel<false>, dim3(grid),
+                              dim3(Roles<false>::kThreads), smem_bytes<false>(), st, p);
         if (tm.end) cudaEventRecord(tm.end, st);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // Every kernel of the call is launched programmatically dependent on the
+    // one before it and waits on the device before touching global memory.
     const int warps = a.B * a.H;
-    decode_merge_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
-        p.part_acc, p.part_ml, a.seq, a.gate, a.out, a.B, a.H, pl.chunk, pl.max_chunks,
-        sparse ? (1 << 30) : a.max_seqlen, sparse ? a.topk : 0);
+    e = launch_after_prev(decode_merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, st,
+                          static_cast<const float*>(p.part_acc), static_cast<const float*>(p.part_ml),
+                          a.seq, a.gate, a.out, a.B, a.H, pl.chunk, pl.max_chunks,
+                          sparse ? (1 << 30) : a.max_seqlen, sparse ? a.topk : 0);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

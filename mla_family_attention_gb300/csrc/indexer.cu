@@ -30,6 +30,8 @@
 // next 11 and the last 10 bits of the k-th key, and a final pass in position
 // order keeps every key above it plus the lowest positions among keys equal
 // to it, writing the output in ascending position order directly.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -134,11 +136,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = p.tile_start[p.B];
-    const int t_begin = int((int64_t(n_tiles) * blockIdx.x) / gridDim.x);
-    const int t_end = int((int64_t(n_tiles) * (blockIdx.x + 1)) / gridDim.x);
 
     if (threadIdx.x == 0) {
+        grid_dep_trigger();
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -154,6 +154,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
     if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&qmap);
+    }
+    // everything above is set-up; the tile list and the cleared histograms
+    // come from the tiles kernel
+    grid_dep_wait();
+    const int n_tiles = p.tile_start[p.B];
+    const int t_begin = int((int64_t(n_tiles) * blockIdx.x) / gridDim.x);
+    const int t_end = int((int64_t(n_tiles) * (blockIdx.x + 1)) / gridDim.x);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -162,8 +172,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&qmap);
             const uint64_t stream_policy = l2_evict_first_policy();
             // Queries are loaded once per sequence into one of two buffers; a
             // buffer is refilled only after the MMAs of the last tile that read
@@ -365,10 +373,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // Tiles per sequence: ceil(T_b/128) when T_b > topk, 0 when every position
 // is kept anyway.  Sequences outside [0, max_seqlen] or past total_keys are
 // reported and get no tiles.
+// Blocks after the first clear the level-1 histograms the scoring pass adds
+// into (B x 2048 counters).
 __global__ void __launch_bounds__(1024) dsa_tiles_kernel(const int64_t* cu, int B, int max_seqlen,
                                                          int64_t total_keys, int topk,
-                                                         int* tile_start, int* status) {
+                                                         int* tile_start, unsigned* hist,
+                                                         int* status) {
     __shared__ int warp_sums[32];
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();
+    if (blockIdx.x > 0) {
+        const size_t n = size_t(B) * kBins;
+        for (size_t i = size_t(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n;
+             i += size_t(gridDim.x - 1) * blockDim.x)
+            hist[i] = 0;
+        return;
+    }
     const int per = (B + blockDim.x - 1) / blockDim.x;
     const int b0 = min(B, int(threadIdx.x) * per), b1 = min(B, b0 + per);
     auto tiles_of = [&](int b) -> int {
@@ -536,10 +556,11 @@ constexpr size_t kTopkSmem = size_t(kStep) * 4 + (kBins + 1024 + kBins + kBins) 
 // Levels 2 and 3 of the radix select histogram the keys that share the prefix
 // found so far; each CTA pushes its partial bins into every CTA's total with
 // remote (distributed shared memory) atomics, so after a cluster barrier all
-// CTAs hold the same totals and find the same bin.  Then each CTA writes its
-// counts of keys above and equal to the k-th key into every CTA, and after a
-// last barrier writes its kept positions at their place in the ascending
-// output.  Four cluster barriers in all.
+// CTAs hold the same totals and find the same bin.  Level 3 runs only when
+// the level-2 bin holds more keys than are still needed.  Then each CTA
+// writes its counts of keys above and equal to the k-th key into every CTA,
+// and after a last barrier writes its kept positions at their place in the
+// ascending output.  Three or four cluster barriers in all.
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
     dsa_topk_cluster_kernel(const TopkParams p) {
     extern __shared__ float4 topk_dyn[];
@@ -555,6 +576,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
     const int b = blockIdx.y;
     const uint32_t rank = cluster_rank();
     const int tid = threadIdx.x;
+    if (tid == 0) grid_dep_trigger();
+    grid_dep_wait();                                // the scores and level-1 bins
     int32_t* oi = p.out_idx + size_t(b) * p.topk;
     float* os = p.out_scores ? p.out_scores + size_t(b) * p.topk : nullptr;
     const int T = seq_len(p, b);                    // the same for the whole cluster
@@ -623,13 +646,24 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
     int bin2, above2;
     find_bin(sum2, kBins, K - above1, sh, &bin2, &above2);
     const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
-    level(0, 1024, pre, sum3);
-    cluster_sync();                                 // (3) level-3 totals everywhere
-    int bin3, above3;
-    find_bin(sum3, 1024, K - above1 - above2, sh, &bin3, &above3);
-    const uint32_t kth = (pre << 10) | uint32_t(bin3);
-    const int need_eq = K - above1 - above2 - above3;
-    const bool all_eq = int(sum3[bin3]) == need_eq;
+    // Keys are compared by their top 32 - kshift bits from here on.  When
+    // every key of the level-2 bin is kept (the usual case: the bin holds
+    // about one key), the 22-bit prefix already separates kept keys from the
+    // rest and level 3 is skipped; the totals are the same in every CTA, so
+    // the whole cluster takes the same branch.
+    uint32_t kth = pre;
+    int kshift = 10;
+    int need_eq = K - above1 - above2;
+    if (int(sum2[bin2]) != need_eq) {
+        level(0, 1024, pre, sum3);
+        cluster_sync();                             // (3) level-3 totals everywhere
+        int bin3, above3;
+        find_bin(sum3, 1024, K - above1 - above2, sh, &bin3, &above3);
+        kth = (pre << 10) | uint32_t(bin3);
+        kshift = 0;
+        need_eq -= above3;
+    }
+    const bool all_eq = int(kshift ? sum2[bin2] : sum3[kth & 1023u]) == need_eq;
 
     // counts of this CTA's range, written into every CTA
     int gt = 0, eq = 0;
@@ -643,7 +677,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u)
             if (i0 + u < hi) {
-                const uint32_t k = okey(vals[u * 1024 + tid]);
+                const uint32_t k = okey(vals[u * 1024 + tid]) >> kshift;
                 gt += k > kth;
                 eq += k == kth;
             }
@@ -675,7 +709,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u)
             if (i0 + u < hi) {
-                const uint32_t k = okey(vals[u * 1024 + tid]);
+                const uint32_t k = okey(vals[u * 1024 + tid]) >> kshift;
                 g |= uint32_t(k > kth) << u;
                 e |= uint32_t(k == kth) << u;
             }
@@ -1079,6 +1113,40 @@ cudaError_t launch_quantize_rows_e4m3(const uint16_t* x, uint8_t* codes, float* 
     return cudaGetLastError();
 }
 
+// Tile list (and cleared level-1 bins), scores, top-k: three kernels, each
+// launched programmatically dependent on the one before it, so it is placed
+// on the SMs its predecessor leaves and does its set-up while that
+// predecessor finishes; every one waits on the device (grid_dep_wait) before
+// it touches global memory.
+template <bool kFp8>
+static cudaError_t launch_score_topk(const IndexArgs& a, const CUtensorMap& kmap,
+                                     const CUtensorMap& qmap, const ScoreParams& p,
+                                     const DeviceInfo& dev, const KernelTimer& tm,
+                                     cudaStream_t st) {
+    const int zero_blocks = int(std::min<int64_t>(1024, (int64_t(a.B) * kBins + 16383) / 16384));
+    cudaError_t e = launch_after_prev(dsa_tiles_kernel, dim3(1 + zero_blocks), dim3(1024), 0, st,
+                                      a.cu, a.B, a.max_seqlen, a.total_keys, a.topk,
+                                      const_cast<int*>(p.tile_start), p.hist, dev.status);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dsa_score_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(ScoreCfg<kFp8>::kSmem));
+    if (e != cudaSuccess) return e;
+    if (tm.begin) cudaEventRecord(tm.begin, st);
+    e = launch_after_prev(dsa_score_kernel<kFp8>, dim3(dev.sms), dim3(kScoreThreads),
+                          ScoreCfg<kFp8>::kSmem, st, kmap, qmap, p);
+    if (tm.end) cudaEventRecord(tm.end, st);
+    if (e != cudaSuccess) return e;
+    TopkParams tp{p.scores, p.hist, a.cu, a.max_seqlen, p.stride, a.topk,
+                  a.total_keys, a.topk_idx, a.topk_scores, dev.status};
+    e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTopkSmem));
+    if (e != cudaSuccess) return e;
+    e = launch_after_prev(dsa_topk_cluster_kernel, dim3(kCluster, a.B), dim3(1024), kTopkSmem, st,
+                          tp);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const DeviceInfo& dev,
                               const Knobs& kn, const KernelTimer& tm, cudaStream_t st) {
     static_assert(ScoreCfg<false>::kSmem <= 227 * 1024 && ScoreCfg<true>::kSmem <= 227 * 1024,
@@ -1096,27 +1164,9 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
                             kIndexDim * 2, 64, kIndexHeads);
     if (e != cudaSuccess) return e;
 
-    e = cudaMemsetAsync(hist, 0, size_t(a.B) * kBins * 4, st);
-    if (e != cudaSuccess) return e;
-    dsa_tiles_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.max_seqlen, a.total_keys, a.topk, tiles,
-                                         dev.status);
-    e = cudaFuncSetAttribute(dsa_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(ScoreCfg<false>::kSmem));
-    if (e != cudaSuccess) return e;
     ScoreParams p{a.w, nullptr, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
                   kn.wait_limit_ns, dev.status};
-    if (tm.begin) cudaEventRecord(tm.begin, st);
-    dsa_score_kernel<false><<<dev.sms, kScoreThreads, ScoreCfg<false>::kSmem, st>>>(kmap, qmap, p);
-    if (tm.end) cudaEventRecord(tm.end, st);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    TopkParams tp{scores, hist, a.cu, a.max_seqlen, score_stride(a.max_seqlen), a.topk,
-                  a.total_keys, a.topk_idx, a.topk_scores, dev.status};
-    e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kTopkSmem));
-    if (e != cudaSuccess) return e;
-    dsa_topk_cluster_kernel<<<dim3(kCluster, a.B), 1024, kTopkSmem, st>>>(tp);
-    return cudaGetLastError();
+    return launch_score_topk<false>(a, kmap, qmap, p, dev, tm, st);
 }
 
 size_t prefill_index_ws(int Tq, int Tk) {
@@ -1175,27 +1225,9 @@ cudaError_t launch_index_topk_fp8(const IndexArgs& a, const IndexFp8Args& f, con
     if (e != cudaSuccess) return e;
     e = encode_tmap_2d_u8(&qmap, q8, 128, uint64_t(qrows), 128, 128, kIndexHeads);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(hist, 0, size_t(a.B) * kBins * 4, st);
-    if (e != cudaSuccess) return e;
-    dsa_tiles_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.max_seqlen, a.total_keys, a.topk, tiles,
-                                         dev.status);
-    e = cudaFuncSetAttribute(dsa_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(ScoreCfg<true>::kSmem));
-    if (e != cudaSuccess) return e;
     ScoreParams p{wq, f.kscale, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
                   kn.wait_limit_ns, dev.status};
-    if (tm.begin) cudaEventRecord(tm.begin, st);
-    dsa_score_kernel<true><<<dev.sms, kScoreThreads, ScoreCfg<true>::kSmem, st>>>(kmap, qmap, p);
-    if (tm.end) cudaEventRecord(tm.end, st);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    TopkParams tp{scores, hist, a.cu, a.max_seqlen, score_stride(a.max_seqlen), a.topk,
-                  a.total_keys, a.topk_idx, a.topk_scores, dev.status};
-    e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kTopkSmem));
-    if (e != cudaSuccess) return e;
-    dsa_topk_cluster_kernel<<<dim3(kCluster, a.B), 1024, kTopkSmem, st>>>(tp);
-    return cudaGetLastError();
+    return launch_score_topk<true>(a, kmap, qmap, p, dev, tm, st);
 }
 
 }  // namespace mla
