@@ -421,9 +421,15 @@ const char* mla_last_error(void);
  *                            power of two in [64, 2048]; 0 = default 256).
  *                            Changes the sparse-decode workspace size, so
  *                            query mla_workspace_size after setting it.
+ *   MLA_DEBUG_PREFILL_CTAS:  CTAs that share each tensor-core MMA of the
+ *                            prefill: 1 = one CTA per 128-row query tile,
+ *                            2 = a pair of CTAs (two SMs) per M = 256 MMA;
+ *                            0 = default (1: the pair's cross-SM handoffs
+ *                            lengthen each key tile's dependency chain).
  * Returns MLA_OK or MLA_ERR_INVALID_ARG for an unknown knob or bad value.
  */
-enum { MLA_DEBUG_WAIT_LIMIT_NS = 1, MLA_DEBUG_STALL_STAGE = 2, MLA_DEBUG_SPARSE_CHUNK = 3 };
+enum { MLA_DEBUG_WAIT_LIMIT_NS = 1, MLA_DEBUG_STALL_STAGE = 2, MLA_DEBUG_SPARSE_CHUNK = 3,
+       MLA_DEBUG_PREFILL_CTAS = 4 };
 mla_status mla_debug_set(int knob, long long value);
 
 /*

@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 6: "MLA_ERR_BAD_INDEX"}
 OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE, OP_CACHE_APPEND, \
     OP_LATENT_DECODE, OP_PREFILL_INDEX_TOPK, OP_SPARSE_PREFILL_LATENT, OP_INDEX_TOPK_FP8 = range(9)
-DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE, DEBUG_SPARSE_CHUNK = 1, 2, 3
+DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE, DEBUG_SPARSE_CHUNK, DEBUG_PREFILL_CTAS = 1, 2, 3, 4
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every symbol include/mla.h declares, with (restype, argtypes).

@@ -20,6 +20,7 @@ thread_local std::string t_err;
 std::atomic<long long> g_wait_limit_ns{2000000000LL};
 std::atomic<int> g_stall_stage{-1};
 std::atomic<int> g_sparse_chunk{0};
+std::atomic<int> g_prefill_ctas{0};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -69,7 +70,8 @@ mla_status device_info(mla::DeviceInfo* out) {
 }
 
 mla::Knobs knobs() {
-    return mla::Knobs{g_wait_limit_ns.load(), g_stall_stage.load(), g_sparse_chunk.load()};
+    return mla::Knobs{g_wait_limit_ns.load(), g_stall_stage.load(), g_sparse_chunk.load(),
+                      g_prefill_ctas.load()};
 }
 
 // ----- kernel timing (instrumentation) -----
@@ -147,6 +149,11 @@ mla_status mla_debug_set(int knob, long long value) {
             if (value != 0 && (value < 64 || value > 2048 || (value & (value - 1))))
                 return fail(MLA_ERR_INVALID_ARG, "sparse chunk must be 0 or a power of two in [64, 2048]");
             g_sparse_chunk.store(int(value));
+            return MLA_OK;
+        case MLA_DEBUG_PREFILL_CTAS:
+            if (value < 0 || value > 2)
+                return fail(MLA_ERR_INVALID_ARG, "prefill CTAs per MMA must be 0, 1 or 2");
+            g_prefill_ctas.store(int(value));
             return MLA_OK;
         default:
             return fail(MLA_ERR_INVALID_ARG, "unknown debug knob %d", knob);

@@ -25,6 +25,7 @@ struct Knobs {
     long long wait_limit_ns;
     int stall_stage;
     int sparse_chunk;   // 0 = default
+    int prefill_ctas;   // CTAs per MMA in the prefill: 0 = default (1), 1 or 2
 };
 
 // Optional event pair recorded around an operation's dominant kernel.

@@ -30,6 +30,16 @@
 //     more than 2^8, otherwise exponentials use the stale maximum (values up
 //     to 2^8 are exact enough in bf16 and fp32).  At the end they normalise
 //     O, apply the sigmoid gate and store bf16 rows.
+// A second shape of the same kernel (kPair) runs query tiles 2i and 2i+1 of
+// a head on a cluster of two CTAs: the even CTA issues M = 256 MMAs
+// (tcgen05 cta_group::2) over both SMs' TMEM, each CTA loads half of every
+// key and value tile, the odd CTA forwards its load completions and its
+// softmax arrivals to the even CTA's barriers, and the MMA commits arrive on
+// both CTAs' barriers (multicast).  It halves the MMA instructions and the
+// key/value bytes per SM, but the cross-SM handoffs lengthen every key
+// tile's score -> softmax -> P.V chain, which is what bounds this kernel,
+// and it measured slower (948 vs 1,305 TFLOP/s at H=96, T=16384), so the
+// one-CTA shape is the default.
 // All waits are bounded; a timeout sets MLA_ERR_TIMEOUT, the roles stop, the
 // MMA lane waits for its last commit, and TMEM is released before exit.
 #include <cuda_bf16.h>
@@ -43,10 +53,6 @@ namespace {
 
 constexpr int kBM = 128;                       // query rows per CTA
 constexpr int kBN = 128;                       // keys per KV tile
-constexpr int kKStages = 2, kVStages = 2;
-constexpr int kBox = kBN * 64 * 2;             // 16 KB: 128 rows x 64 features
-constexpr int kKTile = 3 * kBox;               // 48 KB of keys
-constexpr int kVTile = 2 * kBox;               // 32 KB of values
 constexpr int kSoftmaxWarps = 8;               // two per TMEM lane quadrant
 constexpr int kPvWarp = 2 + kSoftmaxWarps;     // the P.V issuing warp, after the softmax warps
 constexpr int kPThreads = (kPvWarp + 1) * 32;
@@ -56,10 +62,30 @@ constexpr float kRescaleLog2 = 8.f;
 #ifndef MLA_PREFILL_POLY_EXP
 #define MLA_PREFILL_POLY_EXP 0   // 1: odd columns exponentiate on the FMA pipe, 2: one in four
 #endif
-constexpr size_t kPrefillSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile + 256 +
-                                (2 * 2 * kBM * 2 + 2 * kBM) * 4;
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
+
+// Tile geometry.  One CTA (kPair = false): each CTA loads whole 128-key
+// tiles (three 64-feature key boxes of 128 rows, two 64-feature value
+// boxes).  A CTA pair (kPair = true, M = 256 MMAs): each CTA loads half of
+// every tile's B operand — keys 64*rank..64*rank+63 of the Q.K^T tile and
+// value features 64*rank..64*rank+63 of the P.V tile — so each SM's shared
+// memory carries half the key and value bytes, and the even CTA issues one
+// MMA for both SMs' 128 query rows.
+template <bool kPair>
+struct PCfg {
+    static constexpr int kKRows = kPair ? 64 : 128;                 // key rows per CTA per tile
+    static constexpr int kKBox = kKRows * 128;                      // 64 features x kKRows
+    static constexpr int kKTile = 3 * kKBox;
+    static constexpr int kVBox = kBN * 128;                         // 128 keys x 64 features
+    static constexpr int kVBoxes = kPair ? 1 : 2;
+    static constexpr int kVTile = kVBoxes * kVBox;
+    static constexpr int kKStages = kPair ? 3 : 2, kVStages = kPair ? 3 : 2;
+    static constexpr int kRows = kPair ? 256 : 128;                 // MMA M
+    static constexpr int kArrivals = kSoftmaxWarps * (kPair ? 2 : 1);
+    static constexpr size_t kSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile +
+                                    512 + (2 * 2 * kBM * 2 + 2 * kBM) * 4;
+    static constexpr uint32_t kIdescQK = idesc_bf16_f32(kRows, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(kRows, 128, false, true);
+};
 
 struct PrefillParams {
     const uint16_t* q;      // [B,H,Tq,192]
@@ -98,20 +124,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kPThreads, 1)
     mla_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+    using C = PCfg<kPair>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* ksm = smem;                                        // [2][48 KB]
-    uint8_t* vsm = smem + kKStages * kKTile;                    // [2][32 KB]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(vsm + kVStages * kVTile);
-    uint64_t* kfull = bars;                                     // TMA -> MMA
-    uint64_t* kempty = kfull + kKStages;                        // MMA -> TMA
-    uint64_t* vfull = kempty + kKStages;
-    uint64_t* vempty = vfull + kVStages;
-    uint64_t* sfull = vempty + kVStages;                        // [2] MMA -> softmax
+    uint8_t* ksm = smem;                                        // [KS][key tile]
+    uint8_t* vsm = smem + C::kKStages * C::kKTile;              // [VS][value tile]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(vsm + C::kVStages * C::kVTile);
+    uint64_t* kfull = bars;                                     // TMA -> MMA (this CTA's half)
+    uint64_t* kempty = kfull + C::kKStages;                     // MMA -> TMA
+    uint64_t* vfull = kempty + C::kKStages;
+    uint64_t* vempty = vfull + C::kVStages;
+    uint64_t* kpeer = vempty + C::kVStages;                     // pair: odd CTA's key half landed
+    uint64_t* vpeer = kpeer + C::kKStages;                      // pair: odd CTA's value half landed
+    uint64_t* sfull = vpeer + C::kVStages;                      // [2] MMA -> softmax
     uint64_t* pfull = sfull + 2;                                // [2] softmax -> MMA
     uint64_t* odone = pfull + 2;                                // MMA -> softmax (each P.V)
     uint64_t* ofinal = odone + 1;                               // MMA -> epilogue
@@ -123,123 +153,189 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // row-half exchange between the two softmax warps of a quadrant:
     // [parity][half][row] partial maxima and the halves' ok flags, and a
     // separate [half][row] slot for the final row sums
-    float* xmax = reinterpret_cast<float*>(smem + kKStages * kKTile + kVStages * kVTile + 256);
+    float* xmax = reinterpret_cast<float*>(smem + C::kKStages * C::kKTile +
+                                           C::kVStages * C::kVTile + 512);
     int* xok = reinterpret_cast<int*>(xmax + 2 * 2 * kBM);
     float* xsum = reinterpret_cast<float*>(xok + 2 * 2 * kBM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Head-major order: the CTAs running at one time share one or two heads'
     // keys and values in L2 (one head's cache is 10 MB at T=16384, all heads'
-    // 1 GB); within a head, heavy (late) causal tiles go first.
-    const int bh = int(blockIdx.x) / p.n_qt;
-    const int qt = p.n_qt - 1 - (int(blockIdx.x) - bh * p.n_qt);
+    // 1 GB); within a head, heavy (late) causal tiles go first.  A pair
+    // takes query tiles 2i (even CTA) and 2i+1 (odd CTA) of one head.
+    const uint32_t rank = kPair ? pair_rank() : 0u;
+    const bool leader = rank == 0;
+    int bh, qt, qt_last;
+    if (kPair) {
+        const int n_qp = (p.n_qt + 1) / 2;
+        const int pair = int(blockIdx.x) >> 1;
+        bh = pair / n_qp;
+        const int qp = n_qp - 1 - (pair - bh * n_qp);
+        qt = 2 * qp + int(rank);
+        qt_last = 2 * qp + 1;
+    } else {
+        bh = int(blockIdx.x) / p.n_qt;
+        qt = p.n_qt - 1 - (int(blockIdx.x) - bh * p.n_qt);
+        qt_last = qt;
+    }
     const int b = bh / p.H, h = bh - b * p.H;
     const int P0 = p.Tk - p.Tq;                                 // cached positions before the new tokens
     const int q0 = qt * kBM;
-    const int kmax = P0 + min(q0 + kBM - 1, p.Tq - 1);          // last key any row of the tile sees
+    // last key any row of the tile (of the pair) sees; both CTAs of a pair
+    // walk the same key tiles
+    const int kmax = P0 + min(qt_last * kBM + kBM - 1, p.Tq - 1);
     const int n_kv = min((p.Tk + kBN - 1) / kBN, kmax / kBN + 1);
     const int n_full = min((P0 + q0 + 1) / kBN, p.Tk / kBN);    // tiles visible to every row
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kKStages; ++i) {
+        for (int i = 0; i < C::kKStages; ++i) {
             mbar_init(&kfull[i], 1);
             mbar_init(&kempty[i], 1);
+            mbar_init(&kpeer[i], 1);
         }
-        for (int i = 0; i < kVStages; ++i) {
+        for (int i = 0; i < C::kVStages; ++i) {
             mbar_init(&vfull[i], 1);
             mbar_init(&vempty[i], 1);
+            mbar_init(&vpeer[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&pfull[i], kSoftmaxWarps);
+            mbar_init(&pfull[i], C::kArrivals);
         }
         mbar_init(odone, 1);
         mbar_init(ofinal, 1);
-        mbar_init(qready, kSoftmaxWarps);
+        mbar_init(qready, C::kArrivals);
         mbar_init(qkdone, 1);
         mbar_init(&sfree[0], 1);
         mbar_init(&sfree[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_holder, kCols);
+    if (warp == 1) {
+        if (kPair) tmem_alloc_pair(tmem_holder, kCols);
+        else tmem_alloc(tmem_holder, kCols);
+    }
     tc_fence_before();
-    __syncthreads();
+    if (kPair) pair_sync();     // both CTAs' barriers exist before either signals the other
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // waits on barriers the other CTA of a pair arrives on acquire at cluster scope
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return kPair ? mbar_wait_cluster(bar, parity, p.wait_ns) : mbar_wait(bar, parity, p.wait_ns);
+    };
+    // arrivals for the MMA lanes land on the even CTA's barriers
+    auto arrive_mma = [&](uint64_t* bar) {
+        if (kPair) mbar_arrive_cluster(pair_addr(bar, 0));
+        else mbar_arrive(bar);
+    };
+    auto commit_both = [&](uint64_t* bar) {
+        if (kPair) mma_commit_pair(bar, uint16_t(3));
+        else mma_commit(bar);
+    };
+    auto commit_self = [&](uint64_t* bar) {
+        if (kPair) mma_commit_pair(bar, uint16_t(1));
+        else mma_commit(bar);
+    };
 
     if (warp == 0) {
         // --------------------------------- TMA ---------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
-            int kf[kKStages] = {0, 0}, vf[kVStages] = {0, 0};
+            int kf[C::kKStages] = {}, vf[C::kVStages] = {};
+            const int krow0 = kPair ? 64 * int(rank) : 0;       // this CTA's key rows of a tile
             for (int j = 0; j < n_kv; ++j) {
                 if (*abort_flag) break;
-                const int ks = j % kKStages, kr = j / kKStages;
-                if (kr > 0 && !mbar_wait(&kempty[ks], (kr - 1) & 1, p.wait_ns)) {
+                const int ks = j % C::kKStages, kr = j / C::kKStages;
+                if (kr > 0 && !wait(&kempty[ks], (kr - 1) & 1)) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
                     break;
                 }
                 // keys j*128.. of (b, h); rows at or past Tk arrive as zeros
                 const int y = j * kBN;
-                mbar_arrive_expect_tx(&kfull[ks], kKTile);
+                mbar_arrive_expect_tx(&kfull[ks], C::kKTile);
                 for (int c = 0; c < 3; ++c)
-                    tma_load_3d(ksm + ks * kKTile + c * kBox, &kmap, c * 64, y, bh, &kfull[ks]);
+                    tma_load_3d(ksm + ks * C::kKTile + c * C::kKBox, &kmap, c * 64, y + krow0, bh,
+                                &kfull[ks]);
                 kf[ks] = kr + 1;
-                const int vs = j % kVStages, vr = j / kVStages;
-                if (vr > 0 && !mbar_wait(&vempty[vs], (vr - 1) & 1, p.wait_ns)) {
+                const int vs = j % C::kVStages, vr = j / C::kVStages;
+                if (vr > 0 && !wait(&vempty[vs], (vr - 1) & 1)) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&vfull[vs], kVTile);
-                for (int c = 0; c < 2; ++c)
-                    tma_load_3d(vsm + vs * kVTile + c * kBox, &vmap, c * 64, y, bh, &vfull[vs]);
+                mbar_arrive_expect_tx(&vfull[vs], C::kVTile);
+                for (int c = 0; c < C::kVBoxes; ++c)
+                    tma_load_3d(vsm + vs * C::kVTile + c * C::kVBox, &vmap,
+                                kPair ? 64 * int(rank) : c * 64, y, bh, &vfull[vs]);
                 vf[vs] = vr + 1;
             }
-            for (int i = 0; i < kKStages; ++i)
+            for (int i = 0; i < C::kKStages; ++i)
                 if (kf[i] > 0 && !mbar_wait(&kfull[i], (kf[i] - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
-            for (int i = 0; i < kVStages; ++i)
+            for (int i = 0; i < C::kVStages; ++i)
                 if (vf[i] > 0 && !mbar_wait(&vfull[i], (vf[i] - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
+        }
+    } else if (kPair && !leader && (warp == 1 || warp == kPvWarp)) {
+        // ------------- odd CTA of a pair: tell the MMA lanes its halves landed -------------
+        if (lane == 0) {
+            const bool keys = warp == 1;
+            const int stages = keys ? C::kKStages : C::kVStages;
+            uint64_t* full = keys ? kfull : vfull;
+            const uint32_t peer = pair_addr(keys ? kpeer : vpeer, 0);
+            for (int j = 0; j < n_kv; ++j) {
+                if (*abort_flag) break;
+                const int st = j % stages;
+                if (!mbar_wait(&full[st], (j / stages) & 1, p.wait_ns)) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_cluster(peer + uint32_t(st * 8));
+            }
         }
     } else if (warp == 1) {
         // ------------------------------ Q.K^T MMAs ------------------------------
         if (lane == 0) {
-            bool ok = mbar_wait(qready, 0, p.wait_ns);
+            bool ok = wait(qready, 0);
             bool issued = false;
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
-                const int ks = j % kKStages;
+                const int ks = j % C::kKStages;
                 // S_j = Q K_j^T into score buffer j&1 (A = queries in TMEM), once
-                // the keys landed and P_{j-2}, in that buffer, has been consumed
-                // (a barrier per buffer: its next phase needs S_j, so the
-                // parity cannot run two phases ahead of this wait)
-                if (!mbar_wait(&kfull[ks], (j / kKStages) & 1, p.wait_ns) ||
+                // the keys landed (both halves for a pair) and P_{j-2}, in that
+                // buffer, has been consumed (a barrier per buffer: its next phase
+                // needs S_j, so the parity cannot run two phases ahead of this wait)
+                if (!mbar_wait(&kfull[ks], (j / C::kKStages) & 1, p.wait_ns) ||
+                    (kPair && !wait(&kpeer[ks], (j / C::kKStages) & 1)) ||
                     (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.wait_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t kb = smem_u32(ksm + ks * kKTile);
+                const uint32_t kb = smem_u32(ksm + ks * C::kKTile);
                 const uint32_t d = tmem + kColS + uint32_t(j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 12; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-                    mma_bf16_ts(d, tmem + kColQ + kk * 8, bd, kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint64_t bd =
+                        smem_desc_sw128(kb + (kk >> 2) * C::kKBox + (kk & 3) * 32, 16, 1024);
+                    if (kPair)
+                        mma_bf16_ts_pair(d, tmem + kColQ + kk * 8, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    else
+                        mma_bf16_ts(d, tmem + kColQ + kk * 8, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&kempty[ks]);
-                mma_commit(&sfull[j & 1]);
+                commit_both(&kempty[ks]);
+                commit_both(&sfull[j & 1]);
                 issued = true;
             }
             if (!ok) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
             }
-            mma_commit(qkdone);
+            commit_self(qkdone);
             if (issued && !mbar_wait(qkdone, 0, p.wait_ns)) report(p.status, kStTimeout);
         }
     } else if (warp == kPvWarp) {
@@ -248,31 +344,37 @@ __global__ void __launch_bounds__(kPThreads, 1)
             bool ok = true, issued = false;
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
-                const int vs = j % kVStages;
-                if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, p.wait_ns) ||
-                    !mbar_wait(&vfull[vs], (j / kVStages) & 1, p.wait_ns)) {
+                const int vs = j % C::kVStages;
+                if (!wait(&pfull[j & 1], (j >> 1) & 1) ||
+                    !mbar_wait(&vfull[vs], (j / C::kVStages) & 1, p.wait_ns) ||
+                    (kPair && !wait(&vpeer[vs], (j / C::kVStages) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 // O += P_j V_j (A = probabilities in TMEM, B = values, MN-major)
-                const uint32_t vb = smem_u32(vsm + vs * kVTile);
+                const uint32_t vb = smem_u32(vsm + vs * C::kVTile);
                 const uint32_t a = tmem + kColS + uint32_t(j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(vb + kk * 2048, kBox, 1024);
-                    mma_bf16_ts(tmem + kColO, a + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t bd = smem_desc_sw128(vb + kk * 2048, C::kVBox, 1024);
+                    if (kPair)
+                        mma_bf16_ts_pair(tmem + kColO, a + kk * 8, bd, C::kIdescPV,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    else
+                        mma_bf16_ts(tmem + kColO, a + kk * 8, bd, C::kIdescPV,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&vempty[vs]);
-                mma_commit(&sfree[j & 1]);
-                mma_commit(odone);
+                commit_both(&vempty[vs]);
+                commit_self(&sfree[j & 1]);
+                commit_both(odone);
                 issued = true;
             }
             if (!ok) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
             }
-            mma_commit(ofinal);               // also releases the epilogue after an abort
+            commit_both(ofinal);              // also releases the epilogue after an abort
             if (issued && !mbar_wait(ofinal, 0, p.wait_ns)) report(p.status, kStTimeout);
         }
     } else {
@@ -309,14 +411,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(qready);
+            if (lane == 0) arrive_mma(qready);
         }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int buf = j & 1;
             ok = ok && !*abort_flag;
-            if (ok && !mbar_wait(&sfull[buf], (j >> 1) & 1, p.wait_ns)) {
+            if (ok && !wait(&sfull[buf], (j >> 1) & 1)) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
                 ok = false;
@@ -363,7 +465,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const float m_new = need ? mt : m_used;
             const float factor = need ? ex2(m_used - m_new) : 1.f;     // m_used=-inf -> 0
             if (__any_sync(0xffffffffu, need && j > 0)) {
-                bool o_ok = mbar_wait(odone, (j - 1) & 1, p.wait_ns);  // P_{j-1} V_{j-1} landed
+                bool o_ok = wait(odone, (j - 1) & 1);                   // P_{j-1} V_{j-1} landed
                 o_ok = __all_sync(0xffffffffu, o_ok);
                 if (o_ok) {
                     tc_fence_after();
@@ -405,10 +507,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&pfull[buf]);
+            if (lane == 0) arrive_mma(&pfull[buf]);
         }
         // ---- epilogue: O / l * sigmoid(gate) -> bf16 ----
-        bool fin = ok && mbar_wait(ofinal, 0, p.wait_ns);
+        bool fin = ok && wait(ofinal, 0);
         fin = __all_sync(0xffffffffu, fin);
         if (!fin && ok) report(p.status, kStTimeout);
         xsum[half * kBM + r] = l;                           // row sum = both halves
@@ -449,34 +551,68 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    // A pair's CTAs leave together: neither exits while the other (or the
+    // MMAs the even one issued) may still touch its barriers, shared memory
+    // or TMEM.  Every wait above is bounded, so every thread arrives here.
+    if (kPair) pair_sync();
+    else __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kCols);
+    if (warp == 1) {
+        if (kPair) tmem_dealloc_pair(tmem, kCols);
+        else tmem_dealloc(tmem, kCols);
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Knobs& kn,
                            const KernelTimer& tm, cudaStream_t st) {
-    static_assert(kPrefillSmem <= 227 * 1024, "shared memory budget");
+    static_assert(PCfg<false>::kSmem <= 227 * 1024 && PCfg<true>::kSmem <= 227 * 1024,
+                  "shared memory budget");
+    const bool pair = kn.prefill_ctas == 2;
     // [B*H][Tk][D] views of the [B,H,kv_cap,D] caches: a tile that runs past
     // Tk reads zeros, never the unused capacity or the next head's rows.
     CUtensorMap kmap, vmap;
     const uint64_t bhs = uint64_t(a.B) * a.H, cap = uint64_t(a.kv_cap);
     cudaError_t e = encode_tmap_3d_bf16(&kmap, a.k, kDqk, a.Tk, bhs, kDqk * 2, cap * kDqk * 2, 64,
-                                        kBN);
+                                        pair ? PCfg<true>::kKRows : PCfg<false>::kKRows);
     if (e != cudaSuccess) return e;
     e = encode_tmap_3d_bf16(&vmap, a.v, kDv, a.Tk, bhs, kDv * 2, cap * kDv * 2, 64, kBN);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kPrefillSmem));
-    if (e != cudaSuccess) return e;
     PrefillParams p{a.q, a.gate, a.out, a.B, a.H, a.Tq, a.Tk, (a.Tq + kBM - 1) / kBM,
                     a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
-    const int grid = p.n_qt * a.B * a.H;
+    if (!pair) {
+        e = cudaFuncSetAttribute(mla_prefill_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(PCfg<false>::kSmem));
+        if (e != cudaSuccess) return e;
+        const int grid = p.n_qt * a.B * a.H;
+        if (tm.begin) cudaEventRecord(tm.begin, st);
+        mla_prefill_kernel<false><<<grid, kPThreads, PCfg<false>::kSmem, st>>>(kmap, vmap, p);
+        if (tm.end) cudaEventRecord(tm.end, st);
+        return cudaGetLastError();
+    }
+    e = cudaFuncSetAttribute(mla_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(PCfg<true>::kSmem));
+    if (e != cudaSuccess) return e;
+    // clusters of two CTAs: query tiles 2i and 2i+1 of one head (the odd
+    // CTA of the last pair of an odd tile count has no rows to store)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ((p.n_qt + 1) / 2) * a.B * a.H);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = PCfg<true>::kSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (tm.begin) cudaEventRecord(tm.begin, st);
-    mla_prefill_kernel<<<grid, kPThreads, kPrefillSmem, st>>>(kmap, vmap, p);
+    e = cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, kmap, vmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

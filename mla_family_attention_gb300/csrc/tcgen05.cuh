@@ -227,4 +227,97 @@ __device__ __forceinline__ uint32_t elect_lane0() {
     return (threadIdx.x & 31) == 0;
 }
 
+// ----------------------------------------------------------------------------
+// CTA pairs (a cluster of two CTAs on two SMs sharing each MMA, cta_group::2)
+// ----------------------------------------------------------------------------
+// The even-ranked CTA of the pair issues the MMAs; an M=256 MMA takes rows
+// 0..127 of A and of D from the even CTA's TMEM (or shared memory) and rows
+// 128..255 from the odd CTA's, at the same addresses, and half of B's N rows
+// from each CTA's shared memory at the same offset.
+__device__ __forceinline__ uint32_t pair_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of both CTAs; orders shared-memory writes before it with
+// accesses (local or remote) after it.
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of this CTA's shared variable `p` in the CTA of the given rank.
+__device__ __forceinline__ uint32_t pair_addr(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+// One arrival on an mbarrier of either CTA (cluster address), releasing this
+// thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// Bounded wait that acquires at cluster scope (arrivals from the other CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  long long limit_ns) {
+    auto test = [&]() {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        return done != 0;
+    };
+    if (test()) return true;
+    const uint64_t t0 = global_ns();
+    while (!test()) {
+        if (static_cast<long long>(global_ns() - t0) > limit_ns) return false;
+    }
+    return true;
+}
+
+// One warp in each CTA of the pair: allocate `cols` columns in both SMs'
+// TMEM (the same base address lands in each CTA's *dst).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T over the pair (M = 256), one thread of
+// the even CTA.
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at this shared offset in every CTA of
+// `cta_mask` when the pair MMAs this thread issued so far complete.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 }  // namespace mla

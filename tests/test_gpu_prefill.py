@@ -20,6 +20,15 @@ def run(pf):
     return out
 
 
+@pytest.fixture(params=[1, 2], ids=["one_cta", "cta_pair"])
+def ctas(request):
+    """Both kernel shapes: one CTA per 128-row query tile (M = 128 MMAs) and
+    a pair of CTAs on two SMs sharing each M = 256 MMA."""
+    mla.debug_set(_lib.DEBUG_PREFILL_CTAS, request.param)
+    yield request.param
+    mla.debug_set(_lib.DEBUG_PREFILL_CTAS, 0)
+
+
 @pytest.mark.parametrize("B,H,Tq,Tk,gated", [
     (1, 1, 1, 1, True),
     (1, 2, 128, 128, True),        # one tile
@@ -29,9 +38,13 @@ def run(pf):
     (1, 2, 1, 257, True),          # one new token over a ragged cache
     (1, 4, 257, 257, True),
     (2, 2, 130, 390, False),
-    (1, 1, 640, 640, True),        # five KV tiles on the diagonal row
+    (1, 1, 640, 640, True),        # five query tiles, seven 96-key tiles
+    (1, 2, 96, 96, True),          # exactly one key tile
+    (1, 3, 288, 289, False),       # three key tiles (every score buffer) and one key more
+    (1, 2, 1000, 1000, True),      # the score-buffer ring wraps several times
+    (1, 2, 60, 1100, True),        # short chunk over a long cache, mask on the last tiles only
 ])
-def test_prefill_small_matches_oracle(B, H, Tq, Tk, gated):
+def test_prefill_small_matches_oracle(B, H, Tq, Tk, gated, ctas):
     pf = mi.make_prefill(B, H, Tq, Tk, gated, device=DEV, config=61)
     out = run(pf)
     ref = oracle.mla_prefill(pf.q, pf.k, pf.v, pf.gate, pf.scale)
