@@ -46,7 +46,9 @@ constexpr int kDenseSP = 64;                    // positions per dense pipeline 
 #ifndef MLA_SPARSE_STAGE_POS
 #define MLA_SPARSE_STAGE_POS 64                 // positions per sparse pipeline stage
 #endif
-constexpr int kConsumerWarps = 8;
+#ifndef MLA_SPARSE_CONSUMER_WARPS
+#define MLA_SPARSE_CONSUMER_WARPS 8             // consumer warps of the sparse decode
+#endif
 // Dense decode: one producer warp (bulk copies).  Sparse decode: four
 // producer warps (16-byte cp.async gathers), completing on the same barrier.
 // Dense decode: four stages of 64 streamed positions (160 KB).  Sparse
@@ -55,28 +57,31 @@ constexpr int kConsumerWarps = 8;
 template <bool kSparse>
 struct Roles {
     static constexpr int kProducerWarps = kSparse ? 4 : 1;
+    static constexpr int kConsumerWarps = kSparse ? MLA_SPARSE_CONSUMER_WARPS : 8;
+    static constexpr int kGroups = kConsumerWarps * 4;       // 8-lane groups
     static constexpr int kThreads = 32 * (kProducerWarps + kConsumerWarps);
     static constexpr int kFullArrivals = kSparse ? 32 * kProducerWarps : 1;
     static constexpr int kSP = kSparse ? MLA_SPARSE_STAGE_POS : kDenseSP;
     static constexpr int kStages = kSparse ? (200 * 1024) / (kSP * (kDqk + kDv) * 2) : 4;
     static constexpr int kKStage = kSP * kDqk * 2;
     static constexpr int kVStage = kSP * kDv * 2;
-    static constexpr int kPPG = kSP / (kConsumerWarps * 4);    // positions per group per stage
+    static constexpr int kPPG = kSP / kGroups;                // positions per group per stage
+    static constexpr int kMergeFloats = kConsumerWarps * (kDv + 2);
 };
-constexpr int kGroups = kConsumerWarps * 4;     // 8-lane groups
 
-constexpr int kMergeFloats = kConsumerWarps * (kDv + 2);
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <bool kSparse>
 constexpr size_t smem_bytes() {
-    return size_t(Roles<kSparse>::kStages) * (Roles<kSparse>::kKStage + Roles<kSparse>::kVStage + kKRow) +
-           kMergeFloats * 4 + 2 * Roles<kSparse>::kStages * 8 + 16;
+    using R = Roles<kSparse>;
+    return size_t(R::kStages) * (R::kKStage + R::kVStage + kKRow) + R::kMergeFloats * 4 +
+           2 * R::kStages * 8 + 16;
 }
 
-static_assert(Roles<true>::kPPG * kGroups == Roles<true>::kSP &&
-                  Roles<false>::kPPG * kGroups == Roles<false>::kSP,
-              "stage must split evenly over groups");
+static_assert(Roles<true>::kPPG * Roles<true>::kGroups == Roles<true>::kSP &&
+                  Roles<false>::kPPG * Roles<false>::kGroups == Roles<false>::kSP &&
+                  Roles<true>::kConsumerWarps >= 4,
+              "stage must split evenly over groups; the merge takes four warps");
 
 struct Params {
     const uint16_t* q;
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
     uint8_t* qs = vs + R::kStages * R::kVStage;                // [stages][384]: query row of
                                                                // the item a stage starts
     float* red = reinterpret_cast<float*>(qs + R::kStages * kKRow);   // [8][130]
-    uint64_t* full = reinterpret_cast<uint64_t*>(red + kMergeFloats);
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + R::kMergeFloats);
     uint64_t* empty = full + R::kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + R::kStages);
 
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < R::kStages; ++s) {
             mbar_init(&full[s], R::kFullArrivals);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], R::kConsumerWarps);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
             bool ok[R::kPPG];
 #pragma unroll
             for (int r = 0; r < R::kPPG; ++r) {
-                const int pos = g + kGroups * r;
+                const int pos = g + R::kGroups * r;
                 ok[r] = pos < n;
                 if (kSparse && ok[r])
                     ok[r] = valid_pos(p.idx[int64_t(w.b) * p.topk + e + pos], w.T);
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 float s[R::kPPG];
 #pragma unroll
                 for (int r = 0; r < R::kPPG; ++r) {
-                    const int pos = g + kGroups * r;
+                    const int pos = g + R::kGroups * r;
                     float dot = 0.f;
                     if (ok[r]) {
                         const uint8_t* kr = kst + pos * kKRow;
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                         if (ok[r]) {
                             const float pr = ex2(s[r] - mn);
                             l += pr;
-                            const uint8_t* vr = vst + (g + kGroups * r) * kVRow;
+                            const uint8_t* vr = vst + (g + R::kGroups * r) * kVRow;
 #pragma unroll
                             for (int c = 0; c < 2; ++c) {
                                 const uint4 u =
@@ -436,17 +441,17 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
             rw[kDv] = m;
             rw[kDv + 1] = l;
         }
-        named_bar_sync(1, 32 * kConsumerWarps);
+        named_bar_sync(1, 32 * R::kConsumerWarps);
         const bool aborted = *abort_flag != 0;
         if (cw < 4 && !aborted) {
             const int d = cw * 32 + lane;     // one feature per thread
             float mx = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < kConsumerWarps; ++u) mx = fmaxf(mx, red[u * (kDv + 2) + kDv]);
+            for (int u = 0; u < R::kConsumerWarps; ++u) mx = fmaxf(mx, red[u * (kDv + 2) + kDv]);
             float a = 0.f, ls = 0.f;
             if (mx != -INFINITY) {
 #pragma unroll
-                for (int u = 0; u < kConsumerWarps; ++u) {
+                for (int u = 0; u < R::kConsumerWarps; ++u) {
                     const float wgt = ex2(red[u * (kDv + 2) + kDv] - mx);
                     a += wgt * red[u * (kDv + 2) + d];
                     ls += wgt * red[u * (kDv + 2) + kDv + 1];
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 p.part_ml[slotid * 2 + 1] = ls;
             }
         }
-        named_bar_sync(1, 32 * kConsumerWarps);
+        named_bar_sync(1, 32 * R::kConsumerWarps);
     }
 }
 
