@@ -8,19 +8,21 @@
 //
 // Design (one CTA per 128-row query tile of one (b, h); CTAs ordered head by
 // head so concurrent CTAs share K/V in L2, heavy causal tiles first):
-//   * TMEM (512 columns): the query tile (192 bf16 features = 96 columns),
-//     two 128-column score buffers S0/S1, and the 128-column output O.  The
-//     softmax writes P (bf16) back over the first 64 columns of its score
-//     buffer, so both products read their A operand from TMEM: shared
-//     memory only carries K and V, whose bandwidth is the binding limit for
-//     192-feature keys.
-//   * warp 0: TMA producer for a 2-stage key ring (three 64-feature boxes of
-//     128 keys, 128-byte swizzle) and a 2-stage value ring;
+//   * TMEM (512 columns): three 128-column score buffers S0/S1/S2 and the
+//     128-column output O.  The softmax writes P (bf16) back over the first
+//     64 columns of its score buffer, so P.V reads its A operand from TMEM.
+//     The query tile (192 features, 48 KB) stays in shared memory for the
+//     whole CTA as Q.K^T's A operand; keeping it in TMEM instead (96
+//     columns) left room for only two score buffers and measured 2-3 %
+//     slower.
+//   * warp 0: TMA producer for the query tile, a 2-stage key ring (three
+//     64-feature boxes of 128 keys, 128-byte swizzle) and a 2-stage value
+//     ring;
 //   * warp 1: owns TMEM; one lane issues S_j = Q K_j^T; warp 10: one lane
 //     issues O += P_j V_j.  tcgen05.mma blocks the issuing thread until the
 //     pipe accepts it, so with two issuing threads one's barrier waits and
 //     commits overlap the other's MMAs; the next scores are computed while
-//     the softmax of the current tile runs.  S_{j+2} reuses the buffer whose
+//     the softmax of the current tile runs.  S_{j+3} reuses the buffer whose
 //     P_j the P.V of tile j reads, so it waits for that P.V to complete;
 //   * warps 2-9: two threads per query row, each owning 64 of the tile's 128
 //     key columns (and 64 of the 128 output features).  They load their half
@@ -57,7 +59,10 @@ constexpr int kSoftmaxWarps = 8;               // two per TMEM lane quadrant
 constexpr int kPvWarp = 2 + kSoftmaxWarps;     // the P.V issuing warp, after the softmax warps
 constexpr int kPThreads = (kPvWarp + 1) * 32;
 constexpr uint32_t kCols = 512;
-constexpr uint32_t kColQ = 0, kColS = 128, kColO = 384;
+constexpr int kNB = 3;                        // score buffers
+constexpr uint32_t kColS = 0, kColO = 384;     // S_i at kColS + 128 i
+constexpr int kQBox = kBM * 128;               // 128 query rows x 64 features
+constexpr int kQTile = 3 * kQBox;              // the query tile, 48 KB
 constexpr float kRescaleLog2 = 8.f;
 #ifndef MLA_PREFILL_POLY_EXP
 #define MLA_PREFILL_POLY_EXP 0   // 1: odd columns exponentiate on the FMA pipe, 2: one in four
@@ -82,7 +87,7 @@ struct PCfg {
     static constexpr int kRows = kPair ? 256 : 128;                 // MMA M
     static constexpr int kArrivals = kSoftmaxWarps * (kPair ? 2 : 1);
     static constexpr size_t kSmem = 1024 + size_t(kKStages) * kKTile + size_t(kVStages) * kVTile +
-                                    512 + (2 * 2 * kBM * 2 + 2 * kBM) * 4;
+                                    kQTile + 512 + (2 * 2 * kBM * 2 + 2 * kBM) * 4;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(kRows, 128, false, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(kRows, 128, false, true);
 };
@@ -127,34 +132,37 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <bool kPair>
 __global__ void __launch_bounds__(kPThreads, 1)
     mla_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                       const __grid_constant__ CUtensorMap vmap,
+                       const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
     using C = PCfg<kPair>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ksm = smem;                                        // [KS][key tile]
     uint8_t* vsm = smem + C::kKStages * C::kKTile;              // [VS][value tile]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(vsm + C::kVStages * C::kVTile);
+    uint8_t* qsm = vsm + C::kVStages * C::kVTile;               // [3][16 KB] query tile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + kQTile);
     uint64_t* kfull = bars;                                     // TMA -> MMA (this CTA's half)
     uint64_t* kempty = kfull + C::kKStages;                     // MMA -> TMA
     uint64_t* vfull = kempty + C::kKStages;
     uint64_t* vempty = vfull + C::kVStages;
     uint64_t* kpeer = vempty + C::kVStages;                     // pair: odd CTA's key half landed
     uint64_t* vpeer = kpeer + C::kKStages;                      // pair: odd CTA's value half landed
-    uint64_t* sfull = vpeer + C::kVStages;                      // [2] MMA -> softmax
-    uint64_t* pfull = sfull + 2;                                // [2] softmax -> MMA
-    uint64_t* odone = pfull + 2;                                // MMA -> softmax (each P.V)
+    uint64_t* sfull = vpeer + C::kVStages;                      // [3] MMA -> softmax
+    uint64_t* pfull = sfull + kNB;                              // [3] softmax -> MMA
+    uint64_t* odone = pfull + kNB;                              // MMA -> softmax (each P.V)
     uint64_t* ofinal = odone + 1;                               // MMA -> epilogue
-    uint64_t* qready = ofinal + 1;                              // softmax -> MMA
-    uint64_t* qkdone = qready + 1;                              // Q.K^T lane's drain
-    uint64_t* sfree = qkdone + 1;                               // [2] P.V -> Q.K^T (buffer's P read)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sfree + 2);
+    uint64_t* qready = ofinal + 1;                              // TMA -> MMA (this CTA's queries)
+    uint64_t* qpeer = qready + 1;                               // pair: odd CTA's queries landed
+    uint64_t* qkdone = qpeer + 1;                               // Q.K^T lane's drain
+    uint64_t* sfree = qkdone + 1;                               // [3] P.V -> Q.K^T (buffer's P read)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sfree + kNB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     // row-half exchange between the two softmax warps of a quadrant:
     // [parity][half][row] partial maxima and the halves' ok flags, and a
     // separate [half][row] slot for the final row sums
     float* xmax = reinterpret_cast<float*>(smem + C::kKStages * C::kKTile +
-                                           C::kVStages * C::kVTile + 512);
+                                           C::kVStages * C::kVTile + kQTile + 512);
     int* xok = reinterpret_cast<int*>(xmax + 2 * 2 * kBM);
     float* xsum = reinterpret_cast<float*>(xok + 2 * 2 * kBM);
 
@@ -198,16 +206,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(&vempty[i], 1);
             mbar_init(&vpeer[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNB; ++i) {
             mbar_init(&sfull[i], 1);
             mbar_init(&pfull[i], C::kArrivals);
+            mbar_init(&sfree[i], 1);
         }
         mbar_init(odone, 1);
         mbar_init(ofinal, 1);
-        mbar_init(qready, C::kArrivals);
+        mbar_init(qready, 1);
+        mbar_init(qpeer, 1);
         mbar_init(qkdone, 1);
-        mbar_init(&sfree[0], 1);
-        mbar_init(&sfree[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -243,8 +251,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
+            tma_prefetch_desc(&qmap);
             int kf[C::kKStages] = {}, vf[C::kVStages] = {};
             const int krow0 = kPair ? 64 * int(rank) : 0;       // this CTA's key rows of a tile
+            // this CTA's 128 query rows (rows at or past Tq arrive as zeros)
+            mbar_arrive_expect_tx(qready, kQTile);
+            for (int c = 0; c < 3; ++c)
+                tma_load_3d(qsm + c * kQBox, &qmap, c * 64, q0, bh, qready);
             for (int j = 0; j < n_kv; ++j) {
                 if (*abort_flag) break;
                 const int ks = j % C::kKStages, kr = j / C::kKStages;
@@ -278,6 +291,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int i = 0; i < C::kVStages; ++i)
                 if (vf[i] > 0 && !mbar_wait(&vfull[i], (vf[i] - 1) & 1, p.wait_ns))
                     report(p.status, kStTimeout);
+            if (!mbar_wait(qready, 0, p.wait_ns)) report(p.status, kStTimeout);
         }
     } else if (kPair && !leader && (warp == 1 || warp == kPvWarp)) {
         // ------------- odd CTA of a pair: tell the MMA lanes its halves landed -------------
@@ -286,6 +300,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int stages = keys ? C::kKStages : C::kVStages;
             uint64_t* full = keys ? kfull : vfull;
             const uint32_t peer = pair_addr(keys ? kpeer : vpeer, 0);
+            if (keys) {                                     // the query tile first
+                if (mbar_wait(qready, 0, p.wait_ns)) {
+                    mbar_arrive_cluster(pair_addr(qpeer, 0));
+                } else {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                }
+            }
             for (int j = 0; j < n_kv; ++j) {
                 if (*abort_flag) break;
                 const int st = j % stages;
@@ -300,35 +322,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ Q.K^T MMAs ------------------------------
         if (lane == 0) {
-            bool ok = wait(qready, 0);
+            bool ok = mbar_wait(qready, 0, p.wait_ns) && (!kPair || wait(qpeer, 0));
             bool issued = false;
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
                 const int ks = j % C::kKStages;
-                // S_j = Q K_j^T into score buffer j&1 (A = queries in TMEM), once
-                // the keys landed (both halves for a pair) and P_{j-2}, in that
-                // buffer, has been consumed (a barrier per buffer: its next phase
-                // needs S_j, so the parity cannot run two phases ahead of this wait)
+                // S_j = Q K_j^T into score buffer j%3 (A = queries in shared
+                // memory), once the keys landed (both halves for a pair) and
+                // P_{j-3}, in that buffer, has been consumed (a barrier per
+                // buffer: its next phase needs S_j, so the parity cannot run
+                // two phases ahead of this wait)
+                const int sb = j % kNB;
                 if (!mbar_wait(&kfull[ks], (j / C::kKStages) & 1, p.wait_ns) ||
                     (kPair && !wait(&kpeer[ks], (j / C::kKStages) & 1)) ||
-                    (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.wait_ns))) {
+                    (j >= kNB && !mbar_wait(&sfree[sb], ((j - kNB) / kNB) & 1, p.wait_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t kb = smem_u32(ksm + ks * C::kKTile);
-                const uint32_t d = tmem + kColS + uint32_t(j & 1) * 128;
+                const uint32_t qb = smem_u32(qsm);
+                const uint32_t d = tmem + kColS + uint32_t(sb) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 12; ++kk) {
+                    const uint64_t ad =
+                        smem_desc_sw128(qb + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd =
                         smem_desc_sw128(kb + (kk >> 2) * C::kKBox + (kk & 3) * 32, 16, 1024);
                     if (kPair)
-                        mma_bf16_ts_pair(d, tmem + kColQ + kk * 8, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                        mma_bf16_ss_pair(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
                     else
-                        mma_bf16_ts(d, tmem + kColQ + kk * 8, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                        mma_bf16_ss(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 commit_both(&kempty[ks]);
-                commit_both(&sfull[j & 1]);
+                commit_both(&sfull[sb]);
                 issued = true;
             }
             if (!ok) {
@@ -345,7 +372,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
                 const int vs = j % C::kVStages;
-                if (!wait(&pfull[j & 1], (j >> 1) & 1) ||
+                const int sb = j % kNB;
+                if (!wait(&pfull[sb], (j / kNB) & 1) ||
                     !mbar_wait(&vfull[vs], (j / C::kVStages) & 1, p.wait_ns) ||
                     (kPair && !wait(&vpeer[vs], (j / C::kVStages) & 1))) {
                     ok = false;
@@ -354,7 +382,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc_fence_after();
                 // O += P_j V_j (A = probabilities in TMEM, B = values, MN-major)
                 const uint32_t vb = smem_u32(vsm + vs * C::kVTile);
-                const uint32_t a = tmem + kColS + uint32_t(j & 1) * 128;
+                const uint32_t a = tmem + kColS + uint32_t(sb) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bd = smem_desc_sw128(vb + kk * 2048, C::kVBox, 1024);
@@ -366,7 +394,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                     (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 commit_both(&vempty[vs]);
-                commit_self(&sfree[j & 1]);
+                commit_self(&sfree[sb]);
                 commit_both(odone);
                 issued = true;
             }
@@ -391,34 +419,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int row = q0 + r;                             // query index
         const int qa = P0 + row;                            // absolute position
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
-        // queries of this row, features 96*half..96*half+95 -> TMEM columns 48*half..
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.q + ((size_t(bh) * p.Tq + size_t(row < p.Tq ? row : 0)) * kDqk)) + half * 12;
-            uint32_t w[16];
-#pragma unroll
-            for (int c = 0; c < 3; ++c) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint4 x = row < p.Tq ? __ldg(src + c * 4 + u) : make_uint4(0, 0, 0, 0);
-                    w[4 * u] = x.x;
-                    w[4 * u + 1] = x.y;
-                    w[4 * u + 2] = x.z;
-                    w[4 * u + 3] = x.w;
-                }
-                tmem_st16(tmem + lane_off + kColQ + half * 48 + c * 16, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) arrive_mma(qready);
-        }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            const int buf = j & 1;
+            const int buf = j % kNB;
+            const int par = j & 1;                          // row-half exchange slot
             ok = ok && !*abort_flag;
-            if (ok && !wait(&sfull[buf], (j >> 1) & 1)) {
+            if (ok && !wait(&sfull[buf], (j / kNB) & 1)) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
                 ok = false;
@@ -453,11 +460,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             }
             // swap with the other half of the row (double-buffered by tile parity)
-            xmax[(buf * 2 + half) * kBM + r] = mloc;
-            xok[(buf * 2 + half) * kBM + r] = ok;
+            xmax[(par * 2 + half) * kBM + r] = mloc;
+            xok[(par * 2 + half) * kBM + r] = ok;
             named_bar_sync(bar_id, 64);
-            const float mo = xmax[(buf * 2 + (half ^ 1)) * kBM + r];
-            ok = __all_sync(0xffffffffu, ok && xok[(buf * 2 + (half ^ 1)) * kBM + r] != 0);
+            const float mo = xmax[(par * 2 + (half ^ 1)) * kBM + r];
+            ok = __all_sync(0xffffffffu, ok && xok[(par * 2 + (half ^ 1)) * kBM + r] != 0);
             if (!ok) break;                                  // both warps of the pair
             const float mt = fmaxf(mloc, mo) * p.scale_log2; // scale > 0 keeps the order
             // lazy rescale: only when the row maximum grows by more than 2^8
@@ -579,6 +586,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Kn
     if (e != cudaSuccess) return e;
     e = encode_tmap_3d_bf16(&vmap, a.v, kDv, a.Tk, bhs, kDv * 2, cap * kDv * 2, 64, kBN);
     if (e != cudaSuccess) return e;
+    // [B*H][Tq][192] view of the queries: rows past Tq read as zeros
+    CUtensorMap qmap;
+    e = encode_tmap_3d_bf16(&qmap, a.q, kDqk, a.Tq, bhs, kDqk * 2, uint64_t(a.Tq) * kDqk * 2, 64,
+                            kBM);
+    if (e != cudaSuccess) return e;
     PrefillParams p{a.q, a.gate, a.out, a.B, a.H, a.Tq, a.Tk, (a.Tq + kBM - 1) / kBM,
                     a.scale * 1.4426950408889634f, kn.wait_limit_ns, dev.status};
     if (!pair) {
@@ -588,7 +600,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Kn
         if (e != cudaSuccess) return e;
         const int grid = p.n_qt * a.B * a.H;
         if (tm.begin) cudaEventRecord(tm.begin, st);
-        mla_prefill_kernel<false><<<grid, kPThreads, PCfg<false>::kSmem, st>>>(kmap, vmap, p);
+        mla_prefill_kernel<false><<<grid, kPThreads, PCfg<false>::kSmem, st>>>(kmap, vmap, qmap, p);
         if (tm.end) cudaEventRecord(tm.end, st);
         return cudaGetLastError();
     }
@@ -610,7 +622,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Kn
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (tm.begin) cudaEventRecord(tm.begin, st);
-    e = cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, kmap, vmap, p);
+    e = cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, kmap, vmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
