@@ -84,6 +84,9 @@ def test_debug_knobs(lib):
     assert lib.mla_debug_set(12345, 0) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_debug_set(_lib.DEBUG_WAIT_LIMIT_NS, 0) == _lib.MLA_OK
     assert lib.mla_debug_set(_lib.DEBUG_STALL_STAGE, -1) == _lib.MLA_OK
+    for v in (1, 2, 0):
+        assert lib.mla_debug_set(_lib.DEBUG_PREFILL_CTAS, v) == _lib.MLA_OK
+    assert lib.mla_debug_set(_lib.DEBUG_PREFILL_CTAS, 3) == _lib.MLA_ERR_INVALID_ARG
 
 
 def test_binding_raises_when_library_missing(tmp_path):
