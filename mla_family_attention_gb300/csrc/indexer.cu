@@ -603,19 +603,29 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u) vals[u * 1024 + tid] = v[u];
     };
-    for (int i = tid; i < kBins; i += blockDim.x) {
-        sum2[i] = 0;
-        hist1[i] = p.hist1[size_t(b) * kBins + i];
-    }
-    for (int i = tid; i < 1024; i += blockDim.x) sum3[i] = 0;
+    // level-1 bins and this CTA's scores: both loads are issued before either
+    // is stored, so their latencies overlap
+    static_assert(kBins == 2 * 1024, "two level-1 bins per thread");
+    unsigned hv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) hv[k] = p.hist1[size_t(b) * kBins + tid + k * 1024];
     if (resident) stage(lo);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        sum2[tid + k * 1024] = 0;
+        hist1[tid + k * 1024] = hv[k];
+    }
+    sum3[tid] = 0;
     __syncthreads();
     int bin1, above1;
     find_bin(hist1, kBins, K, sh, &bin1, &above1);
     cluster_sync();                                 // (1) every CTA's totals are zero
 
-    // One refinement level: partial bins of the keys with top bits == pre.
+    // One refinement level: partial bins of the keys with top bits == pre
+    // (and, per thread, the number of keys whose top bits are above pre).
+    int n_above = 0;
     auto level = [&](int shift, int nb, uint32_t pre, unsigned* total) {
+        n_above = 0;
         for (int i = tid; i < nb; i += blockDim.x) part[i] = 0;
         __syncthreads();
         for (int t0 = lo; t0 < hi; t0 += kStep) {
@@ -628,8 +638,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
             for (int u = 0; u < kSelPer; ++u) {
                 if (i0 + u < hi) {
                     const uint32_t k = okey(vals[u * 1024 + tid]);
-                    if ((k >> (shift + (nb == 1024 ? 10 : 11))) == pre)
+                    const uint32_t top = k >> (shift + (nb == 1024 ? 10 : 11));
+                    if (top == pre)
                         atomicAdd(&part[(k >> shift) & uint32_t(nb - 1)], 1u);
+                    n_above += top > pre;
                 }
             }
             if (!resident) __syncthreads();
@@ -666,25 +678,39 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
     const bool all_eq = int(kshift ? sum2[bin2] : sum3[kth & 1023u]) == need_eq;
 
     // counts of this CTA's range, written into every CTA
-    int gt = 0, eq = 0;
-    for (int t0 = lo; t0 < hi; t0 += kStep) {
-        if (!resident) {
-            __syncthreads();
-            stage(t0);
-            __syncthreads();
-        }
-        const int i0 = t0 + tid * kSelPer;
-#pragma unroll
-        for (int u = 0; u < kSelPer; ++u)
-            if (i0 + u < hi) {
-                const uint32_t k = okey(vals[u * 1024 + tid]) >> kshift;
-                gt += k > kth;
-                eq += k == kth;
-            }
-    }
     int tg, te;
-    block_excl_scan(gt, sh, &tg);
-    block_excl_scan(eq, sh, &te);
+    if (kshift) {
+        // level 3 skipped: this CTA's keys above the 22-bit k-th prefix are
+        // those above bin1 plus its level-2 bins above bin2, and the equal
+        // ones its level-2 bin bin2 (`part` still holds its level-2 counts)
+        int gt = n_above;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + k * 1024;
+            if (i > bin2) gt += int(part[i]);
+        }
+        block_excl_scan(gt, sh, &tg);
+        te = int(part[bin2]);
+    } else {
+        int gt = 0, eq = 0;
+        for (int t0 = lo; t0 < hi; t0 += kStep) {
+            if (!resident) {
+                __syncthreads();
+                stage(t0);
+                __syncthreads();
+            }
+            const int i0 = t0 + tid * kSelPer;
+#pragma unroll
+            for (int u = 0; u < kSelPer; ++u)
+                if (i0 + u < hi) {
+                    const uint32_t k = okey(vals[u * 1024 + tid]);
+                    gt += k > kth;
+                    eq += k == kth;
+                }
+        }
+        block_excl_scan(gt, sh, &tg);
+        block_excl_scan(eq, sh, &te);
+    }
     if (tid < kCluster) {
         dsmem_st(dsmem_addr(&cnts[2 * rank], uint32_t(tid)), tg);
         dsmem_st(dsmem_addr(&cnts[2 * rank + 1], uint32_t(tid)), te);
