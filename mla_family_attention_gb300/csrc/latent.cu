@@ -76,7 +76,10 @@ constexpr int kThreadsOf = (kPvWarp<kSrc> + 1) * 32;
 constexpr int kRec = 656;                        // FP8 record: 512 codes, 4 fp32 scales, 64 bf16
 constexpr int kColO = 2 * kLT;                   // O^T columns start after the score buffers
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kAhead = 4;                        // tiles prefetched into L2 ahead of the ring
+// FP8 records are prefetched into L2 this many tiles ahead of the producer
+// threads' loads (1 measured best of 0, 1, 2, 4, 8, 12; the TMA path measured
+// best with no prefetch: bulk prefetches share the TMA unit with its loads).
+constexpr int kAheadFp8 = 1;
 constexpr size_t kExtra = (2 * 2 * 128 + 2 * 128 + 128 + 128) * 4 + 256;
 constexpr size_t kLatSmem = 1024 + kQBytes + kPBytes + size_t(kSlots) * kSlot + kExtra;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kLT, false, false);
@@ -99,7 +102,7 @@ struct LatParams {
     const int64_t* cu;       // decode: [B+1] packed positions of each sequence
     const int32_t* idx;      // sparse prefill: [B][topk] selections, else null
     int topk, P;             // sparse prefill: selection width; cached positions before token 0
-    const uint16_t* ckv;     // for L2 prefetches ahead of the ring
+    const uint16_t* ckv;     // the latent cache (the gather producer reads its selected rows)
     int64_t total;           // rows of ckv
     float* part;             // [slots][H][512] unnormalised O of segments of spanning sequences
     float* ml;               // [slots][H][2]: max (log2 units), sum
@@ -276,10 +279,10 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 if (r1 > r0) prefetch_l2(p.rec + r0 * kRec, uint32_t((r1 - r0) * kRec));
             };
             if (!sparse && ptid == 0)
-                for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
+                for (int t = t0; t < min(t1, t0 + kAheadFp8); ++t) prefetch_tile(t);
             bool ok = true;
             for (int t = t0; t < t1 && ok; ++t) {
-                if (!sparse && ptid == 0 && t + kAhead < t1) prefetch_tile(t + kAhead);
+                if (!sparse && ptid == 0 && t + kAheadFp8 < t1) prefetch_tile(t + kAheadFp8);
                 cur.advance(t);
                 const int b = cur.b;
                 const SeqDesc sd = seq_desc(p, b);
@@ -446,9 +449,9 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
         }
     } else if (warp == 0) {
         // ------------------------------- TMA -------------------------------
-        // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.  The
-        // ring holds little more than one tile, so HBM latency is covered by
-        // prefetching the tiles kAhead ahead into L2.
+        // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.  (An
+        // L2 prefetch of the next tiles measured slower at every distance
+        // tried: it competes with these loads for the TMA unit.)
         if (t0 < t1 && lane == 0) {
             tma_prefetch_desc(&cmap);
             tma_prefetch_desc(&qmap);
@@ -456,20 +459,10 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
             int filled[kSlots];
             for (int s = 0; s < kSlots; ++s) filled[s] = 0;
             int nseg = 0, fill = 0;
-            Cursor cur{ts}, ahead{ts};
+            Cursor cur{ts};
             cur.seek(t0, B);
-            ahead.seek(t0, B);
-            auto prefetch_tile = [&](int t) {
-                ahead.advance(t);
-                const int64_t r0 = p.cu[ahead.b] + int64_t(t - ts[ahead.b]) * kLT;
-                const int64_t r1 = min(r0 + kLT, p.total);
-                if (r1 > r0)
-                    prefetch_l2(p.ckv + r0 * kCkv, uint32_t((r1 - r0) * kCkv * 2));
-            };
-            for (int t = t0; t < min(t1, t0 + kAhead); ++t) prefetch_tile(t);
             bool ok = true;
             for (int t = t0; t < t1 && ok; ++t) {
-                if (t + kAhead < t1) prefetch_tile(t + kAhead);
                 cur.advance(t);
                 const int b = cur.b;
                 if (t == t0 || t == ts[b]) {
