@@ -111,21 +111,27 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
-def traffic_for(kernel: str):
+def traffic_for(kernel: str, units=None):
     """DRAM bytes per launch from a committed ncu summary, if the kernel's source
-    has not changed since the capture."""
+    has not changed since the capture.  The summary records the algorithmic
+    units (bytes or flops) of the launch it describes; a launch of the same
+    kernel on another workload gets that traffic scaled by its own units
+    (these kernels' traffic grows with the work they are given)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path)).get(kernel)
-    if not d:
+    if not d or d.get("dram_bytes_per_launch") is None:
         return None
     src = os.path.join(ROOT, d["source"])
     if not os.path.exists(src):
         return None
     if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha256_16"]:
         return None
-    return d["dram_bytes_per_launch"]
+    ref = d.get("algorithmic_per_launch")
+    if units is None or not ref:
+        return d["dram_bytes_per_launch"]
+    return int(round(d["dram_bytes_per_launch"] * units / ref))
 
 
 def dist_setup():
@@ -703,7 +709,7 @@ def roofline(work, kern):
     r = {"bound": work.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
          "frac": round(achieved / peak, 4), "peak_source": peak_kind,
          f"frac_of_nominal_{int(nominal)}": round(achieved / nominal, 4), "kernel": kname,
-         "kernel_ms": round(k_ms, 4), "traffic": traffic_for(kname),
+         "kernel_ms": round(k_ms, 4), "traffic": traffic_for(kname, units),
          f"algorithmic_{per}_per_launch": units}
     others = {}
     for kn, km, ku, kb in kern:

@@ -27,6 +27,10 @@ def test_traffic_table_entries_match_current_sources():
         got = bench.traffic_for(kernel)
         if digest == entry["source_sha256_16"]:
             assert got == entry["dram_bytes_per_launch"], kernel
+            units = entry.get("algorithmic_per_launch")
+            if got is not None and units:
+                # traffic of a launch with twice the work: twice the bytes
+                assert bench.traffic_for(kernel, 2 * units) == pytest.approx(2 * got, rel=1e-9)
         else:
             assert got is None, kernel
 
@@ -38,9 +42,11 @@ def test_traffic_withheld_for_a_changed_source(tmp_path, monkeypatch):
     src.write_text("kernel v1\n")
     digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
     (prof / "traffic.json").write_text(json.dumps(
-        {"k": {"source": "k.cu", "source_sha256_16": digest, "dram_bytes_per_launch": 123}}))
+        {"k": {"source": "k.cu", "source_sha256_16": digest, "dram_bytes_per_launch": 123,
+               "algorithmic_per_launch": 100}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.traffic_for("k") == 123
+    assert bench.traffic_for("k", 1000) == 1230     # another launch of the kernel, 10x the work
     src.write_text("kernel v2\n")
     assert bench.traffic_for("k") is None
     assert bench.traffic_for("unknown") is None
@@ -53,7 +59,7 @@ class _Work:
 def test_roofline_takes_the_longest_kernel_of_the_bound(monkeypatch):
     monkeypatch.setattr(bench, "peaks", lambda bound="hbm": (
         (2000.0, "TFLOP/s", "test") if bound == "tensor" else (8000.0, "GB/s", "test")))
-    monkeypatch.setattr(bench, "traffic_for", lambda k: None)
+    monkeypatch.setattr(bench, "traffic_for", lambda k, units=None: None)
     kern = [("small", 0.01, 4e7, "hbm"), ("big", 2.0, 16e9, "hbm"), ("mma", 3.0, 3e12, "tensor")]
     r = bench.roofline(_Work(), kern)
     assert r["kernel"] == "big"
