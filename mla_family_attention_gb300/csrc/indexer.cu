@@ -14,22 +14,32 @@
 // 32-head dot products therefore run on the tensor cores as one
 // M=128 (positions) x N=32 (index heads) x K=128 tcgen05.mma tile per 128
 // positions, accumulating in TMEM:
-//   warp 0  TMA producer: 128 key rows (two 64-feature swizzled boxes) and the
-//           sequence's 32 index queries into a 4-stage shared-memory ring;
-//   warp 1  allocates 64 TMEM columns (two 32-column accumulators) and one
+//   warp 0  TMA producer: 128 key rows (two 64-feature swizzled boxes) per
+//           shared-memory ring stage, and each sequence's 32 index queries;
+//   warp 1  allocates 128 TMEM columns (four 32-column accumulators) and one
 //           lane issues the eight K=16 MMAs per tile, committing to mbarriers;
-//   warps 2-5 read the accumulator (thread = position, 32 columns = heads),
-//           apply ReLU and the head weights, write the fp32 score and count it
-//           in a 2048-bin histogram of its top 11 order-preserving key bits.
+//   warps 2-17, four groups of four warps, one group per accumulator: read it
+//           (thread = position, 32 columns = heads), apply ReLU and the head
+//           weights, write the fp32 score and count it in a 2048-bin
+//           histogram of its top 11 order-preserving key bits.
 // Tiles are assigned to CTAs in contiguous ranges so the histogram of one
-// sequence is flushed to global memory a few times, not per tile.
+// sequence is flushed to global memory a few times, not per tile.  The FP8
+// variant reads 128 e4m3 codes per position and applies the key's scale in
+// the epilogue.
 //
-// Top-k (dsa_topk_kernel, one CTA per sequence).  An exact radix select on
-// order-preserving 32-bit keys: the first 11 bits come from the histogram the
-// scoring pass built, two more passes over the (L2-resident) scores find the
-// next 11 and the last 10 bits of the k-th key, and a final pass in position
-// order keeps every key above it plus the lowest positions among keys equal
-// to it, writing the output in ascending position order directly.
+// Top-k (dsa_topk_cluster_kernel, a cluster of eight CTAs per sequence).  An
+// exact radix select on order-preserving 32-bit keys: the first 11 bits come
+// from the histogram the scoring pass built, a pass over the (L2-resident)
+// scores held in shared memory finds the next 11 bits of the k-th key (and,
+// only when that bin holds more keys than are still needed, another pass the
+// last 10), the CTAs sum their bins through distributed shared memory, and a
+// final pass in position order keeps every key above the k-th plus the
+// lowest positions among keys equal to it, writing the output in ascending
+// position order directly.
+//
+// The tile-list, scoring and top-k kernels are launched as programmatic
+// dependents of one another: each waits on the device before it touches
+// global memory, and does its set-up while its predecessor drains.
 #include <algorithm>
 
 #include <cuda.h>
