@@ -92,3 +92,52 @@ def test_debug_knobs(lib):
 def test_binding_raises_when_library_missing(tmp_path):
     with pytest.raises(RuntimeError):
         _lib.load(str(tmp_path / "nope.so"))
+
+
+def test_host_validation_of_the_other_entry_points(lib):
+    """Each entry point rejects malformed calls on the host, before any CUDA
+    call, with the documented status and a message naming the problem."""
+    P = ctypes.c_void_p
+    g = P(1 << 20)                       # a 16-byte aligned stand-in pointer
+    bad = P((1 << 20) + 2)               # misaligned
+    E = _lib
+
+    # prefill: Tq > Tk, null pointer, misaligned pointer, bad scale
+    assert lib.mla_prefill(g, g, g, None, g, 1, 1, 8, 4, 0.1, None, 0, None) == E.MLA_ERR_INVALID_ARG
+    assert lib.mla_prefill(None, g, g, None, g, 1, 1, 8, 8, 0.1, None, 0, None) == E.MLA_ERR_INVALID_ARG
+    assert "null" in _err(lib)
+    assert lib.mla_prefill(bad, g, g, None, g, 1, 1, 8, 8, 0.1, None, 0, None) == E.MLA_ERR_INVALID_ARG
+    assert "aligned" in _err(lib)
+    assert lib.mla_prefill(g, g, g, None, g, 1, 1, 8, 8, 0.0, None, 0, None) == E.MLA_ERR_INVALID_ARG
+    assert "scale" in _err(lib)
+
+    # cache append: the uniform start must leave room for the new rows
+    assert lib.mla_cache_append(g, g, g, g, None, 10, 1, 1, 8, 16, None) == E.MLA_ERR_INVALID_ARG
+    assert "kv_capacity" in _err(lib)
+    # chunked prefill: P + Tq past the capacity
+    assert lib.mla_prefill_chunk(g, g, g, g, g, None, g, 1, 1, 8, 10, 16, 0.1, None, 0,
+                                 None) == E.MLA_ERR_INVALID_ARG
+
+    # DSA indexer: 32 index heads only, topk at most 2048, B >= 1
+    assert lib.dsa_index_topk(g, g, g, g, 1, 16, 100, 100, 64, g, None, g, 1 << 20,
+                              None) == E.MLA_ERR_UNSUPPORTED
+    assert lib.dsa_index_topk(g, g, g, g, 1, 32, 100, 100, 4096, g, None, g, 1 << 20,
+                              None) == E.MLA_ERR_UNSUPPORTED
+    assert lib.dsa_index_topk(g, g, g, g, 0, 32, 100, 100, 64, g, None, g, 1 << 20,
+                              None) == E.MLA_ERR_INVALID_ARG
+    assert lib.dsa_index_topk_fp8(g, g, g, g, g, 1, 16, 100, 100, 64, g, None, g, 1 << 20,
+                                  None) == E.MLA_ERR_UNSUPPORTED
+    assert lib.dsa_prefill_index_topk(g, g, g, 8, 4, 32, 64, g, None, g, 1 << 20,
+                                      None) == E.MLA_ERR_INVALID_ARG
+
+    # latent decode: head counts that are multiples of 16 up to 96
+    assert lib.mla_decode_latent(g, g, g, 100, 1, 40, 100, g, g, None, g, 0.1, g, 1 << 20,
+                                 None) == E.MLA_ERR_UNSUPPORTED
+    assert lib.mla_decode_latent(g, g, g, 100, 1, 96, 100, g, None, None, g, 0.1, g, 1 << 20,
+                                 None) == E.MLA_ERR_INVALID_ARG
+    assert lib.mla_sparse_prefill_latent(g, g, g, 8, 4, 64, 96, g, g, None, g, 0.1, g, 1 << 20,
+                                         None) == E.MLA_ERR_INVALID_ARG
+
+    # quantisers: negative counts
+    assert lib.dsa_quantize_index_keys(g, g, g, -1, None) == E.MLA_ERR_INVALID_ARG
+    assert lib.mla_quantize_latent_cache(g, g, -1, None) == E.MLA_ERR_INVALID_ARG
