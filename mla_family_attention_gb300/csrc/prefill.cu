@@ -40,7 +40,7 @@
 // both CTAs' barriers (multicast).  It halves the MMA instructions and the
 // key/value bytes per SM, but the cross-SM handoffs lengthen every key
 // tile's score -> softmax -> P.V chain, which is what bounds this kernel,
-// and it measured slower (948 vs 1,305 TFLOP/s at H=96, T=16384), so the
+// and it measured slower (982 vs 1,343 TFLOP/s at H=96, T=16384), so the
 // one-CTA shape is the default.
 // All waits are bounded; a timeout sets MLA_ERR_TIMEOUT, the roles stop, the
 // MMA lane waits for its last commit, and TMEM is released before exit.
