@@ -6,7 +6,10 @@
   dequantised value within half an e4m3 step (relative 2^-4) of the input,
   and an all-zero row has scale 0;
 * when every query and key feature is already an e4m3 value and the row
-  maxima are 448, the FP8 scores equal the bf16-path scores exactly.
+  maxima are 448, the FP8 scores equal the bf16-path scores exactly; when
+  such rows are further multiplied by per-row powers of two, the scales are
+  exactly those powers and the FP8 scores still equal the exact scores (so
+  a dropped or misapplied key or query scale fails).
 """
 import numpy as np
 
@@ -63,6 +66,27 @@ def test_fp8_scores_equal_bf16_scores_on_representable_inputs():
     cu = np.arange(0, B * T + 1, T, dtype=np.int64)
     k8, ks = oracle.quantize_e4m3_rows(k)
     assert (ks == 1.0).all()
+    got = oracle.dsa_index_scores_fp8(q, k8, ks, w, cu)
+    ref = oracle.dsa_index_scores(q, k, w, cu)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_fp8_scores_apply_each_scale_exactly():
+    grid = oracle.e4m3_values(np.arange(0, 0x7E, dtype=np.uint8).reshape(1, -1))[0]
+    grid = np.concatenate([grid, -grid])
+    B, T = 2, 30
+    q = RNG.choice(grid, size=(B, 32, 128))
+    q[..., 0] = 448.0
+    q *= 2.0 ** RNG.integers(-3, 4, size=(B, 32, 1))
+    k = RNG.choice(grid, size=(B * T, 128))
+    k[:, 0] = 448.0
+    kpow = 2.0 ** RNG.integers(-4, 5, size=(B * T, 1))
+    k *= kpow
+    w = RNG.normal(size=(B, 32))
+    cu = np.arange(0, B * T + 1, T, dtype=np.int64)
+    k8, ks = oracle.quantize_e4m3_rows(k)
+    np.testing.assert_array_equal(ks, kpow[:, 0].astype(np.float32))
+    assert len(np.unique(ks)) > 1
     got = oracle.dsa_index_scores_fp8(q, k8, ks, w, cu)
     ref = oracle.dsa_index_scores(q, k, w, cu)
     np.testing.assert_array_equal(got, ref)
