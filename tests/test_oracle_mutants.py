@@ -33,6 +33,19 @@ MUTANTS = {
                                       "const double* qb = q + ((int64_t)h * B + b) * Dqk;\n"
                                       "            err |= attend(qb, kb, vb, NULL, T,"),
     "sparse skips position 0": ("if (s >= 0) pos[n++] = s;", "if (s > 0) pos[n++] = s;"),
+    "sparse reads padding as position 0": ("if (s >= 0) pos[n++] = s;",
+                                           "pos[n++] = s < 0 ? 0 : s;"),
+    "index weights of the first sequence": ("acc += w[(int64_t)b * NH + h] *",
+                                            "acc += w[h] *"),
+    "index query of the first sequence": ("dot(iq + ((int64_t)b * NH + h) * Di, ks, Di)",
+                                          "dot(iq + (int64_t)h * Di, ks, Di)"),
+    "index scores without the sequence offset": ("scores[cu[b] + s] = acc;",
+                                                 "scores[s] = acc;"),
+    "top-k left in rank order": ("qsort(row, (size_t)kk, sizeof(int32_t), by_value);", ""),
+    "prefill keys of head 0": ("const double* kb = k + ((int64_t)b * H + h) * Tk * Dqk;",
+                               "const double* kb = k + ((int64_t)b * H) * Tk * Dqk;"),
+    "probabilities not normalised": ("double pj = exp(s[j] - m) / denom;",
+                                     "double pj = exp(s[j] - m);"),
 }
 
 
