@@ -31,6 +31,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -176,21 +178,39 @@ def oracle_inputs(dec, n_seq: int):
                 scale=dec.scale)
 
 
-def oracle_decode_sample(dec, n_seq: int, min_seconds: float):
-    """Time the fp64 oracle over the first n_seq sequences (all heads), repeated
-    until min_seconds of CPU work; returns (GB/s, seconds, threads, repeats, n_seq)."""
-    import oracle
-    threads = oracle.set_threads(len(os.sched_getaffinity(0)))
-    x = oracle_inputs(dec, n_seq)
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _repeat(fn, seconds: float):
+    """Run fn until `seconds` of wall time have passed (at least once);
+    returns (seconds elapsed, repeats)."""
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.mla_decode(**x)
+        fn()
         reps += 1
         el = time.perf_counter() - t0
-        if el >= min_seconds:
-            break
-    nbytes = acc.decode_kv_bytes(dec.lengths[:n_seq], dec.H) * reps
-    return nbytes / el / 1e9, el, threads, reps, n_seq
+        if el >= seconds:
+            return el, reps
+
+
+def _cpu_result(units_per_s, unit_scale, unit, sample, extrapolated=False):
+    import oracle
+    return {"value": round(units_per_s / unit_scale, 6), "unit": unit,
+            "cores": oracle.set_threads(0), "kind": "oracle",
+            "sample": sample + (" (extrapolated)" if extrapolated else "")}
+
+
+def _decode_seq_inputs(dec, b: int, heads: int):
+    """fp64 oracle inputs for sequence b of a packed decode cache, first `heads` heads."""
+    H, T = dec.H, dec.lengths[b]
+    o = int(dec.cu_seqlens[b].item()) * H
+    k = dec.k[o * 192:(o + H * T) * 192].view(H, T, 192)[:heads]
+    v = dec.v[o * 128:(o + H * T) * 128].view(H, T, 128)[:heads]
+    return dict(q=_f64(dec.q[b:b + 1, :heads]), k=_f64(k).reshape(-1), v=_f64(v).reshape(-1),
+                cu_seqlens=np.array([0, T], dtype=np.int64),
+                gate=None if dec.gate is None else _f64(dec.gate[b:b + 1, :heads * 128]),
+                scale=dec.scale)
 
 
 def run_reference(args, world, rank):
@@ -277,10 +297,18 @@ class DecodeWork:
                             scale=d.scale, ws=self.ws, stream=stream)
 
     def cpu_sample(self, seconds):
-        gbs, el, threads, reps, n_seq = oracle_decode_sample(self.dec, 1, seconds)
-        return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                "sample": f"{n_seq} of {self.B} sequences x {self.H} heads x "
-                          f"{self.lengths[0]} positions, {reps} repeats, {el:.1f} s"}
+        """The oracle over sequence 0 (all heads when it has at most 8192
+        positions, else as many heads as 8192*96 position-heads allow)."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        T = self.lengths[0]
+        heads = min(self.H, max(1, 8192 * self.H // T))
+        x = _decode_seq_inputs(self.dec, 0, heads)
+        el, reps = _repeat(lambda: oracle.mla_decode(**x), seconds)
+        nbytes = T * heads * (192 + 128) * 2 * reps
+        return _cpu_result(nbytes / el, 1e9, "GB/s",
+                           f"sequence 0 of {self.B} ({T} positions) x {heads} of {self.H} "
+                           f"heads, {reps} repeats, {el:.1f} s")
 
     def e2e(self, dev, stream, world, steps):
         """Same metric through the public API with pinned host buffers: every step
@@ -345,6 +373,38 @@ class DsaWork:
         self.mla.dsa_sparse_decode(m.q, m.k, m.v, m.cu_seqlens, self.idx, gate=m.gate,
                                    out=self.out, scale=m.scale, ws=self.ws_s, stream=stream)
 
+    def cpu_sample(self, seconds):
+        """Sequence 0: the oracle's index scores and top-k over all its
+        positions, then its 96-head sparse gated decode.  The rows the
+        selection names are gathered into a compact cache before timing (the
+        oracle reads only those rows; copying 8 GB of unselected cache to
+        the host would time the copy, not the oracle)."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        d, m, T, H, K = self.d, self.d.main, self.lengths[0], self.H, self.topk
+        iq, ik, w = _f64(d.index_q[:1]), _f64(d.index_k[:T]), _f64(d.w[:1])
+        cu = np.array([0, T], dtype=np.int64)
+        sel = oracle.dsa_topk(oracle.dsa_index_scores(iq, ik, w, cu), cu, K)[0]
+        rows = torch.from_numpy(sel[sel >= 0].astype(np.int64)).to(m.k.device)
+        n = int(rows.numel())
+        ks = m.k[:H * T * 192].view(H, T, 192).index_select(1, rows)
+        vs = m.v[:H * T * 128].view(H, T, 128).index_select(1, rows)
+        x = dict(q=_f64(m.q[:1]), k=_f64(ks).reshape(-1), v=_f64(vs).reshape(-1),
+                 cu_seqlens=np.array([0, n], dtype=np.int64),
+                 idx=np.where(np.arange(K) < n, np.arange(K), -1).astype(np.int32)[None],
+                 gate=_f64(m.gate[:1]), scale=m.scale)
+
+        def one():
+            s64 = oracle.dsa_index_scores(iq, ik, w, cu)
+            oracle.dsa_topk(s64, cu, K)
+            oracle.dsa_sparse_decode(**x)
+
+        el, reps = _repeat(one, seconds)
+        nbytes = (acc.index_key_bytes([T]) + acc.sparse_kv_bytes([T], H, K)) * reps
+        return _cpu_result(nbytes / el, 1e9, "GB/s",
+                           f"sequence 0 of {self.B} ({T} positions): index scores, top-{K}, "
+                           f"{H}-head sparse decode; {reps} repeats, {el:.1f} s")
+
     def free(self):
         del self.d, self.idx, self.out, self.ws_i, self.ws_s
 
@@ -378,6 +438,19 @@ class IndexWork:
         self.mla.dsa_index_topk(d.index_q, d.index_k, d.w, self.cu, self.max_len, self.topk,
                                 topk_idx=self.idx, ws=self.ws_i, stream=stream)
 
+    def cpu_sample(self, seconds):
+        """The oracle's index scores and top-k over sequence 0."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        T = self.lengths[0]
+        iq, ik, w = _f64(self.d.index_q[:1]), _f64(self.d.index_k[:T]), _f64(self.d.w[:1])
+        cu = np.array([0, T], dtype=np.int64)
+        el, reps = _repeat(lambda: oracle.dsa_topk(oracle.dsa_index_scores(iq, ik, w, cu), cu,
+                                                   self.topk), seconds)
+        return _cpu_result(acc.index_key_bytes([T]) * reps / el, 1e9, "GB/s",
+                           f"sequence 0 of {self.B} ({T} positions), {reps} repeats, "
+                           f"{el:.1f} s")
+
     def free(self):
         del self.d, self.idx, self.ws_i
 
@@ -400,6 +473,21 @@ class IndexFp8Work(IndexWork):
         d = self.d
         self.mla.dsa_index_topk_fp8(d.index_q, self.k8, self.ks, d.w, self.cu, self.max_len,
                                     self.topk, topk_idx=self.idx, ws=self.ws_i, stream=stream)
+
+    def cpu_sample(self, seconds):
+        """The oracle's FP8 index scores (query quantisation included) and
+        top-k over sequence 0."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        T = self.lengths[0]
+        iq, w = self.d.index_q[:1].cpu(), _f64(self.d.w[:1])
+        k8, ks = self.k8[:T].cpu(), self.ks[:T].cpu()
+        cu = np.array([0, T], dtype=np.int64)
+        el, reps = _repeat(lambda: oracle.dsa_topk(
+            oracle.dsa_index_scores_fp8(iq, k8, ks, w, cu), cu, self.topk), seconds)
+        return _cpu_result(acc.index_key_bytes_fp8([T]) * reps / el, 1e9, "GB/s",
+                           f"sequence 0 of {self.B} ({T} positions), {reps} repeats, "
+                           f"{el:.1f} s")
 
     def free(self):
         del self.k8, self.ks
@@ -431,6 +519,26 @@ class PrefillWork:
         pf = self.pf
         self.mla.mla_prefill(pf.q, pf.k, pf.v, pf.gate, out=self.out, scale=pf.scale,
                              stream=stream)
+
+    def cpu_sample(self, seconds):
+        """The oracle over the whole prompt when it is short (T <= 1024);
+        otherwise over head 0 and the prompt's last 128 query rows, each of
+        which sees ~T keys (the rate of that sample stands for the whole)."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        pf, T = self.pf, self.T
+        if T <= 1024:
+            x = (_f64(pf.q), _f64(pf.k), _f64(pf.v), None if pf.gate is None else _f64(pf.gate))
+            flops, what, ext = self.work, f"the whole prompt ({self.H} heads x {T} rows)", False
+        else:
+            R = 128
+            x = (_f64(pf.q[:, :1, T - R:]), _f64(pf.k[:, :1]), _f64(pf.v[:, :1]),
+                 None if pf.gate is None else _f64(pf.gate[:, T - R:, :128]))
+            flops, ext = acc.prefill_flops(1, 1, R, T), True
+            what = f"head 0 of {self.H}, query rows {T - R}..{T - 1} of {T}"
+        el, reps = _repeat(lambda: oracle.mla_prefill(*x, pf.scale), seconds)
+        return _cpu_result(flops * reps / el, 1e12, "TFLOP/s",
+                           f"{what}, {reps} repeats, {el:.1f} s", ext)
 
     def free(self):
         del self.pf, self.out
@@ -476,6 +584,25 @@ class ChunkedPrefillWork:
                                        i * self.c, gate=self.g[i], out=self.out[i],
                                        scale=self.scale, stream=stream)
 
+    def cpu_sample(self, seconds):
+        """The oracle's chunked prefill of the last chunk's last 128 query
+        rows, head 0, over the cache the earlier chunks filled (the rate of
+        that sample stands for the whole prompt)."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        R, n = 128, len(self.q)
+        P = (n - 1) * self.c
+        kc = _f64(torch.cat([k[:, :1] for k in self.kn[:-1]], 2))
+        vc = _f64(torch.cat([v[:, :1] for v in self.vn[:-1]], 2))
+        q = _f64(self.q[-1][:, :1, self.c - R:])
+        kn, vn = _f64(self.kn[-1][:, :1]), _f64(self.vn[-1][:, :1])
+        g = None if self.g[-1] is None else _f64(self.g[-1][:, self.c - R:, :128])
+        el, reps = _repeat(lambda: oracle.mla_prefill_chunk(q, kc, vc, kn, vn, P, g, self.scale),
+                           seconds)
+        return _cpu_result(acc.prefill_flops(1, 1, R, self.T) * reps / el, 1e12, "TFLOP/s",
+                           f"head 0 of {self.H}, last {R} rows of chunk {n - 1} (cache of "
+                           f"{P} positions), {reps} repeats, {el:.1f} s", True)
+
     def free(self):
         del self.q, self.kn, self.vn, self.g, self.kc, self.vc, self.out
 
@@ -511,6 +638,19 @@ class DecodeCachedWork:
                                    k_new=cd.k_new, v_new=cd.v_new, gate=cd.gate, out=self.out,
                                    scale=cd.scale, ws=self.ws, stream=stream)
 
+    def cpu_sample(self, seconds):
+        """The oracle's decode step (current token appended) for sequence 0,
+        all heads."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        cd, L = self.cd, self.T - 1
+        x = (_f64(cd.q[:1]), _f64(cd.k_cache[:1, :, :L]), _f64(cd.v_cache[:1, :, :L]), [L],
+             _f64(cd.k_new[:1]), _f64(cd.v_new[:1]), _f64(cd.gate[:1]), cd.scale)
+        el, reps = _repeat(lambda: oracle.mla_decode_cached(*x), seconds)
+        return _cpu_result(acc.decode_kv_bytes([self.T], self.H) * reps / el, 1e9, "GB/s",
+                           f"sequence 0 of {self.B} ({self.T} positions) x {self.H} heads, "
+                           f"{reps} repeats, {el:.1f} s")
+
     def free(self):
         del self.cd, self.seqlens, self.out, self.ws
 
@@ -545,6 +685,33 @@ class LatentDecodeWork:
                                    gate=d.gate, out=self.out, scale=d.scale, ws=self.ws,
                                    stream=stream)
 
+    CPU_HEADS = 8
+
+    def _cpu_cache(self, T):
+        return _f64(self.d.ckv[:T])
+
+    def _cpu_call(self, oracle, q, cache, cu, wk, wv, g):
+        return oracle.mla_decode_latent(q, cache, cu, wk, wv, g, self.d.scale)
+
+    def _cpu_bytes(self, T):
+        return acc.latent_kv_bytes([T])
+
+    def cpu_sample(self, seconds):
+        """The oracle over sequence 0 with 8 of the 96 heads.  The cache bytes
+        are shared by all heads while the oracle's work grows with them, so
+        the time is scaled by 96/8 (extrapolated)."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        d, T, hs = self.d, self.lengths[0], self.CPU_HEADS
+        q, g = _f64(d.q[:1, :hs]), _f64(d.gate[:1, :hs * 128])
+        wk, wv = _f64(d.w_kc[:hs]), _f64(d.w_vc[:hs])
+        cache, cu = self._cpu_cache(T), np.array([0, T], dtype=np.int64)
+        el, reps = _repeat(lambda: self._cpu_call(oracle, q, cache, cu, wk, wv, g), seconds)
+        full = el / reps * self.H / hs
+        return _cpu_result(self._cpu_bytes(T) / full, 1e9, "GB/s",
+                           f"sequence 0 of {self.B} ({T} positions) x {hs} of {self.H} heads, "
+                           f"{reps} repeats, {el:.1f} s, time scaled by {self.H}/{hs}", True)
+
     def free(self):
         del self.d, self.out, self.ws
 
@@ -563,6 +730,15 @@ class LatentDecodeFp8Work(LatentDecodeWork):
         self.mla.mla_decode_latent_fp8(d.q, self.rec, d.cu_seqlens, self.max_len, d.w_kc, d.w_vc,
                                        gate=d.gate, out=self.out, scale=d.scale, ws=self.ws,
                                        stream=stream)
+
+    def _cpu_cache(self, T):
+        return self.rec[:T].cpu()
+
+    def _cpu_call(self, oracle, q, cache, cu, wk, wv, g):
+        return oracle.mla_decode_latent_fp8(q, cache, cu, wk, wv, g, self.d.scale)
+
+    def _cpu_bytes(self, T):
+        return acc.latent_kv_bytes_fp8([T])
 
     def free(self):
         del self.rec
@@ -604,6 +780,35 @@ class DsaPrefillWork:
         self.mla.mla_sparse_prefill_latent(d.q, d.ckv, self.idx, d.w_kc, d.w_vc, gate=d.gate,
                                            out=self.out, scale=d.scale, ws=self.ws_a,
                                            stream=stream)
+
+    def cpu_sample(self, seconds):
+        """The prompt's last token: the oracle's index scores over its
+        T visible positions and its top-k (timed), then its gated MLA over its
+        selection with 4 of the 96 heads (timed, scaled by 96/4); flops are the
+        token's index flops plus its all-head attention flops (extrapolated)."""
+        import oracle
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        d, T, K, H, hs = self.d, self.T, self.K, self.H, 4
+        i = T - 1
+        iq, ik, w = d.index_q[i:i + 1].cpu(), d.index_k.cpu(), d.w[i:i + 1].cpu()
+        half = seconds / 2
+
+        def index():
+            return oracle.dsa_prefill_topk(oracle.dsa_prefill_index_scores(iq, ik, w), K)
+
+        sel = index()
+        el_i, reps_i = _repeat(index, half)
+        q, g = _f64(d.q[i:i + 1, :hs]), _f64(d.gate[i:i + 1, :hs * 128])
+        ckv, wk, wv = _f64(d.ckv), _f64(d.w_kc[:hs]), _f64(d.w_vc[:hs])
+        el_a, reps_a = _repeat(lambda: oracle.dsa_prefill_latent(q, ckv, wk, wv, sel, g, d.scale),
+                               half)
+        t = el_i / reps_i + el_a / reps_a * H / hs
+        flops = (acc.dsa_prefill_index_flops(1, T) +
+                 acc.sparse_latent_attention_flops(1, T, H, K))
+        return _cpu_result(flops / t, 1e12, "TFLOP/s",
+                           f"token {i} of {T}: index + top-{K} ({reps_i} repeats, {el_i:.1f} s), "
+                           f"MLA over its selection with {hs} of {H} heads ({reps_a} repeats, "
+                           f"{el_a:.1f} s, time scaled by {H}/{hs})", True)
 
     def free(self):
         del self.d, self.idx, self.out, self.ws_i, self.ws_a
@@ -724,7 +929,28 @@ def roofline(work, kern):
     return r
 
 
+ALSO_FIELDS = ["value", "unit", "ms_per_step", "roofline.frac", "roofline.kernel_ms",
+               "cpu_baseline.value"]
+
+
+def _sig(x, digits=4):
+    return None if x is None else float(f"{x:.{digits}g}")
+
+
+def _compact(entry):
+    """The figures of one workload that the one-line summary keeps, in the
+    order of ALSO_FIELDS: value, step time, the dominant kernel's roofline
+    fraction and time, and the oracle's rate in the same unit."""
+    r = entry["roofline"]
+    c = entry.get("cpu_baseline") or {}
+    return [entry["value"], entry["unit"], entry["ms_per_step"], r["frac"], r["kernel_ms"],
+            _sig(c.get("value"))]
+
+
 def run_ours(args, world, rank, local):
+    """Time the headline workload (full detail in the JSON line), then every
+    other workload of the hot path (compact figures in the line's `also`;
+    the full per-workload records go to stderr, one JSON object per line)."""
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -735,11 +961,12 @@ def run_ours(args, world, rank, local):
     ms, kern = time_work(work, args.steps, args.warmup, dev, stream, world, sampler)
     clocks = sampler.finish()
     value = work.work * world / (ms * 1e-3) / _scale(work)
+    roof = roofline(work, kern)
+    others = roof.pop("other_kernels", None)
     line = {"metric": METRIC, "value": round(value, 2), "unit": work.unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(name, work.B),
-            "roofline": roofline(work, kern),
+            "data": "synthetic", "config": workload_config(name, work.B), "roofline": roof,
             "gpu_launches": work.launches_per_step * args.steps * world, "clocks": clocks}
     if hasattr(work, "e2e"):
         in_bytes = sum(getattr(work.dec, n).numel() * getattr(work.dec, n).element_size()
@@ -750,30 +977,39 @@ def run_ours(args, world, rank, local):
             line["e2e"] = {"value": None, "unit": work.unit,
                            "skipped": f"inputs of {in_bytes / 1e9:.0f} GB exceed the "
                                       f"{E2E_HOST_LIMIT / 1e9:.0f} GB pinned host budget"}
-    if rank == 0 and not args.no_cpu_baseline and hasattr(work, "cpu_sample"):
+    cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if cpu_ok and hasattr(work, "cpu_sample"):
         line["cpu_baseline"] = work.cpu_sample(args.cpu_seconds)
+    if rank == 0 and others:
+        print(json.dumps({"workload": name, "other_kernels": others}), file=sys.stderr,
+              flush=True)
     work.free()
     del work
     torch.cuda.empty_cache()
     # the other workloads of the hot path, timed the same way (shorter)
     if not args.only and not args.batch:
-        also = {}
+        also = {"fields": ALSO_FIELDS}
         for other, w in mi.WORKLOADS.items():
             if other == name or w["kind"] not in WORK_KINDS or w.get("profile_only"):
                 continue
             wk = WORK_KINDS[w["kind"]](other, dev)
             k_steps = max(3, min(args.steps, 20))
             ms_o, kern_o = time_work(wk, k_steps, 3, dev, stream, world)
-            also[other] = {"value": round(wk.work * world / (ms_o * 1e-3) / _scale(wk), 2),
-                           "unit": wk.unit, "ms_per_step": round(ms_o, 4), "steps": k_steps,
-                           "roofline": roofline(wk, kern_o)}
+            entry = {"value": round(wk.work * world / (ms_o * 1e-3) / _scale(wk), 2),
+                     "unit": wk.unit, "ms_per_step": round(ms_o, 4), "steps": k_steps,
+                     "roofline": roofline(wk, kern_o)}
+            if cpu_ok and hasattr(wk, "cpu_sample"):
+                entry["cpu_baseline"] = wk.cpu_sample(args.also_cpu_seconds)
             line["gpu_launches"] += wk.launches_per_step * (2 * k_steps + 3) * world
+            also[other] = _compact(entry)
+            if rank == 0:
+                print(json.dumps({"workload": other, **entry}), file=sys.stderr, flush=True)
             wk.free()
             del wk
             torch.cuda.empty_cache()
         line["also"] = also
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 def main():
@@ -787,7 +1023,10 @@ def main():
     ap.add_argument("--only", action="store_true",
                     help="time only --workload (skip the other workloads' short runs)")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle time for the headline workload's cpu_baseline")
+    ap.add_argument("--also-cpu-seconds", type=float, default=3.0,
+                    help="oracle time for each other workload's cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first N sequences (small profiling case)")

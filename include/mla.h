@@ -130,7 +130,9 @@ mla_status mla_decode(const mla_bf16* q, const mla_bf16* k, const mla_bf16* v,
  *     the array (B=32, H=96, max_seqlen=8192 needs about 12.8 MB and fits).
  *   - The first call on each device, with that device current, looks up the
  *     array's device address; make that first call before any stream
- *     capture.
+ *     capture.  The address belongs to the device's current context: after
+ *     a device reset (a new context) the next call looks it up again, so
+ *     make that call before any capture too.
  *   - Every call shares the array and it keeps the last call's contents;
  *     nothing in it needs to start at zero.  Calls whose kernels overlap on
  *     the GPU race on the array: order them (one stream, or events).

@@ -25,6 +25,7 @@ std::atomic<int> g_prefill_ctas{0};
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 mla::DeviceInfo g_dev[kMaxDevices];
+unsigned long long g_dev_ctx[kMaxDevices];   // context the cached facts belong to
 
 mla_status fail(mla_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 mla_status fail(mla_status s, const char* fmt, ...) {
@@ -42,7 +43,8 @@ mla_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // Device facts and the status word address for the current device; set up
-// once per device on first use.
+// on first use in each context of the device (a device reset creates a new
+// context, in which the status word has a new address).
 mla_status device_info(mla::DeviceInfo* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -50,7 +52,8 @@ mla_status device_info(mla::DeviceInfo* out) {
     if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device %d", dev);
     std::lock_guard<std::mutex> lk(g_dev_mu);
     mla::DeviceInfo& d = g_dev[dev];
-    if (d.status == nullptr) {
+    const unsigned long long ctx = mla::current_context_id();
+    if (d.status == nullptr || ctx == 0 || ctx != g_dev_ctx[dev]) {
         int major = 0, minor = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -64,6 +67,7 @@ mla_status device_info(mla::DeviceInfo* out) {
         e = cudaGetSymbolAddress(&p, g_status);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
         d.status = static_cast<int*>(p);
+        g_dev_ctx[dev] = mla::current_context_id();   // the lookup made one current
     }
     *out = d;
     return MLA_OK;

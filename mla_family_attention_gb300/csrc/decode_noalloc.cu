@@ -12,7 +12,9 @@
 // library holds its MLA_NOALLOC_SCRATCH_BYTES until the process exits.  Host
 // code cannot use the variable's name as a device address; the first call
 // on each device (with that device current) looks the address up with
-// cudaGetSymbolAddress and caches it.
+// cudaGetSymbolAddress and caches it with the id of the context it belongs
+// to.  After a device reset the device has a new context, in which the
+// array lives elsewhere, so the next call looks the address up again.
 //
 // Every call shares the one array, and it keeps the previous call's
 // contents.  Nothing in it has to start at zero: the decode kernels write
@@ -34,20 +36,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCR
 constexpr int kMaxDev = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDev];
+unsigned long long g_scratch_ctx[kMaxDev];
 
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array on the current device (set up once
+// per context of the device).
 mla_status scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return mla::set_error(MLA_ERR_CUDA, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDev) return mla::set_error(MLA_ERR_UNSUPPORTED, "device ordinal");
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    const unsigned long long ctx = mla::current_context_id();
+    if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr)
             return mla::set_error(MLA_ERR_CUDA, "cudaGetSymbolAddress(scratch) failed");
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = mla::current_context_id();
     }
     *out = g_scratch_ptr[dev];
     return MLA_OK;

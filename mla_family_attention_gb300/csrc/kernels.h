@@ -100,6 +100,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, bool sparse,
                           const DeviceInfo& dev, const Knobs& kn, const KernelTimer& tm,
                           cudaStream_t st);
 
+// Unique id of the CUDA context current on this thread, 0 if there is none
+// (or the driver cannot tell).  Device addresses of the library's __device__
+// variables are valid for one context: a device reset makes a new one.
+unsigned long long current_context_id();
+
 // --------------------------- TMA tensor maps ------------------------------
 // 2-D bf16 map over a row-major [outer][inner] array with 128-byte swizzle.
 cudaError_t encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

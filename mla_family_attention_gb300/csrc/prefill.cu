@@ -64,9 +64,6 @@ constexpr uint32_t kColS = 0, kColO = 384;     // S_i at kColS + 128 i
 constexpr int kQBox = kBM * 128;               // 128 query rows x 64 features
 constexpr int kQTile = 3 * kQBox;              // the query tile, 48 KB
 constexpr float kRescaleLog2 = 8.f;
-#ifndef MLA_PREFILL_POLY_EXP
-#define MLA_PREFILL_POLY_EXP 0   // 1: odd columns exponentiate on the FMA pipe, 2: one in four
-#endif
 
 // Tile geometry.  One CTA (kPair = false): each CTA loads whole 128-key
 // tiles (three 64-feature key boxes of 128 rows, two 64-feature value
@@ -101,28 +98,6 @@ struct PrefillParams {
     long long wait_ns;
     int* status;
 };
-
-// 2^t on the FMA and integer pipes, for the share of the exponentials the
-// special-function unit (16 per clock per SM) cannot keep up with.  Range
-// reduction t = k + f with k = round(t), f in [-1/2, 1/2]: adding 1.5*2^23
-// rounds t to an integer in the significand (one FADD, no conversion
-// instruction, which would run on the special-function pipe too); 2^f from a
-// cubic fitted (weighted least squares refined to equal ripple) on
-// [-1/2, 1/2], relative error below 1.5e-4 evaluated in fp32; 2^k added to
-// the exponent field as an integer.  t < -126 gives 0.  The result is
-// rounded to bf16 next, whose step is 2^-9.
-__device__ __forceinline__ float exp2_fma(float t) {
-    const float magic = 12582912.f;                 // 1.5 * 2^23
-    const float tc = fmaxf(t, -127.f);
-    const float y = tc + magic;
-    const float k = y - magic;
-    const float f = tc - k;
-    const float q = fmaf(fmaf(fmaf(0.055171642f, f, 0.24261113f), f, 0.69326097f), f,
-                         0.99992806f);
-    const int ki = __float_as_int(y) - __float_as_int(magic);
-    const float r = __int_as_float(__float_as_int(q) + (ki << 23));
-    return t < -126.f ? 0.f : r;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -502,9 +477,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const float p0 = ex2(fmaf(s[c * 32 + 2 * u], p.scale_log2, nme));
-                    const float t1 = fmaf(s[c * 32 + 2 * u + 1], p.scale_log2, nme);
-                    const bool poly = MLA_PREFILL_POLY_EXP == 1 || (MLA_PREFILL_POLY_EXP == 2 && (u & 1));
-                    const float p1 = poly ? exp2_fma(t1) : ex2(t1);
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * u + 1], p.scale_log2, nme));
                     ls[u & 3] += p0 + p1;
                     w[u] = pack_bf16(p0, p1);
                 }

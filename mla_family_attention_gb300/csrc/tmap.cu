@@ -13,7 +13,33 @@ namespace mla {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void* entry_point(const char* name, int version) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return fn;
+    return nullptr;
+}
 }  // namespace
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(
+            entry_point("cuCtxGetCurrent", 4000));
+        g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(entry_point("cuCtxGetId", 12000));
+    });
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext c = nullptr;
+    if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    return g_ctx_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {

@@ -25,15 +25,32 @@ def run_index(d, topk):
     return idx, sc
 
 
-def check_rows(d, idx, sc, topk, rows=None):
+def oracle_row(d, i, topk):
+    """Token i's index scores over its visible prefix and its top-k, both from
+    the oracle on a one-token slice: with Tq = 1 and Tk = n = P+i+1 the token
+    sits at position n-1 and sees every position of the slice, so the full
+    [Tq, Tk] score matrix is never built."""
     Tq, Tk = d.index_q.shape[0], d.index_k.shape[0]
-    P = Tk - Tq
+    n = Tk - Tq + i + 1
+    s = oracle.dsa_prefill_index_scores(d.index_q[i:i + 1], d.index_k[:n], d.w[i:i + 1])
+    return s[0], oracle.dsa_prefill_topk(s, topk)[0], n
+
+
+def check_rows(d, idx, sc, topk, rows=None):
+    """Every row equals the oracle's selection, or differs from it only by
+    positions whose oracle score lies in the 1e-5 band around the k-th score
+    (check_selection proves that for the rows that differ).  Returns the
+    number of rows that differ."""
+    Tq = d.index_q.shape[0]
     rows = range(Tq) if rows is None else rows
-    iq, ik, w = (oracle._f64(x) for x in (d.index_q, d.index_k, d.w))
+    got = idx.cpu().numpy()
+    differ = 0
     for i in rows:
-        n = P + i + 1
-        s = np.einsum("h,hs->s", w[i], np.maximum(iq[i] @ ik[:n].T, 0.0))
+        s, ref, n = oracle_row(d, i, topk)
         check_selection(idx[i:i + 1], sc[i:i + 1], s, [n], topk)
+        if not np.array_equal(got[i], ref):
+            differ += 1
+    return differ
 
 
 @pytest.mark.parametrize("Tq,Tk,topk", [
@@ -49,10 +66,11 @@ def test_prefill_index_topk_matches_oracle(Tq, Tk, topk):
     idx, sc = run_index(d, topk)
     check_rows(d, idx, sc, topk)
     if Tq <= 130 and Tk <= 400:
+        # the whole-prompt oracle call agrees with the per-token slices
         ref = oracle.dsa_prefill_topk(oracle.dsa_prefill_index_scores(d.index_q, d.index_k, d.w),
                                       topk)
-        short = np.array([Tk - Tq + i + 1 <= topk for i in range(Tq)])
-        assert np.array_equal(idx.cpu().numpy()[short], ref[short])
+        for i in range(Tq):
+            assert np.array_equal(ref[i], oracle_row(d, i, topk)[1])
 
 
 def test_prefill_index_topk_is_deterministic():
@@ -146,18 +164,22 @@ def test_sparse_prefill_bad_index_is_reported():
 
 
 def test_dsa_prefill_path_small():
-    """Indexer + top-k + sparse prefill on the GPU; the oracle runs the same
-    three steps on its own (rows with a tie at the k-th score are skipped)."""
+    """Indexer + top-k + sparse prefill on the GPU against the oracle running
+    the same three steps.  Every row whose GPU selection differs from the
+    oracle's must differ only inside the tie band; those rows are then
+    attended over the oracle's selection, so every row's output is compared."""
     from parity import assert_close
     Tq, Tk, H, topk = 96, 500, 32, 128
     d = mi.make_dsa_prefill(Tq, Tk, H, device=DEV, config=97)
-    gidx, _ = run_index(d, topk)
-    out = run_sparse(d, gidx)
+    gidx, gsc = run_index(d, topk)
+    check_rows(d, gidx, gsc, topk)
     idx = oracle_selection(d, topk)
+    differ = ~(gidx.cpu().numpy() == idx).all(axis=1)
+    used = gidx.clone()
+    used[torch.from_numpy(differ).to(DEV)] = torch.from_numpy(idx[differ]).to(DEV)
+    out = run_sparse(d, used)
     ref = oracle.dsa_prefill_latent(d.q, d.ckv, d.w_kc, d.w_vc, idx, d.gate, d.scale)
-    same = (gidx.cpu().numpy() == idx).all(axis=1)
-    assert same.mean() > 0.9
-    assert_close(out[torch.from_numpy(same).to(DEV)], ref[same], what="DSA prefill path")
+    assert_close(out, ref, what="DSA prefill path")
 
 
 def test_sparse_prefill_full_size_sampled():
@@ -168,13 +190,10 @@ def test_sparse_prefill_full_size_sampled():
     w = mi.WORKLOADS["dsa_prefill_t16384"]
     T, H, K = w["T"], w["H"], w["topk"]
     d = mi.make_dsa_prefill(T, T, H, device=DEV, config=w["config"])
-    gidx, _ = run_index(d, K)
+    gidx, gsc = run_index(d, K)
     rows = [0, 5, 2047, 2048, 9000, T - 1]
-    iq, ik, ww = (oracle._f64(x) for x in (d.index_q[rows], d.index_k, d.w[rows]))
-    sel = np.full((len(rows), K), -1, np.int32)
-    for r, i in enumerate(rows):
-        s = np.einsum("h,hs->s", ww[r], np.maximum(iq[r] @ ik[:i + 1].T, 0.0))
-        sel[r] = oracle.dsa_topk(s, np.array([0, i + 1], dtype=np.int64), K)[0]
+    check_rows(d, gidx, gsc, K, rows)
+    sel = np.stack([oracle_row(d, i, K)[1] for i in rows])
     gidx[rows] = torch.from_numpy(sel).to(DEV)
     out = run_sparse(d, gidx)
     ref = oracle.dsa_prefill_latent(d.q[rows], d.ckv, d.w_kc, d.w_vc,

@@ -1,11 +1,13 @@
 """mla_decode_noalloc: the decode entry point for callers that cannot allocate
 device memory (its scratch is a fixed array inside the library).
 
-It is checked against mla_decode, which takes a caller workspace, on two
-calls in a row with different shapes (the second call runs on scratch that
-still holds the first call's contents), and it must reject a problem whose
-scratch need exceeds the built-in array. Kept in a file that pytest collects
-last.
+Each of two calls in a row with different shapes (the second runs on scratch
+that still holds the first call's contents) is checked against the fp64
+oracle at the parity tolerance, and bit for bit against mla_decode, which
+runs the same kernels on a caller workspace: leftover scratch reaching the
+output would show as a difference even where it is below the tolerance.
+It must also reject a problem whose scratch need exceeds the built-in array.
+Kept in a file that pytest collects last.
 """
 import ctypes
 
@@ -13,6 +15,7 @@ import pytest
 import torch
 
 import mla_inputs as mi
+import oracle
 import mla_family_attention_gb300 as mla
 from mla_family_attention_gb300 import _lib
 from parity import assert_close
@@ -35,17 +38,19 @@ def noalloc_decode(dec, max_seqlen):
     return out
 
 
-def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
+def test_noalloc_matches_oracle_and_workspace_decode_on_two_calls_in_a_row():
     cases = [([3000, 1500, 8192, 64], 8, 8192, 41),   # several chunks per (b,h)
              ([700, 129, 1], 3, 1024, 42)]             # smaller problem on reused scratch
     for lengths, H, max_len, cfg in cases:
         dec = mi.make_decode(lengths, H, True, device="cuda", config=cfg)
         got = noalloc_decode(dec, max_len)
         mla.check_device_status()
-        ref = mla.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, max_len, gate=dec.gate,
-                             scale=dec.scale)
+        ref = oracle.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, dec.gate, dec.scale)
+        assert_close(got, ref, what=f"noalloc vs oracle {lengths}")
+        ws_out = mla.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, max_len, gate=dec.gate,
+                                scale=dec.scale)
         mla.check_device_status()
-        assert_close(got, ref.double().cpu().numpy(), what=f"noalloc vs decode {lengths}")
+        assert torch.equal(got, ws_out), f"noalloc vs workspace decode {lengths}"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
