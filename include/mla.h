@@ -56,7 +56,10 @@ typedef enum {
     MLA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
     MLA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     MLA_ERR_TIMEOUT = 5,      /* a device-side pipeline wait ran out (device status) */
-    MLA_ERR_BAD_INDEX = 6     /* a selected position outside its sequence (device status) */
+    MLA_ERR_BAD_INDEX = 6,    /* a selected position outside its sequence (device status) */
+    MLA_ERR_CHECK = 7         /* bounds-checked debug build (-DMLA_CHECKS) only: a kernel's
+                                 own index or offset check failed (device status; the
+                                 message names the source file and line) */
 } mla_status;
 
 /* Operation ids for mla_workspace_size. */
@@ -69,7 +72,8 @@ enum {
     MLA_OP_LATENT_DECODE = 5,
     MLA_OP_PREFILL_INDEX_TOPK = 6,
     MLA_OP_SPARSE_PREFILL_LATENT = 7,
-    MLA_OP_INDEX_TOPK_FP8 = 8
+    MLA_OP_INDEX_TOPK_FP8 = 8,
+    MLA_OP_GATHER_PROBE = 9     /* timing only (mla_gather_probe); no workspace */
 };
 
 /*
@@ -450,6 +454,25 @@ mla_status mla_debug_set(int knob, long long value);
  */
 mla_status mla_timing_enable(int on);
 mla_status mla_timing_read(int op, double* total_ms, long long* launches);
+
+/*
+ * Measurement aid; the pages have no counterpart.  Gathers, with plain
+ * 16-byte loads and no arithmetic, exactly the rows dsa_sparse_decode reads
+ * for the same arguments: for every sequence b, head h and entry e with
+ * 0 <= topk_idx[b,e] < T_b, the 384-byte key row and 256-byte value row of
+ * that position in the packed cache (k, v, cu_seqlens as in
+ * dsa_sparse_decode).  Entries outside [0, T_b) are skipped.  The words read
+ * are XOR-reduced into one 32-bit value per CTA in `sink` (device memory of
+ * at least mla_gather_probe_blocks() words, caller-owned), so the rate it
+ * reaches (timed under MLA_OP_GATHER_PROBE) is what a gather of these rows
+ * can achieve on this GPU, the ceiling against which the sparse decode's
+ * rate is read.  Asynchronous on `stream`; MLA_ERR_INVALID_ARG for null or
+ * misaligned pointers or bad sizes.
+ */
+int mla_gather_probe_blocks(void);
+mla_status mla_gather_probe(const mla_bf16* k, const mla_bf16* v, const int64_t* cu_seqlens,
+                            const int32_t* topk_idx, int topk, int B, int H, uint32_t* sink,
+                            mla_stream stream);
 
 #ifdef __cplusplus
 }

@@ -541,6 +541,26 @@ def debug_set(knob: int, value: int) -> None:
     _lib.check(lib.mla_debug_set(int(knob), int(value)), lib)
 
 
+def gather_probe(k, v, cu_seqlens, topk_idx, H, sink=None, stream=None):
+    """Measurement aid: gather the rows dsa_sparse_decode(k, v, cu_seqlens,
+    topk_idx, ...) reads, with plain loads and no arithmetic (the achievable
+    gather rate for that kernel).  Returns the per-CTA XOR words (uint32 as
+    int32)."""
+    torch = _torch()
+    lib = _lib.load()
+    _need(topk_idx, "topk_idx", torch.int32)
+    B, topk = topk_idx.shape
+    dev = topk_idx.device
+    _need(k, "k", torch.bfloat16, device=dev)
+    _need(v, "v", torch.bfloat16, device=dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int64, (B + 1,), device=dev)
+    if sink is None:
+        sink = torch.empty(lib.mla_gather_probe_blocks(), dtype=torch.int32, device=dev)
+    _lib.check(lib.mla_gather_probe(_ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(topk_idx), topk, B,
+                                    H, _ptr(sink), _stream(stream)), lib)
+    return sink
+
+
 def timing_enable(on: bool = True) -> None:
     """Record CUDA events around each call's dominant kernel (instrumentation)."""
     lib = _lib.load()

@@ -10,15 +10,18 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libmla_gb300.so")
+# MLA_GB300_LIB names another build of the library to load instead (the
+# bounds-checked debug variant, for its tests).
+LIB_PATH = os.environ.get("MLA_GB300_LIB") or os.path.join(_HERE, "_build", "libmla_gb300.so")
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA, \
-    MLA_ERR_TIMEOUT, MLA_ERR_BAD_INDEX = range(7)
+    MLA_ERR_TIMEOUT, MLA_ERR_BAD_INDEX, MLA_ERR_CHECK = range(8)
 STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT",
-                6: "MLA_ERR_BAD_INDEX"}
+                6: "MLA_ERR_BAD_INDEX", 7: "MLA_ERR_CHECK"}
 OP_PREFILL, OP_DECODE, OP_INDEX_TOPK, OP_SPARSE_DECODE, OP_CACHE_APPEND, \
-    OP_LATENT_DECODE, OP_PREFILL_INDEX_TOPK, OP_SPARSE_PREFILL_LATENT, OP_INDEX_TOPK_FP8 = range(9)
+    OP_LATENT_DECODE, OP_PREFILL_INDEX_TOPK, OP_SPARSE_PREFILL_LATENT, OP_INDEX_TOPK_FP8, \
+    OP_GATHER_PROBE = range(10)
 DEBUG_WAIT_LIMIT_NS, DEBUG_STALL_STAGE, DEBUG_SPARSE_CHUNK, DEBUG_PREFILL_CTAS = 1, 2, 3, 4
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -57,6 +60,8 @@ SIGNATURES = {
     "mla_timing_enable": (_I, [_I]),
     "mla_timing_read": (_I, [_I, ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_longlong)]),
+    "mla_gather_probe_blocks": (_I, []),
+    "mla_gather_probe": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
 }
 
 _lock = threading.Lock()

@@ -14,7 +14,9 @@
 
 namespace {
 
-__device__ int g_status;   // device status word (one per device context)
+// Device status: the first error a kernel recorded, and (bounds-checked
+// debug build) the site of a failed check.  One per device context.
+__device__ int g_status[2];
 
 thread_local std::string t_err;
 std::atomic<long long> g_wait_limit_ns{2000000000LL};
@@ -85,7 +87,7 @@ struct TimerPool {
     std::vector<mla::KernelTimer> ev;
     size_t used = 0;
 };
-constexpr int kOps = 9;   // MLA_OP_PREFILL .. MLA_OP_INDEX_TOPK_FP8
+constexpr int kOps = 10;  // MLA_OP_PREFILL .. MLA_OP_GATHER_PROBE
 TimerPool g_pool[kOps];
 
 // Next event pair for `op` when timing is on, else an empty timer.
@@ -227,12 +229,13 @@ mla_status mla_check_device_status(mla_stream stream) {
     if (s != MLA_OK) return s;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_status, sizeof v);
+    int w[2] = {0, 0};
+    e = cudaMemcpyFromSymbol(w, g_status, sizeof w);
     if (e != cudaSuccess) return cuda_fail(e, "read status");
-    const int zero = 0;
-    e = cudaMemcpyToSymbol(g_status, &zero, sizeof zero);
+    const int zero[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_status, zero, sizeof zero);
     if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    const int v = w[0];
     switch (v) {
         case 0: return MLA_OK;
         case MLA_ERR_TIMEOUT: return fail(MLA_ERR_TIMEOUT, "a device pipeline wait ran out");
@@ -240,6 +243,13 @@ mla_status mla_check_device_status(mla_stream stream) {
             return fail(MLA_ERR_BAD_INDEX, "a selected position lies outside its sequence");
         case MLA_ERR_INVALID_ARG:
             return fail(MLA_ERR_INVALID_ARG, "a sequence length is outside [1, max_seqlen]");
+        case MLA_ERR_CHECK: {
+            static const char* const files[] = {"?", "decode.cu", "prefill.cu", "indexer.cu",
+                                                "latent.cu", "cache.cu", "probe.cu"};
+            const int id = w[1] / 100000, line = w[1] % 100000;
+            return fail(MLA_ERR_CHECK, "bounds check failed at %s:%d",
+                        files[id >= 0 && id <= 6 ? id : 0], line);
+        }
         default: return fail(static_cast<mla_status>(v), "device status %d", v);
     }
 }
@@ -655,3 +665,26 @@ mla_status check_decode_args(const void* q, const void* k, const void* v, const 
 }
 
 }  // namespace mla
+
+extern "C" int mla_gather_probe_blocks(void) {
+    mla::DeviceInfo d;
+    return device_info(&d) == MLA_OK ? mla::gather_probe_blocks(d) : 0;
+}
+
+extern "C" mla_status mla_gather_probe(const mla_bf16* k, const mla_bf16* v,
+                                       const int64_t* cu_seqlens, const int32_t* topk_idx,
+                                       int topk, int B, int H, uint32_t* sink,
+                                       mla_stream stream) {
+    REQUIRE(k && v && cu_seqlens && topk_idx && sink, MLA_ERR_INVALID_ARG, "null pointer");
+    REQUIRE(aligned16(k) && aligned16(v), MLA_ERR_INVALID_ARG,
+            "cache pointers must be 16-byte aligned");
+    REQUIRE(B >= 1 && H >= 1 && topk >= 1 && topk <= mla::kMaxTopk, MLA_ERR_INVALID_ARG,
+            "need B >= 1, H >= 1, 1 <= topk <= %d", mla::kMaxTopk);
+    mla::DeviceInfo d;
+    mla_status s = device_info(&d);
+    if (s != MLA_OK) return s;
+    cudaError_t e = mla::launch_gather_probe(k, v, cu_seqlens, topk_idx, topk, B, H, sink, d,
+                                             take_timer(MLA_OP_GATHER_PROBE),
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "gather probe launch");
+}

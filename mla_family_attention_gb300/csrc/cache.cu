@@ -8,6 +8,7 @@
 // Each (b, h) contributes one contiguous span of Tn*384 key bytes and one of
 // Tn*256 value bytes on both sides, so the copy is a stream of 16-byte
 // vectors: pure HBM traffic (read + write of Tn*640 bytes per (b, h)).
+#define MLA_FILE_ID 5   // site ids of the bounds-checked debug build
 #include "common.cuh"
 #include "kernels.h"
 
@@ -34,6 +35,8 @@ struct AppendParams {
 __device__ __forceinline__ void copy_span(const AppendParams& p, int bh, int64_t s, int r,
                                           int kspan, int span, uint4& x, bool load) {
     if (r >= span) return;
+    // the destination rows s .. s+Tn-1 of (b, h) lie inside the capacity
+    MLA_CHECK(bh >= 0 && bh < p.BH && s >= 0 && s + p.Tn <= p.cap && r >= 0, p.status);
     if (r < kspan) {
         if (load) x = __ldcs(p.k_new + int64_t(bh) * kspan + r);
         else p.k_cache[(int64_t(bh) * p.cap + s) * kKVec + r] = x;

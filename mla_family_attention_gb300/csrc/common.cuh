@@ -8,10 +8,34 @@
 namespace mla {
 
 // Device status codes (the same values as mla_status in include/mla.h).
-enum : int { kStInvalid = 1, kStTimeout = 5, kStBadIndex = 6 };
+enum : int { kStInvalid = 1, kStTimeout = 5, kStBadIndex = 6, kStCheck = 7 };
 
 // First error wins; later ones are dropped until the host clears the word.
 __device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Bounds-checked debug build.  Compiled with -DMLA_CHECKS, MLA_CHECK(cond,
+// status) tests a kernel's own index arithmetic (ring slots, TMEM columns,
+// swizzled shared-memory offsets, histogram bins, output positions) and, when
+// the condition fails, records MLA_ERR_CHECK in the status word and the site
+// (file id * 100000 + line) in the word after it; nothing traps.  Without
+// MLA_CHECKS the macro compiles to nothing.  Each kernel file defines
+// MLA_FILE_ID before including this header.
+#ifndef MLA_FILE_ID
+#define MLA_FILE_ID 0
+#endif
+__device__ __forceinline__ void check_failed(int* status, int site) {
+    if (atomicCAS(status, 0, kStCheck) == 0) atomicExch(status + 1, site);
+}
+#ifdef MLA_CHECKS
+#define MLA_CHECK(cond, status)                                                   \
+    do {                                                                          \
+        if (!(cond)) ::mla::check_failed((status), MLA_FILE_ID * 100000 + __LINE__); \
+    } while (0)
+#else
+#define MLA_CHECK(cond, status) \
+    do {                        \
+    } while (0)
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -34,6 +34,7 @@
 // bounded) for the copies it has in flight and returns.
 #include <cuda_bf16.h>
 
+#define MLA_FILE_ID 1   // site ids of the bounds-checked debug build
 #include "common.cuh"
 #include "kernels.h"
 
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 }
                 if (it == p.stall_stage) continue;   // test hook: withhold this stage
                 const int n = min(R::kSP, w.e1 - e);
+                MLA_CHECK(slot < R::kStages && n >= 1 && n <= R::kSP && w.row0 >= 0, p.status);
                 if (lane == 0) {
                     const int64_t row = w.row0 + e;
                     mbar_arrive_expect_tx(&full[slot], n * (kKRow + kVRow) + (st == 0 ? kKRow : 0));
@@ -281,6 +283,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < R::kSP * 24 / 128; ++i) {
                     const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
+                    MLA_CHECK(slot < R::kStages && j < R::kSP && off + 16 <= kKRow, p.status);
                     if (valid_pos(selk[i], w.T))
                         cp_async16(ks + slot * R::kKStage + j * kKRow + off,
                                    kb + (rbase + selk[i]) * kKRow + off);
@@ -290,6 +293,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < R::kSP * 16 / 128; ++i) {
                     const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
+                    MLA_CHECK(j < R::kSP && off + 16 <= kVRow, p.status);
                     if (valid_pos(selv[i], w.T))
                         cp_async16(vs + slot * R::kVStage + j * kVRow + off,
                                    vb + (rbase + selv[i]) * kVRow + off);
@@ -357,6 +361,7 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < R::kPPG; ++r) {
                     const int pos = g + R::kGroups * r;
+                    MLA_CHECK(pos < R::kSP && slot < R::kStages, p.status);
                     float dot = 0.f;
                     if (ok[r]) {
                         const uint8_t* kr = kst + pos * kKRow;
@@ -457,6 +462,8 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                     ls += wgt * red[u * (kDv + 2) + kDv + 1];
                 }
             }
+            MLA_CHECK(w.b >= 0 && w.b < p.B && w.h >= 0 && w.h < p.H && w.c >= 0 &&
+                          w.c < p.max_chunks && d < kDv, p.status);
             const int64_t slotid = (int64_t(w.b) * p.H + w.h) * p.max_chunks + w.c;
             p.part_acc[slotid * kDv + d] = a;
             if (d == 0) {
@@ -515,7 +522,8 @@ __global__ void __launch_bounds__(1024) decode_items_kernel(const SeqLayout seq,
 // One warp per (b,h): log-sum-exp merge of the chunk partials, then the gate.
 __global__ void __launch_bounds__(256) decode_merge_kernel(
     const float* part_acc, const float* part_ml, const SeqLayout seq, const uint16_t* gate,
-    uint16_t* out, int B, int H, int chunk, int max_chunks, int max_seqlen, int sparse_topk) {
+    uint16_t* out, int B, int H, int chunk, int max_chunks, int max_seqlen, int sparse_topk,
+    int* status) {
     if (threadIdx.x == 0) grid_dep_trigger();
     grid_dep_wait();                           // the partial kernel's chunk states
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -526,6 +534,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(
     if (T < 1 || T > max_seqlen) return;        // reported by the item pass
     const int span = sparse_topk > 0 ? sparse_topk : int(T);
     const int nch = (span + chunk - 1) / chunk;
+    MLA_CHECK(nch >= 1 && nch <= max_chunks, status);
     const int64_t s0 = int64_t(gw) * max_chunks;
     // Chunks go 32 at a time: lane c holds chunk c's (max, sum), and every
     // lane's accumulator loads of the 32 chunks are issued together.
@@ -658,7 +667,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, bool sparse
     e = launch_after_prev(decode_merge_kernel, dim3((warps + 7) / 8), dim3(256), 0, st,
                           static_cast<const float*>(p.part_acc), static_cast<const float*>(p.part_ml),
                           a.seq, a.gate, a.out, a.B, a.H, pl.chunk, pl.max_chunks,
-                          sparse ? (1 << 30) : a.max_seqlen, sparse ? a.topk : 0);
+                          sparse ? (1 << 30) : a.max_seqlen, sparse ? a.topk : 0, dev.status);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -45,6 +45,7 @@
 #include <cuda.h>
 #include <cuda_fp8.h>
 
+#define MLA_FILE_ID 3   // site ids of the bounds-checked debug build
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -57,6 +58,14 @@ constexpr int kTile = 128;                                   // positions per MM
 #define MLA_INDEX_STAGES 6
 #endif
 constexpr int kIStages = MLA_INDEX_STAGES;
+// Tiles the TMA producer prefetches into L2 ahead of its loads (bf16 keys;
+// 0 = none).  On B=8, T=131072: 4 ahead took the scoring kernel from 49.6
+// to 46.7 us and the call from 63.9 to 62.7 us; 8 and 16 ahead were slower
+// (the prefetches share the TMA unit with the loads); FP8 keys gained
+// nothing at any distance, so their producer prefetches nothing.
+#ifndef MLA_INDEX_PREFETCH
+#define MLA_INDEX_PREFETCH 4
+#endif
 constexpr int kAHalf = kTile * 64 * 2;                       // 16 KB: 128 rows x 128 B
 constexpr int kBHalf = kIndexHeads * 64 * 2;                 // 4 KB: 32 rows x 128 B
 constexpr int kStageBytes = 2 * kAHalf;                      // 32 KB of index keys
@@ -86,6 +95,8 @@ struct ScoreCfg {
 };
 
 struct ScoreParams {
+    const void* keys;        // the key rows the tensor map reads (for L2 prefetches)
+    int64_t total_keys;
     const float* w;          // head weights (FP8: with the query scales folded in)
     const float* kscale;     // FP8: per-position key scale, else null
     const int64_t* cu;
@@ -96,6 +107,11 @@ struct ScoreParams {
     long long wait_ns;
     int* status;
 };
+
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ uint32_t okey(float f) {
     const uint32_t u = __float_as_uint(f);
@@ -223,6 +239,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 }
                 last_use[(seg - 1) & 1] = j;
                 const int row = row0 + t * kTile;
+                if (!kFp8 && MLA_INDEX_PREFETCH > 0 && t + MLA_INDEX_PREFETCH < t_end) {
+                    // the key rows MLA_INDEX_PREFETCH tiles further on (past a
+                    // sequence boundary they need not be that tile's rows: the
+                    // prefetch is then wasted, and clamped to the key array)
+                    const int64_t r0 = int64_t(row) + int64_t(MLA_INDEX_PREFETCH) * kTile;
+                    const int64_t r1 = r0 + kTile < p.total_keys ? r0 + kTile : p.total_keys;
+                    if (r1 > r0 && r0 >= 0)
+                        prefetch_l2_bytes(static_cast<const uint8_t*>(p.keys) + r0 * (C::kStage / kTile),
+                                          uint32_t((r1 - r0) * (C::kStage / kTile)));
+                }
+                MLA_CHECK(slot < C::kStages && row >= 0, p.status);
                 uint8_t* st = smem + slot * C::kStage;
                 mbar_arrive_expect_tx(&full[slot], C::kStage);
                 tma_load_2d_hint(st, &kmap, 0, row, &full[slot], stream_policy);
@@ -345,6 +372,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) continue;                     // (no barrier inside a tile's work)
             tc_fence_after();
+            MLA_CHECK(acc < kAcc && uint32_t(acc * 32 + 32) <= kTmemCols && r < kTile, p.status);
             float d[32];
             tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + acc * 32, d);
             tmem_ld_wait();
@@ -357,11 +385,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int h = 0; h < kIndexHeads; ++h) s = fmaf(wr[h], fmaxf(d[h], 0.f), s);
             if (kFp8) s *= ksc;
             s += 0.0f;                             // -0 -> +0: equal scores compare equal
+            MLA_CHECK(!in || (pos >= 0 && pos < p.stride && b < p.B), p.status);
             if (in) p.scores[size_t(b) * p.stride + pos] = s;
             // histogram of the top 11 key bits, one atomic per distinct bin per warp
             const unsigned mask = __ballot_sync(0xffffffffu, in);
             if (in) {
                 const unsigned bin = okey(s) >> 21;
+                MLA_CHECK(bin < unsigned(kBins), p.status);
                 const unsigned peers = __match_any_sync(mask, bin);
                 if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], unsigned(__popc(peers)));
             }
@@ -612,6 +642,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
         load16(s, i0, hi, v);
 #pragma unroll
         for (int u = 0; u < kSelPer; ++u) vals[u * 1024 + tid] = v[u];
+        MLA_CHECK((kSelPer - 1) * 1024 + tid < kStep, p.status);
     };
     // level-1 bins and this CTA's scores: both loads are issued before either
     // is stored, so their latencies overlap
@@ -667,6 +698,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
     cluster_sync();                                 // (2) level-2 totals everywhere
     int bin2, above2;
     find_bin(sum2, kBins, K - above1, sh, &bin2, &above2);
+    MLA_CHECK(bin1 >= 0 && bin1 < kBins && bin2 >= 0 && bin2 < kBins, p.status);
     const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
     // Keys are compared by their top 32 - kshift bits from here on.  When
     // every key of the level-2 bin is kept (the usual case: the bin holds
@@ -681,6 +713,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
         cluster_sync();                             // (3) level-3 totals everywhere
         int bin3, above3;
         find_bin(sum3, 1024, K - above1 - above2, sh, &bin3, &above3);
+        MLA_CHECK(bin3 >= 0 && bin3 < 1024, p.status);
         kth = (pre << 10) | uint32_t(bin3);
         kshift = 0;
         need_eq -= above3;
@@ -995,6 +1028,7 @@ __global__ void __launch_bounds__(1024) dsa_prefill_topk_kernel(const PrefillTop
             load16(s, t0 + tid * kSelPer, n, v);
 #pragma unroll
             for (int u = 0; u < kSelPer; ++u) vals[u * 1024 + tid] = v[u];
+        MLA_CHECK((kSelPer - 1) * 1024 + tid < kStep, p.status);
         };
         __syncthreads();                                    // previous row fully consumed
         if (resident) stage(0);
@@ -1200,8 +1234,8 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
                             kIndexDim * 2, 64, kIndexHeads);
     if (e != cudaSuccess) return e;
 
-    ScoreParams p{a.w, nullptr, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
-                  kn.wait_limit_ns, dev.status};
+    ScoreParams p{a.index_k, a.total_keys, a.w, nullptr, a.cu, tiles, scores, hist, a.B,
+                  score_stride(a.max_seqlen), kn.wait_limit_ns, dev.status};
     return launch_score_topk<false>(a, kmap, qmap, p, dev, tm, st);
 }
 
@@ -1261,8 +1295,8 @@ cudaError_t launch_index_topk_fp8(const IndexArgs& a, const IndexFp8Args& f, con
     if (e != cudaSuccess) return e;
     e = encode_tmap_2d_u8(&qmap, q8, 128, uint64_t(qrows), 128, 128, kIndexHeads);
     if (e != cudaSuccess) return e;
-    ScoreParams p{wq, f.kscale, a.cu, tiles, scores, hist, a.B, score_stride(a.max_seqlen),
-                  kn.wait_limit_ns, dev.status};
+    ScoreParams p{f.k8, a.total_keys, wq, f.kscale, a.cu, tiles, scores, hist, a.B,
+                  score_stride(a.max_seqlen), kn.wait_limit_ns, dev.status};
     return launch_score_topk<true>(a, kmap, qmap, p, dev, tm, st);
 }
 

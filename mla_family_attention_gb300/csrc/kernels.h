@@ -234,4 +234,12 @@ cudaError_t launch_quantize_latent(const uint16_t* ckv, uint8_t* rec, int64_t ro
 cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& p, const DeviceInfo& dev,
                                  const Knobs& kn, const KernelTimer& tm, cudaStream_t st);
 
+// --------------------------- measurement aid ---------------------------
+// Plain gather of the rows dsa_sparse_decode reads (XOR-reduced into one
+// word per CTA of `sink`, gather_probe_blocks(dev) words).
+int gather_probe_blocks(const DeviceInfo& dev);
+cudaError_t launch_gather_probe(const uint16_t* k, const uint16_t* v, const int64_t* cu,
+                                const int32_t* idx, int topk, int B, int H, uint32_t* sink,
+                                const DeviceInfo& dev, const KernelTimer& tm, cudaStream_t st);
+
 }  // namespace mla

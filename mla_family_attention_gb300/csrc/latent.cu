@@ -44,6 +44,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#define MLA_FILE_ID 4   // site ids of the bounds-checked debug build
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -429,6 +430,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                         break;
                     }
                     uint8_t* dst = ring + slot * kSlot + sw;
+                    MLA_CHECK(slot < kSlots && sw + 7 * 1024 + 16 <= uint32_t(kHalf), p.status);
                     if (i == 0) {                      // shared-key features 512..575
 #pragma unroll
                         for (int m = 0; m < 4; ++m)
@@ -486,6 +488,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                         break;
                     }
                     uint8_t* dst = ring + slot * kSlot;
+                    MLA_CHECK(slot < kSlots && row >= 0, p.status);
                     if (i == 0) {              // shared-key features 512..575
                         mbar_arrive_expect_tx(&full[slot], kHalf);
                         tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
@@ -547,6 +550,9 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                     if (kSrc == kSrcGather) fence_async_smem();
                     tc_fence_after();
                     const uint64_t b0 = kdesc + uint32_t(slot) * kSlotU;
+                    MLA_CHECK(slot < kSlots && (8 * H + 128) * 128 <= kQBytes &&
+                                  uint32_t(j & 1) * kLT + kLT <= uint32_t(kColO),
+                              p.status);
                     if (i == 0) {                        // shared-key features
                         const uint64_t a0 = qdesc + 8 * qblk;
 #pragma unroll
@@ -613,6 +619,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint64_t a0 = cdesc + uint32_t(sl) * kSlotU;
+                    MLA_CHECK(sl < kSlots && kColO + uint32_t((u + 1) * H) <= 512u, p.status);
                     const uint32_t d = tmem + kColO + uint32_t(u * H);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -747,6 +754,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 w[i] = pack2(a, bq);
             }
             l += ps_sum;
+            MLA_CHECK(!real || (r >> 3) * 1024 + (r & 7) * 128 + 128 <= kPBytes, p.status);
             if (real) {
                 uint8_t* row = ps + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
@@ -779,6 +787,8 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 tc_fence_after();
                 for (int uu = 0; uu < 2; ++uu) {
                     const int u = 2 * half + uu, dim = u * 128 + quad * 32 + lane;
+                    MLA_CHECK(dim < kLatent && b < B && kColO + uint32_t((u + 1) * H) <= 512u,
+                              p.status);
                     for (int c0 = 0; c0 < H; c0 += 16) {
                         float v[16];
                         tmem_ld16(lane_base + kColO + u * H + c0, v);

@@ -46,6 +46,7 @@
 // MMA lane waits for its last commit, and TMEM is released before exit.
 #include <cuda_bf16.h>
 
+#define MLA_FILE_ID 2   // site ids of the bounds-checked debug build
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -236,6 +237,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int j = 0; j < n_kv; ++j) {
                 if (*abort_flag) break;
                 const int ks = j % C::kKStages, kr = j / C::kKStages;
+                MLA_CHECK(ks < C::kKStages && (ks + 1) * C::kKTile <= C::kKStages * C::kKTile,
+                          p.status);
                 if (kr > 0 && !wait(&kempty[ks], (kr - 1) & 1)) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
@@ -254,6 +257,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
+                MLA_CHECK(vs < C::kVStages && y >= 0, p.status);
                 mbar_arrive_expect_tx(&vfull[vs], C::kVTile);
                 for (int c = 0; c < C::kVBoxes; ++c)
                     tma_load_3d(vsm + vs * C::kVTile + c * C::kVBox, &vmap,
@@ -317,6 +321,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc_fence_after();
                 const uint32_t kb = smem_u32(ksm + ks * C::kKTile);
                 const uint32_t qb = smem_u32(qsm);
+                MLA_CHECK(kColS + uint32_t(sb) * 128 + 128 <= kColO, p.status);
                 const uint32_t d = tmem + kColS + uint32_t(sb) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 12; ++kk) {
@@ -407,6 +412,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             ok = __all_sync(0xffffffffu, ok);
             const uint32_t sb = tmem + lane_off + kColS + uint32_t(buf) * 128;
+            // this thread's 64 score columns and its 64 output columns lie
+            // inside its buffer and inside O
+            MLA_CHECK(buf < kNB && kColS + uint32_t(buf) * 128 + half * 64 + 64 <= kColO &&
+                          kColO + half * 64 + 64 <= kCols && r < kBM,
+                      p.status);
             float s[64];
             float mloc = -INFINITY;
             if (ok) {

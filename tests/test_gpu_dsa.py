@@ -66,6 +66,8 @@ def run_index(d, lengths, topk, max_seqlen=None):
     ([3000, 129, 777], 64),
     ([400], 1),
     ([131072], 2048),
+    ([2100 + 37 * i for i in range(40)], 2048),   # many sequences per CTA, ragged tails
+    ([70000, 1, 2049, 130000, 5, 9000, 2048, 33000], 1000),
 ])
 def test_index_topk_matches_oracle(lengths, topk):
     d = mi.make_dsa(lengths, device=DEV, config=51, with_main=False)
