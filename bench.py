@@ -409,6 +409,42 @@ class DsaWork:
         del self.d, self.idx, self.out, self.ws_i, self.ws_s
 
 
+class GatherProbeWork:
+    """Reference rate for the sparse decode: the same rows of the same cache
+    (selected once by the GPU indexer, outside the timed region), gathered
+    with plain 16-byte loads and no arithmetic (mla_gather_probe)."""
+
+    def __init__(self, name, dev, batch=0):
+        import mla_family_attention_gb300 as mla
+        from mla_family_attention_gb300 import _lib
+        self.mla, self.lib = mla, _lib
+        w = mi.WORKLOADS[name]
+        lengths = mi.workload_lengths(name)
+        if batch:
+            lengths = lengths[:batch]
+        self.name, self.lengths, self.H, self.B = name, lengths, w["H"], len(lengths)
+        self.topk = w["topk"]
+        self.d = mi.make_dsa(lengths, H=self.H, device=dev, config=w["config"])
+        cu = mi.cu_from_lengths(lengths).to(dev)
+        self.idx = mla.dsa_index_topk(self.d.index_q, self.d.index_k, self.d.w, cu,
+                                      max(lengths), self.topk)
+        mla.check_device_status()
+        self.sink = torch.empty(_lib.load().mla_gather_probe_blocks(), dtype=torch.int32,
+                                device=dev)
+        self.work = acc.sparse_kv_bytes(lengths, self.H, self.topk)
+        self.unit, self.bound = "GB/s", "hbm"
+        self.launches_per_step = 1
+        self.kernels = [(_lib.OP_GATHER_PROBE, "gather_probe_kernel", self.work)]
+
+    def step(self, stream):
+        m = self.d.main
+        self.mla.gather_probe(m.k, m.v, m.cu_seqlens, self.idx, self.H, sink=self.sink,
+                              stream=stream)
+
+    def free(self):
+        del self.d, self.idx, self.sink
+
+
 class IndexWork:
     """The DSA indexer alone: scores and top-k (rows a7-a8)."""
 
@@ -514,6 +550,13 @@ class PrefillWork:
         in_bytes = sum(t.numel() * t.element_size() for t in
                        (self.pf.q, self.pf.k, self.pf.v) + ((self.pf.gate,) if w["gated"] else ()))
         self.flush_l2 = in_bytes < 4 * (129 << 20)
+        if self.flush_l2:
+            # a short prompt's 0.5 GFLOP take microseconds: its kernel is read
+            # against the I/O floor (inputs read once, outputs written once)
+            # at the HBM peak, not against the tensor peak
+            io = in_bytes + self.out.numel() * self.out.element_size()
+            self.bound = "hbm"
+            self.kernels = [(_lib.OP_PREFILL, "mla_prefill_kernel", io, "hbm")]
 
     def step(self, stream):
         pf = self.pf
@@ -818,7 +861,7 @@ WORK_KINDS = {"decode": DecodeWork, "latent_decode": LatentDecodeWork,
               "dsa_prefill": DsaPrefillWork, "index_fp8": IndexFp8Work,
               "latent_decode_fp8": LatentDecodeFp8Work, "dsa": DsaWork, "index": IndexWork,
               "prefill": PrefillWork, "chunked_prefill": ChunkedPrefillWork,
-              "decode_cached": DecodeCachedWork}
+              "decode_cached": DecodeCachedWork, "gather_probe": GatherProbeWork}
 
 
 def _time_e2e(one, work, dev, world, steps, h2d, d2h):
@@ -906,7 +949,7 @@ def _scale(work):
 def roofline(work, kern):
     """Roofline object for the dominant (longest) kernel of a step."""
     peak, unit, peak_kind = peaks(work.bound)
-    sc = _scale(work)
+    sc = 1e12 if work.bound == "tensor" else 1e9
     kname, k_ms, units, _ = max((k for k in kern if k[3] == work.bound), key=lambda x: x[1])
     achieved = units / (k_ms * 1e-3) / sc
     nominal = 2250.0 if work.bound == "tensor" else 7900.0

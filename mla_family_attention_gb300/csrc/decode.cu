@@ -47,6 +47,9 @@ constexpr int kDenseSP = 64;                    // positions per dense pipeline 
 #ifndef MLA_SPARSE_STAGE_POS
 #define MLA_SPARSE_STAGE_POS 64                 // positions per sparse pipeline stage
 #endif
+#ifndef MLA_SPARSE_PRODUCER_WARPS
+#define MLA_SPARSE_PRODUCER_WARPS 8             // gathering warps of the sparse decode
+#endif
 #ifndef MLA_SPARSE_CONSUMER_WARPS
 #define MLA_SPARSE_CONSUMER_WARPS 8             // consumer warps of the sparse decode
 #endif
@@ -57,7 +60,8 @@ constexpr int kDenseSP = 64;                    // positions per dense pipeline 
 // to arrive and a stage is only complete when its slowest row has landed.
 template <bool kSparse>
 struct Roles {
-    static constexpr int kProducerWarps = kSparse ? 4 : 1;
+    static constexpr int kProducerWarps = kSparse ? MLA_SPARSE_PRODUCER_WARPS : 1;
+    static constexpr int kPT = 32 * kProducerWarps;            // producer threads
     static constexpr int kConsumerWarps = kSparse ? MLA_SPARSE_CONSUMER_WARPS : 8;
     static constexpr int kGroups = kConsumerWarps * 4;       // 8-lane groups
     static constexpr int kThreads = 32 * (kProducerWarps + kConsumerWarps);
@@ -79,6 +83,9 @@ constexpr size_t smem_bytes() {
            2 * R::kStages * 8 + 16;
 }
 
+static_assert((Roles<true>::kSP * 24) % Roles<true>::kPT == 0 &&
+                  (Roles<true>::kSP * 16) % Roles<true>::kPT == 0,
+              "a stage's key and value pieces must split evenly over the producer threads");
 static_assert(Roles<true>::kPPG * Roles<true>::kGroups == Roles<true>::kSP &&
                   Roles<false>::kPPG * Roles<false>::kGroups == Roles<false>::kSP &&
                   Roles<true>::kConsumerWarps >= 4,
@@ -237,10 +244,10 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
     }
     if (kSparse && warp < R::kProducerWarps) {
         // ------------------------ producers (sparse) ------------------------
-        // 128 threads gather the selected rows in 16-byte pieces: a stage holds
+        // kPT threads gather the selected rows in 16-byte pieces: a stage holds
         // 64 x 24 key pieces and 64 x 16 value pieces; consecutive threads take
         // consecutive pieces of a row.  Each thread's copies complete with one
-        // arrival on the stage's barrier (expected count 128).
+        // arrival on the stage's barrier (expected count kPT).
         const int pt = threadIdx.x;
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k);
         const uint8_t* vb = reinterpret_cast<const uint8_t*>(p.v);
@@ -258,15 +265,15 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                 // slot, so their latency hides behind the wait.
                 const int n = min(R::kSP, w.e1 - e);
                 const int32_t* ix = p.idx + int64_t(w.b) * p.topk + e;
-                int selk[R::kSP * 24 / 128], selv[R::kSP * 16 / 128];
+                int selk[R::kSP * 24 / R::kPT], selv[R::kSP * 16 / R::kPT];
 #pragma unroll
-                for (int i = 0; i < R::kSP * 24 / 128; ++i) {
-                    const int j = (pt + 128 * i) / 24;
+                for (int i = 0; i < R::kSP * 24 / R::kPT; ++i) {
+                    const int j = (pt + R::kPT * i) / 24;
                     selk[i] = j < n ? ix[j] : -1;
                 }
 #pragma unroll
-                for (int i = 0; i < R::kSP * 16 / 128; ++i) {
-                    const int j = (pt + 128 * i) >> 4;
+                for (int i = 0; i < R::kSP * 16 / R::kPT; ++i) {
+                    const int j = (pt + R::kPT * i) >> 4;
                     selv[i] = j < n ? ix[j] : -1;
                 }
                 if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
@@ -281,8 +288,8 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                                reinterpret_cast<const uint8_t*>(p.q) +
                                    (int64_t(w.b) * p.H + w.h) * kKRow + pt * 16);
 #pragma unroll
-                for (int i = 0; i < R::kSP * 24 / 128; ++i) {
-                    const int c = pt + 128 * i, j = c / 24, off = (c - j * 24) * 16;
+                for (int i = 0; i < R::kSP * 24 / R::kPT; ++i) {
+                    const int c = pt + R::kPT * i, j = c / 24, off = (c - j * 24) * 16;
                     MLA_CHECK(slot < R::kStages && j < R::kSP && off + 16 <= kKRow, p.status);
                     if (valid_pos(selk[i], w.T))
                         cp_async16(ks + slot * R::kKStage + j * kKRow + off,
@@ -291,8 +298,8 @@ __global__ void __launch_bounds__(Roles<kSparse>::kThreads, 1)
                         report(p.status, kStBadIndex);
                 }
 #pragma unroll
-                for (int i = 0; i < R::kSP * 16 / 128; ++i) {
-                    const int c = pt + 128 * i, j = c >> 4, off = (c & 15) * 16;
+                for (int i = 0; i < R::kSP * 16 / R::kPT; ++i) {
+                    const int c = pt + R::kPT * i, j = c >> 4, off = (c & 15) * 16;
                     MLA_CHECK(j < R::kSP && off + 16 <= kVRow, p.status);
                     if (valid_pos(selv[i], w.T))
                         cp_async16(vs + slot * R::kVStage + j * kVRow + off,

@@ -100,6 +100,11 @@ struct PrefillParams {
     int* status;
 };
 
+// Prefetch the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
@@ -171,7 +176,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int n_kv = min((p.Tk + kBN - 1) / kBN, kmax / kBN + 1);
     const int n_full = min((P0 + q0 + 1) / kBN, p.Tk / kBN);    // tiles visible to every row
 
+    // One CTA per tile (no pair): thread 0, the TMA producer, requests the
+    // query tile and the first key and value tiles as soon as their barriers
+    // exist, before the CTA-wide set-up barrier (the loads then overlap the
+    // TMEM allocation); a short prompt's whole run is a few such latencies.
+    const bool early = !kPair && n_kv > 0;
     if (threadIdx.x == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        tma_prefetch_desc(&qmap);
         for (int i = 0; i < C::kKStages; ++i) {
             mbar_init(&kfull[i], 1);
             mbar_init(&kempty[i], 1);
@@ -194,6 +207,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(qkdone, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        if (early) {
+            mbar_arrive_expect_tx(qready, kQTile);
+            for (int c = 0; c < 3; ++c)
+                tma_load_3d(qsm + c * kQBox, &qmap, c * 64, q0, bh, qready);
+            mbar_arrive_expect_tx(&kfull[0], C::kKTile);
+            for (int c = 0; c < 3; ++c)
+                tma_load_3d(ksm + c * C::kKBox, &kmap, c * 64, 0, bh, &kfull[0]);
+            mbar_arrive_expect_tx(&vfull[0], C::kVTile);
+            for (int c = 0; c < C::kVBoxes; ++c)
+                tma_load_3d(vsm + c * C::kVBox, &vmap, c * 64, 0, bh, &vfull[0]);
+        }
     }
     if (warp == 1) {
         if (kPair) tmem_alloc_pair(tmem_holder, kCols);
@@ -225,16 +249,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 0) {
         // --------------------------------- TMA ---------------------------------
         if (lane == 0) {
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            tma_prefetch_desc(&qmap);
             int kf[C::kKStages] = {}, vf[C::kVStages] = {};
             const int krow0 = kPair ? 64 * int(rank) : 0;       // this CTA's key rows of a tile
-            // this CTA's 128 query rows (rows at or past Tq arrive as zeros)
-            mbar_arrive_expect_tx(qready, kQTile);
-            for (int c = 0; c < 3; ++c)
-                tma_load_3d(qsm + c * kQBox, &qmap, c * 64, q0, bh, qready);
-            for (int j = 0; j < n_kv; ++j) {
+            if (early) {
+                kf[0] = vf[0] = 1;                              // requested before the set-up barrier
+            } else {
+                // this CTA's 128 query rows (rows at or past Tq arrive as zeros)
+                mbar_arrive_expect_tx(qready, kQTile);
+                for (int c = 0; c < 3; ++c)
+                    tma_load_3d(qsm + c * kQBox, &qmap, c * 64, q0, bh, qready);
+            }
+            for (int j = early ? 1 : 0; j < n_kv; ++j) {
                 if (*abort_flag) break;
                 const int ks = j % C::kKStages, kr = j / C::kKStages;
                 MLA_CHECK(ks < C::kKStages && (ks + 1) * C::kKTile <= C::kKStages * C::kKTile,
@@ -399,6 +424,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int row = q0 + r;                             // query index
         const int qa = P0 + row;                            // absolute position
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        // this thread's output row and its 64 gate logits (128 bytes): the
+        // logits are prefetched into L2 now, so the epilogue's loads of them
+        // do not wait on HBM after the last P.V
+        const size_t orow = (size_t(b) * p.Tq + size_t(row < p.Tq ? row : 0)) * p.H + h;
+        const uint4* g = p.gate ? reinterpret_cast<const uint4*>(p.gate + orow * kDv) + half * 8
+                                : nullptr;
+        if (g && row < p.Tq) prefetch_l2_line(g);
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
@@ -500,6 +532,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (lane == 0) arrive_mma(&pfull[buf]);
         }
         // ---- epilogue: O / l * sigmoid(gate) -> bf16 ----
+        // the gate logits are loaded before the wait for the last P.V, so
+        // their latency overlaps it
+        uint4 gl[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            gl[k] = (g && row < p.Tq) ? __ldg(g + k) : make_uint4(0u, 0u, 0u, 0u);
         bool fin = ok && wait(ofinal, 0);
         fin = __all_sync(0xffffffffu, fin);
         if (!fin && ok) report(p.status, kStTimeout);
@@ -509,10 +547,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (fin) {
             tc_fence_after();
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const size_t orow = (size_t(b) * p.Tq + size_t(row < p.Tq ? row : 0)) * p.H + h;
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDv) + half * 8;
-            const uint4* g = p.gate ? reinterpret_cast<const uint4*>(p.gate + orow * kDv) + half * 8
-                                    : nullptr;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float o[32];
@@ -525,7 +560,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) z[e] = o[u * 8 + e] * inv;
                         if (g) {
-                            const uint4 gw = __ldg(g + c * 4 + u);
+                            const uint4 gw = gl[c * 4 + u];
                             const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {

@@ -297,6 +297,10 @@ WORKLOADS = {
     # history and attending over its own top-2048 of the latent cache
     "dsa_prefill_t16384": dict(kind="dsa_prefill", config=6, B=1, H=96, T=16384, topk=2048,
                                gated=True),
+    # a reference rate, not a step of the method: the rows the DSA decode's
+    # sparse attention reads, gathered with plain loads and no arithmetic
+    "dsa_gather_probe_b8_t131072": dict(kind="gather_probe", config=4, B=8, H=96, T=131072,
+                                        topk=2048),
     # smaller cases of the same kernels, a few GB on the device, for ncu captures
     "dsa_decode_b2_t16384": dict(kind="dsa", config=4, B=2, H=96, T=16384, topk=2048,
                                  profile_only=True),
