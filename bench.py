@@ -556,7 +556,7 @@ class PrefillWork:
             # at the HBM peak, not against the tensor peak
             io = in_bytes + self.out.numel() * self.out.element_size()
             self.bound = "hbm"
-            self.kernels = [(_lib.OP_PREFILL, "mla_prefill_kernel", io, "hbm")]
+            self.kernels = [(_lib.OP_PREFILL, "mla_prefill_kernel<short>", io, "hbm")]
 
     def step(self, stream):
         pf = self.pf

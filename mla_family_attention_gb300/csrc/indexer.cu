@@ -527,7 +527,10 @@ __device__ __forceinline__ void find_bin(const unsigned* hist, int nbins, int K,
 
 constexpr int kSelPer = 16;                        // positions per thread per pass step
 constexpr int kStep = 1024 * kSelPer;              // positions per CTA per pass step
-constexpr int kCluster = 8;                        // CTAs cooperating on one sequence
+#ifndef MLA_TOPK_CLUSTER
+#define MLA_TOPK_CLUSTER 8
+#endif
+constexpr int kCluster = MLA_TOPK_CLUSTER;         // CTAs cooperating on one sequence
 
 // Load this thread's 16 consecutive scores (positions i0..i0+15, rows padded
 // to 16 bytes so the float4 reads stay inside the row).
@@ -601,8 +604,8 @@ constexpr size_t kTopkSmem = size_t(kStep) * 4 + (kBins + 1024 + kBins + kBins) 
 // writes its counts of keys above and equal to the k-th key into every CTA,
 // and after a last barrier writes its kept positions at their place in the
 // ascending output.  Three or four cluster barriers in all.
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(1024)
-    dsa_topk_cluster_kernel(const TopkParams p) {
+// (cluster size set at launch: 16 is a non-portable size)
+__global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams p) {
     extern __shared__ float4 topk_dyn[];
     // scores of one step: element u of thread t (position t0 + 16t + u) at
     // vals[u*1024 + t], so a warp's accesses hit 32 different banks
@@ -1211,8 +1214,28 @@ static cudaError_t launch_score_topk(const IndexArgs& a, const CUtensorMap& kmap
     e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kTopkSmem));
     if (e != cudaSuccess) return e;
-    e = launch_after_prev(dsa_topk_cluster_kernel, dim3(kCluster, a.B), dim3(1024), kTopkSmem, st,
-                          tp);
+    if (kCluster > 8) {
+        e = cudaFuncSetAttribute(dsa_topk_cluster_kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = kCluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kCluster, a.B);
+        cfg.blockDim = dim3(1024);
+        cfg.dynamicSmemBytes = kTopkSmem;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, dsa_topk_cluster_kernel, tp);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

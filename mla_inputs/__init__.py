@@ -304,6 +304,8 @@ WORKLOADS = {
     # smaller cases of the same kernels, a few GB on the device, for ncu captures
     "dsa_decode_b2_t16384": dict(kind="dsa", config=4, B=2, H=96, T=16384, topk=2048,
                                  profile_only=True),
+    "dsa_gather_probe_b2_t16384": dict(kind="gather_probe", config=4, B=2, H=96, T=16384,
+                                       topk=2048, profile_only=True),
     "prefill_b1_h8_t16384": dict(kind="prefill", config=3, B=1, H=8, T=16384, gated=True,
                                  profile_only=True),
     "dsa_prefill_t4096": dict(kind="dsa_prefill", config=6, B=1, H=96, T=4096, topk=2048,
