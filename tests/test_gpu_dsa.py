@@ -184,3 +184,34 @@ def test_dsa_decode_full_size_sampled():
             assert_close(out[b:b + 1, h * 128:(h + 1) * 128], ref, what=f"b{b} h{h}")
     del d, m
     torch.cuda.empty_cache()
+
+
+def test_gather_probe_reads_exactly_the_selected_rows():
+    """The measurement aid reads each selected (key, value) row pair once: the
+    XOR of all its per-CTA words equals the XOR of every 32-bit word of the
+    rows the selection names (entries -1 and past T_b skipped)."""
+    lengths = [3000, 700, 1]
+    H, topk = 4, 256
+    d = mi.make_dsa(lengths, H=H, device=DEV, config=57)
+    m = d.main
+    g = torch.Generator(device="cpu").manual_seed(12)
+    idx = torch.full((3, topk), -1, dtype=torch.int32)
+    idx[0] = torch.randperm(3000, generator=g)[:topk].to(torch.int32)
+    idx[1, :200] = torch.randperm(700, generator=g)[:200].to(torch.int32)
+    idx[2, :1] = 0
+    idx[1, 250] = 700                              # past the sequence: skipped
+    sink = mla.gather_probe(m.k, m.v, m.cu_seqlens, idx.to(DEV), H)
+    torch.cuda.synchronize()
+    got = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))
+    k32 = m.k.view(torch.int32).cpu().numpy().view(np.uint32)
+    v32 = m.v.view(torch.int32).cpu().numpy().view(np.uint32)
+    want = np.uint32(0)
+    cu = [0, 3000, 3700, 3701]
+    for b, T in enumerate(lengths):
+        for h in range(H):
+            for s in idx[b].tolist():
+                if 0 <= s < T:
+                    row = cu[b] * H + h * T + s
+                    want ^= np.bitwise_xor.reduce(k32[row * 96:(row + 1) * 96])
+                    want ^= np.bitwise_xor.reduce(v32[row * 64:(row + 1) * 64])
+    assert got == want
