@@ -171,3 +171,17 @@ def test_sparse_all_skipped_gives_zero():
     out = mla.dsa_sparse_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, idx, gate=dec.gate)
     mla.check_device_status()
     assert torch.all(out == 0)
+
+
+def test_decode_one_million_positions():
+    """One sequence of 1,048,576 cached positions (2 heads): 1,024 split-KV
+    chunks per head merged by log-sum-exp."""
+    from parity import assert_close
+    T = 1 << 20
+    dec = mi.make_decode([T, 300], 2, True, device="cuda", config=47)
+    out = mla.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, T, gate=dec.gate, scale=dec.scale)
+    mla.check_device_status()
+    ref = oracle.mla_decode(dec.q, dec.k, dec.v, dec.cu_seqlens, dec.gate, dec.scale)
+    assert_close(out, ref, what="decode over 1M positions")
+    del dec
+    torch.cuda.empty_cache()

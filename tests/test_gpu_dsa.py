@@ -215,3 +215,17 @@ def test_gather_probe_reads_exactly_the_selected_rows():
                     want ^= np.bitwise_xor.reduce(k32[row * 96:(row + 1) * 96])
                     want ^= np.bitwise_xor.reduce(v32[row * 64:(row + 1) * 64])
     assert got == want
+
+
+@pytest.mark.parametrize("lengths", [[300000, 2049], [1048576]])
+def test_index_topk_long_contexts(lengths):
+    """Sequences whose share of the 8-CTA top-k exceeds one 16,384-score
+    shared-memory step (every pass then re-stages its scores from L2), up to
+    the million-position context the DSA post's complexity section takes."""
+    d = mi.make_dsa(lengths, device=DEV, config=58, with_main=False)
+    idx, sc = run_index(d, lengths, 2048)
+    cu = mi.cu_from_lengths(lengths)
+    s64 = oracle.dsa_index_scores(d.index_q, d.index_k, d.w, cu)
+    check_selection(idx, sc, s64, lengths, 2048)
+    del d
+    torch.cuda.empty_cache()
