@@ -497,20 +497,58 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
     return r;
 }
 
+// Distributed shared memory: the address of `p` in cluster CTA `rank`, and
+// remote add / store / load through it.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ void dsmem_add(uint32_t addr, unsigned v) {
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned dsmem_ld(uint32_t addr) {
+    unsigned v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Bin holding the K-th largest key given a histogram (bins ordered by key):
-// count(bins above) < K <= count(bins at or above).
-__device__ __forceinline__ void find_bin(const unsigned* hist, int nbins, int K, int* sh,
-                                         int* out_bin, int* out_above) {
+// count(bins above) < K <= count(bins at or above).  With own > 0 the
+// histogram is a cluster total kept by owners: bin i in CTA i / own.  Each
+// thread then fetches its bins from their owner and leaves a copy in its own
+// `hist`, so the whole total can be read locally after the call.
+__device__ __forceinline__ void find_bin(unsigned* hist, int nbins, int K, int* sh,
+                                         int* out_bin, int* out_above, int own = 0,
+                                         uint32_t rank = 0) {
     const int per = nbins / 1024;                  // 1 or 2 bins per thread
     const int hi = nbins - 1 - int(threadIdx.x) * per;
+    unsigned c2[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        if (i < per) {
+            const uint32_t r = own ? uint32_t((hi - i) / own) : rank;
+            c2[i] = r != rank ? dsmem_ld(dsmem_addr(&hist[hi - i], r)) : hist[hi - i];
+        }
     int local = 0;
-    for (int i = 0; i < per; ++i) local += int(hist[hi - i]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        if (i < per) {
+            if (own && uint32_t((hi - i) / own) != rank) hist[hi - i] = c2[i];
+            local += int(c2[i]);
+        }
     int total;
     const int above = block_excl_scan(local, sh, &total);
     if (above < K && K <= above + local) {
         int cum = above;
         for (int i = 0; i < per; ++i) {
-            const int c = int(hist[hi - i]);
+            const int c = int(c2[i]);
             if (cum + c >= K) {
                 sh[32] = hi - i;
                 sh[33] = cum;
@@ -559,6 +597,14 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work that can run between them.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 struct TopkParams {
     const float* scores;     // [B][stride]
     const unsigned* hist1;   // [B][2048]  top 11 key bits (built by the scoring pass)
@@ -576,34 +622,30 @@ __device__ __forceinline__ int seq_len(const TopkParams& p, int b) {
     return ok ? int(T) : 0;
 }
 
-__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
-    return a;
-}
 
-__device__ __forceinline__ void dsmem_add(uint32_t addr, unsigned v) {
-    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void dsmem_st(uint32_t addr, int v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
+// Keys that share the k-th key's 22-bit prefix are ranked one against another
+// when there are at most kCand of them (the usual case: a handful).
+constexpr int kCand = 256;
 constexpr size_t kTopkSmem = size_t(kStep) * 4 + (kBins + 1024 + kBins + kBins) * 4 +
-                             2 * kCluster * 4;
+                             2 * kCluster * 4 + size_t(kCluster) * kCand * 8 + kCluster * 4 +
+                             kCand * 4;
 
 // Top-k of one sequence per cluster of eight CTAs; CTA r owns positions
 // [r*span, (r+1)*span) and keeps them in shared memory when they fit (one
 // 16,384-position step; otherwise every pass re-reads its steps from L2).
-// Levels 2 and 3 of the radix select histogram the keys that share the prefix
-// found so far; each CTA pushes its partial bins into every CTA's total with
-// remote (distributed shared memory) atomics, so after a cluster barrier all
-// CTAs hold the same totals and find the same bin.  Level 3 runs only when
-// the level-2 bin holds more keys than are still needed.  Then each CTA
-// writes its counts of keys above and equal to the k-th key into every CTA,
-// and after a last barrier writes its kept positions at their place in the
-// ascending output.  Three or four cluster barriers in all.
+// Level 1 of the radix select (top 11 key bits) comes with the scores; level 2
+// histograms the next 11 bits of the keys inside the level-1 bin.  Bin i of
+// the level-2 cluster total is kept by CTA i / (bins / cluster size): each CTA
+// adds its partial bins into the owners' totals with remote (distributed
+// shared memory) atomics, one per nonzero bin, and after a cluster barrier
+// every CTA reads the whole total back from the owners, so all CTAs find the
+// same bin.  The keys above its 22-bit prefix are kept; of the keys sharing
+// it (the candidates, usually a handful), the larger ones are kept, lower
+// positions first among equal keys.  Up to kCand candidates are exchanged
+// with their positions and ranked in every CTA; with more, a third 10-bit
+// level (same scheme) finds the exact k-th key, and a count exchange follows.
+// Each CTA then writes its kept positions at their place in the ascending
+// output.  Three cluster barriers, four when level 3 runs.
 // (cluster size set at launch: 16 is a non-portable size)
 __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams p) {
     extern __shared__ float4 topk_dyn[];
@@ -615,6 +657,10 @@ __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams
     unsigned* hist1 = sum3 + 1024;                                // [2048] level 1
     unsigned* part = hist1 + kBins;                               // [2048] this CTA's bins
     int* cnts = reinterpret_cast<int*>(part + kBins);             // [kCluster][2]
+    uint32_t* ckey = reinterpret_cast<uint32_t*>(cnts + 2 * kCluster);  // [kCluster][kCand]
+    int* cpos = reinterpret_cast<int*>(ckey + kCluster * kCand);         // [kCluster][kCand]
+    int* ccnt = cpos + kCluster * kCand;                                 // [kCluster]
+    int* ckeep = ccnt + kCluster;                                        // [kCand]
     __shared__ int sh[40];
     const int b = blockIdx.y;
     const uint32_t rank = cluster_rank();
@@ -660,15 +706,17 @@ __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams
         hist1[tid + k * 1024] = hv[k];
     }
     sum3[tid] = 0;
+    if (tid == 0) sh[36] = 0;                       // this CTA's candidate count
     __syncthreads();
+    cluster_arrive();                               // (1) every CTA's totals are zero ...
     int bin1, above1;
     find_bin(hist1, kBins, K, sh, &bin1, &above1);
-    cluster_sync();                                 // (1) every CTA's totals are zero
 
     // One refinement level: partial bins of the keys with top bits == pre
-    // (and, per thread, the number of keys whose top bits are above pre).
+    // (and, per thread, the number of keys whose top bits are above pre),
+    // then added into the owners' totals.
     int n_above = 0;
-    auto level = [&](int shift, int nb, uint32_t pre, unsigned* total) {
+    auto hist_level = [&](int shift, int nb, uint32_t pre) {
         n_above = 0;
         for (int i = tid; i < nb; i += blockDim.x) part[i] = 0;
         __syncthreads();
@@ -691,54 +739,52 @@ __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams
             if (!resident) __syncthreads();
         }
         __syncthreads();
+    };
+    auto push_level = [&](int nb, unsigned* total) {
+        const int own = nb / kCluster;
         for (int i = tid; i < nb; i += blockDim.x) {
             const unsigned c = part[i];
-            if (c)
-                for (uint32_t r = 0; r < kCluster; ++r) dsmem_add(dsmem_addr(&total[i], r), c);
+            if (c) dsmem_add(dsmem_addr(&total[i], uint32_t(i / own)), c);
         }
     };
-    level(10, kBins, uint32_t(bin1), sum2);
-    cluster_sync();                                 // (2) level-2 totals everywhere
+    hist_level(10, kBins, uint32_t(bin1));
+    cluster_wait();                                 // (1) ... before anyone adds into them
+    push_level(kBins, sum2);
+    cluster_sync();                                 // (2) level-2 totals at their owners
     int bin2, above2;
-    find_bin(sum2, kBins, K - above1, sh, &bin2, &above2);
+    find_bin(sum2, kBins, K - above1, sh, &bin2, &above2, kBins / kCluster, rank);
     MLA_CHECK(bin1 >= 0 && bin1 < kBins && bin2 >= 0 && bin2 < kBins, p.status);
     const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
-    // Keys are compared by their top 32 - kshift bits from here on.  When
-    // every key of the level-2 bin is kept (the usual case: the bin holds
-    // about one key), the 22-bit prefix already separates kept keys from the
-    // rest and level 3 is skipped; the totals are the same in every CTA, so
-    // the whole cluster takes the same branch.
+    // Keys are compared by their top 32 - kshift bits from here on: kth is
+    // the k-th key's prefix, need_eq the number of keys sharing it that are
+    // kept.  The totals are the same in every CTA, so the whole cluster takes
+    // the same branch below.
     uint32_t kth = pre;
     int kshift = 10;
     int need_eq = K - above1 - above2;
-    if (int(sum2[bin2]) != need_eq) {
-        level(0, 1024, pre, sum3);
-        cluster_sync();                             // (3) level-3 totals everywhere
-        int bin3, above3;
-        find_bin(sum3, 1024, K - above1 - above2, sh, &bin3, &above3);
-        MLA_CHECK(bin3 >= 0 && bin3 < 1024, p.status);
-        kth = (pre << 10) | uint32_t(bin3);
-        kshift = 0;
-        need_eq -= above3;
-    }
-    const bool all_eq = int(kshift ? sum2[bin2] : sum3[kth & 1023u]) == need_eq;
-
-    // counts of this CTA's range, written into every CTA
-    int tg, te;
-    if (kshift) {
-        // level 3 skipped: this CTA's keys above the 22-bit k-th prefix are
-        // those above bin1 plus its level-2 bins above bin2, and the equal
-        // ones its level-2 bin bin2 (`part` still holds its level-2 counts)
+    const int n_c = int(sum2[bin2]);                // keys of the sequence with prefix pre
+    const bool cand = n_c <= kCand;
+    int gt_before = 0, eq_before = 0, keep_before = 0;
+    // This CTA's keys above the 22-bit prefix: those above bin1 plus its
+    // level-2 bins above bin2 (`part` still holds its level-2 counts).
+    auto count_above = [&]() {
         int gt = n_above;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int i = tid + k * 1024;
             if (i > bin2) gt += int(part[i]);
         }
+        int tg;
         block_excl_scan(gt, sh, &tg);
-        te = int(part[bin2]);
-    } else {
-        int gt = 0, eq = 0;
+        return tg;
+    };
+    if (cand) {
+        // The few keys with prefix pre are sent, with their positions, to
+        // every CTA (CTA r's into rows r of ckey / cpos), and so is this
+        // CTA's count of keys above; after one barrier each CTA ranks the
+        // candidates itself (larger key first, then lower position) and keeps
+        // the first need_eq.
+        const int tg = count_above();
         for (int t0 = lo; t0 < hi; t0 += kStep) {
             if (!resident) {
                 __syncthreads();
@@ -750,26 +796,108 @@ __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams
             for (int u = 0; u < kSelPer; ++u)
                 if (i0 + u < hi) {
                     const uint32_t k = okey(vals[u * 1024 + tid]);
-                    gt += k > kth;
-                    eq += k == kth;
+                    if ((k >> 10) == pre) {
+                        const int j = atomicAdd(&sh[36], 1);
+                        MLA_CHECK(j < kCand, p.status);
+                        if (j < kCand)
+                            for (uint32_t r = 0; r < kCluster; ++r) {
+                                dsmem_st(dsmem_addr(&ckey[rank * kCand + j], r), int(k));
+                                dsmem_st(dsmem_addr(&cpos[rank * kCand + j], r), i0 + u);
+                            }
+                    }
                 }
         }
-        block_excl_scan(gt, sh, &tg);
-        block_excl_scan(eq, sh, &te);
+        __syncthreads();
+        if (tid < kCluster) {
+            dsmem_st(dsmem_addr(&ccnt[rank], uint32_t(tid)), min(sh[36], kCand));
+            dsmem_st(dsmem_addr(&cnts[2 * rank], uint32_t(tid)), tg);
+        }
+        for (int i = tid; i < kCand; i += blockDim.x) ckeep[i] = 0;
+        if (tid == 0) sh[37] = sh[38] = 0;
+        cluster_sync();                             // (3) candidates and counts everywhere; last remote access
+        for (int i = tid; i < kCluster * kCand; i += blockDim.x) {
+            const int r = i / kCand;
+            if (i - r * kCand >= ccnt[r]) continue;
+            const uint32_t ki = ckey[i];
+            const int pi = cpos[i];
+            int before = 0, order = 0;              // rank, and rank by position alone
+            for (int r2 = 0; r2 < kCluster; ++r2)
+                for (int j = 0; j < ccnt[r2]; ++j) {
+                    const uint32_t kj = ckey[r2 * kCand + j];
+                    const int pj = cpos[r2 * kCand + j];
+                    before += kj > ki || (kj == ki && pj < pi);
+                    order += pj < pi;
+                }
+            const bool kept = before < need_eq;
+            MLA_CHECK(order < kCand, p.status);
+            if (order < kCand) ckeep[order] = kept;
+            if (pi < lo) {
+                atomicAdd(&sh[37], 1);
+                if (kept) atomicAdd(&sh[38], 1);
+            }
+        }
+        for (int r = 0; r < int(rank); ++r) gt_before += cnts[2 * r];
+        __syncthreads();
+        eq_before = sh[37];
+        keep_before = sh[38];
+    } else {
+        // Many keys share the prefix: a third 10-bit level when the bin holds
+        // more keys than are still needed, then the counts of this CTA's
+        // keys above and equal to the k-th one go to every CTA.
+        if (n_c != need_eq) {
+            hist_level(0, 1024, pre);
+            push_level(1024, sum3);
+            cluster_sync();                         // (3) level-3 totals at their owners
+            int bin3, above3;
+            find_bin(sum3, 1024, K - above1 - above2, sh, &bin3, &above3, 1024 / kCluster, rank);
+            MLA_CHECK(bin3 >= 0 && bin3 < 1024, p.status);
+            kth = (pre << 10) | uint32_t(bin3);
+            kshift = 0;
+            need_eq -= above3;
+        }
     }
-    if (tid < kCluster) {
-        dsmem_st(dsmem_addr(&cnts[2 * rank], uint32_t(tid)), tg);
-        dsmem_st(dsmem_addr(&cnts[2 * rank + 1], uint32_t(tid)), te);
-    }
-    cluster_sync();                                 // (4) all counts everywhere; last remote access
-    int gt_before = 0, eq_before = 0;
-    for (uint32_t r = 0; r < rank; ++r) {
-        gt_before += cnts[2 * r];
-        eq_before += cnts[2 * r + 1];
+    const bool all_eq = int(kshift ? n_c : sum3[kth & 1023u]) == need_eq;
+
+    if (!cand) {
+        // counts of this CTA's range, written into every CTA
+        int tg, te;
+        if (kshift) {                               // level 3 skipped
+            tg = count_above();
+            te = int(part[bin2]);
+        } else {
+            int gt = 0, eq = 0;
+            for (int t0 = lo; t0 < hi; t0 += kStep) {
+                if (!resident) {
+                    __syncthreads();
+                    stage(t0);
+                    __syncthreads();
+                }
+                const int i0 = t0 + tid * kSelPer;
+#pragma unroll
+                for (int u = 0; u < kSelPer; ++u)
+                    if (i0 + u < hi) {
+                        const uint32_t k = okey(vals[u * 1024 + tid]);
+                        gt += k > kth;
+                        eq += k == kth;
+                    }
+            }
+            block_excl_scan(gt, sh, &tg);
+            block_excl_scan(eq, sh, &te);
+        }
+        if (tid < kCluster) {
+            dsmem_st(dsmem_addr(&cnts[2 * rank], uint32_t(tid)), tg);
+            dsmem_st(dsmem_addr(&cnts[2 * rank + 1], uint32_t(tid)), te);
+        }
+        cluster_sync();                             // (4) all counts everywhere; last remote access
+        for (uint32_t r = 0; r < rank; ++r) {
+            gt_before += cnts[2 * r];
+            eq_before += cnts[2 * r + 1];
+        }
+        keep_before = min(eq_before, need_eq);      // equal keys are kept lowest position first
     }
 
     // emit in position order
-    int out = gt_before + min(eq_before, need_eq), eq_seen = eq_before;
+    int out = gt_before + keep_before, eq_seen = eq_before;
     for (int t0 = lo; t0 < hi; t0 += kStep) {
         if (!resident) {
             __syncthreads();
@@ -786,12 +914,14 @@ __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams
                 e |= uint32_t(k == kth) << u;
             }
         uint32_t keep = e;
-        if (!all_eq) {                              // lowest positions among equal keys
+        if (!all_eq) {                              // which of the keys equal to the k-th are kept
             int e_total;
             int r = eq_seen + block_excl_scan(__popc(e), sh, &e_total);
             keep = 0;
-            for (uint32_t m = e; m; m &= m - 1, ++r)
-                if (r < need_eq) keep |= m & (~m + 1);
+            for (uint32_t m = e; m; m &= m - 1, ++r) {
+                MLA_CHECK(!cand || r < kCand, p.status);
+                if (cand ? (r < kCand && ckeep[r] != 0) : r < need_eq) keep |= m & (~m + 1);
+            }
             eq_seen += e_total;
         }
         const uint32_t take = g | keep;
@@ -807,6 +937,357 @@ __global__ void __launch_bounds__(1024) dsa_topk_cluster_kernel(const TopkParams
             }
         }
         out += total;
+    }
+}
+
+// Inverse of okey: the score whose order key is k.
+__device__ __forceinline__ float okey_inv(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Bin search with two block barriers: every warp scans its bins (taken from
+// the top, `per` per thread), the 32 warp sums go through shared memory, and
+// each warp forms its own prefix from them.  The bin holding the K-th largest
+// key, the count of the bins above it and its own count go to sh[32..34]
+// (1 <= K <= total is the caller's to ensure).  With own > 0 the histogram is
+// a cluster total kept by owners (bin i in CTA i / own).  Uses sh[0..34].
+__device__ __forceinline__ void find_bin_fast(const unsigned* hist, int nbins, int K, int* sh,
+                                              int own, uint32_t rank) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = nbins / 1024;                  // 1 or 2 bins per thread
+    const int hi = nbins - 1 - int(threadIdx.x) * per;
+    unsigned c2[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        if (i < per) {
+            const uint32_t r = own ? uint32_t((hi - i) / own) : rank;
+            c2[i] = r != rank ? dsmem_ld(dsmem_addr(&hist[hi - i], r)) : hist[hi - i];
+        }
+    const int local = int(c2[0] + c2[1]);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    const int ws = sh[lane];
+    int wincl = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += y;
+    }
+    const int above = __shfl_sync(0xffffffffu, wincl - ws, warp) + incl - local;
+    if (above < K && K <= above + local) {
+        const bool first = above + int(c2[0]) >= K;
+        sh[32] = first ? hi : hi - 1;
+        sh[33] = first ? above : above + int(c2[0]);
+        sh[34] = int(first ? c2[0] : c2[1]);
+    }
+    __syncthreads();
+}
+
+// Sum over the block of one value per thread (two warp reductions around one
+// barrier); `slot` is a shared word cleared before the previous barrier.
+__device__ __forceinline__ int block_sum(int v, int* slot) {
+    const int w = __reduce_add_sync(0xffffffffu, v);
+    if ((threadIdx.x & 31) == 0 && w) atomicAdd(slot, w);
+    __syncthreads();
+    return *slot;
+}
+
+#ifndef MLA_TOPK_RCLUSTER
+#define MLA_TOPK_RCLUSTER 8
+#endif
+constexpr int kRC = MLA_TOPK_RCLUSTER;             // CTAs per sequence
+constexpr int kRPer = 16 * 8 / kRC;                // positions per thread
+constexpr int kRStep = 1024 * kRPer;               // positions per CTA
+static_assert(kRPer == 8 || kRPer == 16, "8 or 16 CTAs per sequence");
+constexpr int kRCand = 64;                         // candidates ranked one against another
+struct RegsSmem {
+    unsigned hist1[kBins];                         // level 1 (from the scoring pass)
+    unsigned sum2[kBins];                          // level-2 cluster totals (owners + copies)
+    unsigned part[kBins];                          // this CTA's level-2 (then level-3) bins
+    unsigned sum3[1024];                           // level-3 cluster totals
+    uint32_t kept[kRStep / 32];                     // kept candidates of this range, by position
+    uint32_t ckey[kRC * kRCand];              // candidates of CTA r in row r
+    int cpos[kRC * kRCand];
+    int ccnt[kRC];
+    int cnts[2 * kRC];                        // counts of every CTA's range
+};
+
+// Top-k of one sequence of at most 8 x 16,384 positions per cluster of eight
+// CTAs (the same selection as dsa_topk_cluster_kernel).  Each thread holds the
+// order keys of its 16 positions in registers from the first load to the
+// output, so no pass re-reads them:
+//   level 1: the bin from the scoring pass's histogram (while the scores load);
+//   level 2: this CTA's histogram of the level-1 bin's keys, added into the
+//     owners' totals (remote atomics), one barrier, the bin from the totals;
+//   the keys above the 22-bit prefix are kept; those sharing it (at most
+//     kRCand, else level 3 below) go with their positions to every CTA, and
+//     so does this CTA's count of keys above; after one barrier every CTA
+//     ranks the candidates (larger key first, lower position first among
+//     equal keys) and keeps the first need_eq;
+//   output: one block scan over the kept positions of each thread.
+// With more candidates, a 10-bit level 3 finds the exact k-th key and a
+// count exchange gives each CTA its offsets (two more barriers).
+__global__ void __launch_bounds__(1024) dsa_topk_regs_kernel(const TopkParams p) {
+    extern __shared__ uint4 regs_dyn[];
+    RegsSmem& S = *reinterpret_cast<RegsSmem*>(regs_dyn);
+    __shared__ int sh[48];
+    const int b = blockIdx.y;
+    const uint32_t rank = cluster_rank();
+    const int tid = threadIdx.x;
+    if (tid == 0) grid_dep_trigger();
+    grid_dep_wait();                                // the scores and level-1 bins
+    int32_t* oi = p.out_idx + size_t(b) * p.topk;
+    float* os = p.out_scores ? p.out_scores + size_t(b) * p.topk : nullptr;
+    const int T = seq_len(p, b);                    // the same for the whole cluster
+    if (T <= p.topk) {                              // every position is kept
+        if (rank == 0)
+            for (int i = tid; i < p.topk; i += blockDim.x) {
+                oi[i] = i < T ? i : -1;
+                if (os) os[i] = -INFINITY;
+            }
+        return;
+    }
+    const int K = p.topk;
+    const int span = ((T + kRC - 1) / kRC + kRPer - 1) / kRPer * kRPer;
+    const int lo = int(rank) * span, hi = min(T, lo + span);
+    MLA_CHECK(span <= kRStep, p.status);
+    const int i0 = lo + tid * kRPer;              // this thread's first position
+
+    // loads: level-1 bins, then this thread's 16 scores (in flight during
+    // the level-1 bin search)
+    unsigned hv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) hv[k] = p.hist1[size_t(b) * kBins + tid + k * 1024];
+    float v[kRPer];
+    {
+        const float4* s4 = reinterpret_cast<const float4*>(p.scores + size_t(b) * p.stride);
+#pragma unroll
+        for (int q = 0; q < kRPer / 4; ++q) {
+            const float4 x = i0 + 4 * q < hi ? s4[(i0 >> 2) + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        S.hist1[tid + k * 1024] = hv[k];
+        S.sum2[tid + k * 1024] = 0;
+        S.part[tid + k * 1024] = 0;
+    }
+    S.sum3[tid] = 0;
+    if (tid < kRStep / 32) S.kept[tid] = 0;
+    if (tid < 8) sh[40 + tid] = 0;                  // counters
+    __syncthreads();
+    cluster_arrive();                               // (1) every CTA's totals are zero ...
+    find_bin_fast(S.hist1, kBins, K, sh, 0, rank);
+    const int bin1 = sh[32], above1 = sh[33];
+    uint32_t key[kRPer];
+#pragma unroll
+    for (int u = 0; u < kRPer; ++u) key[u] = okey(v[u]);
+    // positions past the end: only in the thread that holds the end
+    constexpr uint32_t kAll = (1u << kRPer) - 1u;
+    const uint32_t valid = hi - i0 >= kRPer ? kAll : (hi > i0 ? (1u << (hi - i0)) - 1u : 0u);
+    // level 2: the next 11 bits of the keys in bin1; in1 / g1 mark this
+    // thread's keys in and above bin1
+    uint32_t in1 = 0, g1 = 0;
+#pragma unroll
+    for (int u = 0; u < kRPer; ++u) {
+        const uint32_t top = key[u] >> 21;
+        const bool in = top == uint32_t(bin1) && ((valid >> u) & 1u);
+        if (in) atomicAdd(&S.part[(key[u] >> 10) & (kBins - 1)], 1u);
+        in1 |= uint32_t(in) << u;
+        g1 |= uint32_t(top > uint32_t(bin1)) << u;
+    }
+    g1 &= valid;
+    __syncthreads();
+    cluster_wait();                                 // (1) ... before anyone adds into them
+    {
+        constexpr int own = kBins / kRC;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + k * 1024;
+            const unsigned c = S.part[i];
+            if (c) dsmem_add(dsmem_addr(&S.sum2[i], uint32_t(i / own)), c);
+        }
+    }
+    cluster_sync();                                 // (2) level-2 totals at their owners
+    find_bin_fast(S.sum2, kBins, K - above1, sh, kBins / kRC, rank);
+    const int bin2 = sh[32], above2 = sh[33], n_c = sh[34];
+    MLA_CHECK(bin1 >= 0 && bin1 < kBins && bin2 >= 0 && bin2 < kBins, p.status);
+    const uint32_t pre = (uint32_t(bin1) << 11) | uint32_t(bin2);
+    int need_eq = K - above1 - above2;              // keys with prefix pre that are kept
+    int gt_before = 0, keep_before = 0;
+    uint32_t take;
+    if (n_c <= kRCand) {
+        // keys above the prefix (g) and sharing it (e): the keys above bin1,
+        // and those of bin1 by their level-2 bin
+        uint32_t g = g1, e = 0;
+        if (in1) {
+#pragma unroll
+            for (int u = 0; u < kRPer; ++u)
+                if ((in1 >> u) & 1u) {
+                    const uint32_t l2 = (key[u] >> 10) & (kBins - 1);
+                    g |= uint32_t(l2 > uint32_t(bin2)) << u;
+                    e |= uint32_t(l2 == uint32_t(bin2)) << u;
+                }
+        }
+        if (e) {
+#pragma unroll
+            for (int u = 0; u < kRPer; ++u)       // this CTA's candidates into its own row
+                if ((e >> u) & 1u) {
+                    const int j = atomicAdd(&sh[41], 1);
+                    MLA_CHECK(j < kRCand, p.status);
+                    if (j < kRCand) {
+                        S.ckey[rank * kRCand + j] = key[u];
+                        S.cpos[rank * kRCand + j] = i0 + u;
+                    }
+                }
+        }
+        const int tg = block_sum(__popc(g), &sh[40]);
+        const int mine = min(sh[41], kRCand);
+        // the row, its length and the count of keys above go to the other
+        // CTAs, one remote store pair per thread
+        if (tid < kRC * mine) {
+            const uint32_t r = uint32_t(tid % kRC);
+            const int j = tid / kRC;
+            if (r != rank) {
+                dsmem_st(dsmem_addr(&S.ckey[rank * kRCand + j], r), int(S.ckey[rank * kRCand + j]));
+                dsmem_st(dsmem_addr(&S.cpos[rank * kRCand + j], r), S.cpos[rank * kRCand + j]);
+            }
+        }
+        if (tid < kRC) {
+            dsmem_st(dsmem_addr(&S.ccnt[rank], uint32_t(tid)), mine);
+            dsmem_st(dsmem_addr(&S.cnts[2 * rank], uint32_t(tid)), tg);
+        }
+        cluster_sync();                             // (3) candidates and counts everywhere; last remote access
+        // every CTA's candidate count and count of keys above, read at once
+        int cc[kRC];
+        int n = 0;
+#pragma unroll
+        for (int r = 0; r < kRC; ++r) {
+            cc[r] = S.ccnt[r];
+            n += cc[r];
+            gt_before += r < int(rank) ? S.cnts[2 * r] : 0;
+        }
+        MLA_CHECK(n == n_c, p.status);
+        // candidate c: entry c of the rows taken in order
+        auto cand = [&](int c, uint32_t* k, int* pos) {
+            int r = 0;
+#pragma unroll
+            for (int q = 0; q < kRC; ++q)
+                if (r == q && c >= cc[q]) {
+                    c -= cc[q];
+                    r = q + 1;
+                }
+            const int i = min(r, kRC - 1) * kRCand + c;
+            *k = S.ckey[i];
+            *pos = S.cpos[i];
+        };
+        // warp w ranks candidates w and w + 32: lane l compares them with
+        // candidates l and l + 32 (larger key first, then lower position)
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int c = warp; c < n; c += 32) {
+            uint32_t kc, kj;
+            int pc, pj;
+            cand(c, &kc, &pc);
+            int before = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = lane + 32 * h;
+                bool beats = false;
+                if (j < n) {
+                    cand(j, &kj, &pj);
+                    beats = kj > kc || (kj == kc && pj < pc);
+                }
+                before += __popc(__ballot_sync(0xffffffffu, beats));
+            }
+            if (lane == 0 && before < need_eq) {
+                if (pc < lo) {
+                    atomicAdd(&sh[42], 1);
+                } else if (pc < hi) {
+                    MLA_CHECK(pc - lo < kRStep, p.status);
+                    atomicOr(&S.kept[(pc - lo) >> 5], 1u << ((pc - lo) & 31));
+                }
+            }
+        }
+        __syncthreads();
+        keep_before = sh[42];
+        take = g | (e & ((S.kept[(tid * kRPer) >> 5] >> ((tid * kRPer) & 31)) & kAll));
+    } else {
+        // level 3 over the keys with prefix pre (part's level-2 counts were
+        // read by the pushes before barrier (2))
+        S.part[tid] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kRPer; ++u)
+            if (((in1 >> u) & 1u) && ((key[u] >> 10) & (kBins - 1)) == uint32_t(bin2))
+                atomicAdd(&S.part[key[u] & 1023u], 1u);
+        __syncthreads();
+        {
+            constexpr int own = 1024 / kRC;
+            const unsigned c = S.part[tid];
+            if (c) dsmem_add(dsmem_addr(&S.sum3[tid], uint32_t(tid / own)), c);
+        }
+        cluster_sync();                             // (3) level-3 totals at their owners
+        find_bin_fast(S.sum3, 1024, need_eq, sh, 1024 / kRC, rank);
+        const int bin3 = sh[32], above3 = sh[33], n_eq = sh[34];
+        MLA_CHECK(bin3 >= 0 && bin3 < 1024, p.status);
+        const uint32_t kth = (pre << 10) | uint32_t(bin3);
+        need_eq -= above3;
+        uint32_t g = 0, e = 0;
+#pragma unroll
+        for (int u = 0; u < kRPer; ++u) {
+            g |= uint32_t(key[u] > kth) << u;
+            e |= uint32_t(key[u] == kth) << u;
+        }
+        g &= valid;
+        e &= valid;
+        const int tg = block_sum(__popc(g), &sh[43]);
+        const int te = block_sum(__popc(e), &sh[44]);
+        if (tid < kRC) {
+            dsmem_st(dsmem_addr(&S.cnts[2 * rank], uint32_t(tid)), tg);
+            dsmem_st(dsmem_addr(&S.cnts[2 * rank + 1], uint32_t(tid)), te);
+        }
+        cluster_sync();                             // (4) all counts everywhere; last remote access
+        int eq_before = 0;
+        for (uint32_t r = 0; r < rank; ++r) {
+            gt_before += S.cnts[2 * r];
+            eq_before += S.cnts[2 * r + 1];
+        }
+        keep_before = min(eq_before, need_eq);
+        take = g | e;
+        if (n_eq != need_eq) {                      // equal keys: lowest positions first
+            int e_total;
+            int r = eq_before + block_excl_scan(__popc(e), sh, &e_total);
+            uint32_t keep = 0;
+            for (uint32_t m = e; m; m &= m - 1, ++r)
+                if (r < need_eq) keep |= m & (~m + 1);
+            take = g | keep;
+        }
+    }
+    // output: this thread's kept positions at their place in ascending order
+    int total;
+    int o = gt_before + keep_before + block_excl_scan(__popc(take), sh, &total);
+    if (take) {
+#pragma unroll
+        for (int u = 0; u < kRPer; ++u)
+            if ((take >> u) & 1u) {
+                if (o < K) {
+                    oi[o] = i0 + u;
+                    if (os) os[o] = okey_inv(key[u]);
+                } else {
+                    report(p.status, kStInvalid);   // cannot happen for consistent counts
+                }
+                ++o;
+            }
     }
 }
 
@@ -1211,12 +1692,17 @@ static cudaError_t launch_score_topk(const IndexArgs& a, const CUtensorMap& kmap
     if (e != cudaSuccess) return e;
     TopkParams tp{p.scores, p.hist, a.cu, a.max_seqlen, p.stride, a.topk,
                   a.total_keys, a.topk_idx, a.topk_scores, dev.status};
-    e = cudaFuncSetAttribute(dsa_topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kTopkSmem));
+    // every CTA's range fits in registers (16 positions a thread) up to
+    // 8 x 16,384 positions; longer sequences take the general kernel
+    const bool regs = int64_t(a.max_seqlen) <= int64_t(kRC) * kRStep;
+    void (*const topk_kernel)(TopkParams) = regs ? dsa_topk_regs_kernel : dsa_topk_cluster_kernel;
+    const size_t topk_smem = regs ? sizeof(RegsSmem) : kTopkSmem;
+    const int cluster = regs ? kRC : kCluster;
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(topk_smem));
     if (e != cudaSuccess) return e;
-    if (kCluster > 8) {
-        e = cudaFuncSetAttribute(dsa_topk_cluster_kernel,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (cluster > 8) {
+        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     {
@@ -1224,17 +1710,17 @@ static cudaError_t launch_score_topk(const IndexArgs& a, const CUtensorMap& kmap
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = kCluster;
+        attr[1].val.clusterDim.x = cluster;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kCluster, a.B);
+        cfg.gridDim = dim3(cluster, a.B);
         cfg.blockDim = dim3(1024);
-        cfg.dynamicSmemBytes = kTopkSmem;
+        cfg.dynamicSmemBytes = topk_smem;
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, dsa_topk_cluster_kernel, tp);
+        e = cudaLaunchKernelEx(&cfg, topk_kernel, tp);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -68,6 +68,7 @@ def run_index(d, lengths, topk, max_seqlen=None):
     ([131072], 2048),
     ([2100 + 37 * i for i in range(40)], 2048),   # many sequences per CTA, ragged tails
     ([70000, 1, 2049, 130000, 5, 9000, 2048, 33000], 1000),
+    ([131073, 5000], 2048),                       # one past the register-resident bound
 ])
 def test_index_topk_matches_oracle(lengths, topk):
     d = mi.make_dsa(lengths, device=DEV, config=51, with_main=False)
@@ -77,13 +78,22 @@ def test_index_topk_matches_oracle(lengths, topk):
     check_selection(idx, sc, s64, lengths, topk)
 
 
-def test_index_topk_exact_ties_prefer_lower_positions():
-    """Keys drawn from 40 distinct rows: scores tie exactly in fp32 and fp64,
-    so the selection must equal the oracle's bit for bit."""
+@pytest.mark.parametrize("T,rows", [
+    (6000, 200),       # 37 keys tie with the k-th: ranked one against another
+    (60000, 2000),     # 42 tie, eight full ranges
+    (6000, 100),       # 62 tie
+    (6000, 40),        # 134 tie: the third radix level, then ties by position
+    (6000, 10),        # 604 tie
+    (300000, 2000),    # 162 tie, over ranges re-read in steps: ranked
+    (300000, 300),     # 1025 tie: the third level
+])
+def test_index_topk_exact_ties_prefer_lower_positions(T, rows):
+    """Keys drawn from a few distinct rows: scores tie exactly in fp32 and
+    fp64, so the selection must equal the oracle's bit for bit."""
     g = torch.Generator(device="cpu").manual_seed(9)
-    T, topk = 6000, 2048
-    base = torch.randn((40, 128), generator=g).to(torch.bfloat16)
-    pick = torch.randint(0, 40, (T,), generator=g)
+    topk = 2048
+    base = torch.randn((rows, 128), generator=g).to(torch.bfloat16)
+    pick = torch.randint(0, rows, (T,), generator=g)
     ik = base[pick].contiguous()
     iq = torch.randn((1, 32, 128), generator=g).to(torch.bfloat16)
     w = torch.randn((1, 32), generator=g)
@@ -117,6 +127,16 @@ def test_index_topk_negative_weights_and_zero_scores():
     mla.check_device_status()
     s64 = oracle.dsa_index_scores(iq, ik, w, cu)
     check_selection(idx, None, s64, [T], topk)
+
+
+def test_index_topk_short_sequences_under_a_long_bound():
+    """A bound above 8 x 16,384 positions selects the general top-k kernel even
+    for sequences that would fit the register-resident one."""
+    lengths = [5000, 20000, 2100]
+    d = mi.make_dsa(lengths, device=DEV, config=53, with_main=False)
+    idx, sc = run_index(d, lengths, 2048, max_seqlen=200000)
+    s64 = oracle.dsa_index_scores(d.index_q, d.index_k, d.w, mi.cu_from_lengths(lengths))
+    check_selection(idx, sc, s64, lengths, 2048)
 
 
 def test_index_topk_is_deterministic():
