@@ -96,6 +96,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     return true;
 }
 
+// The same wait by every lane of a converged warp (the MMA-issuing and TMA
+// roles run as whole warps); the result is the same in every lane.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
+}
+
+// A whole-warp wait that gives up at once when another role has set *abort
+// after a failure of its own.
+__device__ __forceinline__ bool warp_wait_abortable(uint64_t* bar, uint32_t parity,
+                                                    long long limit_ns, volatile int* abort) {
+    const bool ok = mbar_test(bar, parity) || (!*abort && mbar_wait(bar, parity, limit_ns));
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------------
 // Bulk copies (TMA, non-tensor): global -> shared, completion counted in bytes
 // on an mbarrier.  Both addresses 16-byte aligned, size a multiple of 16.

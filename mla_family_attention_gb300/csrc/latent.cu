@@ -451,12 +451,15 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
         }
     } else if (warp == 0) {
         // ------------------------------- TMA -------------------------------
-        // Decode: lane 0 issues tiled loads of 64 contiguous cache rows.  (An
-        // L2 prefetch of the next tiles measured slower at every distance
+        // Decode: the whole warp walks the tiles and waits on the ring; one
+        // elected lane issues the tiled loads of 64 contiguous cache rows.
+        // (An L2 prefetch of the next tiles measured slower at every distance
         // tried: it competes with these loads for the TMA unit.)
-        if (t0 < t1 && lane == 0) {
-            tma_prefetch_desc(&cmap);
-            tma_prefetch_desc(&qmap);
+        if (t0 < t1) {
+            if (elect_one()) {
+                tma_prefetch_desc(&cmap);
+                tma_prefetch_desc(&qmap);
+            }
             const uint64_t policy = l2_evict_first_policy();
             int filled[kSlots];
             for (int s = 0; s < kSlots; ++s) filled[s] = 0;
@@ -469,51 +472,59 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                 const int b = cur.b;
                 if (t == t0 || t == ts[b]) {
                     // q~ of sequence b, once the previous segment's Q.K^T is done
-                    if (nseg > 0 && !mbar_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
-                        fail();
+                    if (nseg > 0 && !warp_wait(qfree, (nseg - 1) & 1, p.wait_ns)) {
+                        if (elect_one()) fail();
                         break;
                     }
-                    mbar_arrive_expect_tx(qfull, 9 * H * 128);
-                    for (int kb = 0; kb < 9; ++kb)
-                        tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(qfull, 9 * H * 128);
+                        for (int kb = 0; kb < 9; ++kb)
+                            tma_load_2d(qs + kb * H * 128, &qmap, kb * 64, b * H, qfull);
+                    }
+                    __syncwarp();
                     ++nseg;
                 }
                 const int row = int(p.cu[b]) + (t - ts[b]) * kLT;
                 for (int i = 0; i < kFills; ++i, ++fill) {
                     const int slot = fill % kSlots, round = fill / kSlots;
                     if (*abort_flag) { ok = false; break; }
-                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
-                        fail();
+                    if (round > 0 && !warp_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                        if (elect_one()) fail();
                         ok = false;
                         break;
                     }
                     uint8_t* dst = ring + slot * kSlot;
                     MLA_CHECK(slot < kSlots && row >= 0, p.status);
-                    if (i == 0) {              // shared-key features 512..575
-                        mbar_arrive_expect_tx(&full[slot], kHalf);
-                        tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
-                    } else {                   // latent features 128*(i-1) .. +127
-                        mbar_arrive_expect_tx(&full[slot], kSlot);
-                        tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot], policy);
-                        tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
-                                         &full[slot], policy);
+                    if (elect_one()) {
+                        if (i == 0) {          // shared-key features 512..575
+                            mbar_arrive_expect_tx(&full[slot], kHalf);
+                            tma_load_2d_hint(dst, &cmap, kLatent, row, &full[slot], policy);
+                        } else {               // latent features 128*(i-1) .. +127
+                            mbar_arrive_expect_tx(&full[slot], kSlot);
+                            tma_load_2d_hint(dst, &cmap, 128 * (i - 1), row, &full[slot], policy);
+                            tma_load_2d_hint(dst + kHalf, &cmap, 128 * (i - 1) + 64, row,
+                                             &full[slot], policy);
+                        }
                     }
+                    __syncwarp();
                     filled[slot] = round + 1;
                 }
             }
             for (int s = 0; s < kSlots; ++s)
-                if (filled[s] > 0 && !mbar_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns))
+                if (filled[s] > 0 && !warp_wait(&full[s], (filled[s] - 1) & 1, p.wait_ns) &&
+                    elect_one())
                     report(p.status, kStTimeout);
-            if (nseg > 0 && !mbar_wait(qfull, (nseg - 1) & 1, p.wait_ns))
+            if (nseg > 0 && !warp_wait(qfull, (nseg - 1) & 1, p.wait_ns) && elect_one())
                 report(p.status, kStTimeout);
         }
     } else if (warp == 1) {
         // ---------------------------- Q.K^T MMAs ----------------------------
-        // One thread, in order: for each tile, the five fills' S (+)= Q~ K^T
-        // into the tile's score buffer.  Descriptors are built once and
+        // The whole warp, in order: for each tile, the five fills' S (+)= Q~
+        // K^T into the tile's score buffer; every lane waits, one elected
+        // lane issues each MMA and commit.  Descriptors are built once and
         // advanced by their 16-byte address units; the ring slot and phase
         // advance with the fills.
-        if (lane == 0 && t0 < t1) {
+        if (t0 < t1) {
             const uint64_t qdesc = smem_desc_sw128(smem_u32(qs), 16, 1024);     // Q~, K-major
             const uint64_t kdesc = smem_desc_sw128(smem_u32(ring), 16, 1024);   // keys, K-major
             const uint32_t qblk = uint32_t(H) * 8;       // one [H x 64] block of Q~
@@ -522,8 +533,7 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
             int slot = 0;                                // ring slot of the next fill
             uint32_t phase = 0;                          // and the parity of its phase
             auto wait_bar = [&](uint64_t* bar, uint32_t par) -> bool {
-                if (mbar_test(bar, par)) return true;
-                return !*abort_flag && mbar_wait(bar, par, p.wait_ns);
+                return warp_wait_abortable(bar, par, p.wait_ns, abort_flag);
             };
             Cursor cur{ts};
             cur.seek(t0, B);
@@ -557,29 +567,34 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                         const uint64_t a0 = qdesc + 8 * qblk;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(d, a0 + 2 * kk, b0 + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
-                        mma_commit(&empty[slot]);
+                            if (elect_one())
+                                mma_bf16_ss(d, a0 + 2 * kk, b0 + 2 * kk, kIdescQK, kk > 0 ? 1u : 0u);
+                        if (elect_one()) mma_commit(&empty[slot]);
                     } else {                             // latent block i-1
                         const uint64_t a0 = qdesc + uint32_t(2 * (i - 1)) * qblk;
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16_ss(d, a0 + hf * qblk + 2 * kk, b0 + hf * kHalfU + 2 * kk,
-                                            kIdescQK, 1u);
+                                if (elect_one())
+                                    mma_bf16_ss(d, a0 + hf * qblk + 2 * kk,
+                                                b0 + hf * kHalfU + 2 * kk, kIdescQK, 1u);
                     }
+                    __syncwarp();
                     if (++slot == kSlots) {
                         slot = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (last) mma_commit(qfree);
-                mma_commit(&sfull[j & 1]);
+                if (last && elect_one()) mma_commit(qfree);
+                if (elect_one()) mma_commit(&sfull[j & 1]);
+                __syncwarp();
             }
-            if (!ok) fail();
-            mma_commit(&mdone[0]);
-            if (!mbar_wait(&mdone[0], 0, p.wait_ns)) report(p.status, kStTimeout);
+            if (!ok && elect_one()) fail();
+            if (elect_one()) mma_commit(&mdone[0]);
+            __syncwarp();
+            if (!warp_wait(&mdone[0], 0, p.wait_ns) && elect_one()) report(p.status, kStTimeout);
         }
     } else if (warp == kPvWarp<kSrc>) {
         // ----------------------------- P.V MMAs -----------------------------
@@ -587,15 +602,15 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
         // the latent blocks' ring slots are released as their MMAs finish.
         // A tile's P.V follows its softmax, which followed its Q.K^T, so the
         // slots' Q.K^T reads are complete when these commits free them.
-        if (lane == 0 && t0 < t1) {
+        // Whole warp, one elected lane issuing (as for Q.K^T).
+        if (t0 < t1) {
             const uint32_t idesc_pv = idesc_bf16_f32(128, H, true, false);
             const uint64_t cdesc = smem_desc_sw128(smem_u32(ring), kHalf, 1024);  // C^T, MN-major
             const uint64_t pdesc = smem_desc_sw128(smem_u32(ps), 16, 1024);     // P, K-major
             constexpr uint32_t kSlotU = kSlot >> 4;
             bool ok = true;
             auto wait_bar = [&](uint64_t* bar, uint32_t par) -> bool {
-                if (mbar_test(bar, par)) return true;
-                return !*abort_flag && mbar_wait(bar, par, p.wait_ns);
+                return warp_wait_abortable(bar, par, p.wait_ns, abort_flag);
             };
             Cursor cur{ts};
             cur.seek(t0, B);
@@ -623,22 +638,25 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
                     const uint32_t d = tmem + kColO + uint32_t(u * H);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_bf16_ss(d, a0 + 128 * k, pdesc + 2 * k, idesc_pv,
-                                    (first && k == 0) ? 0u : 1u);
-                    mma_commit(&empty[sl]);
+                        if (elect_one())
+                            mma_bf16_ss(d, a0 + 128 * k, pdesc + 2 * k, idesc_pv,
+                                        (first && k == 0) ? 0u : 1u);
+                    if (elect_one()) mma_commit(&empty[sl]);
                     if (++sl == kSlots) sl = 0;
                 }
-                mma_commit(pfree);
-                if (last) mma_commit(ofinal);
+                if (elect_one()) mma_commit(pfree);
+                if (last && elect_one()) mma_commit(ofinal);
+                __syncwarp();
                 s1 += kFills;
                 if (s1 >= kSlots) s1 -= kSlots;
             }
-            if (!ok) {
+            if (!ok && elect_one()) {
                 fail();
                 mma_commit(ofinal);
             }
-            mma_commit(&mdone[1]);
-            if (!mbar_wait(&mdone[1], 0, p.wait_ns)) report(p.status, kStTimeout);
+            if (elect_one()) mma_commit(&mdone[1]);
+            __syncwarp();
+            if (!warp_wait(&mdone[1], 0, p.wait_ns) && elect_one()) report(p.status, kStTimeout);
         }
     } else {
         // ------------------------- softmax / epilogue ------------------------

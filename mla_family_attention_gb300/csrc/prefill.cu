@@ -248,54 +248,66 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (warp == 0) {
         // --------------------------------- TMA ---------------------------------
-        if (lane == 0) {
+        // The whole warp walks the tiles and waits; one elected lane issues.
+        {
             int kf[C::kKStages] = {}, vf[C::kVStages] = {};
             const int krow0 = kPair ? 64 * int(rank) : 0;       // this CTA's key rows of a tile
             if (early) {
                 kf[0] = vf[0] = 1;                              // requested before the set-up barrier
-            } else {
+            } else if (elect_one()) {
                 // this CTA's 128 query rows (rows at or past Tq arrive as zeros)
                 mbar_arrive_expect_tx(qready, kQTile);
                 for (int c = 0; c < 3; ++c)
                     tma_load_3d(qsm + c * kQBox, &qmap, c * 64, q0, bh, qready);
             }
+            __syncwarp();
             for (int j = early ? 1 : 0; j < n_kv; ++j) {
                 if (*abort_flag) break;
                 const int ks = j % C::kKStages, kr = j / C::kKStages;
                 MLA_CHECK(ks < C::kKStages && (ks + 1) * C::kKTile <= C::kKStages * C::kKTile,
                           p.status);
-                if (kr > 0 && !wait(&kempty[ks], (kr - 1) & 1)) {
-                    report(p.status, kStTimeout);
-                    *abort_flag = 1;
+                if (kr > 0 && !__all_sync(0xffffffffu, wait(&kempty[ks], (kr - 1) & 1))) {
+                    if (elect_one()) {
+                        report(p.status, kStTimeout);
+                        *abort_flag = 1;
+                    }
                     break;
                 }
                 // keys j*128.. of (b, h); rows at or past Tk arrive as zeros
                 const int y = j * kBN;
-                mbar_arrive_expect_tx(&kfull[ks], C::kKTile);
-                for (int c = 0; c < 3; ++c)
-                    tma_load_3d(ksm + ks * C::kKTile + c * C::kKBox, &kmap, c * 64, y + krow0, bh,
-                                &kfull[ks]);
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&kfull[ks], C::kKTile);
+                    for (int c = 0; c < 3; ++c)
+                        tma_load_3d(ksm + ks * C::kKTile + c * C::kKBox, &kmap, c * 64, y + krow0,
+                                    bh, &kfull[ks]);
+                }
+                __syncwarp();
                 kf[ks] = kr + 1;
                 const int vs = j % C::kVStages, vr = j / C::kVStages;
-                if (vr > 0 && !wait(&vempty[vs], (vr - 1) & 1)) {
-                    report(p.status, kStTimeout);
-                    *abort_flag = 1;
+                if (vr > 0 && !__all_sync(0xffffffffu, wait(&vempty[vs], (vr - 1) & 1))) {
+                    if (elect_one()) {
+                        report(p.status, kStTimeout);
+                        *abort_flag = 1;
+                    }
                     break;
                 }
                 MLA_CHECK(vs < C::kVStages && y >= 0, p.status);
-                mbar_arrive_expect_tx(&vfull[vs], C::kVTile);
-                for (int c = 0; c < C::kVBoxes; ++c)
-                    tma_load_3d(vsm + vs * C::kVTile + c * C::kVBox, &vmap,
-                                kPair ? 64 * int(rank) : c * 64, y, bh, &vfull[vs]);
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&vfull[vs], C::kVTile);
+                    for (int c = 0; c < C::kVBoxes; ++c)
+                        tma_load_3d(vsm + vs * C::kVTile + c * C::kVBox, &vmap,
+                                    kPair ? 64 * int(rank) : c * 64, y, bh, &vfull[vs]);
+                }
+                __syncwarp();
                 vf[vs] = vr + 1;
             }
             for (int i = 0; i < C::kKStages; ++i)
-                if (kf[i] > 0 && !mbar_wait(&kfull[i], (kf[i] - 1) & 1, p.wait_ns))
+                if (kf[i] > 0 && !warp_wait(&kfull[i], (kf[i] - 1) & 1, p.wait_ns) && elect_one())
                     report(p.status, kStTimeout);
             for (int i = 0; i < C::kVStages; ++i)
-                if (vf[i] > 0 && !mbar_wait(&vfull[i], (vf[i] - 1) & 1, p.wait_ns))
+                if (vf[i] > 0 && !warp_wait(&vfull[i], (vf[i] - 1) & 1, p.wait_ns) && elect_one())
                     report(p.status, kStTimeout);
-            if (!mbar_wait(qready, 0, p.wait_ns)) report(p.status, kStTimeout);
+            if (!warp_wait(qready, 0, p.wait_ns) && elect_one()) report(p.status, kStTimeout);
         }
     } else if (kPair && !leader && (warp == 1 || warp == kPvWarp)) {
         // ------------- odd CTA of a pair: tell the MMA lanes its halves landed -------------
@@ -325,8 +337,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------ Q.K^T MMAs ------------------------------
-        if (lane == 0) {
-            bool ok = mbar_wait(qready, 0, p.wait_ns) && (!kPair || wait(qpeer, 0));
+        // The whole warp waits; one elected lane issues each MMA and commit.
+        {
+            bool ok = __all_sync(0xffffffffu,
+                                 mbar_wait(qready, 0, p.wait_ns) && (!kPair || wait(qpeer, 0)));
             bool issued = false;
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
@@ -337,9 +351,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // buffer: its next phase needs S_j, so the parity cannot run
                 // two phases ahead of this wait)
                 const int sb = j % kNB;
-                if (!mbar_wait(&kfull[ks], (j / C::kKStages) & 1, p.wait_ns) ||
-                    (kPair && !wait(&kpeer[ks], (j / C::kKStages) & 1)) ||
-                    (j >= kNB && !mbar_wait(&sfree[sb], ((j - kNB) / kNB) & 1, p.wait_ns))) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&kfull[ks], (j / C::kKStages) & 1, p.wait_ns) &&
+                                    (!kPair || wait(&kpeer[ks], (j / C::kKStages) & 1)) &&
+                                    (j < kNB ||
+                                     mbar_wait(&sfree[sb], ((j - kNB) / kNB) & 1, p.wait_ns)))) {
                     ok = false;
                     break;
                 }
@@ -354,33 +370,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         smem_desc_sw128(qb + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd =
                         smem_desc_sw128(kb + (kk >> 2) * C::kKBox + (kk & 3) * 32, 16, 1024);
-                    if (kPair)
-                        mma_bf16_ss_pair(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
-                    else
-                        mma_bf16_ss(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    if (elect_one()) {
+                        if (kPair)
+                            mma_bf16_ss_pair(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                        else
+                            mma_bf16_ss(d, ad, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    }
                 }
-                commit_both(&kempty[ks]);
-                commit_both(&sfull[sb]);
+                if (elect_one()) commit_both(&kempty[ks]);
+                if (elect_one()) commit_both(&sfull[sb]);
+                __syncwarp();
                 issued = true;
             }
-            if (!ok) {
+            if (!ok && elect_one()) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
             }
-            commit_self(qkdone);
-            if (issued && !mbar_wait(qkdone, 0, p.wait_ns)) report(p.status, kStTimeout);
+            if (elect_one()) commit_self(qkdone);
+            __syncwarp();
+            if (issued && !warp_wait(qkdone, 0, p.wait_ns) && elect_one())
+                report(p.status, kStTimeout);
         }
     } else if (warp == kPvWarp) {
         // ------------------------------- P.V MMAs -------------------------------
-        if (lane == 0) {
+        // The whole warp waits; one elected lane issues each MMA and commit.
+        {
             bool ok = true, issued = false;
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (*abort_flag) { ok = false; break; }
                 const int vs = j % C::kVStages;
                 const int sb = j % kNB;
-                if (!wait(&pfull[sb], (j / kNB) & 1) ||
-                    !mbar_wait(&vfull[vs], (j / C::kVStages) & 1, p.wait_ns) ||
-                    (kPair && !wait(&vpeer[vs], (j / C::kVStages) & 1))) {
+                if (!__all_sync(0xffffffffu,
+                                wait(&pfull[sb], (j / kNB) & 1) &&
+                                    mbar_wait(&vfull[vs], (j / C::kVStages) & 1, p.wait_ns) &&
+                                    (!kPair || wait(&vpeer[vs], (j / C::kVStages) & 1)))) {
                     ok = false;
                     break;
                 }
@@ -391,24 +414,29 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bd = smem_desc_sw128(vb + kk * 2048, C::kVBox, 1024);
-                    if (kPair)
-                        mma_bf16_ts_pair(tmem + kColO, a + kk * 8, bd, C::kIdescPV,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
-                    else
-                        mma_bf16_ts(tmem + kColO, a + kk * 8, bd, C::kIdescPV,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    if (elect_one()) {
+                        if (kPair)
+                            mma_bf16_ts_pair(tmem + kColO, a + kk * 8, bd, C::kIdescPV,
+                                             (j > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_bf16_ts(tmem + kColO, a + kk * 8, bd, C::kIdescPV,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                commit_both(&vempty[vs]);
-                commit_self(&sfree[sb]);
-                commit_both(odone);
+                if (elect_one()) commit_both(&vempty[vs]);
+                if (elect_one()) commit_self(&sfree[sb]);
+                if (elect_one()) commit_both(odone);
+                __syncwarp();
                 issued = true;
             }
-            if (!ok) {
+            if (!ok && elect_one()) {
                 report(p.status, kStTimeout);
                 *abort_flag = 1;
             }
-            commit_both(ofinal);              // also releases the epilogue after an abort
-            if (issued && !mbar_wait(ofinal, 0, p.wait_ns)) report(p.status, kStTimeout);
+            if (elect_one()) commit_both(ofinal);   // also releases the epilogue after an abort
+            __syncwarp();
+            if (issued && !warp_wait(ofinal, 0, p.wait_ns) && elect_one())
+                report(p.status, kStTimeout);
         }
     } else {
         // ------------------------- softmax / epilogue --------------------------

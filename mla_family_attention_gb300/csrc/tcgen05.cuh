@@ -223,8 +223,21 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() {
-    return (threadIdx.x & 31) == 0;
+// True in one lane of the (converged) calling warp.  The MMA-issuing roles
+// run as whole warps: every lane executes the waits and the loop, and each
+// tcgen05.mma / commit sits in its own `if (elect_one())`.  In a converged
+// warp the same lane is elected every time, so the commits track the MMAs
+// that lane issued.  Measured on GB300 (M=128, N=64, K=16, both operands in
+// shared memory, one CTA per SM): 48 cycles per MMA issued this way, with an
+// mbarrier wait every 8 MMAs costing nothing; 58 cycles from one thread in a
+// lane-0 branch, and 77 with the same waits (each wait or shared-memory load
+// in that thread leaves the tensor pipe idle for its latency).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r));
+    return r != 0;
 }
 
 // ----------------------------------------------------------------------------
