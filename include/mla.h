@@ -298,7 +298,8 @@ mla_status mla_sparse_prefill_latent_fp8(const mla_bf16* q, const uint8_t* rec,
  * total_keys < 2^31.  A sequence with T_b outside [0, max_seqlen] or rows
  * past total_keys gets an all -1 output and MLA_ERR_INVALID_ARG in the
  * device status.  Workspace: mla_workspace_size(MLA_OP_INDEX_TOPK, B, 0,
- * max_seqlen, topk) bytes (fp32 scores, histograms, tile table).
+ * max_seqlen, topk) bytes (fp32 scores, histograms, tile table, per-sequence
+ * tile claim counters).
  */
 mla_status dsa_index_topk(const mla_bf16* index_q, const mla_bf16* index_k, const float* w,
                           const int64_t* cu_seqlens, int B, int NH, int64_t total_keys,

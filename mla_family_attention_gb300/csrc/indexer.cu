@@ -58,14 +58,21 @@ constexpr int kTile = 128;                                   // positions per MM
 #define MLA_INDEX_STAGES 6
 #endif
 constexpr int kIStages = MLA_INDEX_STAGES;
-// Tiles the TMA producer prefetches into L2 ahead of its loads (bf16 keys;
-// 0 = none).  On B=8, T=131072: 4 ahead took the scoring kernel from 49.6
-// to 46.7 us and the call from 63.9 to 62.7 us; 8 and 16 ahead were slower
-// (the prefetches share the TMA unit with the loads); FP8 keys gained
-// nothing at any distance, so their producer prefetches nothing.
+// The TMA producer prefetches into L2 the key rows of the next chunk it has
+// claimed (bf16 keys; 0 = none): 2-4 tiles ahead of its loads.  With
+// contiguous ranges, 4 tiles ahead had taken the scoring kernel from 49.6
+// to 46.7 us on B=8, T=131072, and 8 and 16 ahead were slower (the
+// prefetches share the TMA unit with the loads); FP8 keys gained nothing,
+// so their producer prefetches nothing.
 #ifndef MLA_INDEX_PREFETCH
-#define MLA_INDEX_PREFETCH 4
+#define MLA_INDEX_PREFETCH 1
 #endif
+// Tiles per claim.  The scoring CTAs take their tiles from per-sequence
+// counters, two at a time: each starts on a home sequence (the one holding
+// tile c*n/G, so ~n/G tiles per CTA) and moves to the following sequences
+// once it is used up.  With fixed contiguous ranges the 152 CTAs finished
+// between 38.5 and 43.4 us (B=8, T=131072): their rates differ by ~10 %.
+constexpr int kClaim = 2;
 constexpr int kAHalf = kTile * 64 * 2;                       // 16 KB: 128 rows x 128 B
 constexpr int kBHalf = kIndexHeads * 64 * 2;                 // 4 KB: 32 rows x 128 B
 constexpr int kStageBytes = 2 * kAHalf;                      // 32 KB of index keys
@@ -88,10 +95,12 @@ struct ScoreCfg {
     static constexpr int kStage = kFp8 ? kTile * 128 : kStageBytes;
     static constexpr int kStages = kFp8 ? 2 * kIStages : kIStages;
     static constexpr int kQ = kFp8 ? kIndexHeads * 128 : kQBytes;
-    // barriers: 2*kStages ring + 2*kAcc accumulator + 2 query, then the TMEM
-    // address and the abort flag
-    static constexpr size_t kBarBytes = (2 * kStages + 2 * kAcc + 2) * 8 + 16;
-    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStage + 2 * kQ + kBins * 4 + kBarBytes;
+    // barriers: 2*kStages ring + 2*kAcc accumulator + 2 query + kAcc tile
+    // notices, then the TMEM address and the abort flag; then the tile of
+    // each ring stage and of each accumulator (int2 each)
+    static constexpr size_t kBarBytes = (2 * kStages + 3 * kAcc + 2) * 8 + 16;
+    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStage + 2 * kQ + kBins * 4 + kBarBytes +
+                                    (kStages + kAcc) * 8;
 };
 
 struct ScoreParams {
@@ -101,6 +110,7 @@ struct ScoreParams {
     const float* kscale;     // FP8: per-position key scale, else null
     const int64_t* cu;
     const int* tile_start;   // [B+1]
+    int* claim;              // [B] tiles of each sequence claimed so far (zeroed by the tiles kernel)
     float* scores;           // [B][stride]
     unsigned* hist;          // [B][2048]
     int B, stride;
@@ -158,8 +168,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + kAcc;
     uint64_t* qfull = tempty + kAcc;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qfull + 2);
+    uint64_t* tnote = qfull + 2;                                // [kAcc] accumulator's tile known
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tnote + kAcc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // (tile, sequence) of each ring stage (tile -1: no more tiles) and of
+    // each accumulator, written by the producer and the MMA warp
+    int2* stage_tile = reinterpret_cast<int2*>(tmem_holder + 4);
+    int2* acc_tile = stage_tile + C::kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -172,6 +187,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 4);
+            mbar_init(&tnote[a], 1);
         }
         mbar_init(&qfull[0], 1);
         mbar_init(&qfull[1], 1);
@@ -184,12 +200,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&qmap);
     }
-    // everything above is set-up; the tile list and the cleared histograms
-    // come from the tiles kernel
+    // everything above is set-up; the tile list, the cleared histograms and
+    // claim counters come from the tiles kernel
     grid_dep_wait();
     const int n_tiles = p.tile_start[p.B];
-    const int t_begin = int((int64_t(n_tiles) * blockIdx.x) / gridDim.x);
-    const int t_end = int((int64_t(n_tiles) * (blockIdx.x + 1)) / gridDim.x);
+    // home sequence: the one holding tile c*n/G (its level-1 bins are kept in
+    // shared memory; tiles of other sequences add theirs to global memory)
+    const int home = n_tiles > 0
+        ? tile_owner(p.tile_start, p.B, int((int64_t(n_tiles) * blockIdx.x) / gridDim.x))
+        : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -206,56 +225,144 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             for (int i = 0; i < C::kStages; ++i) filled[i] = 0;
             int qfilled[2] = {0, 0}, last_use[2] = {-1, -1};
             int cur_b = -1, seg = 0, row0 = 0;   // row0: first key row of sequence cur_b
-            SeqCursor cs;
-            if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
-            for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
+            // claims: chunk = (first tile, tiles, sequence); seq is the
+            // sequence of the latest claim
+            int seq = home;
+            auto ntiles = [&](int b) { return p.tile_start[b + 1] - p.tile_start[b]; };
+            // Blocking claim from seq onwards (cyclically): the claim counters
+            // of eight sequences are read at once, the first one with tiles
+            // left is claimed; a claim that lost the race probes again.
+            auto claim_next = [&]() -> int3 {
+                for (int attempt = 0; attempt < 4 * p.B + 4; ++attempt) {
+                    int found = -1;
+                    for (int k0 = 0; k0 < p.B && found < 0; k0 += 8) {
+                        int c[8], nt[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            int b = seq + k0 + k;
+                            b -= b >= p.B ? p.B : 0;
+                            const bool in = k0 + k < p.B;
+                            c[k] = in ? *reinterpret_cast<volatile int*>(p.claim + b) : 0;
+                            nt[k] = in ? ntiles(b) : 0;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (found < 0 && c[k] < nt[k]) {
+                                found = seq + k0 + k;
+                                found -= found >= p.B ? p.B : 0;
+                            }
+                    }
+                    if (found < 0) break;
+                    seq = found;
+                    const int base = int(atomicAdd(reinterpret_cast<unsigned*>(p.claim + seq),
+                                                   unsigned(kClaim)));
+                    if (base < ntiles(seq))
+                        return make_int3(p.tile_start[seq] + base, min(kClaim, ntiles(seq) - base),
+                                         seq);
+                }
+                return make_int3(0, 0, -1);
+            };
+            auto prefetch_chunk = [&](int3 ch) {
+                if (kFp8 || MLA_INDEX_PREFETCH == 0 || ch.y <= 0) return;
+                const int64_t r0 = int64_t(p.cu[ch.z]) + int64_t(ch.x - p.tile_start[ch.z]) * kTile;
+                int64_t r1 = r0 + int64_t(ch.y) * kTile;
+                if (r1 > p.cu[ch.z + 1]) r1 = p.cu[ch.z + 1];
+                if (r1 > r0 && r0 >= 0 && r1 <= p.total_keys)
+                    prefetch_l2_bytes(static_cast<const uint8_t*>(p.keys) + r0 * (C::kStage / kTile),
+                                      uint32_t((r1 - r0) * (C::kStage / kTile)));
+            };
+            // The first 2*kClaim tiles of each CTA need no claim: CTA c is the
+            // r-th of the CTAs homed on sequence h and takes tiles 4r..4r+3 of
+            // it (the tiles kernel started h's counter past them).
+            int3 cur = make_int3(0, 0, -1), nxt = make_int3(0, 0, -1);
+            if (n_tiles > 0) {
+                const int64_t G = gridDim.x, n = n_tiles;
+                const int r = int(blockIdx.x) - int((int64_t(p.tile_start[home]) * G + n - 1) / n);
+                const int nt = ntiles(home), f0 = 2 * kClaim * r;
+                if (f0 < nt) cur = make_int3(p.tile_start[home] + f0, min(kClaim, nt - f0), home);
+                if (f0 + kClaim < nt)
+                    nxt = make_int3(p.tile_start[home] + f0 + kClaim, min(kClaim, nt - f0 - kClaim),
+                                    home);
+            }
+            if (cur.y == 0) {
+                cur = claim_next();
+                nxt = cur.y > 0 ? claim_next() : make_int3(0, 0, -1);
+            } else if (nxt.y == 0) {
+                nxt = claim_next();
+            }
+            int j = 0;
+            bool ok = true;
+            while (ok && cur.y > 0) {
+                // the claim after nxt, in flight while cur's tiles are issued
+                const bool pending = nxt.y > 0;
+                const unsigned pend =
+                    pending ? atomicAdd(reinterpret_cast<unsigned*>(p.claim + seq), unsigned(kClaim))
+                            : 0u;
+                prefetch_chunk(nxt);
+                for (int t = cur.x; t < cur.x + cur.y; ++t, ++j) {
+                    const int slot = j % C::kStages, round = j / C::kStages;
+                    if (*abort_flag) { ok = false; break; }
+                    if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
+                        report(p.status, kStTimeout);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    const int b = cur.z;
+                    if (b != cur_b) {
+                        const int qb = seg & 1;
+                        const int lu = last_use[qb];
+                        if (lu >= 0 && j - lu < C::kStages &&
+                            !mbar_wait(&empty[lu % C::kStages], (lu / C::kStages) & 1, p.wait_ns)) {
+                            report(p.status, kStTimeout);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&qfull[qb], C::kQ);
+                        tma_load_2d(qbuf + qb * C::kQ, &qmap, 0, b * kIndexHeads, &qfull[qb]);
+                        if (!kFp8)
+                            tma_load_2d(qbuf + qb * C::kQ + kBHalf, &qmap, 64, b * kIndexHeads,
+                                        &qfull[qb]);
+                        qfilled[qb] = (seg >> 1) + 1;
+                        cur_b = b;
+                        row0 = int(p.cu[b]) - p.tile_start[b] * kTile;
+                        ++seg;
+                    }
+                    last_use[(seg - 1) & 1] = j;
+                    const int row = row0 + t * kTile;
+                    MLA_CHECK(slot < C::kStages && row >= 0, p.status);
+                    stage_tile[slot] = make_int2(t, b);
+                    uint8_t* st = smem + slot * C::kStage;
+                    mbar_arrive_expect_tx(&full[slot], C::kStage);
+                    tma_load_2d_hint(st, &kmap, 0, row, &full[slot], stream_policy);
+                    if (!kFp8)
+                        tma_load_2d_hint(st + kAHalf, &kmap, 64, row, &full[slot], stream_policy);
+                    filled[slot] = round + 1;
+                }
+                if (!ok) break;
+                int3 after = make_int3(0, 0, -1);
+                if (pending) {
+                    if (int(pend) < ntiles(seq))
+                        after = make_int3(p.tile_start[seq] + int(pend),
+                                          min(kClaim, ntiles(seq) - int(pend)), seq);
+                    else
+                        after = claim_next();
+                }
+                cur = nxt;
+                nxt = after;
+            }
+            if (ok) {
+                // no more tiles: the stage after the last one carries tile -1
                 const int slot = j % C::kStages, round = j / C::kStages;
-                if (*abort_flag) break;
                 if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1, p.wait_ns)) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
-                    break;
+                } else {
+                    stage_tile[slot] = make_int2(-1, -1);
+                    mbar_arrive(&full[slot]);
+                    filled[slot] = round + 1;
                 }
-                cs.advance(p.tile_start, t);
-                const int b = cs.b;
-                if (b != cur_b) {
-                    const int qb = seg & 1;
-                    const int lu = last_use[qb];
-                    if (lu >= 0 && j - lu < C::kStages &&
-                        !mbar_wait(&empty[lu % C::kStages], (lu / C::kStages) & 1, p.wait_ns)) {
-                        report(p.status, kStTimeout);
-                        *abort_flag = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&qfull[qb], C::kQ);
-                    tma_load_2d(qbuf + qb * C::kQ, &qmap, 0, b * kIndexHeads, &qfull[qb]);
-                    if (!kFp8)
-                        tma_load_2d(qbuf + qb * C::kQ + kBHalf, &qmap, 64, b * kIndexHeads,
-                                    &qfull[qb]);
-                    qfilled[qb] = (seg >> 1) + 1;
-                    cur_b = b;
-                    row0 = int(p.cu[b]) - p.tile_start[b] * kTile;
-                    ++seg;
-                }
-                last_use[(seg - 1) & 1] = j;
-                const int row = row0 + t * kTile;
-                if (!kFp8 && MLA_INDEX_PREFETCH > 0 && t + MLA_INDEX_PREFETCH < t_end) {
-                    // the key rows MLA_INDEX_PREFETCH tiles further on (past a
-                    // sequence boundary they need not be that tile's rows: the
-                    // prefetch is then wasted, and clamped to the key array)
-                    const int64_t r0 = int64_t(row) + int64_t(MLA_INDEX_PREFETCH) * kTile;
-                    const int64_t r1 = r0 + kTile < p.total_keys ? r0 + kTile : p.total_keys;
-                    if (r1 > r0 && r0 >= 0)
-                        prefetch_l2_bytes(static_cast<const uint8_t*>(p.keys) + r0 * (C::kStage / kTile),
-                                          uint32_t((r1 - r0) * (C::kStage / kTile)));
-                }
-                MLA_CHECK(slot < C::kStages && row >= 0, p.status);
-                uint8_t* st = smem + slot * C::kStage;
-                mbar_arrive_expect_tx(&full[slot], C::kStage);
-                tma_load_2d_hint(st, &kmap, 0, row, &full[slot], stream_policy);
-                if (!kFp8)
-                    tma_load_2d_hint(st + kAHalf, &kmap, 64, row, &full[slot], stream_policy);
-                filled[slot] = round + 1;
             }
             for (int i = 0; i < C::kStages; ++i)
                 if (filled[i] > 0 && !mbar_wait(&full[i], (filled[i] - 1) & 1, p.wait_ns))
@@ -266,28 +373,48 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer -------------------------------
+        // Takes each stage's tile from the producer, hands it on to the
+        // epilogue group of the stage's accumulator (acc_tile + tnote), and
+        // after the last tile posts "no more tiles" to all four groups.
         if (lane == 0) {
             int last_acc = -1, last_phase = 0;
             int cur_b = -1, seg = 0;
-            SeqCursor cs;
-            if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
-            for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
+            for (int j = 0;; ++j) {
                 const int slot = j % C::kStages, acc = j % kAcc;
                 if (*abort_flag) break;
-                cs.advance(p.tile_start, t);
-                const int b = cs.b;
+                if (!mbar_wait(&full[slot], (j / C::kStages) & 1, p.wait_ns)) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int2 tb = stage_tile[slot];
+                if (tb.x < 0) {                           // no more tiles
+                    for (int k = 0; k < kAcc; ++k) {
+                        const int jj = j + k, a = jj % kAcc;
+                        if (jj >= kAcc && !mbar_wait(&tempty[a], ((jj / kAcc) - 1) & 1, p.wait_ns)) {
+                            report(p.status, kStTimeout);
+                            *abort_flag = 1;
+                            break;
+                        }
+                        acc_tile[a] = make_int2(-1, -1);
+                        mbar_arrive(&tnote[a]);
+                    }
+                    break;
+                }
                 bool ok = true;
-                if (b != cur_b) {                     // this sequence's queries
+                if (tb.y != cur_b) {                      // this sequence's queries
                     ok = mbar_wait(&qfull[seg & 1], (seg >> 1) & 1, p.wait_ns);
-                    cur_b = b;
+                    cur_b = tb.y;
                     ++seg;
                 }
-                if (!ok || !mbar_wait(&full[slot], (j / C::kStages) & 1, p.wait_ns) ||
+                if (!ok ||
                     (j >= kAcc && !mbar_wait(&tempty[acc], ((j / kAcc) - 1) & 1, p.wait_ns))) {
                     report(p.status, kStTimeout);
                     *abort_flag = 1;
                     break;
                 }
+                acc_tile[acc] = tb;
+                mbar_arrive(&tnote[acc]);
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(smem + slot * C::kStage);
                 const uint32_t b0 = smem_u32(qbuf + ((seg - 1) & 1) * C::kQ);
@@ -320,34 +447,34 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
     } else {
         // ------------------------------- epilogue --------------------------------
-        // kEpiGroups groups of four warps take turns (group g the tiles with
-        // j % kEpiGroups == g, i.e. TMEM accumulator g); every group walks
-        // every tile's sequence bookkeeping so all meet the same
-        // histogram-flush barriers.
+        // kEpiGroups groups of four warps take turns: group g the tiles of
+        // accumulator g (steps j = g, g + kEpiGroups, ...), each told by the
+        // MMA warp which tile its next step holds.  Scores of the home
+        // sequence are counted in the shared histogram (added to global
+        // memory once, at the end); those of other sequences directly in
+        // global memory.
         const int grp = (warp - 2) >> 2;
         const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
         const int r = quad * 32 + lane;            // position within the tile
+        const int acc = grp;
         int cur_b = -1, T = 0, tstart = 0;
         int64_t kbase = 0;                         // first key row of the current sequence
         float wr[kIndexHeads];                     // head weights of the current sequence
-        SeqCursor cs;
-        if (t_begin < t_end) cs.init(p.tile_start, p.B, t_begin);
-        for (int t = t_begin, j = 0; t < t_end; ++t, ++j) {
-            const int acc = j % kAcc;
-            cs.advance(p.tile_start, t);
-            const int b = cs.b;
-            if (b != cur_b) {
-                if (cur_b >= 0) {                  // flush the previous sequence's bins
-                    named_bar_sync(1, kEpiThreads);
-                    for (int i = threadIdx.x - 64; i < kBins; i += kEpiThreads) {
-                        const unsigned c = hist[i];
-                        if (c) {
-                            atomicAdd(&p.hist[size_t(cur_b) * kBins + i], c);
-                            hist[i] = 0;
-                        }
-                    }
-                    named_bar_sync(1, kEpiThreads);
+        for (int j = grp;; j += kEpiGroups) {
+            const uint32_t par = (j / kAcc) & 1;
+            bool ok = !*abort_flag && mbar_wait(&tnote[acc], par, p.wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
                 }
+                break;
+            }
+            const int2 tb = acc_tile[acc];
+            if (tb.x < 0) break;                   // no more tiles
+            const int t = tb.x, b = tb.y;
+            if (b != cur_b) {
                 cur_b = b;
                 kbase = p.cu[b];
                 T = int(p.cu[b + 1] - kbase);
@@ -355,22 +482,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
                 for (int h = 0; h < kIndexHeads; ++h) wr[h] = __ldg(p.w + size_t(b) * kIndexHeads + h);
             }
-            if (j % kEpiGroups != grp) continue;   // another group's tile
             const int pos = (t - tstart) * kTile + r;
             const bool in = pos < T;
             // FP8: the key scale is loaded before the accumulator wait so its
             // latency overlaps it
             const float ksc = (kFp8 && in) ? __ldg(p.kscale + kbase + pos) : 1.f;
-            // After a timeout every warp keeps walking the tile list without
-            // touching TMEM, so all four warps meet the same named barriers.
-            bool ok = !*abort_flag;
-            if (ok && !mbar_wait(&tfull[acc], (j / kAcc) & 1, p.wait_ns)) {
-                report(p.status, kStTimeout);
-                *abort_flag = 1;
-                ok = false;
-            }
+            ok = mbar_wait(&tfull[acc], par, p.wait_ns);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) continue;                     // (no barrier inside a tile's work)
+            if (!ok) {
+                if (lane == 0) {
+                    report(p.status, kStTimeout);
+                    *abort_flag = 1;
+                }
+                break;
+            }
             tc_fence_after();
             MLA_CHECK(acc < kAcc && uint32_t(acc * 32 + 32) <= kTmemCols && r < kTile, p.status);
             float d[32];
@@ -393,14 +518,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 const unsigned bin = okey(s) >> 21;
                 MLA_CHECK(bin < unsigned(kBins), p.status);
                 const unsigned peers = __match_any_sync(mask, bin);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], unsigned(__popc(peers)));
+                if (lane == __ffs(peers) - 1) {
+                    if (b == home)
+                        atomicAdd(&hist[bin], unsigned(__popc(peers)));
+                    else
+                        atomicAdd(&p.hist[size_t(b) * kBins + bin], unsigned(__popc(peers)));
+                }
             }
         }
         named_bar_sync(1, kEpiThreads);
-        if (cur_b >= 0) {
+        if (n_tiles > 0) {
             for (int i = threadIdx.x - 64; i < kBins; i += kEpiThreads) {
                 const unsigned c = hist[i];
-                if (c) atomicAdd(&p.hist[size_t(cur_b) * kBins + i], c);
+                if (c) atomicAdd(&p.hist[size_t(home) * kBins + i], c);
             }
         }
     }
@@ -414,11 +544,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // is kept anyway.  Sequences outside [0, max_seqlen] or past total_keys are
 // reported and get no tiles.
 // Blocks after the first clear the level-1 histograms the scoring pass adds
-// into (B x 2048 counters).
+// into (B x 2048 counters).  Block 0 also starts each sequence's claim
+// counter past the tiles the G scoring CTAs homed on it take without a
+// claim (2 * kClaim each; CTA c is homed on the sequence holding tile
+// floor(c * n / G), so the CTAs homed on b are ceil(start_b * G / n) ..
+// ceil(start_{b+1} * G / n) - 1).
 __global__ void __launch_bounds__(1024) dsa_tiles_kernel(const int64_t* cu, int B, int max_seqlen,
                                                          int64_t total_keys, int topk,
                                                          int* tile_start, unsigned* hist,
-                                                         int* status) {
+                                                         int* claim, int G, int* status) {
     __shared__ int warp_sums[32];
     if (threadIdx.x == 0) grid_dep_trigger();
     grid_dep_wait();
@@ -461,11 +595,17 @@ __global__ void __launch_bounds__(1024) dsa_tiles_kernel(const int64_t* cu, int 
     }
     __syncthreads();
     int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
+    const int64_t n = warp_sums[31];               // all tiles
+    auto first_cta = [&](int64_t t) { return n > 0 ? (t * G + n - 1) / n : int64_t(0); };
     for (int b = b0; b < b1; ++b) {
         tile_start[b] = run;
         const int64_t T = cu[b + 1] - cu[b];
+        int nt = 0;
         if (!(T < 0 || T > max_seqlen || cu[b] < 0 || cu[b + 1] > total_keys))
-            run += T > topk ? int((T + kTile - 1) / kTile) : 0;
+            nt = T > topk ? int((T + kTile - 1) / kTile) : 0;
+        const int64_t homed = nt > 0 ? first_cta(run + nt) - first_cta(run) : 0;
+        claim[b] = int(min(int64_t(nt), homed * 2 * kClaim));
+        run += nt;
     }
     if (threadIdx.x == blockDim.x - 1) tile_start[B] = run;
 }
@@ -1642,13 +1782,14 @@ int score_stride(int max_seqlen) { return (max_seqlen + 3) & ~3; }
 }  // namespace
 
 IndexPlan plan_index(int B, int max_seqlen, bool fp8) {
-    // scores | level-1 histograms | tile table | FP8: query codes, scales, folded weights
+    // scores | level-1 histograms | tile table | claim counters | FP8: query
+    // codes, scales, folded weights
     IndexPlan p{};
     p.scores_off = 0;
     p.hist_off = align256(size_t(B) * score_stride(max_seqlen) * 4);
-    p.counts_off = p.hist_off + align256(size_t(B) * kBins * 4);
-    p.tiles_off = p.counts_off;
-    p.total = p.tiles_off + align256(size_t(B + 1) * 4);
+    p.tiles_off = p.hist_off + align256(size_t(B) * kBins * 4);
+    p.claims_off = p.tiles_off + align256(size_t(B + 1) * 4);
+    p.total = p.claims_off + align256(size_t(B) * 4);
     if (fp8) {
         p.q8_off = p.total;
         p.qs_off = p.q8_off + align256(size_t(B) * kIndexHeads * 128);
@@ -1680,7 +1821,8 @@ static cudaError_t launch_score_topk(const IndexArgs& a, const CUtensorMap& kmap
     const int zero_blocks = int(std::min<int64_t>(1024, (int64_t(a.B) * kBins + 16383) / 16384));
     cudaError_t e = launch_after_prev(dsa_tiles_kernel, dim3(1 + zero_blocks), dim3(1024), 0, st,
                                       a.cu, a.B, a.max_seqlen, a.total_keys, a.topk,
-                                      const_cast<int*>(p.tile_start), p.hist, dev.status);
+                                      const_cast<int*>(p.tile_start), p.hist, p.claim, dev.sms,
+                                      dev.status);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dsa_score_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(ScoreCfg<kFp8>::kSmem));
@@ -1734,6 +1876,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
     float* scores = reinterpret_cast<float*>(ws + pl.scores_off);
     unsigned* hist = reinterpret_cast<unsigned*>(ws + pl.hist_off);
     int* tiles = reinterpret_cast<int*>(ws + pl.tiles_off);
+    int* claims = reinterpret_cast<int*>(ws + pl.claims_off);
 
     CUtensorMap kmap, qmap;
     const uint64_t rows = a.total_keys > 0 ? uint64_t(a.total_keys) : 1;
@@ -1743,7 +1886,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const IndexPlan& pl, const Dev
                             kIndexDim * 2, 64, kIndexHeads);
     if (e != cudaSuccess) return e;
 
-    ScoreParams p{a.index_k, a.total_keys, a.w, nullptr, a.cu, tiles, scores, hist, a.B,
+    ScoreParams p{a.index_k, a.total_keys, a.w, nullptr, a.cu, tiles, claims, scores, hist, a.B,
                   score_stride(a.max_seqlen), kn.wait_limit_ns, dev.status};
     return launch_score_topk<false>(a, kmap, qmap, p, dev, tm, st);
 }
@@ -1791,6 +1934,7 @@ cudaError_t launch_index_topk_fp8(const IndexArgs& a, const IndexFp8Args& f, con
     float* scores = reinterpret_cast<float*>(ws + pl.scores_off);
     unsigned* hist = reinterpret_cast<unsigned*>(ws + pl.hist_off);
     int* tiles = reinterpret_cast<int*>(ws + pl.tiles_off);
+    int* claims = reinterpret_cast<int*>(ws + pl.claims_off);
     uint8_t* q8 = ws + pl.q8_off;
     float* qs = reinterpret_cast<float*>(ws + pl.qs_off);
     float* wq = reinterpret_cast<float*>(ws + pl.wq_off);
@@ -1804,7 +1948,7 @@ cudaError_t launch_index_topk_fp8(const IndexArgs& a, const IndexFp8Args& f, con
     if (e != cudaSuccess) return e;
     e = encode_tmap_2d_u8(&qmap, q8, 128, uint64_t(qrows), 128, 128, kIndexHeads);
     if (e != cudaSuccess) return e;
-    ScoreParams p{f.k8, a.total_keys, wq, f.kscale, a.cu, tiles, scores, hist, a.B,
+    ScoreParams p{f.k8, a.total_keys, wq, f.kscale, a.cu, tiles, claims, scores, hist, a.B,
                   score_stride(a.max_seqlen), kn.wait_limit_ns, dev.status};
     return launch_score_topk<true>(a, kmap, qmap, p, dev, tm, st);
 }

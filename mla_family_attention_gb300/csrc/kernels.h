@@ -134,7 +134,7 @@ struct IndexArgs {
 };
 
 struct IndexPlan {
-    size_t scores_off, hist_off, counts_off, tiles_off, total;
+    size_t scores_off, hist_off, tiles_off, claims_off, total;
     size_t q8_off = 0, qs_off = 0, wq_off = 0;   // FP8 variant only
 };
 
