@@ -181,7 +181,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // exist, before the CTA-wide set-up barrier (the loads then overlap the
     // TMEM allocation); a short prompt's whole run is a few such latencies.
     const bool early = !kPair && n_kv > 0;
+    // Launched as a programmatic dependent of the stream's previous kernel:
+    // the set-up below (barriers, TMEM) may overlap that kernel's tail, and
+    // every thread waits for it (grid_dep_wait) before touching global
+    // memory, since it may have written the inputs.  The next kernel may be
+    // placed as soon as this one starts.
     if (threadIdx.x == 0) {
+        grid_dep_trigger();
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
         tma_prefetch_desc(&qmap);
@@ -207,6 +213,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(qkdone, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        grid_dep_wait();
         if (early) {
             mbar_arrive_expect_tx(qready, kQTile);
             for (int c = 0; c < 3; ++c)
@@ -223,6 +230,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (kPair) tmem_alloc_pair(tmem_holder, kCols);
         else tmem_alloc(tmem_holder, kCols);
     }
+    grid_dep_wait();
     tc_fence_before();
     if (kPair) pair_sync();     // both CTAs' barriers exist before either signals the other
     else __syncthreads();
@@ -646,8 +654,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Kn
         if (e != cudaSuccess) return e;
         const int grid = p.n_qt * a.B * a.H;
         if (tm.begin) cudaEventRecord(tm.begin, st);
-        mla_prefill_kernel<false><<<grid, kPThreads, PCfg<false>::kSmem, st>>>(kmap, vmap, qmap, p);
+        e = launch_after_prev(mla_prefill_kernel<false>, dim3(grid), dim3(kPThreads),
+                              PCfg<false>::kSmem, st, kmap, vmap, qmap, p);
         if (tm.end) cudaEventRecord(tm.end, st);
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
     e = cudaFuncSetAttribute(mla_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -655,18 +665,20 @@ cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, const Kn
     if (e != cudaSuccess) return e;
     // clusters of two CTAs: query tiles 2i and 2i+1 of one head (the odd
     // CTA of the last pair of an odd tile count has no rows to store)
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * ((p.n_qt + 1) / 2) * a.B * a.H);
     cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = PCfg<true>::kSmem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (tm.begin) cudaEventRecord(tm.begin, st);
     e = cudaLaunchKernelEx(&cfg, mla_prefill_kernel<true>, kmap, vmap, qmap, p);
     if (tm.end) cudaEventRecord(tm.end, st);

@@ -151,4 +151,7 @@ def test_compact_keeps_the_summary_figures():
     got = bench._compact(entry)
     assert dict(zip(bench.ALSO_FIELDS, got)) == {
         "value": 1.5, "unit": "GB/s", "ms_per_step": 2.0, "roofline.frac": 0.5,
-        "roofline.kernel_ms": 1.9, "cpu_baseline.value": 0.01}
+        "roofline.kernel_ms": 1.9, "cpu_baseline.value": 0.01,
+        "latency_after_l2_flush_ms": None}
+    entry["latency_after_l2_flush_ms"] = 0.0146
+    assert bench._compact(entry)[-1] == 0.0146
