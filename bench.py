@@ -563,13 +563,12 @@ class PrefillWork:
             self.bound = "hbm"
             self.kernels = [(_lib.OP_PREFILL, "mla_prefill_kernel<short>", io, "hbm")]
             # inputs that fit in L2: N copies, together over 4x L2, read in
-            # turn, so no step finds its inputs in L2
+            # turn, so no step finds its inputs in L2 (one output buffer)
             self.rotating = -(-4 * (129 << 20) // io)
             for _ in range(self.rotating - 1):
                 pf = self.pf
                 self.sets.append((pf.q.clone(), pf.k.clone(), pf.v.clone(),
-                                  None if pf.gate is None else pf.gate.clone(),
-                                  torch.empty_like(self.out)))
+                                  None if pf.gate is None else pf.gate.clone(), self.out))
 
     def step(self, stream):
         q, k, v, g, out = self.sets[self.i % len(self.sets)]

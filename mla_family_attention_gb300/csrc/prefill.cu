@@ -466,7 +466,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const size_t orow = (size_t(b) * p.Tq + size_t(row < p.Tq ? row : 0)) * p.H + h;
         const uint4* g = p.gate ? reinterpret_cast<const uint4*>(p.gate + orow * kDv) + half * 8
                                 : nullptr;
-        if (g && row < p.Tq) prefetch_l2_line(g);
+        // A prompt of one key tile leaves the second key stage unused: the
+        // logits are copied there (cp.async) at once, 128 bytes a thread;
+        // otherwise they are prefetched into L2 now and loaded before the
+        // last P.V wait.  Either way their sigmoids are computed while the
+        // last P.V runs (a sigmoid is a tanh on the special-function unit,
+        // ~1 us for a CTA's 16,384).
+        const bool gate_smem = !kPair && n_kv == 1 && g && row < p.Tq;
+        uint8_t* gsm = ksm + C::kKTile + size_t(half * kBM + r) * 128;
+        MLA_CHECK(!gate_smem || C::kKStages >= 2 && (2 * kBM) * 128 <= C::kKTile, p.status);
+        if (gate_smem) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) cp_async16(gsm + 16 * k, g + k);
+        } else if (g && row < p.Tq) {
+            prefetch_l2_line(g);
+        }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
@@ -570,10 +584,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ---- epilogue: O / l * sigmoid(gate) -> bf16 ----
         // the gate logits are loaded before the wait for the last P.V, so
         // their latency overlaps it
+        // the 64 gates, while the last P.V runs
         uint4 gl[8];
+        if (gate_smem) {
+            cp_async_wait_all();
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            gl[k] = (g && row < p.Tq) ? __ldg(g + k) : make_uint4(0u, 0u, 0u, 0u);
+            for (int k = 0; k < 8; ++k) gl[k] = *reinterpret_cast<const uint4*>(gsm + 16 * k);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                gl[k] = (g && row < p.Tq) ? __ldg(g + k) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float sg[64];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t gg[4] = {gl[k].x, gl[k].y, gl[k].z, gl[k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sg[8 * k + 2 * e] = g ? sigmoidf_fast(bf_lo(gg[e])) : 1.f;
+                sg[8 * k + 2 * e + 1] = g ? sigmoidf_fast(bf_hi(gg[e])) : 1.f;
+            }
+        }
         bool fin = ok && wait(ofinal, 0);
         fin = __all_sync(0xffffffffu, fin);
         if (!fin && ok) report(p.status, kStTimeout);
@@ -584,29 +615,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc_fence_after();
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDv) + half * 8;
+            float o[64];
+            tmem_ld32(tmem + lane_off + kColO + half * 64, *reinterpret_cast<float(*)[32]>(o));
+            tmem_ld32(tmem + lane_off + kColO + half * 64 + 32,
+                      *reinterpret_cast<float(*)[32]>(o + 32));
+            tmem_ld_wait();
+            if (row < p.Tq) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float o[32];
-                tmem_ld32(tmem + lane_off + kColO + half * 64 + c * 32, o);
-                tmem_ld_wait();
-                if (row < p.Tq) {
+                for (int u = 0; u < 8; ++u) {
+                    float z[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float z[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) z[e] = o[u * 8 + e] * inv;
-                        if (g) {
-                            const uint4 gw = gl[c * 4 + u];
-                            const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                z[2 * e] *= sigmoidf_fast(bf_lo(gg[e]));
-                                z[2 * e + 1] *= sigmoidf_fast(bf_hi(gg[e]));
-                            }
-                        }
-                        dst[c * 4 + u] = make_uint4(pack_bf16(z[0], z[1]), pack_bf16(z[2], z[3]),
-                                                    pack_bf16(z[4], z[5]), pack_bf16(z[6], z[7]));
-                    }
+                    for (int e = 0; e < 8; ++e) z[e] = o[u * 8 + e] * inv * sg[u * 8 + e];
+                    dst[u] = make_uint4(pack_bf16(z[0], z[1]), pack_bf16(z[2], z[3]),
+                                        pack_bf16(z[4], z[5]), pack_bf16(z[6], z[7]));
                 }
             }
         }
