@@ -825,7 +825,10 @@ class DsaPrefillWork:
         self.work = fi + fa
         self.unit, self.bound, self.scale_unit = "TFLOP/s", "tensor", 1e12
         self.launches_per_step = 7      # score, top-k, absorb, schedule, attention, fixup, out
-        self.kernels = [(_lib.OP_LATENT_DECODE, "mla_latent_kernel<gather>", fa),
+        # the attention kernel is read against its own flops (the absorption
+        # and W^V projection run in the absorb and out kernels)
+        self.kernels = [(_lib.OP_LATENT_DECODE, "mla_latent_kernel<gather>",
+                         acc.sparse_latent_core_flops(T, T, H, K)),
                         (_lib.OP_PREFILL_INDEX_TOPK, "dsa_prefill_score_kernel", fi)]
 
     def step(self, stream):

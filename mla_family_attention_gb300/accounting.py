@@ -52,14 +52,21 @@ def dsa_prefill_index_flops(Tq: int, Tk: int) -> int:
     return 2 * INDEX_HEADS * INDEX_DIM * causal_pairs(Tq, Tk)
 
 
-def sparse_latent_attention_flops(Tq: int, Tk: int, H: int, topk: int) -> int:
-    """Attention of every prompt token over its min(topk, visible) selected
-    positions in the absorbed latent form: 2*(576 + 512) flops per selected
-    (token, position, head), plus the W^K absorption and the W^V projection,
-    2*128*512 flops each per (token, head)."""
+def sparse_latent_core_flops(Tq: int, Tk: int, H: int, topk: int) -> int:
+    """The attention kernel's own part of the sparse latent prefill: every
+    prompt token over its min(topk, visible) selected positions, 2*(576 + 512)
+    flops per selected (token, position, head) (Q.K^T over 576 features,
+    P.V over 512)."""
     P = Tk - Tq
     sel = sum(min(topk, P + i + 1) for i in range(Tq))
-    return sel * H * 2 * (576 + 512) + Tq * H * 2 * 2 * 128 * 512
+    return sel * H * 2 * (576 + 512)
+
+
+def sparse_latent_attention_flops(Tq: int, Tk: int, H: int, topk: int) -> int:
+    """The whole sparse latent prefill: the attention (above) plus the W^K
+    absorption and the W^V projection, 2*128*512 flops each per (token,
+    head), which run in kernels of their own."""
+    return sparse_latent_core_flops(Tq, Tk, H, topk) + Tq * H * 2 * 2 * 128 * 512
 
 
 def latent_kv_bytes_fp8(lengths) -> int:
