@@ -69,6 +69,8 @@ def run_index(d, lengths, topk, max_seqlen=None):
     ([2100 + 37 * i for i in range(40)], 2048),   # many sequences per CTA, ragged tails
     ([70000, 1, 2049, 130000, 5, 9000, 2048, 33000], 1000),
     ([131073, 5000], 2048),                       # one past the register-resident bound
+    ([2100 + 13 * i for i in range(300)], 2048),  # more sequences than scoring CTAs: most
+                                                  # are claimed by CTAs homed elsewhere
 ])
 def test_index_topk_matches_oracle(lengths, topk):
     d = mi.make_dsa(lengths, device=DEV, config=51, with_main=False)
