@@ -839,103 +839,220 @@ __global__ void __launch_bounds__(kThreadsOf<kSrc>, 1)
 }
 
 // q~[b,h,0:512] = W^K_h^T q[b,h,0:128] and q~[b,h,512:576] = q[b,h,128:192],
-// as one small tensor-core GEMM per (head, 128 latent features, up to 128
-// sequences): D[j, b] = sum_d W^K_h[d, j] q[b, h, d] with the latent features
-// as M (A = W^K block, MN-major), the sequences as N (B = queries, K-major)
-// and K = 128.  Bound by the 12.6 MB read of W^K (H = 96).
-constexpr int kAbsorbN = 128;      // sequences per CTA at most
-constexpr size_t kAbsorbSmem = 1024 + 2 * 16384 + 2 * kAbsorbN * 128 + 64;
+// as tensor-core GEMMs D[j, b] = sum_d W^K_h[d, j] q[b, h, d] with the latent
+// features as M (A = W^K_h, MN-major), the sequences as N (B = queries,
+// K-major) and K = 128.  Work items are (head, block of kAbN sequences) in
+// head-major order; each CTA takes a contiguous range of them, so it loads a
+// head's W^K (128 x 512, 128 KB in eight boxes) once per head it visits and
+// streams the query blocks through two stages.  Per item, four M=128 GEMMs
+// (the four 128-feature blocks of j, eight K=16 MMAs each) fill one of two
+// 256-column TMEM buffers while four epilogue warps convert and store the
+// other.  Roles: warp 0 TMA, warp 1 MMA issue (whole warp, one elected lane
+// issuing), warps 2-9 epilogue (thread = latent feature within a block; the
+// two warps of a TMEM lane quadrant take two feature blocks each).
+constexpr int kAbN = 64;                                  // sequences per item
+constexpr int kAbWBytes = 4 * 2 * 16384;                  // W^K_h: 4 blocks x two 64-j boxes
+constexpr int kAbQStage = 2 * kAbN * 128;                 // 64 sequences x 128 d
+constexpr size_t kAbsorbSmem = 1024 + kAbWBytes + 2 * kAbQStage + 128;
+constexpr uint32_t kIdescAbs = idesc_bf16_f32(128, kAbN, true, false);
 
-__global__ void __launch_bounds__(128) latent_absorb_kernel(
+constexpr int kAbThreads = 10 * 32;
+__global__ void __launch_bounds__(kAbThreads, 1) latent_absorb_kernel(
     const __grid_constant__ CUtensorMap wkmap, const __grid_constant__ CUtensorMap qmap,
-    const uint16_t* q, uint16_t* qt, const uint16_t* wv, int B, int H, int nbox,
+    const uint16_t* q, uint16_t* qt, const uint16_t* wv, int B, int H, int nblk,
     long long wait_ns, int* status) {
     // the work split launched next reads none of this kernel's output
     if (threadIdx.x == 0) grid_dep_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 2 * 16384 + 2 * kAbsorbN * 128);
-    uint32_t& tmem_holder = *reinterpret_cast<uint32_t*>(bars + 2);
-    const int jb = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * nbox;
-    const int nb = min(nbox, B - b0);
+    uint8_t* wsm = sm;                                    // [4 blocks][2 halves][128 d][64 j]
+    uint8_t* qsm = sm + kAbWBytes;                        // [2 stages][2 halves][kAbN b][64 d]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(qsm + 2 * kAbQStage);
+    uint64_t* wfull = bars;                               // W^K of the current head landed
+    uint64_t* wfree = bars + 1;                           // MMAs of the previous head done
+    uint64_t* qfull = bars + 2;                           // [2]
+    uint64_t* qempty = bars + 4;                          // [2]
+    uint64_t* tfull = bars + 6;                           // [2] MMA -> epilogue
+    uint64_t* tempty = bars + 8;                          // [2] epilogue -> MMA
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t* wsm = sm;                       // [2 halves][128 d][64 j]
-    uint8_t* qsm = sm + 2 * 16384;           // [2 halves][nbox b][64 d]
+    const int items = H * nblk;
+    const int i0 = int((int64_t(items) * blockIdx.x) / gridDim.x);
+    const int i1 = int((int64_t(items) * (blockIdx.x + 1)) / gridDim.x);
     if (threadIdx.x == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        mbar_init(wfull, 1);
+        mbar_init(wfree, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 8);
+        }
+        *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_holder, 128);
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_holder;
-    bool ok = true;
-    if (threadIdx.x == 32 && blockIdx.z == 0)   // W^V rows of this head's quarter, into L2
-        prefetch_l2(wv + (int64_t(h) * kDv + jb * 32) * kLatent, 32 * kLatent * 2);
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bars[0], 2 * 16384 + 2 * nbox * 128);
-        for (int hf = 0; hf < 2; ++hf) {
-            tma_load_2d(wsm + hf * 16384, &wkmap, jb * 128 + hf * 64, h * 128, &bars[0]);
-            tma_load_3d(qsm + hf * nbox * 128, &qmap, hf * 64, h, b0, &bars[0]);
+    const uint32_t tmem = *tmem_holder;
+    auto fail = [&]() {
+        report(status, kStTimeout);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------- TMA -------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&wkmap);
+            tma_prefetch_desc(&qmap);
+            int cur_h = -1, nheads = 0, wfilled = 0;
+            int qf[2] = {0, 0};
+            for (int it = i0, k = 0; it < i1; ++it, ++k) {
+                if (*abort_flag) break;
+                const int h = it / nblk, blk = it - h * nblk;
+                if (h != cur_h) {
+                    // the previous head's MMAs read W^K before it is replaced
+                    if (nheads > 0 && !mbar_wait(wfree, (nheads - 1) & 1, wait_ns)) {
+                        fail();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(wfull, kAbWBytes);
+                    for (int jb = 0; jb < 4; ++jb)
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_2d(wsm + jb * 32768 + hf * 16384, &wkmap, jb * 128 + hf * 64,
+                                        h * 128, wfull);
+                    // W^V rows of this head, into L2 for the output projection
+                    for (int qq = 0; qq < 4; ++qq)
+                        prefetch_l2(wv + (int64_t(h) * kDv + qq * 32) * kLatent, 32 * kLatent * 2);
+                    cur_h = h;
+                    ++nheads;
+                    wfilled = nheads;
+                }
+                const int s = k & 1;
+                if (k >= 2 && !mbar_wait(&qempty[s], ((k >> 1) - 1) & 1, wait_ns)) {
+                    fail();
+                    break;
+                }
+                mbar_arrive_expect_tx(&qfull[s], kAbQStage);
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d(qsm + s * kAbQStage + hf * kAbN * 128, &qmap, hf * 64, h,
+                                blk * kAbN, &qfull[s]);
+                qf[s] = (k >> 1) + 1;
+            }
+            for (int s = 0; s < 2; ++s)
+                if (qf[s] > 0 && !mbar_wait(&qfull[s], (qf[s] - 1) & 1, wait_ns))
+                    report(status, kStTimeout);
+            if (wfilled > 0 && !mbar_wait(wfull, (wfilled - 1) & 1, wait_ns))
+                report(status, kStTimeout);
         }
-        ok = mbar_wait(&bars[0], 0, wait_ns);
-        if (ok) {
+    } else if (warp == 1) {
+        // ------------------------------- MMA -------------------------------
+        bool ok = true;
+        int cur_h = -1, nheads = 0, last_u = -1, last_par = 0;
+        const uint32_t wa = smem_u32(wsm), qa = smem_u32(qsm);
+        for (int it = i0, k = 0; it < i1 && ok; ++it, ++k) {
+            const int h = it / nblk;
+            if (h != cur_h) {
+                if (nheads > 0 && elect_one()) mma_commit(wfree);   // previous head's reads
+                __syncwarp();
+                if (!warp_wait_abortable(wfull, nheads & 1, wait_ns, abort_flag)) { ok = false; break; }
+                cur_h = h;
+                ++nheads;
+            }
+            const int s = k & 1, u = k & 1;
+            if (!warp_wait_abortable(&qfull[s], (k >> 1) & 1, wait_ns, abort_flag) ||
+                (k >= 2 && !warp_wait_abortable(&tempty[u], ((k >> 1) - 1) & 1, wait_ns, abort_flag))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16_f32(128, nbox, true, false);
-            const uint32_t wa = smem_u32(wsm), qa = smem_u32(qsm);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ad = smem_desc_sw128(wa + kk * 2048, 16384, 1024);
-                const uint64_t bd =
-                    smem_desc_sw128(qa + (kk >> 2) * nbox * 128 + (kk & 3) * 32, 16, 1024);
-                mma_bf16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            for (int jb = 0; jb < 4; ++jb) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(wa + jb * 32768 + kk * 2048, 16384, 1024);
+                    const uint64_t bd = smem_desc_sw128(
+                        qa + s * kAbQStage + (kk >> 2) * kAbN * 128 + (kk & 3) * 32, 16, 1024);
+                    if (elect_one())
+                        mma_bf16_ss(tmem + uint32_t(u * 256 + jb * kAbN), ad, bd, kIdescAbs,
+                                    kk > 0 ? 1u : 0u);
+                }
             }
-        } else {
+            if (elect_one()) mma_commit(&qempty[s]);
+            if (elect_one()) mma_commit(&tfull[u]);
+            __syncwarp();
+            last_u = u;
+            last_par = (k >> 1) & 1;
+        }
+        if (!ok && elect_one()) fail();
+        // the accumulators must not be released while an MMA still writes them
+        if (last_u >= 0 && !warp_wait(&tfull[last_u], last_par, wait_ns) && elect_one())
             report(status, kStTimeout);
-        }
-        mma_commit(&bars[1]);
-    }
-    __syncwarp();
-    if (!mbar_wait(&bars[1], 0, wait_ns) && lane == 0) report(status, kStTimeout);
-    tc_fence_after();
-    const int j = jb * 128 + warp * 32 + lane;
-    for (int c0 = 0; c0 < nb; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + c0, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (c0 + i < nb) {
-                const __nv_bfloat16 x = __float2bfloat16_rn(v[i]);
-                qt[(int64_t(b0 + c0 + i) * H + h) * kCkv + j] =
-                    *reinterpret_cast<const uint16_t*>(&x);
+    } else {
+        // ----------------------------- epilogue -----------------------------
+        // warp w: TMEM lanes 32*(w%4).. = latent features 32*(w%4).. of the
+        // feature blocks 2*jh and 2*jh+1 (jh = (w-2)/4); 64 columns (one
+        // block's 64 sequences) loaded per wait
+        const int quad = warp & 3, jh = (warp - 2) >> 2;
+        const int et = threadIdx.x - 64;                  // 0..255
+        for (int it = i0, k = 0; it < i1; ++it, ++k) {
+            const int h = it / nblk, blk = it - h * nblk;
+            const int u = k & 1;
+            bool ok = !*abort_flag && mbar_wait(&tfull[u], (k >> 1) & 1, wait_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) fail();
+                break;
             }
-    }
-    if (jb == 0) {
-        // the 64 shared-key features pass through: eight 16-byte pieces per
-        // sequence, all loads issued before the stores
-        uint4 x[kAbsorbN * 8 / 128];
+            tc_fence_after();
+            const int b0 = blk * kAbN;
+#pragma unroll 1
+            for (int jj = 0; jj < 2; ++jj) {
+                const int jb = 2 * jh + jj;
+                const int j = jb * 128 + quad * 32 + lane;
+                float v[kAbN];
 #pragma unroll
-        for (int k = 0; k < kAbsorbN * 8 / 128; ++k) {
-            const int i = threadIdx.x + 128 * k;
-            if (i < nb * 8)
-                x[k] = *reinterpret_cast<const uint4*>(
-                    q + (int64_t(b0 + (i >> 3)) * H + h) * kDqk + 128 + (i & 7) * 8);
-        }
+                for (int c0 = 0; c0 < kAbN; c0 += 16)
+                    tmem_ld16(tmem + (uint32_t(quad * 32) << 16) + uint32_t(u * 256 + jb * kAbN + c0),
+                              *reinterpret_cast<float(*)[16]>(v + c0));
+                tmem_ld_wait();
+                uint16_t* dst = qt + (int64_t(b0) * H + h) * kCkv + j;
 #pragma unroll
-        for (int k = 0; k < kAbsorbN * 8 / 128; ++k) {
-            const int i = threadIdx.x + 128 * k;
-            if (i < nb * 8)
-                *reinterpret_cast<uint4*>(qt + (int64_t(b0 + (i >> 3)) * H + h) * kCkv + kLatent +
-                                          (i & 7) * 8) = x[k];
+                for (int i = 0; i < kAbN; ++i)
+                    if (b0 + i < B) {
+                        const __nv_bfloat16 x = __float2bfloat16_rn(v[i]);
+                        dst[int64_t(i) * H * kCkv] = *reinterpret_cast<const uint16_t*>(&x);
+                    }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[u]);
+            // the 64 shared-key features pass through: eight 16-byte pieces per
+            // sequence, all loads issued before the stores
+            uint4 x[kAbN * 8 / 256];
+#pragma unroll
+            for (int e = 0; e < kAbN * 8 / 256; ++e) {
+                const int i = et + 256 * e, b = b0 + (i >> 3);
+                if (b < B)
+                    x[e] = *reinterpret_cast<const uint4*>(q + (int64_t(b) * H + h) * kDqk + 128 +
+                                                           (i & 7) * 8);
+            }
+#pragma unroll
+            for (int e = 0; e < kAbN * 8 / 256; ++e) {
+                const int i = et + 256 * e, b = b0 + (i >> 3);
+                if (b < B)
+                    *reinterpret_cast<uint4*>(qt + (int64_t(b) * H + h) * kCkv + kLatent + (i & 7) * 8) =
+                        x[e];
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 
@@ -1283,7 +1400,6 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     uint16_t* zbuf = reinterpret_cast<uint16_t*>(ws + pl.z_off);
 
     // W^K as [H*128 rows (h, d)][512], W^V likewise; queries as [B][H][192]
-    const int nabs = a.B < kAbsorbN ? (a.B + 15) / 16 * 16 : kAbsorbN;
     CUtensorMap wkmap, wvmap, q3map, cmap, qmap, zmap;
     cudaError_t e = encode_tmap_2d_bf16(&wkmap, a.w_kc, kLatent, uint64_t(a.H) * 128, kLatent * 2,
                                         64, 128);
@@ -1293,7 +1409,7 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
                             small ? 64 : 128);
     if (e != cudaSuccess) return e;
     e = encode_tmap_3d_bf16(&q3map, a.q, kDqk, a.H, a.B, kDqk * 2, uint64_t(a.H) * kDqk * 2, 64,
-                            1, nabs);
+                            1, kAbN);
     if (e != cudaSuccess) return e;
     const int src = a.rec ? kSrcFp8 : a.idx ? kSrcGather : kSrcTma;
     if (src == kSrcTma) {
@@ -1312,8 +1428,9 @@ cudaError_t launch_latent_decode(const LatentArgs& a, const LatentPlan& pl, cons
     e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kAbsorbSmem));
     if (e != cudaSuccess) return e;
-    latent_absorb_kernel<<<dim3(4, a.H, (a.B + nabs - 1) / nabs), 128, kAbsorbSmem, st>>>(
-        wkmap, q3map, a.q, qt, a.w_vc, a.B, a.H, nabs, kn.wait_limit_ns, dev.status);
+    const int nblk = (a.B + kAbN - 1) / kAbN;
+    latent_absorb_kernel<<<std::min(a.H * nblk, dev.sms), kAbThreads, kAbsorbSmem, st>>>(
+        wkmap, q3map, a.q, qt, a.w_vc, a.B, a.H, nblk, kn.wait_limit_ns, dev.status);
     // the four kernels after the absorption are launched programmatically
     // dependent: each may start while its predecessor finishes and waits on
     // the device for that predecessor's results
