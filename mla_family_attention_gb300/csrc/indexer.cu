@@ -1184,6 +1184,29 @@ __global__ void __launch_bounds__(1024) dsa_topk_regs_kernel(const TopkParams p)
     grid_dep_wait();                                // the scores and level-1 bins
     int32_t* oi = p.out_idx + size_t(b) * p.topk;
     float* os = p.out_scores ? p.out_scores + size_t(b) * p.topk : nullptr;
+    auto span_of = [](int n) { return ((n + kRC - 1) / kRC + kRPer - 1) / kRPer * kRPer; };
+    // This thread's level-1 bins and 16 scores are requested together with
+    // the sequence length: the scores for the span of a sequence of
+    // max_seqlen positions (re-read below when the length gives another),
+    // inside the row's padded stride; past the length they are masked.
+    unsigned hv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) hv[k] = p.hist1[size_t(b) * kBins + tid + k * 1024];
+    const float4* s4 = reinterpret_cast<const float4*>(p.scores + size_t(b) * p.stride);
+    float v[kRPer];
+    auto load_scores = [&](int first) {
+#pragma unroll
+        for (int q = 0; q < kRPer / 4; ++q) {
+            const float4 x = first + 4 * q + 4 <= p.stride ? s4[(first >> 2) + q]
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    };
+    const int span_g = span_of(p.max_seqlen);
+    load_scores(int(rank) * span_g + tid * kRPer);
     const int T = seq_len(p, b);                    // the same for the whole cluster
     if (T <= p.topk) {                              // every position is kept
         if (rank == 0)
@@ -1194,28 +1217,11 @@ __global__ void __launch_bounds__(1024) dsa_topk_regs_kernel(const TopkParams p)
         return;
     }
     const int K = p.topk;
-    const int span = ((T + kRC - 1) / kRC + kRPer - 1) / kRPer * kRPer;
+    const int span = span_of(T);
     const int lo = int(rank) * span, hi = min(T, lo + span);
     MLA_CHECK(span <= kRStep, p.status);
     const int i0 = lo + tid * kRPer;              // this thread's first position
-
-    // loads: level-1 bins, then this thread's 16 scores (in flight during
-    // the level-1 bin search)
-    unsigned hv[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) hv[k] = p.hist1[size_t(b) * kBins + tid + k * 1024];
-    float v[kRPer];
-    {
-        const float4* s4 = reinterpret_cast<const float4*>(p.scores + size_t(b) * p.stride);
-#pragma unroll
-        for (int q = 0; q < kRPer / 4; ++q) {
-            const float4 x = i0 + 4 * q < hi ? s4[(i0 >> 2) + q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-        }
-    }
+    if (span != span_g) load_scores(i0);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         S.hist1[tid + k * 1024] = hv[k];
