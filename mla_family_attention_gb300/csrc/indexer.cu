@@ -22,12 +22,17 @@
 //           (thread = position, 32 columns = heads), apply ReLU and the head
 //           weights, write the fp32 score and count it in a 2048-bin
 //           histogram of its top 11 order-preserving key bits.
-// Tiles are assigned to CTAs in contiguous ranges so the histogram of one
-// sequence is flushed to global memory a few times, not per tile.  The FP8
-// variant reads 128 e4m3 codes per position and applies the key's scale in
-// the epilogue.
+// Each CTA starts on a home sequence and claims tiles two at a time from
+// per-sequence counters (home first, then the following sequences), so the
+// CTAs finish together although their rates differ; home bins are counted
+// in shared memory and added to the global histogram once, at the end, the
+// bins of tiles claimed elsewhere directly.  The FP8 variant reads 128 e4m3
+// codes per position and applies the key's scale in the epilogue.
 //
-// Top-k (dsa_topk_cluster_kernel, a cluster of eight CTAs per sequence).  An
+// Top-k: dsa_topk_regs_kernel for sequences of at most 8 x 16,384
+// positions (each thread's 16 order keys stay in registers; the keys sharing
+// the k-th key's 22-bit prefix are ranked by ballots), else
+// dsa_topk_cluster_kernel, a cluster of eight CTAs per sequence.  Both are an
 // exact radix select on order-preserving 32-bit keys: the first 11 bits come
 // from the histogram the scoring pass built, a pass over the (L2-resident)
 // scores held in shared memory finds the next 11 bits of the k-th key (and,
