@@ -142,22 +142,6 @@ __device__ __forceinline__ int tile_owner(const int* tile_start, int B, int t) {
     return lo;
 }
 
-// Sequence of consecutive tiles t, t+1, ...: found once by binary search,
-// then advanced without searching.
-struct SeqCursor {
-    int b, next;   // sequence of the current tile; first tile of sequence b+1
-    __device__ __forceinline__ void init(const int* tile_start, int B, int t) {
-        b = tile_owner(tile_start, B, t);
-        next = tile_start[b + 1];
-    }
-    __device__ __forceinline__ void advance(const int* tile_start, int t) {
-        while (t >= next) {
-            ++b;
-            next = tile_start[b + 1];
-        }
-    }
-};
-
 template <bool kFp8>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     dsa_score_kernel(const __grid_constant__ CUtensorMap kmap,
